@@ -1,0 +1,400 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises ``AssertionError`` when
+the oracle disagrees with what the pages and the mathematics fix:
+
+  * the FP8-E4M3 / BF16 / F16 decoders against torch's and numpy's casts of
+    every code;
+  * the block-score sheet against a numpy brute force (gather the request's
+    logical keys through the page table, one matrix product, mask, per-block
+    max) and against a hand-worked fixture and a closed-form ramp;
+  * top-k against numpy's lexicographic sort, ties and padding included;
+  * attention against torch's fp64 ``scaled_dot_product_attention`` with GQA
+    expansion on gathered, torch-dequantised keys and values, against a
+    hand-worked fixture and closed forms (uniform logits -> mean of V, one key
+    -> that key's value), and the invariants "selecting every block equals
+    dense decode", "a one-block context is that block's softmax", "permuting
+    pool pages changes nothing", "a selection is a set".
+
+``test_oracle_pins.py`` runs them on the oracle; ``test_oracle_mutants.py``
+runs them on copies of the oracle with planted mistakes and checks that each
+mistake is caught.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+from sparse_paged_decode_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+BS = W.BLOCK_SIZE
+
+
+# ----------------------------------------------------------------- helpers
+
+def tiny_decode(seed, *, lengths=(300, 130, 1, 511), tpr=(2, 1, 1, 3), Hq=4, Hkv=2, D=8, Di=8,
+                NB=4, P=24, K=3, dtype=torch.float32, idx_dtype=None, pad=None, q_dist="normal"):
+    return W.make_decode("tiny", lengths=list(lengths), tokens_per_request=list(tpr), Hq=Hq, Hkv=Hkv,
+                         D=D, Hi=1, Di=Di, NB=NB, P=P, K=K, dtype=dtype, idx_dtype=idx_dtype,
+                         seed=seed, padded_tail=pad, q_dist=q_dist)
+
+
+def corrupt_metadata(w, seed=None):
+    """Add the out-of-domain metadata cases the oracle defines: page ids
+    outside the pool, request rows outside the table, seq_len past the
+    table, negative seq_len."""
+    bt = w.block_table.clone()
+    bt[0, 1] = -1
+    bt[min(1, w.R - 1), 0] = w.P + 3
+    ri = w.req_idx.clone()
+    sl = w.seq_lens.clone()
+    if w.T >= 3:
+        ri[w.T - 1] = w.R + 5
+        sl[w.T - 2] = -7
+    sl[0] = w.NB * BS + 100
+    return bt, ri, sl
+
+
+def e4m3_to_f64(codes: torch.Tensor) -> torch.Tensor:
+    return codes.view(torch.float8_e4m3fn).to(torch.float32).to(torch.float64)
+
+
+def np_valid_slots(bt, r, L, NB, P, blocks=None):
+    """Logical tokens 0..L-1 of request r (optionally only in ``blocks``),
+    ascending, as (tau, slot) pairs; tokens whose page is outside the pool are
+    dropped.  Written independently of the oracle."""
+    R = bt.shape[0]
+    if r < 0 or r >= R or L <= 0:
+        return []
+    L = min(L, NB * BS)
+    out = []
+    for tau in range(L):
+        b = tau // BS
+        if blocks is not None and b not in blocks:
+            continue
+        page = int(bt[r, b])
+        if 0 <= page < P:
+            out.append((tau, page * BS + tau % BS))
+    return out
+
+
+def np_block_score(q_idx, k_idx, bt, ri, sl, idx_scale, NB, P):
+    q = q_idx.to(torch.float64).numpy()
+    k = k_idx.to(torch.float64).numpy()[:, 0, :]
+    T, Hi, _ = q.shape
+    out = np.full((Hi, T, NB), -np.inf)
+    for t in range(T):
+        pairs = np_valid_slots(bt, int(ri[t]), int(sl[t]), NB, P)
+        if not pairs:
+            continue
+        taus = np.array([p[0] for p in pairs])
+        slots = np.array([p[1] for p in pairs])
+        dots = (k[slots] @ q[t].T) * idx_scale  # [n, Hi]
+        blocks = taus // BS
+        for b in np.unique(blocks):
+            out[:, t, b] = dots[blocks == b].max(axis=0)
+    return out
+
+
+def sdpa_reference(w, topk, bt=None, ri=None, sl=None):
+    """torch fp64 SDPA per query token over its selected valid keys."""
+    bt = w.block_table if bt is None else bt
+    ri = w.req_idx if ri is None else ri
+    sl = w.seq_lens if sl is None else sl
+    G = w.Hq // w.Hkv
+    kf = e4m3_to_f64(w.k_cache) * w.k_scale
+    vf = e4m3_to_f64(w.v_cache) * w.v_scale
+    q = w.q.to(torch.float64)
+    out = torch.zeros((w.T, w.Hq, w.D), dtype=torch.float64)
+    for t in range(w.T):
+        for h in range(w.Hkv):
+            if topk is None:
+                blocks = None
+            else:
+                blocks = {int(b) for b in topk[min(h, topk.shape[0] - 1), t] if 0 <= int(b) < w.NB}
+            pairs = np_valid_slots(bt, int(ri[t]), int(sl[t]), w.NB, w.P, blocks)
+            if not pairs:
+                continue
+            slots = torch.tensor([p[1] for p in pairs])
+            kk = kf[slots, h, :][None, None]  # [1,1,n,D]
+            vv = vf[slots, h, :][None, None]
+            qq = q[t, h * G:(h + 1) * G, :][None, :, None, :]  # [1,G,1,D]
+            o = torch.nn.functional.scaled_dot_product_attention(
+                qq, kk.expand(1, G, -1, -1), vv.expand(1, G, -1, -1), scale=w.sm_scale)
+            out[t, h * G:(h + 1) * G, :] = o[0, :, 0, :]
+    return out.numpy()
+
+
+def assert_close(a, b, rtol=1e-12, atol=1e-12, what=""):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    assert a.shape == b.shape, (what, a.shape, b.shape)
+    ninf_a, ninf_b = np.isneginf(a), np.isneginf(b)
+    assert np.array_equal(ninf_a, ninf_b), "%s: -inf pattern differs" % what
+    fa, fb = a[~ninf_a], b[~ninf_b]
+    assert np.all(np.isfinite(fa)) and np.all(np.isfinite(fb)), "%s: non-finite values" % what
+    err = np.abs(fa - fb)
+    assert np.all(err <= atol + rtol * np.abs(fb)), "%s: max err %g" % (what, err.max() if err.size else 0)
+
+
+# ------------------------------------------------------------ the decoders
+
+def pin_e4m3_decoder(o):
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float32).numpy().astype(np.float64)
+    got = np.array([o.e4m3_value(c) for c in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref)), "E4M3 NaN codes"
+    m = ~np.isnan(ref)
+    assert np.array_equal(got[m], ref[m]), "E4M3 values"
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9
+
+
+def pin_bf16_decoder(o):
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    ref = bits.view(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([o.bf16_value(b) for b in range(0, 65536)])
+    m = ~np.isnan(ref)
+    assert np.array_equal(np.isnan(got), np.isnan(ref)), "BF16 NaN codes"
+    assert np.array_equal(got[m], ref[m]), "BF16 values"
+
+
+def pin_f16_decoder(o):
+    ref = np.arange(65536, dtype=np.uint32).astype(np.uint16).view(np.float16).astype(np.float64)
+    got = np.array([o.f16_value(b) for b in range(0, 65536)])
+    m = ~np.isnan(ref)
+    assert np.array_equal(np.isnan(got), np.isnan(ref)), "F16 NaN codes"
+    assert np.array_equal(got[m], ref[m]), "F16 values"
+
+
+# ------------------------------------------------------------ block score
+
+def pin_block_score_bruteforce(o):
+    for seed, dt in ((11, torch.float32), (12, torch.bfloat16)):
+        w = tiny_decode(seed, idx_dtype=dt)
+        bt, ri, sl = corrupt_metadata(w, seed)
+        got = o.block_score(w.q_idx, w.k_idx_cache, bt, ri, sl, w.idx_scale)
+        ref = np_block_score(w.q_idx, w.k_idx_cache, bt, ri, sl, w.idx_scale, w.NB, w.P)
+        assert_close(got, ref, what="block score seed %d" % seed)
+    # two query index heads sharing the single index key head
+    w = tiny_decode(13)
+    q2 = torch.randn((w.T, 2, w.Di), generator=torch.Generator().manual_seed(5))
+    got = o.block_score(q2, w.k_idx_cache, w.block_table, w.req_idx, w.seq_lens, 0.3)
+    ref = np_block_score(q2, w.k_idx_cache, w.block_table, w.req_idx, w.seq_lens, 0.3, w.NB, w.P)
+    assert_close(got, ref, what="block score Hi=2")
+
+
+def pin_block_score_golden(o):
+    with open(os.path.join(GOLDEN, "block_score_ramp.json")) as f:
+        fx = json.load(f)
+    P, NB = fx["pool_pages"], len(fx["block_table"][0])
+    bt = torch.tensor(fx["block_table"], dtype=torch.int32)
+    kidx = torch.full((P * BS, 1, 2), 64.0)
+    for r, sign in ((0, 1.0), (1, -1.0)):
+        n_tok = 300 if r == 0 else 256
+        for tau in range(n_tok):
+            page = int(bt[r, tau // BS])
+            kidx[page * BS + tau % BS, 0, 0] = sign * tau
+            kidx[page * BS + tau % BS, 0, 1] = 0.0
+    q = torch.tensor([[[1.0, 0.0]]] * 3)
+    got = o.block_score(q, kidx, bt, torch.tensor(fx["req_idx"], dtype=torch.int32),
+                        torch.tensor(fx["seq_lens"], dtype=torch.int32), fx["idx_scale"])
+    exp = np.array([[float(v) for v in row] for row in fx["expected"]])[None]
+    assert got.shape == exp.shape
+    assert np.array_equal(got, exp), (got, exp)
+
+
+def pin_block_score_closed_form(o):
+    """q_idx = e0 and key tau = [tau, ...]: every block scores the position of
+    its last valid token times idx_scale."""
+    w = tiny_decode(21, lengths=(333, 129, 512), tpr=(2, 1, 1), NB=4, P=16)
+    kidx = torch.full_like(w.k_idx_cache, 64.0)
+    for r, L in enumerate(w.request_lengths):
+        for tau in range(L):
+            page = int(w.block_table[r, tau // BS])
+            kidx[page * BS + tau % BS, 0, :] = 0.0
+            kidx[page * BS + tau % BS, 0, 0] = float(tau)
+    q = torch.zeros_like(w.q_idx)
+    q[:, 0, 0] = 1.0
+    got = o.block_score(q, kidx, w.block_table, w.req_idx, w.seq_lens, 0.25)
+    for t in range(w.T):
+        L = int(w.seq_lens[t])
+        for b in range(w.NB):
+            exp = -math.inf if b * BS >= L else (min(BS * (b + 1), L) - 1) * 0.25
+            assert got[0, t, b] == exp, (t, b, got[0, t, b], exp)
+
+
+# ------------------------------------------------------------------ top-k
+
+def np_topk(scores, K):
+    s = np.asarray(scores, dtype=np.float64)
+    lead, NB = s.shape[:-1], s.shape[-1]
+    flat = s.reshape(-1, NB)
+    out = np.full((flat.shape[0], K), -1, dtype=np.int32)
+    for i, row in enumerate(flat):
+        cand = [b for b in range(NB) if not (np.isnan(row[b]) or row[b] == -np.inf)]
+        order = np.lexsort((np.array(cand), -row[cand])) if cand else []
+        picked = [cand[j] for j in order][:K]
+        out[i, :len(picked)] = picked
+    return out.reshape(lead + (K,))
+
+
+def pin_topk_sort(o):
+    g = np.random.default_rng(3)
+    s = g.standard_normal((3, 17, 40))
+    s[0, :, 5:9] = 0.5  # ties
+    s[1, 3, :] = -np.inf  # no candidate
+    s[1, 4, ::3] = np.nan
+    s[2, :, 20:] = -np.inf  # short rows
+    s[2, 5, 7] = np.inf
+    for K in (1, 4, 16, 40, 45):
+        assert np.array_equal(o.select_topk(s, K), np_topk(s, K)), "top-%d" % K
+
+
+def pin_topk_closed_form(o):
+    NB = 128
+    desc = -np.arange(NB, dtype=np.float64)[None, :]  # score decreasing in block id
+    assert np.array_equal(o.select_topk(desc, 5)[0], np.arange(5))
+    flat = np.zeros((1, NB))  # all tied -> lowest ids
+    assert np.array_equal(o.select_topk(flat, 7)[0], np.arange(7))
+    none = np.full((1, NB), -np.inf)
+    assert np.array_equal(o.select_topk(none, 4)[0], -np.ones(4))
+    inc = np.arange(NB, dtype=np.float64)[None, :]
+    assert np.array_equal(o.select_topk(inc, 3)[0], [127, 126, 125])
+    # positive rescaling of the sheet does not change the selection
+    g = np.random.default_rng(9)
+    s = g.standard_normal((50, NB))
+    assert np.array_equal(o.select_topk(s, 16), o.select_topk(s * 0.37, 16))
+
+
+# -------------------------------------------------------------- attention
+
+def pin_attention_vs_sdpa(o):
+    for seed, dt, qd in ((31, torch.float32, "normal"), (32, torch.bfloat16, "student_t3")):
+        w = tiny_decode(seed, dtype=dt, q_dist=qd)
+        bt, ri, sl = corrupt_metadata(w, seed)
+        s = o.block_score(w.q_idx, w.k_idx_cache, bt, ri, sl, w.idx_scale)
+        topk = o.select_topk(s, w.K)
+        topk_h = np.concatenate([topk, np.roll(topk, 1, axis=2)], axis=0)  # distinct per kv head
+        got = o.paged_attention(w.q, w.k_cache, w.v_cache, bt, ri, sl, topk_h,
+                                w.sm_scale, w.k_scale, w.v_scale)
+        ref = sdpa_reference(w, topk_h, bt, ri, sl)
+        assert_close(got, ref, rtol=1e-11, atol=1e-12, what="sparse vs sdpa seed %d" % seed)
+        got_d = o.paged_attention(w.q, w.k_cache, w.v_cache, bt, ri, sl, None,
+                                  w.sm_scale, w.k_scale, w.v_scale)
+        ref_d = sdpa_reference(w, None, bt, ri, sl)
+        assert_close(got_d, ref_d, rtol=1e-11, atol=1e-12, what="dense vs sdpa seed %d" % seed)
+
+
+def pin_attention_golden(o):
+    with open(os.path.join(GOLDEN, "attention_two_tokens.json")) as f:
+        fx = json.load(f)
+    P, page, D = fx["pool_pages"], fx["page"], 4
+    k = torch.full((P * BS, 1, D), 448.0)
+    v = torch.full((P * BS, 1, D), 448.0)
+    for i in range(2):
+        k[page * BS + i, 0] = torch.tensor(fx["k_tokens"][i])
+        v[page * BS + i, 0] = torch.tensor(fx["v_tokens"][i])
+    k8, v8 = k.to(torch.float8_e4m3fn), v.to(torch.float8_e4m3fn)
+    q = torch.tensor(fx["q"]).view(1, 1, D)
+    bt = torch.tensor([[page]], dtype=torch.int32)
+    ri = torch.tensor([0], dtype=torch.int32)
+    sl = torch.tensor([fx["seq_len"]], dtype=torch.int32)
+    kscale = math.log(3.0)
+    exp = np.array(fx["expected"])
+    dense = o.paged_attention(q, k8, v8, bt, ri, sl, None, fx["sm_scale"], kscale, fx["v_scale"])
+    assert np.allclose(dense[0, 0], exp, rtol=1e-14, atol=1e-14), dense
+    sparse = o.paged_attention(q, k8, v8, bt, ri, sl, np.array([[[-1, 0]]], dtype=np.int32),
+                               fx["sm_scale"], kscale, fx["v_scale"])
+    assert np.array_equal(sparse, dense)
+    empty = o.paged_attention(q, k8, v8, bt, ri, sl, np.array([[[-1, -1]]], dtype=np.int32),
+                              fx["sm_scale"], kscale, fx["v_scale"])
+    assert np.array_equal(empty, np.zeros_like(empty))
+
+
+def pin_attention_closed_forms(o):
+    w = tiny_decode(41)
+    # uniform logits (q = 0): every head returns the mean of its valid values
+    qz = torch.zeros_like(w.q)
+    got = o.paged_attention(qz, w.k_cache, w.v_cache, w.block_table, w.req_idx, w.seq_lens, None,
+                            w.sm_scale, w.k_scale, w.v_scale)
+    vf = e4m3_to_f64(w.v_cache).numpy() * w.v_scale
+    G = w.Hq // w.Hkv
+    for t in range(w.T):
+        pairs = np_valid_slots(w.block_table, int(w.req_idx[t]), int(w.seq_lens[t]), w.NB, w.P)
+        slots = [p[1] for p in pairs]
+        for g in range(w.Hq):
+            exp = vf[slots, g // G, :].mean(axis=0)
+            assert np.allclose(got[t, g], exp, rtol=1e-12, atol=1e-13), (t, g)
+    # one valid key: the output is that key's value, exactly
+    sl1 = torch.ones_like(w.seq_lens)
+    got1 = o.paged_attention(w.q, w.k_cache, w.v_cache, w.block_table, w.req_idx, sl1, None,
+                             w.sm_scale, w.k_scale, w.v_scale)
+    for t in range(w.T):
+        slot = int(w.block_table[int(w.req_idx[t]), 0]) * BS
+        for g in range(w.Hq):
+            assert np.array_equal(got1[t, g], vf[slot, g // G, :]), (t, g)
+    # padding token: zeros
+    sl0 = w.seq_lens.clone()
+    sl0[:] = 0
+    got0 = o.paged_attention(w.q, w.k_cache, w.v_cache, w.block_table, w.req_idx, sl0, None,
+                             w.sm_scale, w.k_scale, w.v_scale)
+    assert not np.any(got0)
+
+
+def pin_attention_invariants(o):
+    w = tiny_decode(51, lengths=(400, 257, 90), tpr=(3, 2, 1), K=4)
+    args = (w.block_table, w.req_idx, w.seq_lens)
+    dense = o.paged_attention(w.q, w.k_cache, w.v_cache, *args, None, w.sm_scale, w.k_scale, w.v_scale)
+    # selecting every block (any order, with repeats and -1) equals dense, bit for bit
+    allb = np.tile(np.array([3, -1, 0, 2, 1, 2, -5, 9], dtype=np.int32), (1, w.T, 1))
+    sparse = o.paged_attention(w.q, w.k_cache, w.v_cache, *args, allb, w.sm_scale, w.k_scale, w.v_scale)
+    assert np.array_equal(sparse, dense), "select-all != dense"
+    # a selection is a set: repeats and out-of-range ids change nothing
+    sel = np.tile(np.array([2, 0], dtype=np.int32), (1, w.T, 1))
+    sel_rep = np.tile(np.array([2, 0, 0, -1, 2, 17], dtype=np.int32), (1, w.T, 1))
+    a = o.paged_attention(w.q, w.k_cache, w.v_cache, *args, sel, w.sm_scale, w.k_scale, w.v_scale)
+    b = o.paged_attention(w.q, w.k_cache, w.v_cache, *args, sel_rep, w.sm_scale, w.k_scale, w.v_scale)
+    assert np.array_equal(a, b), "repeated ids changed the result"
+    # permuting pool pages (and the table with them) changes nothing
+    perm = torch.randperm(w.P, generator=torch.Generator().manual_seed(8))
+    inv_slots = (perm.to(torch.int64)[:, None] * BS + torch.arange(BS)[None]).reshape(-1)
+    k2 = torch.empty_like(w.k_cache.view(torch.uint8))
+    v2 = torch.empty_like(w.v_cache.view(torch.uint8))
+    k2[inv_slots] = w.k_cache.view(torch.uint8)
+    v2[inv_slots] = w.v_cache.view(torch.uint8)
+    bt2 = perm[w.block_table.to(torch.int64)].to(torch.int32)
+    c = o.paged_attention(w.q, k2, v2, bt2, w.req_idx, w.seq_lens, sel, w.sm_scale, w.k_scale, w.v_scale)
+    assert np.array_equal(a, c), "page permutation changed the result"
+    # one-block context: selecting block 1 alone equals dense decode of a
+    # request whose whole context is that block's valid tokens
+    one = np.tile(np.array([1], dtype=np.int32), (1, w.T, 1))
+    r1 = o.paged_attention(w.q, w.k_cache, w.v_cache, *args, one, w.sm_scale, w.k_scale, w.v_scale)
+    bt1 = w.block_table[:, 1:2].contiguous()
+    sl1 = (w.seq_lens - BS).clamp(min=0, max=BS)
+    r2 = o.paged_attention(w.q, w.k_cache, w.v_cache, bt1, w.req_idx, sl1, None,
+                           w.sm_scale, w.k_scale, w.v_scale)
+    assert np.array_equal(r1, r2), "one-block context != that block's softmax"
+    # linearity in v_scale
+    d2 = o.paged_attention(w.q, w.k_cache, w.v_cache, *args, None, w.sm_scale, w.k_scale, 2 * w.v_scale)
+    assert np.allclose(d2, 2 * dense, rtol=1e-14, atol=0)
+
+
+PINS = [
+    pin_e4m3_decoder,
+    pin_bf16_decoder,
+    pin_f16_decoder,
+    pin_block_score_bruteforce,
+    pin_block_score_golden,
+    pin_block_score_closed_form,
+    pin_topk_sort,
+    pin_topk_closed_form,
+    pin_attention_vs_sdpa,
+    pin_attention_golden,
+    pin_attention_closed_forms,
+    pin_attention_invariants,
+]

@@ -1,0 +1,51 @@
+"""Planted mistakes in a copy of the oracle must each fail at least one pin.
+
+Every mutation below is a plausible slip in ``oracle.c`` (a dropped scale, a
+wrong GQA index, an off-by-one on ``seq_lens``, a reversed tie rule, a wrong
+E4M3 bias ...).  The test compiles the mutated copy in a temporary directory
+and runs the pins against it; a mutation that no pin catches would mean the
+pins leave that part of the oracle unchecked.
+"""
+import os
+
+import pytest
+
+import oracle
+from oracle_pins import PINS
+
+MUTATIONS = [
+    ("gqa index", "int64_t h = g / G;", "int64_t h = g % Hkv;"),
+    ("score seq_len off by one", "if (tau >= L)\n                            break;",
+     "if (tau > L)\n                            break;"),
+    ("score drops idx_scale", "double s = dot * idx_scale;", "double s = dot;"),
+    ("score min instead of max", "if (s > best)", "if (s < best || best == -INFINITY)"),
+    ("attention seq_len off by one", "b * block_size + i < L; ++i)", "b * block_size + i <= L; ++i)"),
+    ("attention drops k_scale", "z[j] = sm_scale * k_scale * dot;", "z[j] = sm_scale * dot;"),
+    ("attention drops v_scale", "o[d] += w * v_scale *", "o[d] += w *"),
+    ("attention ignores selection", "if (!selected[b] || b * block_size >= L)", "if (b * block_size >= L)"),
+    ("top-k tie to higher id", "return (a->block > b->block) - (a->block < b->block);",
+     "return (a->block < b->block) - (a->block > b->block);"),
+    ("top-k pads with 0", "? cells[k].block : -1;", "? cells[k].block : 0;"),
+    ("top-k keeps -inf", "if (!isnan(s) && s != -INFINITY) {", "if (!isnan(s)) {"),
+    ("e4m3 bias", "mag = ldexp(1.0 + (double)mant / 8.0, expo - 7);", "mag = ldexp(1.0 + (double)mant / 8.0, expo - 8);"),
+    ("e4m3 subnormal scale", "mag = ldexp((double)mant / 8.0, -6);", "mag = ldexp((double)mant / 8.0, -7);"),
+    ("bf16 shift", "uint32_t word = (uint32_t)bits << 16;", "uint32_t word = (uint32_t)bits << 15;"),
+    ("clip to one block short", "L = NB * bs;", "L = (NB - 1) * bs;"),
+    ("dense skips last block", "for (int64_t b = 0; b < NB && L > 0; ++b) {", "for (int64_t b = 0; b + 1 < NB && L > 0; ++b) {"),
+    ("no max subtraction guard on empty", "if (n == 0) {", "if (n < 0) {"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_mutant_is_caught(tmp_path, name, old, new):
+    with open(oracle.SOURCE) as f:
+        src = f.read()
+    assert src.count(old) == 1, "mutation anchor not found exactly once: %r" % old
+    m = oracle.mutant(src.replace(old, new), workdir=str(tmp_path))
+    caught = []
+    for pin in PINS:
+        try:
+            pin(m)
+        except (AssertionError, ValueError, RuntimeError) as e:  # noqa: PERF203
+            caught.append(pin.__name__)
+    assert caught, "planted mistake %r passed every pin" % name

@@ -1,0 +1,382 @@
+"""Benchmark of the sparse paged decode hot path.
+
+One step = the three stages over one batch of the EAGLE-style verification
+decode workload (4 request rows x 4 query tokens, 64 q / 8 kv heads, head dim
+128, one index head of dim 128, seq_lens uniform in [2048, 16384] over a
+1024-page pool, top-16 blocks, FP8-E4M3 K/V): msa_block_score ->
+msa_select_topk -> paged_sparse_decode_attention, all through the C ABI.
+
+Printed (rank 0, one JSON line): query rows per second (a query row is one
+non-padding query token with all its heads), the attention kernel's achieved
+HBM bandwidth against the measured peak, the end-to-end rate through the same
+calls with host buffers, and the CPU oracle's rate on a bounded sample.
+
+Timing: CUDA events on the launching stream around each step; between timed
+steps a 256 MiB buffer is rewritten to flush the 129 MB L2 (outside the
+events); W warm-up steps first.  Under torchrun each rank runs its own batch
+(different seed) with no data exchange: weak scaling, max time over ranks.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from sparse_paged_decode_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode query-rows/sec and achieved HBM GB/s vs ~8 TB/s (sparse paged decode)"
+UNIT = "query-rows/s"
+BS = 128
+FLUSH_BYTES = 256 << 20
+
+
+# -------------------------------------------------------------------- helpers
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    return 6800.0, "fallback 6.8 TB/s"
+
+
+def workload_desc(w):
+    return {
+        "workload": "cfg%s: %s" % (w.name[-1], W.CONFIG_NAMES.get(int(w.name[-1]), w.name)),
+        "requests": w.R, "query_rows": w.T, "valid_query_rows": w.n_valid_tokens,
+        "tokens_per_request": w.tokens_per_request, "request_lengths": w.request_lengths,
+        "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.D, "index_heads": w.Hi, "index_dim": w.Di,
+        "block_size": w.block_size, "page_table_blocks": w.NB, "pool_pages": w.P, "top_k": w.K,
+        "kv_dtype": "e4m3 (static scalar scales)", "q_dtype": str(w.q.dtype).replace("torch.", ""),
+        "index_dtype": str(w.q_idx.dtype).replace("torch.", "") if w.q_idx is not None else None,
+        "l2": "flushed between timed steps (256 MiB rewrite, outside the events)",
+    }
+
+
+def attention_bytes(w, topk_np):
+    """Algorithmic bytes of one attention launch: every selected (request, kv
+    head, block) page of K and V read once for its valid tokens (query rows of
+    one request share a page read), plus q, out, topk_idx and the page table."""
+    kv = 0
+    start = 0
+    for r, n in enumerate(w.tokens_per_request):
+        rows = range(start, start + n)
+        start += n
+        L = max((int(w.seq_lens[t]) for t in rows), default=0)
+        for h in range(w.Hkv):
+            blocks = set()
+            for t in rows:
+                if int(w.seq_lens[t]) <= 0:
+                    continue
+                lim = min(int(w.seq_lens[t]), w.NB * BS)
+                ids = range(w.NB) if topk_np is None else topk_np[min(h, topk_np.shape[0] - 1), t]
+                for b in ids:
+                    b = int(b)
+                    if 0 <= b < w.NB and b * BS < lim:
+                        blocks.add(b)
+            for b in blocks:
+                valid = min(BS, min(L, w.NB * BS) - b * BS)
+                kv += 2 * valid * w.D
+    q_bytes = w.q.numel() * w.q.element_size()
+    out_bytes = w.T * w.Hq * w.D * 2
+    tk_bytes = 0 if topk_np is None else w.T * w.K * 4
+    return kv + q_bytes + out_bytes + tk_bytes + w.block_table.numel() * 4 + 2 * w.T * 4
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while a region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------- the CPU baseline
+
+def oracle_rate(w, budget_s=12.0, max_rows=None):
+    """The oracle's three stages, row by row, on a bounded sample of the
+    workload's query rows; returns (rows/s, rows timed, seconds)."""
+    import oracle
+
+    o = oracle.default()
+    rows = [t for t in range(w.T) if int(w.seq_lens[t]) > 0]
+    done, t0 = 0, time.perf_counter()
+    for t in rows:
+        idx = torch.tensor([t])
+        s = o.block_score(w.q_idx[idx], w.k_idx_cache, w.block_table, w.req_idx[idx], w.seq_lens[idx],
+                          float(np.float32(w.idx_scale)))
+        tk = o.select_topk(s, w.K)
+        o.paged_attention(w.q[idx], w.k_cache, w.v_cache, w.block_table, w.req_idx[idx], w.seq_lens[idx], tk,
+                          float(np.float32(w.sm_scale)), float(np.float32(w.k_scale)), float(np.float32(w.v_scale)))
+        done += 1
+        if time.perf_counter() - t0 >= budget_s or (max_rows and done >= max_rows):
+            break
+    dt = time.perf_counter() - t0
+    return done / dt, done, dt
+
+
+# --------------------------------------------------------------------- arms
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    w = W.config(args.config, seed=1000 + args.config)
+    per_step_budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_rate(w, budget_s=per_step_budget / 4, max_rows=1)
+    rates, rows, secs = [], 0, 0.0
+    for _ in range(args.steps):
+        r, n, dt = oracle_rate(w, budget_s=per_step_budget)
+        rates.append(r)
+        rows += n
+        secs += dt
+    value = rows / secs
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_desc(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "%d query rows of the workload through the oracle's three stages "
+                                   "(single-threaded C, fp64), %.1f s per step" % (rows, per_step_budget)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def run_gpu(args, rank, world, local_rank):
+    import sparse_paged_decode_gb300 as spd
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = W.config(args.config, seed=1000 + args.config + 97 * rank)
+    g = w.to(dev)
+    T, NB, K = w.T, w.NB, max(w.K, 1)
+    scores = torch.empty((w.Hi, T, NB), device=dev)
+    topk = torch.empty((w.Hi, T, K), dtype=torch.int32, device=dev)
+    out = torch.empty((T, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(spd.decode_workspace_bytes(T, w.Hq, w.Hkv, w.D, NB), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    dense = w.dense
+
+    def step(gg, evs=None):
+        if not dense:
+            spd.msa_block_score(gg.q_idx, gg.k_idx_cache, gg.block_table, gg.seq_lens, gg.req_idx, BS, scores,
+                                gg.idx_scale)
+            spd.msa_select_topk(scores, topk)
+        if evs is not None:
+            evs[0].record(stream)
+        if dense:
+            spd.paged_decode_attention(gg.q, gg.k_cache, gg.v_cache, gg.block_table, gg.seq_lens, gg.req_idx, out,
+                                       gg.sm_scale, BS, gg.k_scale, gg.v_scale, ws)
+        else:
+            spd.paged_sparse_decode_attention(gg.q, gg.k_cache, gg.v_cache, gg.block_table, gg.seq_lens,
+                                              gg.req_idx, topk.expand(w.Hkv, -1, -1), out, gg.sm_scale, BS,
+                                              gg.k_scale, gg.v_scale, ws)
+        if evs is not None:
+            evs[1].record(stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step(g)
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.25)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    attn = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = spd.launch_count()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        step(g, attn[i])
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    launches = spd.launch_count() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    attn_ms = [a.elapsed_time(b) for a, b in attn]
+    total_ms = sum(step_ms)
+
+    # end to end through the same calls with host buffers: the step's inputs
+    # (queries, index queries, page table, seq_lens, req_idx) copied in from
+    # pinned memory, the attention output copied back; caches stay resident
+    host_in = {k: getattr(w, k).pin_memory() for k in ("q", "q_idx", "block_table", "seq_lens", "req_idx")
+               if getattr(w, k) is not None}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k, t in host_in.items():
+            getattr(g, k).copy_(t, non_blocking=True)
+        step(g)
+        host_out.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if i >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    clocks = sampler.stop() if sampler else None
+
+    # max over ranks
+    t_max = torch.tensor([total_ms, sum(e2e_ms)], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t_max, op=torch.distributed.ReduceOp.MAX)
+    total_ms, e2e_total = float(t_max[0]), float(t_max[1])
+    if rank != 0:
+        return None
+
+    rows = w.n_valid_tokens * world
+    value = rows * args.steps / (total_ms / 1e3)
+    e2e_value = rows * args.steps / (e2e_total / 1e3)
+    topk_np = None if dense else topk.cpu().numpy()
+    abytes = attention_bytes(w, topk_np)
+    attn_mean_s = statistics.mean(attn_ms) / 1e3
+    achieved = abytes / attn_mean_s / 1e9
+    peak, peak_src = measured_peaks()
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "attention_traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            tj = json.load(f)
+        if tj.get("config") == args.config and tj.get("kernel_stamp") == _kernel_stamp():
+            traffic = tj.get("traffic_bytes_per_launch")
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        rate, n, dt = oracle_rate(W.config(args.config, seed=1000 + args.config), budget_s=args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": "%d query rows of this workload through the oracle's three stages "
+                         "(single-threaded C, fp64), %.1f s" % (n, dt)}
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_desc(w),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "kernel": "paged attention launch",
+                     "algorithmic_bytes_per_launch": abytes,
+                     "mean_launch_us": attn_mean_s * 1e6, "peak_source": peak_src},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "attention_ms_median": statistics.median(attn_ms),
+        "step_ms_median": statistics.median(step_ms),
+    }
+
+
+def _kernel_stamp():
+    try:
+        from sparse_paged_decode_gb300 import build as b
+
+        return b._stamp()[:16]
+    except Exception:  # pragma: no cover
+        return None
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=2, choices=[2, 3, 5],
+                    help="workload (2 = EAGLE-style verification decode, the metric's workload)")
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        # the oracle arm runs on rank 0 only; other ranks exit without work
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group(backend="nccl")
+    res = run_gpu(args, rank, world, local_rank)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,218 @@
+/*
+ * spd.h -- C ABI of the sparse paged decode library (libspd.so, sm_103a).
+ *
+ * Three stages of the decode-time attention boundary of an LLM serving engine:
+ *   1. msa_block_score                block-max score sheet over a paged index cache
+ *   2. msa_select_topk                top-k block ids per query row
+ *   3. paged_sparse_decode_attention  paged GQA attention over the selected blocks
+ *      paged_decode_attention         the same over every block (dense decode)
+ *
+ * Contract shared by every entry point ("Kernel ABI" -- Core rules; "Slot
+ * contract" -- 1. The validator owns the boundary):
+ *   - The caller allocates every output (and the workspace) and owns all
+ *     memory; the library allocates nothing, keeps no pointer after a call
+ *     returns and never synchronises the host with the device.
+ *   - Each call writes every logical cell of every output, honouring the
+ *     output's shape, dtype and strides (outputs need not be contiguous), and
+ *     leaves every input unchanged.
+ *   - Work is enqueued on the supplied stream (NULL = the legacy default
+ *     stream) and completes asynchronously; inputs must stay valid until it
+ *     has run.  No device data is read on the host, so a call can be captured
+ *     in a CUDA graph and replayed with new input values at the same
+ *     addresses.
+ *   - Entry points return nothing.  A call that fails host-side validation
+ *     (bad dtype, rank, shape, stride, alignment, an output that overlaps an
+ *     input or itself, a workspace that is too small, a shape outside the
+ *     capability domain) launches nothing and records an error;
+ *     spd_last_error() reports the last call's status on the calling thread.
+ *     Device code never traps: metadata outside its range is excluded as
+ *     described for each call.
+ *
+ * Tensors are passed as spd_tensor descriptors of device memory.  Strides are
+ * in elements and may be any value for inputs (0 broadcasts); outputs need
+ * strictly positive strides that map distinct cells to distinct elements.
+ *
+ * Paged addressing (shared by all calls): the caches hold P pages of
+ * block_size = 128 token slots; logical token tau of request row r lives in
+ * slot block_size * block_table[r][tau / block_size] + tau % block_size.
+ * This page-granular table plays the part of the token-granular
+ * req_to_token + req_pool_indices pair of "Kernel ABI" -- attention.decode:
+ * query token t belongs to request row req_idx[t].  Tokens at or beyond
+ * seq_lens[t] are excluded; seq_lens[t] <= 0 or a req_idx outside [0, R)
+ * gives the token no keys; blocks whose page id lies outside [0, P) are
+ * excluded; seq_lens beyond NB * block_size are clipped to it.
+ */
+#ifndef SPD_H
+#define SPD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SPD_API __attribute__((visibility("default")))
+#else
+#define SPD_API
+#endif
+
+/* cudaStream_t without pulling in the CUDA headers */
+typedef struct CUstream_st *spd_stream_t;
+
+typedef enum {
+    SPD_F32 = 0,  /* IEEE binary32                         */
+    SPD_BF16 = 1, /* bfloat16                              */
+    SPD_F16 = 2,  /* IEEE binary16                         */
+    SPD_E4M3 = 3, /* OCP FP8 E4M3 ("e4m3fn"), max 448      */
+    SPD_I32 = 4   /* int32                                 */
+} spd_dtype;
+
+typedef struct {
+    void *data;        /* device address of element [0, ..., 0]        */
+    int32_t dtype;     /* spd_dtype                                   */
+    int32_t ndim;      /* number of dimensions used, 1..4             */
+    int64_t shape[4];  /* extents of dims 0..ndim-1                   */
+    int64_t stride[4]; /* element strides of dims 0..ndim-1           */
+} spd_tensor;
+
+typedef enum {
+    SPD_OK = 0,
+    SPD_ERR_INVALID_ARGUMENT = 1, /* malformed descriptor or inconsistent shapes     */
+    SPD_ERR_UNSUPPORTED = 2,      /* well formed but outside the capability domain   */
+    SPD_ERR_WORKSPACE = 3,        /* workspace missing, misaligned or too small      */
+    SPD_ERR_ALIASING = 4,         /* an output overlaps an input or itself           */
+    SPD_ERR_CUDA = 5              /* the CUDA runtime refused the launch             */
+} spd_status;
+
+/*
+ * Stage 1 -- block-max score sheet.
+ * "Kernel ABI" -- attention.msa_block_score (the decode score-sheet slot:
+ * "per-request block-max scores"; the validator-side top-k consumes it) and
+ * attention.msa_prefill_block_score (paged index cache "(slots, 1, D)";
+ * queries see keys up to their own position).
+ *
+ *   scores[h][t][b] = max over valid tokens tau of block b of
+ *                     (sum_d q_idx[t][h][d] * k_idx_cache[slot(tau)][0][d]) * idx_scale
+ *   and -inf where block b of token t holds no valid token (including every
+ *   b whose page id is outside the pool).
+ *
+ * q_idx        [T, Hi, Di]  f32 | bf16 | f16   query index heads
+ * k_idx_cache  [P*128, 1, Di] same dtype as q_idx; one index key head
+ * block_table  [R, NB] i32  page id of each logical block
+ * seq_lens     [T] i32      valid keys of each query token (prefill: position + 1)
+ * req_idx      [T] i32      block_table row of each query token
+ * block_size   must be 128
+ * scores       OUT [Hi, T, NB] f32
+ * idx_scale    finite and > 0 (so the max commutes with the scaling)
+ * Domain: Di in [1, 512], Hi >= 1, NB in [1, 1024].  Accumulation is fp32.
+ */
+SPD_API void msa_block_score(const spd_tensor *q_idx, const spd_tensor *k_idx_cache,
+                     const spd_tensor *block_table, const spd_tensor *seq_lens,
+                     const spd_tensor *req_idx, int32_t block_size,
+                     const spd_tensor *scores, float idx_scale, spd_stream_t stream);
+
+/*
+ * Stage 2 -- top-k block selection.
+ * "Kernel ABI" -- attention.decode ("topk_idx: (Hkv,B,K) block IDs"; -1
+ * entries select nothing) and attention.msa_prefill_block_score ("unused
+ * output cells must be -1"); "Slot contract" -- 2. (selection graded by set
+ * overlap).
+ *
+ * For each row (h, t): the K largest candidate cells of scores[h][t][:], in
+ * descending score order with ties broken toward the lower block id; a
+ * candidate is a cell that is neither NaN nor -inf; rows with fewer than K
+ * candidates are padded with -1.  Comparisons are exact on the fp32 values.
+ *
+ * scores    [Hi, T, NB] f32
+ * topk_idx  OUT [Hi, T, K] i32 (K >= 1 taken from its shape; K may exceed NB)
+ * Domain: NB in [1, 1024].
+ */
+SPD_API void msa_select_topk(const spd_tensor *scores, const spd_tensor *topk_idx, spd_stream_t stream);
+
+/*
+ * Stage 3 -- paged sparse GQA decode attention.
+ * "Kernel ABI" -- attention.decode: each query row attends exactly the
+ * supplied non-negative block ids; -1 entries and tokens at or beyond
+ * seq_lens are excluded.  "Kernel ABI" -- attention.sdpa: Hq divisible by
+ * Hkv; q head g reads kv head g / (Hq / Hkv).  "MiniMax-M3 decode through the
+ * ATOM kernel library" -- static scalar K/V scales on FP8 caches.
+ *
+ *   z_tau = sm_scale * k_scale * (q[t][g] . k_cache[slot(tau)][h])
+ *   out[t][g] = sum_tau softmax(z)_tau * v_scale * v_cache[slot(tau)][h]
+ * over the union of the valid tokens of the blocks listed in
+ * topk_idx[h][t][:].  A selection is a set: repeated ids count once; ids
+ * that are negative or >= NB select nothing.  A query row with no valid key
+ * writes zeros.  Logits, softmax and accumulation are fp32; the output is
+ * rounded to bf16 (nearest even).
+ *
+ * q          [T, Hq, D] f32 | bf16 | f16
+ * k_cache    [P*128, Hkv, D] e4m3 } innermost stride 1
+ * v_cache    [P*128, Hkv, D] e4m3 } same shape as k_cache
+ * block_table [R, NB] i32, seq_lens [T] i32, req_idx [T] i32 (see above)
+ * topk_idx   [Hkv, T, K] i32; a stride of 0 on dim 0 shares one selection
+ *            across kv heads (the usual case: one index head)
+ * out        OUT [T, Hq, D] bf16
+ * sm_scale, k_scale, v_scale  finite fp32 scalars
+ * block_size must be 128
+ * workspace  device scratch of at least spd_decode_workspace_bytes(...)
+ *            bytes, 256-byte aligned; contents need no initialisation and
+ *            are overwritten; it must not be shared by calls that may run
+ *            concurrently
+ * Domain: D in [1, 256], Hq / Hkv <= 16, NB in [1, 1024], K >= 1.
+ * Query rows of one request that sit next to each other (the draft tokens
+ * of a verification row) share each K/V page read.
+ */
+SPD_API void paged_sparse_decode_attention(const spd_tensor *q, const spd_tensor *k_cache,
+                                   const spd_tensor *v_cache, const spd_tensor *block_table,
+                                   const spd_tensor *seq_lens, const spd_tensor *req_idx,
+                                   const spd_tensor *topk_idx, const spd_tensor *out,
+                                   float sm_scale, int32_t block_size, float k_scale,
+                                   float v_scale, void *workspace, size_t workspace_bytes,
+                                   spd_stream_t stream);
+
+/*
+ * Dense paged decode attention: paged_sparse_decode_attention with every
+ * block selected (the degenerate case of "Kernel ABI" -- attention.decode
+ * whose selection lists all blocks below ceil(seq_len / 128)).  Same
+ * arguments without topk_idx.
+ */
+SPD_API void paged_decode_attention(const spd_tensor *q, const spd_tensor *k_cache,
+                            const spd_tensor *v_cache, const spd_tensor *block_table,
+                            const spd_tensor *seq_lens, const spd_tensor *req_idx,
+                            const spd_tensor *out, float sm_scale, int32_t block_size,
+                            float k_scale, float v_scale, void *workspace,
+                            size_t workspace_bytes, spd_stream_t stream);
+
+/*
+ * Workspace bytes the two attention calls need for T query rows, Hq q heads,
+ * Hkv kv heads, head dim D and a page table of NB blocks.  Depends on these
+ * capacities only (never on seq_lens or topk_idx), so one allocation serves
+ * every replay of a captured graph.  Returns 0 for shapes outside the domain.
+ */
+SPD_API size_t spd_decode_workspace_bytes(int64_t T, int64_t Hq, int64_t Hkv, int64_t D, int64_t NB,
+                                  int32_t block_size);
+
+/*
+ * Status of the last call made on this thread: SPD_OK or an spd_status code.
+ * When msg is not NULL, up to cap-1 bytes of a NUL-terminated description
+ * are copied into it.
+ */
+SPD_API int spd_last_error(char *msg, size_t cap);
+
+/*
+ * Diagnostics: number of CUDA kernels this library has enqueued in this
+ * process so far (all threads, all streams).  Benchmarks difference it
+ * around a timed region to count their launches.
+ */
+SPD_API uint64_t spd_launch_count(void);
+
+/* Library version string, e.g. "spd 0.1 sm_103a". */
+SPD_API const char *spd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPD_H */

@@ -21,6 +21,7 @@ __all__ = [
     "paged_sparse_decode_attention",
     "paged_decode_attention",
     "decode_workspace_bytes",
+    "launch_count",
     "library_path",
 ]
 

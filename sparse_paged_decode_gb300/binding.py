@@ -1,0 +1,185 @@
+"""Thin ctypes binding of libspd.so: torch tensors in, C ABI call, error check.
+
+Argument marshalling only -- every step of every call runs in the CUDA
+library.  Importing this module loads ``libspd.so`` (built in-tree by
+``sparse_paged_decode_gb300.build``) and raises if it is missing: there is no
+CPU or PyTorch fallback.  Each function enqueues on the current torch CUDA
+stream unless a stream is given, returns None, and raises ``SpdError`` when
+the library rejects the call (see ``include/spd.h``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from .build import LIB_PATH
+
+__all__ = [
+    "SpdError",
+    "msa_block_score",
+    "msa_select_topk",
+    "paged_sparse_decode_attention",
+    "paged_decode_attention",
+    "decode_workspace_bytes",
+    "launch_count",
+    "library_path",
+    "lib",
+]
+
+SPD_F32, SPD_BF16, SPD_F16, SPD_E4M3, SPD_I32 = 0, 1, 2, 3, 4
+_DTYPES = {
+    torch.float32: SPD_F32,
+    torch.bfloat16: SPD_BF16,
+    torch.float16: SPD_F16,
+    torch.float8_e4m3fn: SPD_E4M3,
+    torch.int32: SPD_I32,
+}
+
+
+class SpdError(RuntimeError):
+    """A call rejected by libspd (validation failure or launch error)."""
+
+    def __init__(self, code: int, msg: str):
+        super().__init__("spd error %d: %s" % (code, msg))
+        self.code = code
+
+
+class SpdTensor(ctypes.Structure):
+    _fields_ = [
+        ("data", ctypes.c_void_p),
+        ("dtype", ctypes.c_int32),
+        ("ndim", ctypes.c_int32),
+        ("shape", ctypes.c_int64 * 4),
+        ("stride", ctypes.c_int64 * 4),
+    ]
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            "libspd.so is not built (%s); run `python -m sparse_paged_decode_gb300.build` "
+            "or __graft_entry__.build() -- there is no fallback implementation" % LIB_PATH)
+    L = ctypes.CDLL(LIB_PATH)
+    P = ctypes.POINTER(SpdTensor)
+    vp, f32, i32, sz = ctypes.c_void_p, ctypes.c_float, ctypes.c_int32, ctypes.c_size_t
+    L.msa_block_score.argtypes = [P, P, P, P, P, i32, P, f32, vp]
+    L.msa_block_score.restype = None
+    L.msa_select_topk.argtypes = [P, P, vp]
+    L.msa_select_topk.restype = None
+    L.paged_sparse_decode_attention.argtypes = [P, P, P, P, P, P, P, P, f32, i32, f32, f32, vp, sz, vp]
+    L.paged_sparse_decode_attention.restype = None
+    L.paged_decode_attention.argtypes = [P, P, P, P, P, P, P, f32, i32, f32, f32, vp, sz, vp]
+    L.paged_decode_attention.restype = None
+    L.spd_decode_workspace_bytes.argtypes = [ctypes.c_int64] * 5 + [i32]
+    L.spd_decode_workspace_bytes.restype = sz
+    L.spd_last_error.argtypes = [ctypes.c_char_p, sz]
+    L.spd_last_error.restype = ctypes.c_int
+    L.spd_launch_count.argtypes = []
+    L.spd_launch_count.restype = ctypes.c_uint64
+    L.spd_version.argtypes = []
+    L.spd_version.restype = ctypes.c_char_p
+    return L
+
+
+lib = _load()
+
+
+def _desc(t: Optional[torch.Tensor], name: str):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype not in _DTYPES:
+        raise TypeError("%s: dtype %s is not supported by libspd" % (name, t.dtype))
+    if t.numel() > 0 and not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dim() > 4:
+        raise ValueError("%s has more than 4 dims" % name)
+    d = SpdTensor()
+    d.data = t.data_ptr() if t.numel() > 0 else None
+    d.dtype = _DTYPES[t.dtype]
+    d.ndim = t.dim()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return ctypes.byref(d)
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check():
+    buf = ctypes.create_string_buffer(512)
+    code = lib.spd_last_error(buf, 512)
+    if code != 0:
+        raise SpdError(code, buf.value.decode(errors="replace"))
+
+
+def msa_block_score(q_idx, k_idx_cache, block_table, seq_lens, req_idx, block_size, scores,
+                    idx_scale, stream=None) -> None:
+    """Stage 1: fill ``scores`` [Hi, T, NB] with block-max index scores."""
+    lib.msa_block_score(_desc(q_idx, "q_idx"), _desc(k_idx_cache, "k_idx_cache"),
+                        _desc(block_table, "block_table"), _desc(seq_lens, "seq_lens"),
+                        _desc(req_idx, "req_idx"), int(block_size), _desc(scores, "scores"),
+                        float(idx_scale), _stream(stream))
+    _check()
+
+
+def msa_select_topk(scores, topk_idx, stream=None) -> None:
+    """Stage 2: fill ``topk_idx`` [Hi, T, K] with the top-K block ids per row."""
+    lib.msa_select_topk(_desc(scores, "scores"), _desc(topk_idx, "topk_idx"), _stream(stream))
+    _check()
+
+
+def paged_sparse_decode_attention(q, k_cache, v_cache, block_table, seq_lens, req_idx, topk_idx, out,
+                                  sm_scale, block_size, k_scale, v_scale, workspace, stream=None) -> None:
+    """Stage 3: fill ``out`` [T, Hq, D] (bf16) with attention over the selected blocks.
+
+    ``workspace`` is a CUDA uint8 tensor of at least ``decode_workspace_bytes`` bytes."""
+    ws_ptr, ws_bytes = _workspace(workspace)
+    lib.paged_sparse_decode_attention(
+        _desc(q, "q"), _desc(k_cache, "k_cache"), _desc(v_cache, "v_cache"), _desc(block_table, "block_table"),
+        _desc(seq_lens, "seq_lens"), _desc(req_idx, "req_idx"), _desc(topk_idx, "topk_idx"), _desc(out, "out"),
+        float(sm_scale), int(block_size), float(k_scale), float(v_scale), ws_ptr, ws_bytes, _stream(stream))
+    _check()
+
+
+def paged_decode_attention(q, k_cache, v_cache, block_table, seq_lens, req_idx, out, sm_scale, block_size,
+                           k_scale, v_scale, workspace, stream=None) -> None:
+    """Dense paged decode: attention over every block of each row."""
+    ws_ptr, ws_bytes = _workspace(workspace)
+    lib.paged_decode_attention(
+        _desc(q, "q"), _desc(k_cache, "k_cache"), _desc(v_cache, "v_cache"), _desc(block_table, "block_table"),
+        _desc(seq_lens, "seq_lens"), _desc(req_idx, "req_idx"), _desc(out, "out"), float(sm_scale),
+        int(block_size), float(k_scale), float(v_scale), ws_ptr, ws_bytes, _stream(stream))
+    _check()
+
+
+def _workspace(ws):
+    if ws is None:
+        return None, 0
+    if not isinstance(ws, torch.Tensor) or not ws.is_cuda:
+        raise TypeError("workspace must be a CUDA tensor")
+    return ws.data_ptr(), ws.numel() * ws.element_size()
+
+
+def launch_count() -> int:
+    """Kernels enqueued by libspd in this process so far."""
+    return int(lib.spd_launch_count())
+
+
+def decode_workspace_bytes(T: int, Hq: int, Hkv: int, D: int, NB: int, block_size: int = 128) -> int:
+    """Workspace bytes the attention calls need for these capacities."""
+    return int(lib.spd_decode_workspace_bytes(T, Hq, Hkv, D, NB, block_size))

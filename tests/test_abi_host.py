@@ -1,0 +1,180 @@
+"""The C ABI library on the host (no GPU needed).
+
+* libspd.so loads and exports every function that include/spd.h declares;
+* host-side validation rejects malformed calls before any launch, with the
+  error code the header documents.  Descriptors here carry fake device
+  addresses: validation never dereferences them, and a call that passes
+  validation is only enqueued, so without a GPU it reports SPD_ERR_CUDA.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spd.h")
+
+SPD_OK, SPD_ERR_INVALID_ARGUMENT, SPD_ERR_UNSUPPORTED, SPD_ERR_WORKSPACE, SPD_ERR_ALIASING, SPD_ERR_CUDA = range(6)
+F32, BF16, F16, E4M3, I32 = range(5)
+ES = {F32: 4, BF16: 2, F16: 2, E4M3: 1, I32: 4}
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"^SPD_API\s+[\w\s\*]*?\b(\w+)\s*\(", text, re.M)
+
+
+@pytest.fixture(scope="module")
+def spd():
+    from sparse_paged_decode_gb300 import binding
+
+    return binding
+
+
+def test_exports_every_declared_symbol(spd):
+    names = declared_functions()
+    assert set(names) >= {"msa_block_score", "msa_select_topk", "paged_sparse_decode_attention",
+                          "paged_decode_attention", "spd_decode_workspace_bytes", "spd_last_error",
+                          "spd_version"}
+    for n in names:
+        assert hasattr(spd.lib, n), n
+    assert spd.lib.spd_version().startswith(b"spd ")
+
+
+class Fake:
+    """Descriptor with a fake, aligned device address and contiguous strides."""
+
+    next_addr = 1 << 40
+
+    def __init__(self, shape, dtype, strides=None, addr=None):
+        from sparse_paged_decode_gb300.binding import SpdTensor
+
+        self.d = SpdTensor()
+        n = 1
+        for s in shape:
+            n *= s
+        if addr is None:
+            addr = Fake.next_addr
+            Fake.next_addr += ((n * ES[dtype] + 4095) // 4096 + 1) * 4096
+        self.d.data = addr
+        self.d.dtype = dtype
+        self.d.ndim = len(shape)
+        if strides is None:
+            strides, acc = [], 1
+            for s in reversed(shape):
+                strides.insert(0, acc)
+                acc *= s
+        for i, (s, st) in enumerate(zip(shape, strides)):
+            self.d.shape[i] = s
+            self.d.stride[i] = st
+
+    def ref(self):
+        return ctypes.byref(self.d)
+
+
+def status(spd):
+    buf = ctypes.create_string_buffer(512)
+    return spd.lib.spd_last_error(buf, 512), buf.value.decode()
+
+
+def attn_call(spd, T=4, Hq=8, Hkv=2, D=64, NB=4, P=8, K=2, q_dtype=BF16, out=None, ws_bytes=None,
+              block_size=128, tk=True, k_strides=None, sm_scale=0.125):
+    q = Fake((T, Hq, D), q_dtype)
+    k = Fake((P * 128, Hkv, D), E4M3, strides=k_strides)
+    v = Fake((P * 128, Hkv, D), E4M3)
+    bt = Fake((2, NB), I32)
+    sl = Fake((T,), I32)
+    ri = Fake((T,), I32)
+    topk = Fake((Hkv, T, K), I32, strides=(0, K, 1)) if tk else None
+    o = out or Fake((T, Hq, D), BF16)
+    need = spd.lib.spd_decode_workspace_bytes(T, Hq, Hkv, D, NB, 128)
+    ws = Fake((need + 256,), E4M3)
+    nb = need if ws_bytes is None else ws_bytes
+    if tk:
+        spd.lib.paged_sparse_decode_attention(q.ref(), k.ref(), v.ref(), bt.ref(), sl.ref(), ri.ref(), topk.ref(),
+                                              o.ref(), sm_scale, block_size, 1.0, 1.0, ws.d.data, nb, None)
+    else:
+        spd.lib.paged_decode_attention(q.ref(), k.ref(), v.ref(), bt.ref(), sl.ref(), ri.ref(), o.ref(),
+                                       sm_scale, block_size, 1.0, 1.0, ws.d.data, nb, None)
+    return status(spd)
+
+
+def test_valid_attention_call_reaches_launch(spd):
+    for tk in (True, False):
+        code, msg = attn_call(spd, tk=tk)
+        # validation passed; the launch itself needs a GPU
+        assert code in (SPD_OK, SPD_ERR_CUDA), msg
+
+
+def test_attention_rejections(spd):
+    assert attn_call(spd, block_size=64)[0] == SPD_ERR_UNSUPPORTED
+    assert attn_call(spd, Hq=6, Hkv=4)[0] == SPD_ERR_UNSUPPORTED  # not divisible
+    assert attn_call(spd, Hq=64, Hkv=2)[0] == SPD_ERR_UNSUPPORTED  # group of 32
+    assert attn_call(spd, D=512)[0] == SPD_ERR_UNSUPPORTED
+    assert attn_call(spd, q_dtype=I32)[0] == SPD_ERR_UNSUPPORTED
+    assert attn_call(spd, ws_bytes=16)[0] == SPD_ERR_WORKSPACE
+    assert attn_call(spd, k_strides=(2 * 64 * 2, 64 * 2, 2))[0] == SPD_ERR_UNSUPPORTED  # D not contiguous
+    assert attn_call(spd, sm_scale=float("nan"))[0] == SPD_ERR_INVALID_ARGUMENT
+    # an output whose strides make two cells share one element
+    assert attn_call(spd, out=Fake((4, 8, 64), BF16, strides=(64, 8, 1)))[0] == SPD_ERR_ALIASING
+    # wrong output shape
+    assert attn_call(spd, out=Fake((4, 8, 32), BF16))[0] == SPD_ERR_INVALID_ARGUMENT
+
+
+def test_output_overlapping_input_rejected(spd):
+    q = Fake((2, 1, 32), BF16)
+    k = Fake((128, 1, 32), BF16)
+    bt = Fake((1, 1), I32)
+    sl = Fake((2,), I32)
+    ri = Fake((2,), I32)
+    out = Fake((1, 2, 1), F32, addr=k.d.data + 64)  # lands inside the index cache
+    spd.lib.msa_block_score(q.ref(), k.ref(), bt.ref(), sl.ref(), ri.ref(), 128, out.ref(), 0.5, None)
+    assert status(spd)[0] == SPD_ERR_ALIASING
+
+
+def test_score_and_select_rejections(spd):
+    q = Fake((3, 1, 32), BF16)
+    k = Fake((256, 1, 32), BF16)
+    bt = Fake((2, 2), I32)
+    sl = Fake((3,), I32)
+    ri = Fake((3,), I32)
+    out = Fake((1, 3, 2), F32)
+
+    def score(qq=q, kk=k, o=out, scale=0.5, bs=128, sll=sl):
+        spd.lib.msa_block_score(qq.ref(), kk.ref(), bt.ref(), sll.ref(), ri.ref(), bs, o.ref(), scale, None)
+        return status(spd)[0]
+
+    assert score() in (SPD_OK, SPD_ERR_CUDA)
+    assert score(scale=-1.0) == SPD_ERR_UNSUPPORTED
+    assert score(scale=0.0) == SPD_ERR_UNSUPPORTED
+    assert score(bs=256) == SPD_ERR_UNSUPPORTED
+    assert score(kk=Fake((256, 2, 32), BF16)) == SPD_ERR_UNSUPPORTED  # two index key heads
+    assert score(kk=Fake((256, 1, 32), F32)) == SPD_ERR_UNSUPPORTED  # dtype mismatch
+    assert score(o=Fake((1, 3, 3), F32)) == SPD_ERR_INVALID_ARGUMENT
+    assert score(sll=Fake((2,), I32)) == SPD_ERR_INVALID_ARGUMENT
+    # select
+    s = Fake((1, 3, 2), F32)
+    tk = Fake((1, 3, 5), I32)
+    spd.lib.msa_select_topk(s.ref(), tk.ref(), None)
+    assert status(spd)[0] in (SPD_OK, SPD_ERR_CUDA)
+    spd.lib.msa_select_topk(s.ref(), Fake((1, 3, 0), I32).ref(), None)
+    assert status(spd)[0] == SPD_ERR_INVALID_ARGUMENT
+    spd.lib.msa_select_topk(Fake((1, 3, 2000), F32).ref(), tk.ref(), None)
+    assert status(spd)[0] == SPD_ERR_UNSUPPORTED
+
+
+def test_null_descriptor_and_empty_batch(spd):
+    spd.lib.msa_select_topk(None, None, None)
+    assert status(spd)[0] == SPD_ERR_INVALID_ARGUMENT
+    # T = 0: nothing to write, nothing launched, success
+    code, msg = attn_call(spd, T=0)
+    assert code == SPD_OK, msg
+
+
+def test_workspace_size_depends_on_capacities_only(spd):
+    f = spd.lib.spd_decode_workspace_bytes
+    a = f(16, 64, 8, 128, 128, 128)
+    assert a > 0 and a % 256 == 0
+    assert f(32, 64, 8, 128, 128, 128) >= a
+    assert f(16, 64, 8, 128, 128, 64) == 0

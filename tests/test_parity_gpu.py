@@ -1,0 +1,332 @@
+"""GPU parity: each stage through the C ABI against the CPU oracle.
+
+Every call gets NaN / sentinel-poisoned outputs and its inputs are hashed
+before and after ("Kernel ABI" -- Why the ABI is shaped this way: poisoning
+and input-mutation checks).  Small cases compare every output cell; the
+full-size configurations compare every cell of the score sheet and top-k
+where the oracle runs in seconds, and sampled query rows of attention (each
+row of the output depends only on its own query row, so the oracle runs on
+those rows alone).  Attention is checked with the oracle's top-k fed to both
+sides, and end to end from the GPU's own selection.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import check_attention, check_scores, check_topk, digest, nan_like
+from sparse_paged_decode_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+BS = 128
+DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
+
+
+@pytest.fixture(scope="module")
+def spd():
+    import sparse_paged_decode_gb300 as m
+
+    return m
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.default()
+
+
+# ------------------------------------------------------------------ runners
+
+def gpu_scores(spd, g, Hi=None):
+    T, NB = g.seq_lens.shape[0], g.block_table.shape[1]
+    Hi = g.q_idx.shape[1] if Hi is None else Hi
+    out = nan_like((Hi, T, NB), torch.float32, DEV)
+    before = digest(g.q_idx, g.k_idx_cache, g.block_table, g.seq_lens, g.req_idx)
+    spd.msa_block_score(g.q_idx, g.k_idx_cache, g.block_table, g.seq_lens, g.req_idx, BS, out, g.idx_scale)
+    torch.cuda.synchronize()
+    assert digest(g.q_idx, g.k_idx_cache, g.block_table, g.seq_lens, g.req_idx) == before, "inputs mutated"
+    return out
+
+
+def gpu_topk(spd, scores, K):
+    out = nan_like((scores.shape[0], scores.shape[1], K), torch.int32, DEV)
+    before = digest(scores)
+    spd.msa_select_topk(scores, out)
+    torch.cuda.synchronize()
+    assert digest(scores) == before, "scores mutated"
+    return out
+
+
+def gpu_attention(spd, g, topk):
+    T = g.q.shape[0]
+    out = nan_like((T, g.Hq, g.D), torch.bfloat16, DEV)
+    ws = torch.empty(spd.decode_workspace_bytes(T, g.Hq, g.Hkv, g.D, g.NB), dtype=torch.uint8, device=DEV)
+    ins = (g.q, g.k_cache, g.v_cache, g.block_table, g.seq_lens, g.req_idx, topk)
+    before = digest(*ins)
+    if topk is None:
+        spd.paged_decode_attention(g.q, g.k_cache, g.v_cache, g.block_table, g.seq_lens, g.req_idx, out,
+                                   g.sm_scale, BS, g.k_scale, g.v_scale, ws)
+    else:
+        spd.paged_sparse_decode_attention(g.q, g.k_cache, g.v_cache, g.block_table, g.seq_lens, g.req_idx,
+                                          topk, out, g.sm_scale, BS, g.k_scale, g.v_scale, ws)
+    torch.cuda.synchronize()
+    assert digest(*ins) == before, "inputs mutated"
+    return out
+
+
+def f32(x):
+    return float(np.float32(x))
+
+
+def oracle_rows(orc, w, rows, topk_np):
+    """Oracle attention for the query rows ``rows`` only."""
+    idx = torch.tensor(rows, dtype=torch.int64)
+    tk = None if topk_np is None else np.ascontiguousarray(topk_np[:, rows, :])
+    return orc.paged_attention(w.q[idx], w.k_cache, w.v_cache, w.block_table, w.req_idx[idx],
+                               w.seq_lens[idx], tk, f32(w.sm_scale), f32(w.k_scale), f32(w.v_scale))
+
+
+def full_check(spd, orc, w, attn_rows=None, score_rows=None, per_head_topk=False):
+    """Score + select + sparse attention + dense attention against the oracle."""
+    g = w.to(DEV)
+    res = {}
+    full_s = None
+    if w.q_idx is not None:
+        s = gpu_scores(spd, g)
+        rows = list(range(w.T)) if score_rows is None else score_rows
+        ridx = torch.tensor(rows, dtype=torch.int64)
+        ref_s = orc.block_score(w.q_idx[ridx], w.k_idx_cache, w.block_table, w.req_idx[ridx], w.seq_lens[ridx],
+                                f32(w.idx_scale))
+        if score_rows is None:
+            full_s = ref_s
+        res["score_err"] = check_scores(s.cpu().numpy()[:, rows], ref_s)
+        tk = gpu_topk(spd, s, w.K)
+        res["overlap"] = check_topk(tk.cpu().numpy()[:, rows], ref_s, w.K)
+    if w.q is None:
+        return res
+    rows = list(range(w.T)) if attn_rows is None else attn_rows
+    pad = [i for i, t in enumerate(rows) if int(w.seq_lens[t]) <= 0]
+    if w.K > 0 and w.q_idx is not None:
+        # oracle selection for every token, fed to both sides
+        if full_s is None:
+            full_s = orc.block_score(w.q_idx, w.k_idx_cache, w.block_table, w.req_idx, w.seq_lens,
+                                     f32(w.idx_scale))
+        ref_tk = orc.select_topk(full_s, w.K)  # [1, T, K]
+        if per_head_topk:
+            ref_tk = np.concatenate([np.roll(ref_tk, h, axis=2) for h in range(w.Hkv)], axis=0)
+            tk_dev = torch.from_numpy(ref_tk).to(DEV)
+        else:
+            tk_dev = torch.from_numpy(ref_tk).to(DEV).expand(w.Hkv, -1, -1)
+        out = gpu_attention(spd, g, tk_dev)
+        ref = oracle_rows(orc, w, rows, ref_tk)
+        res["sparse"] = check_attention(out.float().cpu().numpy()[rows], ref, "sparse attention", pad)
+        # end to end: the GPU's own selection feeds the GPU attention
+        out_e2e = gpu_attention(spd, g, tk.expand(w.Hkv, -1, -1))
+        ref_e2e = oracle_rows(orc, w, rows, tk.cpu().numpy())
+        res["e2e"] = check_attention(out_e2e.float().cpu().numpy()[rows], ref_e2e, "end-to-end attention", pad)
+    out_d = gpu_attention(spd, g, None)
+    ref_d = oracle_rows(orc, w, rows, None)
+    res["dense"] = check_attention(out_d.float().cpu().numpy()[rows], ref_d, "dense attention", pad)
+    return res
+
+
+# --------------------------------------------------------------- small cases
+
+SMALL = {
+    "g8_d128_bf16_mixed": dict(lengths=[1500, 700, 129, 2048, 1], tokens_per_request=[4, 4, 1, 16, 1], Hq=64, Hkv=8,
+                               D=128, Di=128, NB=16, P=96, K=5),
+    "g4_d64_f32": dict(lengths=[300, 512, 77], tokens_per_request=[1, 2, 3], Hq=8, Hkv=2, D=64, Di=32, NB=4, P=16,
+                       K=2, dtype=torch.float32),
+    "g16_d128_f16": dict(lengths=[1000, 257], tokens_per_request=[3, 8], Hq=32, Hkv=2, D=128, Di=64, NB=8, P=24,
+                         K=3, dtype=torch.float16),
+    "g1_d96_mha": dict(lengths=[640, 90], tokens_per_request=[2, 1], Hq=4, Hkv=4, D=96, Di=16, NB=6, P=12, K=4),
+    "padded_t3": dict(lengths=[1200, 3000, 400], tokens_per_request=[8, 16, 4], Hq=64, Hkv=8, D=128, Di=128, NB=32,
+                      P=64, K=8, q_dist="student_t3", padded_tail=[3, 16, 0]),
+    "k_above_nb": dict(lengths=[200, 384], tokens_per_request=[1, 4], Hq=16, Hkv=2, D=128, Di=128, NB=3, P=8, K=7),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_cases(spd, orc, name):
+    w = W.make_decode(name, seed=zlib.crc32(name.encode()) % 1000, **SMALL[name])
+    full_check(spd, orc, w)
+
+
+def test_cfg1_tiny(spd, orc):
+    full_check(spd, orc, W.config(1))
+
+
+def test_per_head_selection_and_bad_metadata(spd, orc):
+    w = W.make_decode("meta", lengths=[900, 300, 1700], tokens_per_request=[2, 3, 4], Hq=32, Hkv=4, D=128,
+                      Di=128, NB=16, P=48, K=6, seed=77)
+    # pages outside the pool, a request row outside the table, negative and
+    # over-long seq_lens: excluded, never trapped
+    w.block_table[0, 2] = -1
+    w.block_table[1, 0] = w.P + 5
+    w.req_idx[4] = 9
+    w.seq_lens[5] = -3
+    w.seq_lens[0] = w.NB * BS + 50
+    full_check(spd, orc, w, per_head_topk=True)
+
+
+def test_duplicate_and_out_of_range_ids(spd, orc):
+    w = W.make_decode("dup", lengths=[1000, 600], tokens_per_request=[2, 1], Hq=16, Hkv=2, D=128, Di=128, NB=8,
+                      P=20, K=4, seed=5)
+    tk = np.array([[[3, 3, -1, 0, 99, -7, 5, 3], [1, 2, 2, 2, -1, -1, 7, 0], [4, -1, 4, 0, 1, 1, 1, 1]]],
+                  dtype=np.int32)
+    g = w.to(DEV)
+    out = gpu_attention(spd, g, torch.from_numpy(tk).to(DEV).expand(w.Hkv, -1, -1))
+    ref = orc.paged_attention(w.q, w.k_cache, w.v_cache, w.block_table, w.req_idx, w.seq_lens, tk,
+                              f32(w.sm_scale), f32(w.k_scale), f32(w.v_scale))
+    check_attention(out.float().cpu().numpy(), ref)
+
+
+def test_nan_poison_pages_never_leak(spd, orc):
+    w = W.make_decode("nanpoison", lengths=[700, 333], tokens_per_request=[4, 2], Hq=16, Hkv=2, D=128, Di=128,
+                      NB=8, P=20, K=3, seed=6)
+    owned = set()
+    for r, L in enumerate(w.request_lengths):
+        for tau in range(L):
+            owned.add(int(w.block_table[r, tau // BS]) * BS + tau % BS)
+    mask = torch.ones(w.P * BS, dtype=torch.bool)
+    mask[torch.tensor(sorted(owned))] = False
+    for c in (w.k_cache, w.v_cache):
+        c.view(torch.uint8)[mask] = 0x7F  # NaN codes everywhere no valid token lives
+    kmask = mask.clone()
+    w.k_idx_cache[kmask] = float("nan")
+    res = full_check(spd, orc, w)
+    assert res["dense"][1] >= 0.9999
+
+
+def test_strided_inputs_and_outputs(spd, orc):
+    w = W.make_decode("strided", lengths=[800, 250], tokens_per_request=[3, 2], Hq=16, Hkv=2, D=128, Di=64, NB=8,
+                      P=20, K=3, seed=9)
+    g = w.to(DEV)
+    # q stored head-major and viewed token-major; index queries with a gap
+    q_hm = g.q.transpose(0, 1).contiguous().transpose(0, 1)
+    qi_big = torch.zeros((w.T, 1, w.Di * 2), dtype=g.q_idx.dtype, device=DEV)
+    qi_big[:, :, ::2] = g.q_idx
+    qi = qi_big[:, :, ::2]
+    # outputs are views inside larger poisoned buffers
+    s_big = torch.full((1, w.T, w.NB + 3), 123.0, device=DEV)
+    s_view = s_big[:, :, 1:1 + w.NB]
+    spd.msa_block_score(qi, g.k_idx_cache, g.block_table, g.seq_lens, g.req_idx, BS, s_view, g.idx_scale)
+    tk_big = torch.full((1, w.T, 2 * w.K), 4242, dtype=torch.int32, device=DEV)
+    tk_view = tk_big[:, :, ::2]
+    spd.msa_select_topk(s_view, tk_view)
+    o_big = torch.full((w.T, w.Hq, w.D + 8), 7.0, dtype=torch.bfloat16, device=DEV)
+    o_view = o_big[:, :, 4:4 + w.D]
+    ws = torch.empty(spd.decode_workspace_bytes(w.T, w.Hq, w.Hkv, w.D, w.NB), dtype=torch.uint8, device=DEV)
+    spd.paged_sparse_decode_attention(q_hm, g.k_cache, g.v_cache, g.block_table, g.seq_lens, g.req_idx,
+                                      tk_view.expand(w.Hkv, -1, -1), o_view, g.sm_scale, BS, g.k_scale,
+                                      g.v_scale, ws)
+    torch.cuda.synchronize()
+    ref_s = orc.block_score(w.q_idx, w.k_idx_cache, w.block_table, w.req_idx, w.seq_lens, f32(w.idx_scale))
+    check_scores(s_view.cpu().numpy(), ref_s)
+    assert torch.all(s_big[:, :, 0] == 123.0) and torch.all(s_big[:, :, -2:] == 123.0)
+    check_topk(tk_view.cpu().numpy(), ref_s, w.K)
+    assert torch.all(tk_big[:, :, 1::2] == 4242)
+    ref = orc.paged_attention(w.q, w.k_cache, w.v_cache, w.block_table, w.req_idx, w.seq_lens,
+                              tk_view.cpu().numpy(), f32(w.sm_scale), f32(w.k_scale), f32(w.v_scale))
+    check_attention(o_view.float().cpu().numpy(), ref)
+    assert torch.all(o_big[:, :, :4] == 7.0) and torch.all(o_big[:, :, -4:] == 7.0)
+
+
+def test_graph_capture_and_replay_with_new_inputs(spd, orc):
+    """"Slot contract" -- CUDA graph contract: capture, mutate every dynamic
+    input in place, replay, re-verify."""
+    w = W.make_decode("graph", lengths=[1500, 900], tokens_per_request=[4, 2], Hq=16, Hkv=2, D=128, Di=128,
+                      NB=16, P=40, K=4, seed=13)
+    g = w.to(DEV)
+    s = torch.empty((1, w.T, w.NB), device=DEV)
+    tk = torch.empty((1, w.T, w.K), dtype=torch.int32, device=DEV)
+    out = torch.empty((w.T, w.Hq, w.D), dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(spd.decode_workspace_bytes(w.T, w.Hq, w.Hkv, w.D, w.NB), dtype=torch.uint8, device=DEV)
+
+    def step():
+        spd.msa_block_score(g.q_idx, g.k_idx_cache, g.block_table, g.seq_lens, g.req_idx, BS, s, g.idx_scale)
+        spd.msa_select_topk(s, tk)
+        spd.paged_sparse_decode_attention(g.q, g.k_cache, g.v_cache, g.block_table, g.seq_lens, g.req_idx,
+                                          tk.expand(w.Hkv, -1, -1), out, g.sm_scale, BS, g.k_scale, g.v_scale, ws)
+
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        step()  # warm up outside capture
+    torch.cuda.current_stream().wait_stream(stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for it in range(3):
+        gen = torch.Generator().manual_seed(100 + it)
+        w.q.copy_(torch.randn(w.q.shape, generator=gen).to(w.q.dtype))
+        w.q_idx.copy_(torch.randn(w.q_idx.shape, generator=gen).to(w.q_idx.dtype))
+        w.seq_lens.copy_(torch.clamp(w.seq_lens - 37 * (it + 1), min=0))
+        g.q.copy_(w.q)
+        g.q_idx.copy_(w.q_idx)
+        g.seq_lens.copy_(w.seq_lens)
+        s.fill_(float("nan"))
+        tk.fill_(0x7FFFFFF0)
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        ref_s = orc.block_score(w.q_idx, w.k_idx_cache, w.block_table, w.req_idx, w.seq_lens, f32(w.idx_scale))
+        check_scores(s.cpu().numpy(), ref_s, "replay %d scores" % it)
+        check_topk(tk.cpu().numpy(), ref_s, w.K, "replay %d topk" % it)
+        ref = orc.paged_attention(w.q, w.k_cache, w.v_cache, w.block_table, w.req_idx, w.seq_lens,
+                                  tk.cpu().numpy(), f32(w.sm_scale), f32(w.k_scale), f32(w.v_scale))
+        check_attention(out.float().cpu().numpy(), ref, "replay %d attention" % it)
+
+
+def test_empty_batch(spd):
+    q = torch.empty((0, 8, 64), dtype=torch.bfloat16, device=DEV)
+    k = torch.zeros((128, 1, 64), dtype=torch.float8_e4m3fn, device=DEV)
+    bt = torch.zeros((1, 1), dtype=torch.int32, device=DEV)
+    z = torch.empty((0,), dtype=torch.int32, device=DEV)
+    out = torch.empty((0, 8, 64), dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(spd.decode_workspace_bytes(0, 8, 1, 64, 1), dtype=torch.uint8, device=DEV)
+    spd.paged_decode_attention(q, k, k, bt, z, z, out, 0.1, BS, 1.0, 1.0, ws)
+    torch.cuda.synchronize()
+
+
+# --------------------------------------------------------- full-size configs
+
+def test_cfg2_full(spd, orc):
+    full_check(spd, orc, W.config(2))
+
+
+def test_cfg3_full_dense_sampled(spd, orc):
+    w = W.config(3)
+    g = w.to(DEV)
+    out = gpu_attention(spd, g, None)
+    rows = [0, 11]
+    ref = oracle_rows(orc, w, rows, None)
+    check_attention(out.float().cpu().numpy()[rows], ref, "cfg3 dense")
+    assert torch.isfinite(out.float()).all()
+
+
+def test_cfg4_full_sampled(spd, orc):
+    w = W.config(4)
+    g = w.to(DEV)
+    s = gpu_scores(spd, g)
+    tk = gpu_topk(spd, s, w.K)
+    rng = np.random.default_rng(4)
+    rows = sorted(set(rng.integers(0, w.T, 24).tolist()) | {0, 511, 512, w.T - 1})
+    ridx = torch.tensor(rows)
+    ref_s = orc.block_score(w.q_idx[ridx], w.k_idx_cache, w.block_table, w.req_idx[ridx], w.seq_lens[ridx],
+                            f32(w.idx_scale))
+    check_scores(s.cpu().numpy()[:, rows], ref_s, "cfg4 scores")
+    check_topk(tk.cpu().numpy()[:, rows], ref_s, w.K, "cfg4 topk")
+    # causal visibility: no token selects a block past its own position
+    pos_block = ((g.seq_lens - 1) // BS).view(1, -1, 1)
+    assert torch.all((tk < 0) | (tk <= pos_block))
+
+
+def test_cfg5_full(spd, orc):
+    w = W.config(5)
+    pad = [t for t in range(w.T) if int(w.seq_lens[t]) == 0]
+    long_ = int(torch.argmax(w.seq_lens))
+    rows = sorted({0, long_, w.T - 1, pad[0] if pad else 1, w.T // 2, w.T // 3})
+    full_check(spd, orc, w, attn_rows=rows)

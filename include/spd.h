@@ -208,6 +208,24 @@ SPD_API int spd_last_error(char *msg, size_t cap);
  */
 SPD_API uint64_t spd_launch_count(void);
 
+/*
+ * Diagnostics: kernel selection for the attention calls on this thread's
+ * subsequent calls.  0 (default) picks the tensor-core kernel whenever the
+ * shapes and layouts allow it and the general-layout kernel otherwise; 1
+ * always uses the general-layout kernel (for cross-checking the two).
+ * Returns the previous setting.  Results agree within the stated tolerance
+ * either way.
+ */
+SPD_API int spd_set_attention_kernel(int policy);
+
+/*
+ * Diagnostics: status word an attention call left in its workspace (0 = ok;
+ * bit 0 = a device-side wait timed out and the call's output is not valid).
+ * Synchronises with `stream` to read it -- never call it on a hot path.
+ * Returns -1 when the status cannot be read.
+ */
+SPD_API int spd_workspace_status(const void *workspace, spd_stream_t stream);
+
 /* Library version string, e.g. "spd 0.1 sm_103a". */
 SPD_API const char *spd_version(void);
 

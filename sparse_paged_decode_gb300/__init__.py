@@ -22,6 +22,8 @@ __all__ = [
     "paged_decode_attention",
     "decode_workspace_bytes",
     "launch_count",
+    "set_attention_kernel",
+    "workspace_status",
     "library_path",
 ]
 

@@ -25,6 +25,8 @@ __all__ = [
     "paged_decode_attention",
     "decode_workspace_bytes",
     "launch_count",
+    "set_attention_kernel",
+    "workspace_status",
     "library_path",
     "lib",
 ]
@@ -81,6 +83,10 @@ def _load():
     L.spd_decode_workspace_bytes.restype = sz
     L.spd_last_error.argtypes = [ctypes.c_char_p, sz]
     L.spd_last_error.restype = ctypes.c_int
+    L.spd_set_attention_kernel.argtypes = [ctypes.c_int]
+    L.spd_set_attention_kernel.restype = ctypes.c_int
+    L.spd_workspace_status.argtypes = [vp, vp]
+    L.spd_workspace_status.restype = ctypes.c_int
     L.spd_launch_count.argtypes = []
     L.spd_launch_count.restype = ctypes.c_uint64
     L.spd_version.argtypes = []
@@ -173,6 +179,17 @@ def _workspace(ws):
     if not isinstance(ws, torch.Tensor) or not ws.is_cuda:
         raise TypeError("workspace must be a CUDA tensor")
     return ws.data_ptr(), ws.numel() * ws.element_size()
+
+
+def set_attention_kernel(policy: int) -> int:
+    """0 = tensor-core kernel where it applies (default), 1 = general-layout
+    kernel always.  Applies to this thread; returns the previous policy."""
+    return int(lib.spd_set_attention_kernel(int(policy)))
+
+
+def workspace_status(workspace, stream=None) -> int:
+    """Status word an attention call left in ``workspace`` (synchronises)."""
+    return int(lib.spd_workspace_status(workspace.data_ptr(), _stream(stream)))
 
 
 def launch_count() -> int:

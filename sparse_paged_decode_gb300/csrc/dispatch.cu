@@ -1,6 +1,9 @@
 // dispatch.cu -- picks the kernel for each call.
+#include <stddef.h>
+
 #include <atomic>
 
+#include "plan.cuh"
 #include "spd_dispatch.h"
 
 namespace spd {
@@ -22,20 +25,45 @@ cudaError_t dispatch_select(const SelectArgs &a, cudaStream_t stream) {
     return launch_select_generic(a, stream);
 }
 
+cudaError_t launch_attention_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cudaStream_t stream, bool *used);
+
+namespace {
+thread_local int g_attention_policy = 0;
+}
+
+int set_attention_policy(int policy) {
+    const int old = g_attention_policy;
+    g_attention_policy = policy;
+    return old;
+}
+
 cudaError_t dispatch_attention(const AttnArgs &a, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
-    (void)workspace;
-    (void)workspace_bytes;
+    bool used = false;
+    cudaError_t e = cudaSuccess;
+    if (g_attention_policy == 0) e = launch_attention_tc(a, workspace, workspace_bytes, stream, &used);
+    if (e != cudaSuccess) return e;
+    if (used) {
+        count_launches(2);  // planner + attention
+        return cudaSuccess;
+    }
     count_launches(1);
     return launch_attention_generic(a, stream);
 }
 
+int workspace_status(const void *workspace, cudaStream_t stream) {
+    if (workspace == nullptr) return -1;
+    int32_t status = 0;
+    if (cudaMemcpyAsync(&status, static_cast<const char *>(workspace) + offsetof(PlanHeader, status), sizeof status,
+                        cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return -1;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return -1;
+    return status;
+}
+
 size_t workspace_bytes(int64_t T, int64_t Hq, int64_t Hkv, int64_t D, int64_t NB) {
-    // split-K partials: one fp32 row of D values plus (max, sum) per q head
-    // and split, for up to 2*T*Hq + 16384 rows; plus the work plan.
-    const size_t rows = static_cast<size_t>(2 * T * Hq + 16384);
-    const size_t partials = rows * static_cast<size_t>(D + 2) * sizeof(float);
-    const size_t plan = static_cast<size_t>(T * Hkv + 1) * static_cast<size_t>(NB + 16) * sizeof(int32_t) + 65536;
-    return (partials + plan + 255) / 256 * 256;
+    // the work plan (groups, per-pair block lists, units) and the split-K
+    // partials of the tensor-core path; see plan.cuh
+    return PlanLayout(T, Hq, Hkv, D, NB).total;
 }
 
 }  // namespace spd

@@ -190,6 +190,9 @@ attention_generic_kernel(AttnArgs a) {
             for (int i = 0; i < kBlock; ++i) s += ps[tid][i];
             l_run[tid] = l_run[tid] * alpha_s[tid] + s;
         }
+        // only the block's valid prefix is read: the page tail past seq_len
+        // may hold anything, and 0 * NaN would poison the sum
+        const int n_valid = static_cast<int>(min(static_cast<int64_t>(kBlock), L - static_cast<int64_t>(b) * kBlock));
 #pragma unroll
         for (int c = 0; c < kDPerThread; ++c) {
             const int d = tid + c * kAttnThreads;
@@ -197,7 +200,7 @@ attention_generic_kernel(AttnArgs a) {
             float part[kMaxGroup];
 #pragma unroll
             for (int g = 0; g < kMaxGroup; ++g) part[g] = 0.f;
-            for (int i = 0; i < kBlock; ++i) {
+            for (int i = 0; i < n_valid; ++i) {
                 const float vd = e4m3_to_float(a.v[(base + i) * a.v_s0 + h * a.v_s1 + d]);
 #pragma unroll
                 for (int g = 0; g < kMaxGroup; ++g)

@@ -1,0 +1,111 @@
+// plan.cuh -- the work plan of the tensor-core decode attention, built on the
+// device by one CTA from req_idx / seq_lens / topk_idx (no host reads, so the
+// call stays graph safe), and its layout inside the caller's workspace.
+//
+//   group  a run of consecutive query rows of one request (at most gmax rows):
+//          the draft tokens of a verification row, which share every K/V page
+//   pair   (group, kv head): its block list is the union of the blocks its
+//          rows selected, ascending, each with the mask of rows that selected
+//          it and its page id (blocks whose page lies outside the pool are
+//          dropped here)
+//   unit   a contiguous chunk of a pair's block list: the work item of one CTA;
+//          a pair split over several units leaves per-unit partials (running
+//          max, sum, unnormalised output) that the last unit to finish merges
+#pragma once
+
+#include <stdint.h>
+
+#include "spd_internal.cuh"
+
+namespace spd {
+
+struct PlanHeader {
+    int32_t status;        // bit 0: an attention wait timed out
+    int32_t n_groups;
+    int32_t n_pairs;
+    int32_t n_units;
+    int32_t chunk;         // blocks per unit
+    int32_t partial_rows;  // partial rows in use
+    int32_t gmax;
+    int32_t reserved[57];
+};
+static_assert(sizeof(PlanHeader) == 256, "header is one 256-byte line");
+
+struct PlanGroup {
+    int32_t t0;  // first query row
+    int32_t nt;  // rows in the group
+    int32_t r;   // block_table row (valid only when some row has keys)
+    int32_t pad;
+};
+
+struct PlanPair {
+    int32_t list;      // offset of its block list (entries)
+    int32_t n_blocks;
+    int32_t unit0;     // first unit
+    int32_t n_units;
+};
+
+struct PlanEntry {
+    int32_t page;
+    uint16_t block;
+    uint16_t mask;  // bit j: row j of the group selected the block
+};
+
+struct PlanUnit {
+    int32_t pair;
+    int32_t first;     // first entry of the pair's list
+    int32_t count;     // entries
+    int32_t part_row;  // first partial row, -1 when the pair is not split
+};
+
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanMaxT = 4096;   // query rows the one-CTA planner handles
+constexpr int kPlanMaxNB = 256;   // page-table capacity of the fast path
+constexpr int kUnitExtra = 8192;
+constexpr int kPartialStride = 4; // floats after the D output values: max, sum, pad
+
+// Byte layout of the workspace for capacities (T, Hq, Hkv, D, NB).
+struct PlanLayout {
+    size_t header, groups, pairs, lists, units, counters, partials, total;
+    int64_t unit_cap, rows_cap, pair_cap;
+
+    __host__ __device__ static size_t align(size_t x) { return (x + 255) / 256 * 256; }
+
+    PlanLayout() = default;
+
+    __host__ __device__ PlanLayout(int64_t T, int64_t Hq, int64_t Hkv, int64_t D, int64_t NB) {
+        pair_cap = T * Hkv;
+        unit_cap = pair_cap + kUnitExtra;
+        rows_cap = 2 * T * Hq + 16384;
+        size_t off = 0;
+        header = off;   off += align(sizeof(PlanHeader));
+        groups = off;   off += align(sizeof(PlanGroup) * (size_t)(T > 0 ? T : 1));
+        pairs = off;    off += align(sizeof(PlanPair) * (size_t)(pair_cap > 0 ? pair_cap : 1));
+        lists = off;    off += align(sizeof(PlanEntry) * (size_t)(pair_cap > 0 ? pair_cap : 1) * (size_t)NB);
+        units = off;    off += align(sizeof(PlanUnit) * (size_t)unit_cap);
+        counters = off; off += align(sizeof(int32_t) * (size_t)(pair_cap > 0 ? pair_cap : 1));
+        partials = off; off += align(sizeof(float) * (size_t)rows_cap * (size_t)(D + kPartialStride));
+        total = off;
+    }
+};
+
+struct PlanArgs {
+    const int32_t *ri;
+    int64_t ri_s0;
+    const int32_t *sl;
+    int64_t sl_s0;
+    const int32_t *bt;
+    int64_t bt_s0, bt_s1;
+    const int32_t *tk;  // nullptr: dense
+    int64_t tk_s0, tk_s1, tk_s2;
+    int32_t T, R, NB, K, Hkv, G, gmax;
+    int64_t P;
+    int32_t num_ctas;
+    int32_t units_per_cta;
+    char *ws;
+    PlanLayout lay;
+};
+
+cudaError_t launch_plan(const PlanArgs &a, cudaStream_t stream);
+
+}  // namespace spd

@@ -16,6 +16,11 @@ cudaError_t dispatch_attention(const AttnArgs &a, void *workspace, size_t worksp
 void count_launches(int n);
 uint64_t launch_count();
 
+// Attention kernel policy (spd_set_attention_kernel) and the status word of a
+// workspace (spd_workspace_status).
+int set_attention_policy(int policy);
+int workspace_status(const void *workspace, cudaStream_t stream);
+
 // Workspace bytes for the attention calls (capacities only).
 size_t workspace_bytes(int64_t T, int64_t Hq, int64_t Hkv, int64_t D, int64_t NB);
 

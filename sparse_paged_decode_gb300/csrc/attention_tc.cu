@@ -52,12 +52,14 @@ namespace {
 
 constexpr int kThreads = 192;         // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
 constexpr int kSoftThreads = 128;
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kTile = 128 * 128;      // bytes of one K or V tile
 constexpr int kNMax = 64;             // query rows per group (padded)
-constexpr float kRaise = 6.0f;        // log2 headroom before the offset is raised
-constexpr float kPScale = 4.0f;       // probabilities are stored times 4 (<= 256)
+constexpr int kMaxEntries = kPlanMaxNB;
+constexpr float kRaise = 6.0f;        // log2 headroom before the offset is raised (p <= 64)
 constexpr int kD = 128;
+constexpr int kTerms = 3;             // E4M3 terms per query element (12 significant bits)
+constexpr int kStride = kD + kPartialStride;
 
 struct TcArgs {
     const void *q;
@@ -76,36 +78,45 @@ struct TcArgs {
     PlanLayout lay;
 };
 
-struct __align__(8) Shared {
+struct __align__(16) Shared {
+    float m_run[kNMax];   // running exponent offset per query row (log2 units)
+    float cfac[kNMax];    // logit factor per query row
+    float alpha[kNMax];   // rescale factor of the last offset raise
+    float den[kNMax];     // merge: normaliser per row
+    float red[4][kNMax];  // cross-warp reduction scratch
     uint64_t kv_full[kStages], kv_empty[kStages];
     uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2];
     uint64_t q_full;
     uint32_t tmem_base;
     int abort;
     int combine;
+    int rescale;
     int vote[2][4];
     int unit_vote[4];
-    float m_run[kNMax];   // running exponent offset per query row (log2 units)
-    float cfac[kNMax];    // logit factor per query row
-    float red[4][kNMax];  // cross-warp reduction scratch
-    int colj[kNMax];      // group row of each column
-    int Lj[16];           // key limit of each group row
+    int Lj[16];                  // key limit of each group row
+    PlanEntry ent[kMaxEntries];  // the unit's block list
 };
 
-// dynamic shared memory: K[kStages], V[kStages], Qhi, Qlo, P[2][hi,lo], Shared
+// dynamic shared memory: E4M3 K and V stages, query terms, f16 V and P tiles
+// (double buffered), Shared
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kStages * kTile;
-constexpr int kOffQhi = kOffV + kStages * kTile;
-constexpr int kOffQlo = kOffQhi + kNMax * 128;
-constexpr int kOffP = kOffQlo + kNMax * 128;
-constexpr int kPTile = 128 * kNMax;
-constexpr int kOffShared = kOffP + 4 * kPTile;
+constexpr int kQBytes = kNMax * 128;
+constexpr int kOffQ = kOffV + kStages * kTile;
+constexpr int kV16Tile = 128 * kD * 2;   // [2 d-halves][128 tokens][64 d] f16
+constexpr int kP16Tile = 128 * kNMax * 2;  // [128 tokens][N] f16
+constexpr int kOffV16 = kOffQ + kTerms * kQBytes;
+constexpr int kOffP = kOffV16 + 2 * kV16Tile;
+constexpr int kOffShared = kOffP + 2 * kP16Tile;
 constexpr int kSmemBytes = kOffShared + static_cast<int>(sizeof(Shared)) + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+static_assert(kNMax * kD * 4 <= 2 * kP16Tile, "query staging fits in the P buffers");
 
 __device__ __forceinline__ int pow2_width(int n) { return n <= 16 ? 16 : n <= 32 ? 32 : 64; }
 
-__device__ __forceinline__ tc::Swizzle swz_of(int width) {
-    return width == 16 ? tc::kSwNone : width == 32 ? tc::kSw32 : tc::kSw64;
+// swizzle of an f16 [tokens][n] tile whose rows are 2n bytes
+__device__ __forceinline__ tc::Swizzle p_swizzle(int n) {
+    return n == 16 ? tc::kSw32 : n == 32 ? tc::kSw64 : tc::kSw128;
 }
 
 __device__ __forceinline__ void named_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kSoftThreads) : "memory"); }
@@ -119,6 +130,362 @@ __device__ __forceinline__ bool wait_or_abort(Shared &sh, uint64_t *bar, uint32_
     return false;
 }
 
+// x rounded to 3 fraction bits (4 significant bits), half away from zero:
+// exactly representable in E4M3 whenever |x| lies in its normal range.
+__device__ __forceinline__ float round4(float x) {
+    return __uint_as_float((__float_as_uint(x) + 0x00080000u) & 0xFFF00000u);
+}
+
+__device__ __forceinline__ PlanUnit load_unit(const PlanUnit *units, int u, int n_units) {
+    PlanUnit un{};
+    if (u < n_units) un = units[u];
+    return un;
+}
+
+__device__ __forceinline__ uint32_t pack4(uint16_t a, uint16_t b) {
+    return static_cast<uint32_t>(a) | (static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// What a softmax thread needs besides the kernel arguments.
+struct Soft {
+    Shared *sh;
+    uint8_t *smem;
+    int32_t *status;
+    int32_t *counters;
+    float *partials;
+    uint32_t tS0, tS1, tO, lane_base;
+    int tok, lane, sw, st_id;
+};
+
+// Queries of the unit's group into the three E4M3 term buffers (B operand of
+// Q K^T): rows staged through shared memory with coalesced loads, then per
+// row a power-of-two scale into [128, 256) and x = t0 + t1 + t2, each term
+// the 4-significant-bit rounding of what the previous ones left.
+__device__ __noinline__ void prep_queries(const Soft &c, const TcArgs &a, const PlanUnit &un) {
+    Shared &sh = *c.sh;
+    const int rows = un.nt * a.G;
+    float *stage = reinterpret_cast<float *>(c.smem + kOffP);  // [rows][128]; the P buffers are idle here
+    for (int r0 = 0; r0 < rows; r0 += 8) {
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int row = r0 + k;
+            v[k] = 0.f;
+            if (row < rows) {
+                const int j = row / a.G, g = row % a.G;
+                v[k] = load_float(a.q, a.q_dt,
+                                  (un.t0 + j) * a.q_s0 + (un.h * a.G + g) * a.q_s1 + c.st_id * a.q_s2);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (r0 + k < rows) stage[(r0 + k) * kD + c.st_id] = v[k];
+    }
+    named_sync();
+    uint8_t *qt = c.smem + kOffQ;
+    for (int row = c.sw; row < kNMax; row += 4) {
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if (row < rows) {
+            const float4 v = *reinterpret_cast<const float4 *>(stage + row * kD + c.lane * 4);
+            x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+        }
+        const float amax = warp_max(fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))));
+        float scale = 1.f;
+        if (amax > 0.f && amax < INFINITY) {
+            int ex;
+            frexpf(amax, &ex);
+            scale = ldexpf(1.f, 8 - ex);  // amax * scale in [128, 256)
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[e] *= scale;
+        const uint32_t off = tc::swz_offset(row, c.lane * 4, 128);
+#pragma unroll
+        for (int term = 0; term < kTerms; ++term) {
+            float t[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                t[e] = round4(x[e]);
+                x[e] -= t[e];
+            }
+            *reinterpret_cast<uint32_t *>(qt + term * kQBytes + off) =
+                pack4(tc::f32x2_to_e4m3x2(t[1], t[0]), tc::f32x2_to_e4m3x2(t[3], t[2]));
+        }
+        if (c.lane == 0) sh.cfac[row] = (row < rows) ? a.zscale / scale : 0.f;
+    }
+}
+
+// The last unit of a split pair to finish merges all of them: per-row weights
+// 2^(m_k - max m) into the (idle) P buffers, then every output element sums
+// its units' partials with all loads of a batch in flight together.
+__device__ __noinline__ void merge_partials(const Soft &c, const TcArgs &a, const PlanUnit &un) {
+    Shared &sh = *c.sh;
+    const int rows = un.nt * a.G;
+    const int ns = un.n_split;
+    float *wgt = reinterpret_cast<float *>(c.smem + kOffP);  // [ns][rows]
+    const float *pbase = c.partials + static_cast<int64_t>(un.part_base) * kStride;
+    __threadfence();
+    for (int r = c.st_id; r < rows; r += kSoftThreads) {
+        float mstar = -INFINITY;
+        for (int k = 0; k < ns; ++k)
+            mstar = fmaxf(mstar, __ldcg(pbase + static_cast<int64_t>(k * rows + r) * kStride + kD));
+        float den = 0.f;
+        for (int k = 0; k < ns; ++k) {
+            const float *prow = pbase + static_cast<int64_t>(k * rows + r) * kStride;
+            const float mk = __ldcg(prow + kD);
+            const float w = (mk == -INFINITY) ? 0.f : tc::ex2(mk - mstar);
+            wgt[k * rows + r] = w;
+            den += w * __ldcg(prow + kD + 1);
+        }
+        sh.den[r] = den;
+    }
+    named_sync();
+    const int d = c.tok;
+    for (int r0 = 0; r0 < rows; r0 += 8) {
+        float acc[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+        for (int k = 0; k < ns; ++k) {
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                v[j] = (r0 + j < rows) ? __ldcg(pbase + static_cast<int64_t>(k * rows + r0 + j) * kStride + d) : 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (r0 + j < rows) acc[j] += wgt[k * rows + r0 + j] * v[j];
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int r = r0 + j;
+            if (r < rows) {
+                const float den = sh.den[r];
+                const float val = (den > 0.f) ? acc[j] * (a.v_scale * 256.f) / den : 0.f;
+                const int t = un.t0 + r / a.G, g = r % a.G;
+                a.out[t * a.o_s0 + (un.h * a.G + g) * a.o_s1 + d * a.o_s2] = __float2bfloat16_rn(val);
+            }
+        }
+    }
+}
+
+// One unit's blocks and its epilogue for N = 16*NCH query columns.  Returns
+// false when the CTA must stop (an abort, decided uniformly).
+template <int NCH>
+__device__ __forceinline__ bool unit_body(const Soft &c, const TcArgs &a, const PlanUnit &un, uint32_t gb) {
+    constexpr int N = NCH * 16;
+    Shared &sh = *c.sh;
+    const int rows = un.nt * a.G;
+    const uint64_t gmask = (a.G >= 64) ? ~0ull : ((1ull << a.G) - 1);
+    float lsum[N];
+#pragma unroll
+    for (int col = 0; col < N; ++col) lsum[col] = 0.f;
+
+    for (int i = 0; i < un.count; ++i) {
+        const uint32_t b = gb + i;
+        const int sb = b & 1, stg = b % kStages;
+        const PlanEntry e = sh.ent[i];
+        // columns valid on this token lane: selected by the column's row and
+        // below that row's key limit
+        uint64_t colmask = 0;
+        for (int j = 0; j < un.nt; ++j)
+            if (((e.mask >> j) & 1) && c.tok < sh.Lj[j] - e.block * 128) colmask |= gmask << (j * a.G);
+        wait_or_abort(sh, &sh.s_full[sb], (b >> 1) & 1, c.status);
+        tc::tc_fence_after();
+        float s[N];
+        const uint32_t sbase = (sb ? c.tS1 : c.tS0) + c.lane_base;
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
+            float v[16];
+            tc::tmem_ld16(sbase + ch * 16, v);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) s[ch * 16 + k] = v[k];
+        }
+        tc::tmem_wait_ld();
+        tc::tc_fence_before();
+        tc::mbar_arrive(&sh.s_empty[sb]);
+
+        bool need = false;
+#pragma unroll
+        for (int c4 = 0; c4 < N; c4 += 4) {
+            const float4 cf = *reinterpret_cast<const float4 *>(&sh.cfac[c4]);
+            const float4 mr = *reinterpret_cast<const float4 *>(&sh.m_run[c4]);
+            const float cfs[4] = {cf.x, cf.y, cf.z, cf.w}, mrs[4] = {mr.x, mr.y, mr.z, mr.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int col = c4 + k;
+                s[col] = ((colmask >> col) & 1) ? s[col] * cfs[k] : -INFINITY;
+                need |= s[col] > mrs[k] + kRaise;
+            }
+        }
+        // votes alternate between two slots by block parity: a warp can be at
+        // most one block ahead of the slowest reader
+        const int mine = (__any_sync(0xffffffffu, need) ? 1 : 0) | (aborted(sh) ? 2 : 0);
+        if (c.lane == 0) sh.vote[sb][c.sw] = mine;
+        named_sync();
+        const int vote = sh.vote[sb][0] | sh.vote[sb][1] | sh.vote[sb][2] | sh.vote[sb][3];
+        if (vote & 2) return false;
+        if (vote & 1) {
+            // raise the offsets to the block maximum; rescale O and the sums
+#pragma unroll
+            for (int col = 0; col < N; ++col) {
+                const float mx = warp_max(s[col]);
+                if (c.lane == 0) sh.red[c.sw][col] = mx;
+            }
+            named_sync();
+            if (c.sw == 0) {
+                bool any = false;
+                for (int col = c.lane; col < N; col += 32) {
+                    const float bm = fmaxf(fmaxf(sh.red[0][col], sh.red[1][col]), fmaxf(sh.red[2][col], sh.red[3][col]));
+                    const float old = sh.m_run[col];
+                    float al = 1.f;
+                    if (bm > old) {
+                        al = (old == -INFINITY) ? 0.f : tc::ex2(old - bm);
+                        any |= old != -INFINITY;
+                        sh.m_run[col] = bm;
+                    }
+                    sh.alpha[col] = al;
+                }
+                any = __any_sync(0xffffffffu, any);
+                if (c.lane == 0) sh.rescale = any;
+            }
+            named_sync();
+#pragma unroll
+            for (int col = 0; col < N; ++col) lsum[col] *= sh.alpha[col];
+            if (sh.rescale && i > 0) {
+                // O holds blocks 0..i-1 of this unit: wait for the last PV
+                wait_or_abort(sh, &sh.pv_done[(b - 1) & 1], ((b - 1) >> 1) & 1, c.status);
+                tc::tc_fence_after();
+                for (int ch = 0; ch < NCH; ++ch) {
+                    float v[16];
+                    tc::tmem_ld16(c.tO + c.lane_base + ch * 16, v);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) v[k] *= sh.alpha[ch * 16 + k];
+                    tc::tmem_st16(c.tO + c.lane_base + ch * 16, v);
+                }
+                tc::tmem_wait_st();
+                tc::tc_fence_before();
+            }
+        }
+
+        // V and P buffers sb were read by the PV of block b-2
+        if (b >= 2) wait_or_abort(sh, &sh.pv_done[sb], ((b >> 1) - 1) & 1, c.status);
+        // this token's V row: E4M3 (128-byte swizzled TMA tile) -> f16 * 2^-8
+        // (two 64-d halves, 128-byte swizzle), the A operand of P V; the E4M3
+        // stage is then free for the next TMA load
+        wait_or_abort(sh, &sh.kv_full[stg], (b / kStages) & 1, c.status);
+        {
+            const uint8_t *vsrc = c.smem + kOffV + stg * kTile + c.tok * 128;
+            uint8_t *vdst = c.smem + kOffV16 + sb * kV16Tile + c.tok * 128;
+            const int sw8 = c.tok & 7;
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+                const uint4 x = *reinterpret_cast<const uint4 *>(vsrc + ((cc ^ sw8) << 4));
+                uint32_t f[8];
+                tc::e4m3x4_to_f16x4_scaled(x.x, f[0], f[1]);
+                tc::e4m3x4_to_f16x4_scaled(x.y, f[2], f[3]);
+                tc::e4m3x4_to_f16x4_scaled(x.z, f[4], f[5]);
+                tc::e4m3x4_to_f16x4_scaled(x.w, f[6], f[7]);
+                uint8_t *half = vdst + (cc >> 2) * (128 * 128);
+                *reinterpret_cast<uint4 *>(half + ((((2 * cc) & 7) ^ sw8) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
+                *reinterpret_cast<uint4 *>(half + ((((2 * cc + 1) & 7) ^ sw8) << 4)) = make_uint4(f[4], f[5], f[6], f[7]);
+            }
+        }
+        tc::fence_proxy_async();
+        tc::mbar_arrive(&sh.kv_empty[stg]);
+        // probabilities p = 2^(s - offset) <= 64 in f16 (11-bit significand,
+        // normal down to 2^-14), the B operand of P V
+        uint8_t *pb = c.smem + kOffP + sb * kP16Tile;
+#pragma unroll
+        for (int c8 = 0; c8 < N; c8 += 8) {
+            const float4 m0 = *reinterpret_cast<const float4 *>(&sh.m_run[c8]);
+            const float4 m1 = *reinterpret_cast<const float4 *>(&sh.m_run[c8 + 4]);
+            const float mr[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+            float p[8];
+#pragma unroll
+            for (int e2 = 0; e2 < 8; ++e2) {
+                const int col = c8 + e2;
+                p[e2] = (s[col] == -INFINITY) ? 0.f : tc::ex2(s[col] - mr[e2]);
+                lsum[col] += p[e2];
+            }
+            uint4 w;
+            w.x = tc::f32x2_to_f16x2(p[0], p[1]);
+            w.y = tc::f32x2_to_f16x2(p[2], p[3]);
+            w.z = tc::f32x2_to_f16x2(p[4], p[5]);
+            w.w = tc::f32x2_to_f16x2(p[6], p[7]);
+            *reinterpret_cast<uint4 *>(pb + tc::swz_offset(c.tok, c8 * 2, 2 * N)) = w;
+        }
+        tc::fence_proxy_async();
+        tc::mbar_arrive(&sh.p_full[sb]);
+    }
+
+    // ---- epilogue: row sums over the 128 token lanes, then O (d lane = tok)
+#pragma unroll
+    for (int col = 0; col < N; ++col) {
+        const float v = warp_sum(lsum[col]);
+        if (c.lane == 0) sh.red[c.sw][col] = v;
+    }
+    float o[N];
+#pragma unroll
+    for (int col = 0; col < N; ++col) o[col] = 0.f;
+    if (un.count > 0) {
+        const uint32_t last = gb + un.count - 1;
+        wait_or_abort(sh, &sh.pv_done[last & 1], (last >> 1) & 1, c.status);
+        tc::tc_fence_after();
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
+            float v[16];
+            tc::tmem_ld16(c.tO + c.lane_base + ch * 16, v);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) o[ch * 16 + k] = v[k];
+        }
+        tc::tmem_wait_ld();
+        tc::tc_fence_before();
+    }
+    named_sync();
+    const int d = c.tok;
+    if (un.part_row < 0) {
+#pragma unroll
+        for (int col = 0; col < N; ++col) {
+            if (col < rows) {
+                const float l = sh.red[0][col] + sh.red[1][col] + sh.red[2][col] + sh.red[3][col];
+                const float val = (l > 0.f) ? o[col] * (a.v_scale * 256.f) / l : 0.f;
+                const int t = un.t0 + col / a.G, g = col % a.G;
+                a.out[t * a.o_s0 + (un.h * a.G + g) * a.o_s1 + d * a.o_s2] = __float2bfloat16_rn(val);
+            }
+        }
+    } else {
+        // partial of a split pair: unnormalised O, offset and sum per row
+#pragma unroll
+        for (int col = 0; col < N; ++col) {
+            if (col < rows) {
+                float *prow = c.partials + static_cast<int64_t>(un.part_row + col) * kStride;
+                prow[d] = o[col];
+                if (d == 0) {
+                    prow[kD] = sh.m_run[col];
+                    prow[kD + 1] = sh.red[0][col] + sh.red[1][col] + sh.red[2][col] + sh.red[3][col];
+                }
+            }
+        }
+        __threadfence();
+        named_sync();
+        if (c.st_id == 0) sh.combine = (atomicAdd(&c.counters[un.pair], 1) == un.n_split - 1);
+        named_sync();
+        if (sh.combine) merge_partials(c, a, un);
+    }
+    return true;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                     const TcArgs a) {
@@ -128,18 +495,14 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     PlanHeader *hdr = reinterpret_cast<PlanHeader *>(a.ws + a.lay.header);
-    const PlanGroup *groups = reinterpret_cast<const PlanGroup *>(a.ws + a.lay.groups);
-    const PlanPair *pairs = reinterpret_cast<const PlanPair *>(a.ws + a.lay.pairs);
     const PlanEntry *lists = reinterpret_cast<const PlanEntry *>(a.ws + a.lay.lists);
     const PlanUnit *units = reinterpret_cast<const PlanUnit *>(a.ws + a.lay.units);
-    int32_t *counters = reinterpret_cast<int32_t *>(a.ws + a.lay.counters);
-    float *partials = reinterpret_cast<float *>(a.ws + a.lay.partials);
     const int n_units = hdr->n_units;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             tc::mbar_init(&sh.kv_full[i], 1);
-            tc::mbar_init(&sh.kv_empty[i], 1);
+            tc::mbar_init(&sh.kv_empty[i], kSoftThreads);
         }
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&sh.s_full[i], 1);
@@ -160,24 +523,36 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
 
     if (warp == 0) {
         // ------------------------------------------------------- TMA producer
+        // Metadata is software-pipelined: the next unit record and the next
+        // list entry are loaded one step ahead of their use.
         if (lane == 0) {
             tc::prefetch_tmap(&tmap_k);
             tc::prefetch_tmap(&tmap_v);
             const uint64_t policy = tc::policy_evict_first();
             uint32_t lb = 0;  // blocks loaded by this CTA
-            for (int u = blockIdx.x; u < n_units && !aborted(sh); u += gridDim.x) {
-                const PlanUnit un = units[u];
-                const PlanPair pr = pairs[un.pair];
-                const int h = un.pair % a.Hkv;
+            int u = blockIdx.x;
+            PlanUnit un = load_unit(units, u, n_units);
+            while (u < n_units && !aborted(sh)) {
+                const int u_next = u + gridDim.x;
+                const PlanUnit un_next = load_unit(units, u_next, n_units);
+                PlanEntry e_next{};
+                if (un.count > 0) e_next = lists[un.entry];
+                bool ok = true;
                 for (int i = 0; i < un.count; ++i, ++lb) {
+                    const PlanEntry e = e_next;
+                    if (i + 1 < un.count) e_next = lists[un.entry + i + 1];
                     const int st = lb % kStages;
-                    if (lb >= kStages && !wait_or_abort(sh, &sh.kv_empty[st], ((lb / kStages) - 1) & 1, &hdr->status))
+                    if (lb >= kStages && !wait_or_abort(sh, &sh.kv_empty[st], ((lb / kStages) - 1) & 1, &hdr->status)) {
+                        ok = false;
                         break;
-                    const PlanEntry e = lists[pr.list + un.first + i];
+                    }
                     tc::mbar_arrive_expect_tx(&sh.kv_full[st], 2 * kTile);
-                    tc::tma_load_3d(smem + kOffK + st * kTile, &tmap_k, &sh.kv_full[st], 0, h, e.page * 128, policy);
-                    tc::tma_load_3d(smem + kOffV + st * kTile, &tmap_v, &sh.kv_full[st], 0, h, e.page * 128, policy);
+                    tc::tma_load_3d(smem + kOffK + st * kTile, &tmap_k, &sh.kv_full[st], 0, un.h, e.page * 128, policy);
+                    tc::tma_load_3d(smem + kOffV + st * kTile, &tmap_v, &sh.kv_full[st], 0, un.h, e.page * 128, policy);
                 }
+                if (!ok) break;
+                u = u_next;
+                un = un_next;
             }
             // let every issued copy land before the CTA may exit
             const uint32_t first = lb > kStages ? lb - kStages : 0;
@@ -188,15 +563,19 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         if (lane == 0) {
             uint32_t gb = 0, uc = 0;
             const uint32_t sK = tc::smem_u32(smem + kOffK), sV = tc::smem_u32(smem + kOffV);
-            const uint32_t sQh = tc::smem_u32(smem + kOffQhi), sQl = tc::smem_u32(smem + kOffQlo);
+            const uint32_t sQ = tc::smem_u32(smem + kOffQ);
+            const uint32_t sV16 = tc::smem_u32(smem + kOffV16);
             const uint32_t sP = tc::smem_u32(smem + kOffP);
-            for (int u = blockIdx.x; u < n_units && !aborted(sh); u += gridDim.x, ++uc) {
-                const PlanUnit un = units[u];
-                const PlanGroup gr = groups[un.pair / a.Hkv];
-                const int n = pow2_width(gr.nt * a.G);
-                const uint32_t idesc_qk = tc::idesc_e4m3(n, false, false);
-                const uint32_t idesc_pv = tc::idesc_e4m3(n, true, true);
-                const tc::Swizzle psw = swz_of(n);
+            int u = blockIdx.x;
+            PlanUnit un = load_unit(units, u, n_units);
+            while (u < n_units && !aborted(sh)) {
+                const int u_next = u + gridDim.x;
+                const PlanUnit un_next = load_unit(units, u_next, n_units);
+                const int n = pow2_width(un.nt * a.G);
+                const uint32_t idesc_qk = tc::idesc_m128(n, false, false);  // E4M3 x E4M3, both K-major
+                const uint32_t idesc_pv = tc::idesc_m128(n, true, true);    // F16 x F16, both MN-major
+                const tc::Swizzle psw = p_swizzle(n);
+                const uint32_t prow = 2 * n;  // bytes per token row of the P tile
                 if (!wait_or_abort(sh, &sh.q_full, uc & 1, &hdr->status)) break;
                 tc::tc_fence_after();
                 auto issue_qk = [&](uint32_t b) {
@@ -208,43 +587,39 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
                         const uint64_t ad = tc::smem_desc(sK + st * kTile + ks * 32, 16, 1024, tc::kSw128);
-                        tc::mma_f8(d, ad, tc::smem_desc(sQh + ks * 32, 16, 1024, tc::kSw128), idesc_qk, ks > 0);
-                        tc::mma_f8(d, ad, tc::smem_desc(sQl + ks * 32, 16, 1024, tc::kSw128), idesc_qk, true);
+#pragma unroll
+                        for (int term = 0; term < kTerms; ++term)
+                            tc::mma_f8(d, ad, tc::smem_desc(sQ + term * kQBytes + ks * 32, 16, 1024, tc::kSw128),
+                                       idesc_qk, ks > 0 || term > 0);
                     }
                     tc::mma_commit(&sh.s_full[sb]);
                     return true;
                 };
-                if (un.count > 0 && !issue_qk(gb)) break;
-                bool ok = true;
-                for (int i = 0; i < un.count; ++i) {
+                bool ok = un.count == 0 || issue_qk(gb);
+                for (int i = 0; ok && i < un.count; ++i) {
                     const uint32_t b = gb + i;
                     if (i + 1 < un.count && !issue_qk(b + 1)) { ok = false; break; }
-                    const int st = b % kStages, sb = b & 1;
+                    const int sb = b & 1;
                     if (!wait_or_abort(sh, &sh.p_full[sb], (b >> 1) & 1, &hdr->status)) { ok = false; break; }
                     tc::tc_fence_after();
-                    const uint32_t pbase = sP + sb * 2 * kPTile;
-                    // P tile: [128 tokens][n bytes], MN-major; atoms of 8 tokens
-                    const uint32_t atom = 8 * n;
+                    // O^T[d][n] += V^T[d][tok] P[tok][n]: f16 V (two 64-d atoms, 16 KiB
+                    // apart) and P, 16 tokens per instruction
+                    const uint32_t vb = sV16 + sb * kV16Tile, pb = sP + sb * kP16Tile;
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        const uint64_t ad = tc::smem_desc(sV + st * kTile + ks * 32 * 128, kTile, 1024, tc::kSw128);
-                        const uint32_t poff = ks * 32 * n;
-                        const uint64_t bh = (psw == tc::kSwNone)
-                                                ? tc::smem_desc(pbase + poff, 128, 4096, tc::kSwNone)
-                                                : tc::smem_desc(pbase + poff, 4096, atom, psw);
-                        const uint64_t bl = (psw == tc::kSwNone)
-                                                ? tc::smem_desc(pbase + kPTile + poff, 128, 4096, tc::kSwNone)
-                                                : tc::smem_desc(pbase + kPTile + poff, 4096, atom, psw);
-                        tc::mma_f8(tmem_O, ad, bh, idesc_pv, i > 0 || ks > 0);
-                        tc::mma_f8(tmem_O, ad, bl, idesc_pv, true);
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint64_t ad = tc::smem_desc(vb + ks * 16 * 128, 128 * 128, 1024, tc::kSw128);
+                        const uint64_t bd = tc::smem_desc(pb + ks * 16 * prow, 4096, 8 * prow, psw);
+                        tc::mma_f16(tmem_O, ad, bd, idesc_pv, i > 0 || ks > 0);
                     }
                     tc::mma_commit(&sh.pv_done[sb]);
-                    tc::mma_commit(&sh.kv_empty[st]);
                 }
                 gb += un.count;
+                ++uc;
                 if (!ok) break;
+                u = u_next;
+                un = un_next;
             }
-            if (gb > 0) tc::mbar_wait(&sh.kv_empty[(gb - 1) % kStages], ((gb - 1) / kStages) & 1);
+            if (gb > 0) tc::mbar_wait(&sh.pv_done[(gb - 1) & 1], ((gb - 1) >> 1) & 1);
         }
     } else {
         // ------------------------------------------------ softmax / epilogue
@@ -252,331 +627,56 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         // loops only together: an abort (a timed-out wait anywhere in the
         // CTA) is folded into the per-block vote and acted on after it.
         // Between barriers a timed-out wait only records the abort.
-        const int st_id = threadIdx.x - 64;        // 0..127
+        Soft c;
+        c.sh = &sh;
+        c.smem = smem;
+        c.status = &hdr->status;
+        c.counters = reinterpret_cast<int32_t *>(a.ws + a.lay.counters);
+        c.partials = reinterpret_cast<float *>(a.ws + a.lay.partials);
+        c.st_id = threadIdx.x - 64;
+        c.lane = lane;
+        c.sw = warp - 2;
         const int quad = warp & 3;                 // TMEM lane quadrant
-        const int tok = quad * 32 + lane;          // token lane of S, d lane of O
-        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        const int sw = warp - 2;                   // softmax warp index 0..3
-        uint32_t gb = 0, uc = 0;
+        c.tok = quad * 32 + lane;                  // token lane of S, d lane of O
+        c.lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        c.tS0 = tmem_S0;
+        c.tS1 = tmem_S1;
+        c.tO = tmem_O;
+        uint32_t gb = 0;
         bool stop = false;
-        float lsum[kNMax];
 
-        for (int u = blockIdx.x; u < n_units && !stop; u += gridDim.x, ++uc) {
-            const PlanUnit un = units[u];
-            const PlanPair pr = pairs[un.pair];
-            const PlanGroup gr = groups[un.pair / a.Hkv];
-            const int h = un.pair % a.Hkv;
-            const int rows = gr.nt * a.G;
-            const int n = pow2_width(rows);
-            const int nchunks = n / 16;
-
-            // ---- queries of the group: power-of-two row scale, E4M3 hi + lo
-            uint8_t *qhi = smem + kOffQhi, *qlo = smem + kOffQlo;
-            for (int row = sw; row < kNMax; row += 4) {
-                uint32_t hi4 = 0, lo4 = 0;
-                if (row < rows) {
-                    const int j = row / a.G, g = row % a.G;
-                    const int t = gr.t0 + j;
-                    float x[4];
-                    float amax = 0.f;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        x[e] = load_float(a.q, a.q_dt, t * a.q_s0 + (h * a.G + g) * a.q_s1 + (lane * 4 + e) * a.q_s2);
-                        amax = fmaxf(amax, fabsf(x[e]));
-                    }
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-                    float scale = 1.f;
-                    if (amax > 0.f && amax < INFINITY) {
-                        int ex;
-                        frexpf(amax, &ex);
-                        scale = ldexpf(1.f, 8 - ex);  // amax * scale in [128, 256)
-                    }
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) x[e] *= scale;
-                    const uint16_t h01 = tc::f32x2_to_e4m3x2(x[1], x[0]);
-                    const uint16_t h23 = tc::f32x2_to_e4m3x2(x[3], x[2]);
-                    float b0, b1, b2, b3;
-                    tc::e4m3x2_to_f32x2(h01, b1, b0);
-                    tc::e4m3x2_to_f32x2(h23, b3, b2);
-                    const uint16_t l01 = tc::f32x2_to_e4m3x2(x[1] - b1, x[0] - b0);
-                    const uint16_t l23 = tc::f32x2_to_e4m3x2(x[3] - b3, x[2] - b2);
-                    hi4 = static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16);
-                    lo4 = static_cast<uint32_t>(l01) | (static_cast<uint32_t>(l23) << 16);
-                    if (lane == 0) {
-                        sh.cfac[row] = a.zscale / scale;
-                        sh.colj[row] = j;
-                    }
-                } else if (lane == 0) {
-                    sh.cfac[row] = 0.f;
-                    sh.colj[row] = 0;
-                }
-                const uint32_t off = tc::swz_offset(row, lane * 4, 128);
-                *reinterpret_cast<uint32_t *>(qhi + off) = hi4;
-                *reinterpret_cast<uint32_t *>(qlo + off) = lo4;
-            }
-            if (st_id < 16) {
+        int u = blockIdx.x;
+        PlanUnit un = load_unit(units, u, n_units);
+        while (u < n_units && !stop) {
+            const int u_next = u + gridDim.x;
+            const PlanUnit un_next = load_unit(units, u_next, n_units);
+            for (int i = c.st_id; i < un.count; i += kSoftThreads) sh.ent[i] = lists[un.entry + i];
+            if (c.st_id < 16) {
                 int r;
-                sh.Lj[st_id] = (st_id < gr.nt)
-                                   ? static_cast<int>(token_limit(a.ri, a.ri_s0, a.sl, a.sl_s0, gr.t0 + st_id, a.R,
-                                                                  a.NB, &r))
-                                   : 0;
+                sh.Lj[c.st_id] = (c.st_id < un.nt) ? static_cast<int>(token_limit(a.ri, a.ri_s0, a.sl, a.sl_s0,
+                                                                                  un.t0 + c.st_id, a.R, a.NB, &r))
+                                                    : 0;
             }
-            if (st_id < kNMax) sh.m_run[st_id] = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < kNMax; ++c) lsum[c] = 0.f;
+            if (c.st_id < kNMax) sh.m_run[c.st_id] = -INFINITY;
+            prep_queries(c, a, un);
             tc::fence_proxy_async();
             named_sync();
             tc::mbar_arrive(&sh.q_full);
 
-            // ---- blocks of the unit
-            for (int i = 0; i < un.count; ++i) {
-                const uint32_t b = gb + i;
-                const int sb = b & 1, stg = b % kStages;
-                const PlanEntry e = lists[pr.list + un.first + i];
-                // validity of this token lane for each group row
-                uint32_t vbits = 0;
-                int max_valid = 0;
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    if (j < gr.nt && ((e.mask >> j) & 1)) {
-                        const int lim = sh.Lj[j] - e.block * 128;
-                        max_valid = max(max_valid, lim);
-                        vbits |= static_cast<uint32_t>(tok < lim) << j;
-                    }
-                }
-                wait_or_abort(sh, &sh.s_full[sb], (b >> 1) & 1, &hdr->status);
-                tc::tc_fence_after();
-                float s[kNMax];
-                const uint32_t sbase = (sb ? tmem_S1 : tmem_S0) + lane_base;
-#pragma unroll
-                for (int c = 0; c < kNMax / 16; ++c) {
-                    if (c < nchunks) {
-                        float v[16];
-                        tc::tmem_ld16(sbase + c * 16, v);
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) s[c * 16 + k] = v[k];
-                    }
-                }
-                tc::tmem_wait_ld();
-                tc::tc_fence_before();
-                tc::mbar_arrive(&sh.s_empty[sb]);
-
-                bool need = false;
-#pragma unroll
-                for (int c = 0; c < kNMax; ++c) {
-                    if (c < n) {
-                        const bool valid = c < rows && ((vbits >> sh.colj[c]) & 1);
-                        s[c] = valid ? s[c] * sh.cfac[c] : -INFINITY;
-                        need |= s[c] > sh.m_run[c] + kRaise;
-                    }
-                }
-                // votes alternate between two slots by block parity: a warp can
-                // be at most one block ahead of the slowest reader
-                const int mine = (__any_sync(0xffffffffu, need) ? 1 : 0) | (aborted(sh) ? 2 : 0);
-                if (lane == 0) sh.vote[sb][sw] = mine;
-                named_sync();
-                const int vote = sh.vote[sb][0] | sh.vote[sb][1] | sh.vote[sb][2] | sh.vote[sb][3];
-                if (vote & 2) {
-                    stop = true;
-                    break;
-                }
-                if (vote & 1) {
-                    // raise the offsets to the block maximum; rescale O and the sums
-#pragma unroll
-                    for (int c = 0; c < kNMax; ++c) {
-                        if (c < n) {
-                            float mx = s[c];
-#pragma unroll
-                            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                            if (lane == 0) sh.red[sw][c] = mx;
-                        }
-                    }
-                    named_sync();
-                    float alpha[kNMax];
-                    bool rescale = false;
-#pragma unroll
-                    for (int c = 0; c < kNMax; ++c) {
-                        alpha[c] = 1.f;
-                        if (c < n) {
-                            const float bm =
-                                fmaxf(fmaxf(sh.red[0][c], sh.red[1][c]), fmaxf(sh.red[2][c], sh.red[3][c]));
-                            const float old = sh.m_run[c];
-                            const float nw = fmaxf(old, bm);
-                            if (nw > old) {
-                                alpha[c] = (old == -INFINITY) ? 0.f : tc::ex2(old - nw);
-                                rescale = true;
-                            }
-                            lsum[c] *= alpha[c];
-                        }
-                    }
-                    named_sync();  // every thread has read the old offsets
-                    if (sw == 0) {
-                        for (int c = lane; c < n; c += 32) {
-                            const float bm =
-                                fmaxf(fmaxf(sh.red[0][c], sh.red[1][c]), fmaxf(sh.red[2][c], sh.red[3][c]));
-                            sh.m_run[c] = fmaxf(sh.m_run[c], bm);
-                        }
-                    }
-                    if (rescale && i > 0) {
-                        // O holds blocks 0..i-1 of this unit: wait for the last PV
-                        wait_or_abort(sh, &sh.pv_done[(b - 1) & 1], ((b - 1) >> 1) & 1, &hdr->status);
-                        tc::tc_fence_after();
-#pragma unroll
-                        for (int c = 0; c < kNMax / 16; ++c) {
-                            if (c < nchunks) {
-                                float v[16];
-                                tc::tmem_ld16(tmem_O + lane_base + c * 16, v);
-                                tc::tmem_wait_ld();
-#pragma unroll
-                                for (int k = 0; k < 16; ++k) v[k] *= alpha[c * 16 + k];
-                                tc::tmem_st16(tmem_O + lane_base + c * 16, v);
-                            }
-                        }
-                        tc::tmem_wait_st();
-                        tc::tc_fence_before();
-                    }
-                    named_sync();
-                }
-
-                // P buffer sb was read by the PV of block b-2
-                if (b >= 2) wait_or_abort(sh, &sh.pv_done[sb], ((b >> 1) - 1) & 1, &hdr->status);
-                // value rows past every row's key limit may hold anything
-                // (0 * NaN is NaN in the product): zero them
-                if (tok >= max_valid) {
-                    wait_or_abort(sh, &sh.kv_full[stg], (b / kStages) & 1, &hdr->status);
-                    uint4 *vrow = reinterpret_cast<uint4 *>(smem + kOffV + stg * kTile + tok * 128);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) vrow[k] = make_uint4(0, 0, 0, 0);
-                }
-                uint8_t *phi = smem + kOffP + sb * 2 * kPTile;
-                uint8_t *plo = phi + kPTile;
-#pragma unroll
-                for (int c = 0; c < kNMax; c += 16) {
-                    if (c < n) {
-                        uint32_t wh[4], wl[4];
-#pragma unroll
-                        for (int k = 0; k < 16; k += 4) {
-                            float p[4], hi[4];
-#pragma unroll
-                            for (int e2 = 0; e2 < 4; ++e2) {
-                                const int cc = c + k + e2;
-                                p[e2] = (s[cc] == -INFINITY) ? 0.f : tc::ex2(s[cc] - sh.m_run[cc]) * kPScale;
-                                lsum[cc] += p[e2];
-                            }
-                            const uint16_t h01 = tc::f32x2_to_e4m3x2(p[1], p[0]);
-                            const uint16_t h23 = tc::f32x2_to_e4m3x2(p[3], p[2]);
-                            tc::e4m3x2_to_f32x2(h01, hi[1], hi[0]);
-                            tc::e4m3x2_to_f32x2(h23, hi[3], hi[2]);
-                            const uint16_t l01 = tc::f32x2_to_e4m3x2(p[1] - hi[1], p[0] - hi[0]);
-                            const uint16_t l23 = tc::f32x2_to_e4m3x2(p[3] - hi[3], p[2] - hi[2]);
-                            wh[k / 4] = static_cast<uint32_t>(h01) | (static_cast<uint32_t>(h23) << 16);
-                            wl[k / 4] = static_cast<uint32_t>(l01) | (static_cast<uint32_t>(l23) << 16);
-                        }
-                        const uint32_t off = tc::swz_offset(tok, c, n);
-                        *reinterpret_cast<uint4 *>(phi + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-                        *reinterpret_cast<uint4 *>(plo + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-                    }
-                }
-                tc::fence_proxy_async();
-                tc::mbar_arrive(&sh.p_full[sb]);
-            }
-            if (stop) break;
-            const uint32_t last = gb + un.count - 1;
+            const int nch = pow2_width(un.nt * a.G) / 16;
+            bool ok;
+            if (nch == 1) ok = unit_body<1>(c, a, un, gb);
+            else if (nch == 2) ok = unit_body<2>(c, a, un, gb);
+            else ok = unit_body<4>(c, a, un, gb);
+            if (!ok) break;
             gb += un.count;
-
-            // ---- row sums over all 128 token lanes
-#pragma unroll
-            for (int c = 0; c < kNMax; ++c) {
-                if (c < n) {
-                    float v = lsum[c];
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                    if (lane == 0) sh.red[sw][c] = v;
-                }
-            }
-            // ---- O of this unit (d lane = tok)
-            float o[kNMax];
-#pragma unroll
-            for (int c = 0; c < kNMax; ++c) o[c] = 0.f;
-            if (un.count > 0) {
-                wait_or_abort(sh, &sh.pv_done[last & 1], (last >> 1) & 1, &hdr->status);
-                tc::tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < kNMax / 16; ++c) {
-                    if (c < nchunks) {
-                        float v[16];
-                        tc::tmem_ld16(tmem_O + lane_base + c * 16, v);
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) o[c * 16 + k] = v[k];
-                    }
-                }
-                tc::tmem_wait_ld();
-                tc::tc_fence_before();
-            }
-            named_sync();
-            const int d = tok;
-            if (un.part_row < 0) {
-#pragma unroll
-                for (int c = 0; c < kNMax; ++c) {
-                    if (c < rows) {
-                        const float l = sh.red[0][c] + sh.red[1][c] + sh.red[2][c] + sh.red[3][c];
-                        const float val = (l > 0.f) ? o[c] * a.v_scale / l : 0.f;
-                        const int t = gr.t0 + c / a.G, g = c % a.G;
-                        a.out[t * a.o_s0 + (h * a.G + g) * a.o_s1 + d * a.o_s2] = __float2bfloat16_rn(val);
-                    }
-                }
-            } else {
-                // partial of a split pair: unnormalised O, offset and sum per row
-#pragma unroll
-                for (int c = 0; c < kNMax; ++c) {
-                    if (c < rows) {
-                        float *prow = partials + static_cast<int64_t>(un.part_row + c) * (kD + kPartialStride);
-                        prow[d] = o[c];
-                        if (d == 0) {
-                            prow[kD] = sh.m_run[c];
-                            prow[kD + 1] = sh.red[0][c] + sh.red[1][c] + sh.red[2][c] + sh.red[3][c];
-                        }
-                    }
-                }
-                __threadfence();
-                named_sync();
-                if (st_id == 0) {
-                    const int done = atomicAdd(&counters[un.pair], 1);
-                    sh.combine = (done == pr.n_units - 1);
-                }
-                named_sync();
-                if (sh.combine) {
-                    __threadfence();
-                    // the last unit of the pair to finish merges all of them
-                    for (int c = 0; c < rows; ++c) {
-                        float mstar = -INFINITY;
-                        for (int k = 0; k < pr.n_units; ++k) {
-                            const PlanUnit uk = units[pr.unit0 + k];
-                            const float *prow = partials + static_cast<int64_t>(uk.part_row + c) * (kD + kPartialStride);
-                            mstar = fmaxf(mstar, __ldcg(prow + kD));
-                        }
-                        float num = 0.f, den = 0.f;
-                        for (int k = 0; k < pr.n_units; ++k) {
-                            const PlanUnit uk = units[pr.unit0 + k];
-                            const float *prow = partials + static_cast<int64_t>(uk.part_row + c) * (kD + kPartialStride);
-                            const float mk = __ldcg(prow + kD);
-                            if (mk == -INFINITY) continue;
-                            const float wgt = tc::ex2(mk - mstar);
-                            num += wgt * __ldcg(prow + d);
-                            den += wgt * __ldcg(prow + kD + 1);
-                        }
-                        const float val = (den > 0.f) ? num * a.v_scale / den : 0.f;
-                        const int t = gr.t0 + c / a.G, g = c % a.G;
-                        a.out[t * a.o_s0 + (h * a.G + g) * a.o_s1 + d * a.o_s2] = __float2bfloat16_rn(val);
-                    }
-                }
-            }
             // unit-level abort decision, uniform over the four warps
-            if (lane == 0) sh.unit_vote[sw] = aborted(sh) ? 1 : 0;
+            if (lane == 0) sh.unit_vote[c.sw] = aborted(sh) ? 1 : 0;
             named_sync();
             stop = (sh.unit_vote[0] | sh.unit_vote[1] | sh.unit_vote[2] | sh.unit_vote[3]) != 0;
             named_sync();
+            u = u_next;
+            un = un_next;
         }
     }
 
@@ -667,7 +767,7 @@ cudaError_t launch_attention_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cu
     p.gmax = std::min(16, kNMax / G);
     p.P = a.P;
     p.num_ctas = dev.sms;
-    p.units_per_cta = 8;
+    p.units_per_cta = 4;
     p.ws = static_cast<char *>(ws);
     p.lay = lay;
     cudaError_t e = launch_plan(p, stream);

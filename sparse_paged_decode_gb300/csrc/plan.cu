@@ -228,15 +228,22 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanArgs a) {
     for (int p = tid; p < n_pairs; p += kPlanThreads) {
         const int n = pairs[p].n_blocks;
         const int u = max(1, (n + chunk - 1) / chunk);
-        const int rows_per_unit = groups[p / a.Hkv].nt * a.G;
+        const PlanGroup gr = groups[p / a.Hkv];
+        const int rows_per_unit = gr.nt * a.G;
         pairs[p].unit0 = u_off;
         pairs[p].n_units = u;
         for (int c = 0; c < u; ++c) {
             PlanUnit un;
-            un.pair = p;
-            un.first = static_cast<int>((static_cast<int64_t>(n) * c) / u);
-            un.count = static_cast<int>((static_cast<int64_t>(n) * (c + 1)) / u) - un.first;
+            const int first = static_cast<int>((static_cast<int64_t>(n) * c) / u);
+            un.entry = pairs[p].list + first;
+            un.count = static_cast<int>((static_cast<int64_t>(n) * (c + 1)) / u) - first;
             un.part_row = (u > 1) ? r_off + c * rows_per_unit : -1;
+            un.pair = p;
+            un.t0 = gr.t0;
+            un.nt = static_cast<int16_t>(gr.nt);
+            un.h = static_cast<int16_t>(p % a.Hkv);
+            un.part_base = (u > 1) ? r_off : -1;
+            un.n_split = u;
             units[u_off + c] = un;
         }
         u_off += u;

@@ -51,12 +51,19 @@ struct PlanEntry {
     uint16_t mask;  // bit j: row j of the group selected the block
 };
 
+// Everything a CTA needs about its work item, in one 32-byte record.
 struct PlanUnit {
-    int32_t pair;
-    int32_t first;     // first entry of the pair's list
-    int32_t count;     // entries
-    int32_t part_row;  // first partial row, -1 when the pair is not split
+    int32_t entry;      // first block-list entry (index into the entry array)
+    int32_t count;      // entries
+    int32_t part_row;   // first partial row, -1 when the pair is not split
+    int32_t pair;       // group * Hkv + kv head
+    int32_t t0;         // first query row of the group
+    int16_t nt;         // rows in the group
+    int16_t h;          // kv head
+    int32_t part_base;  // first partial row of the pair's first unit
+    int32_t n_split;    // units of the pair
 };
+static_assert(sizeof(PlanUnit) == 32, "unit record is 32 bytes");
 
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanMaxT = 4096;   // query rows the one-CTA planner handles

@@ -121,6 +121,17 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_
         : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem], kind::f16 (A and B both f16), one thread.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
+        : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread
 // has completed.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
@@ -172,9 +183,10 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
            (static_cast<uint64_t>(sw) << 61);
 }
 
-// Instruction descriptor of kind::f8f6f4 with E4M3 A and B, fp32 accumulate,
-// M = 128 and the given N; a_mn / b_mn select MN-major operands.
-__host__ __device__ constexpr uint32_t idesc_e4m3(uint32_t n, bool a_mn, bool b_mn) {
+// Instruction descriptor with fp32 accumulate, M = 128 and the given N;
+// a_mn / b_mn select MN-major operands.  Format code 0 for A and B means
+// E4M3 under kind::f8f6f4 and F16 under kind::f16.
+__host__ __device__ constexpr uint32_t idesc_m128(uint32_t n, bool a_mn, bool b_mn) {
     return (1u << 4)                              // D format: f32
            | (0u << 7) | (0u << 10)               // A, B: E4M3
            | (static_cast<uint32_t>(a_mn) << 15)  // A major
@@ -202,6 +214,18 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float hi, float lo) {
     return r;
 }
 
+// Four E4M3 bytes -> four f16 values scaled by 2^-8, exactly, by moving bits:
+// an E4M3 code s.eeee.mmm becomes the f16 s.0eeee.mmm0000000, whose value is
+// the E4M3 value times 2^-8 for normal and subnormal codes alike (the f16
+// exponent bias is 8 more than E4M3's).  Returns {bytes 0,1} and {bytes 2,3}
+// as f16x2 words, low byte in the low half.
+__device__ __forceinline__ void e4m3x4_to_f16x4_scaled(uint32_t x, uint32_t &lo, uint32_t &hi) {
+    const uint32_t w0 = __byte_perm(x, 0u, 0x4140);  // [b0, 0, b1, 0]
+    const uint32_t w1 = __byte_perm(x, 0u, 0x4342);  // [b2, 0, b3, 0]
+    lo = (w0 + (w0 & 0x00800080u)) << 7;
+    hi = (w1 + (w1 & 0x00800080u)) << 7;
+}
+
 // Packed E4M3x2 -> two fp32 (exact).
 __device__ __forceinline__ void e4m3x2_to_f32x2(uint16_t v, float &hi, float &lo) {
     uint32_t h2;
@@ -209,6 +233,12 @@ __device__ __forceinline__ void e4m3x2_to_f32x2(uint16_t v, float &hi, float &lo
     __half2 h = *reinterpret_cast<__half2 *>(&h2);
     hi = __high2float(h);
     lo = __low2float(h);
+}
+
+// Two fp32 -> f16x2 (round to nearest even); `lo` in the low half.
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
 }
 
 __device__ __forceinline__ float ex2(float x) {

@@ -147,10 +147,30 @@ SMALL = {
 }
 
 
+@pytest.fixture(params=[0, 1], ids=["auto_kernel", "general_kernel"])
+def kernel_policy(request, spd):
+    """Run a test through the default kernel choice and through the
+    general-layout kernel."""
+    old = spd.set_attention_kernel(request.param)
+    yield request.param
+    spd.set_attention_kernel(old)
+
+
 @pytest.mark.parametrize("name", sorted(SMALL))
-def test_small_cases(spd, orc, name):
+def test_small_cases(spd, orc, name, kernel_policy):
     w = W.make_decode(name, seed=zlib.crc32(name.encode()) % 1000, **SMALL[name])
     full_check(spd, orc, w)
+
+
+def test_large_logits(spd, orc, kernel_policy):
+    """Heavy-tailed queries scaled up: logits of tens of units and outputs
+    dominated by a few keys, where rounding of the queries or of the
+    probabilities shows first."""
+    w = W.make_decode("large", lengths=[3000, 1700, 600], tokens_per_request=[4, 8, 1], Hq=64, Hkv=8, D=128,
+                      Di=128, NB=32, P=64, K=8, seed=21, q_dist="student_t3")
+    w.q = (w.q.float() * 4.0).to(w.q.dtype)
+    res = full_check(spd, orc, w)
+    assert res["dense"][1] >= 0.9999
 
 
 def test_cfg1_tiny(spd, orc):

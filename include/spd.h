@@ -186,6 +186,36 @@ SPD_API void paged_decode_attention(const spd_tensor *q, const spd_tensor *k_cac
                             size_t workspace_bytes, spd_stream_t stream);
 
 /*
+ * paged_sparse_decode_attention without a caller-provided workspace.
+ *
+ * The pages have no counterpart to this call: it exists for callers that
+ * cannot allocate device memory -- for example a kernel slot inside a host
+ * engine that hands it only its input and output buffers and keeps every
+ * device allocation to its own memory planner, or code that must not call an
+ * allocator on its decode path.  Such a caller passes the same inputs and
+ * output as to paged_sparse_decode_attention and gets the same result; the
+ * scratch comes from a 16 MiB device array built into the library instead of
+ * the workspace argument.  The call allocates nothing.
+ *
+ * - Limit: shapes whose spd_decode_workspace_bytes(...) exceeds 16 MiB are
+ *   rejected with SPD_ERR_UNSUPPORTED (use the workspace entry point).
+ * - The array exists once per GPU on which this call is used and is held
+ *   until the process exits.
+ * - The first call on a device looks up the array's device address, with
+ *   that device current; make that first call before any stream capture.
+ * - Every call shares the one array and it keeps the last call's contents
+ *   (each call rewrites whatever it needs zeroed).  Calls that could run on
+ *   the GPU at the same time -- on different streams, or from different host
+ *   threads -- race on it: serialise them.
+ */
+SPD_API void paged_sparse_decode_attention_noalloc(const spd_tensor *q, const spd_tensor *k_cache,
+                                                   const spd_tensor *v_cache, const spd_tensor *block_table,
+                                                   const spd_tensor *seq_lens, const spd_tensor *req_idx,
+                                                   const spd_tensor *topk_idx, const spd_tensor *out,
+                                                   float sm_scale, int32_t block_size, float k_scale,
+                                                   float v_scale, spd_stream_t stream);
+
+/*
  * Workspace bytes the two attention calls need for T query rows, Hq q heads,
  * Hkv kv heads, head dim D and a page table of NB blocks.  Depends on these
  * capacities only (never on seq_lens or topk_idx), so one allocation serves

@@ -20,6 +20,7 @@ __all__ = [
     "msa_select_topk",
     "paged_sparse_decode_attention",
     "paged_decode_attention",
+    "paged_sparse_decode_attention_noalloc",
     "decode_workspace_bytes",
     "launch_count",
     "set_attention_kernel",

@@ -23,6 +23,7 @@ __all__ = [
     "msa_select_topk",
     "paged_sparse_decode_attention",
     "paged_decode_attention",
+    "paged_sparse_decode_attention_noalloc",
     "decode_workspace_bytes",
     "launch_count",
     "set_attention_kernel",
@@ -77,6 +78,8 @@ def _load():
     L.msa_select_topk.restype = None
     L.paged_sparse_decode_attention.argtypes = [P, P, P, P, P, P, P, P, f32, i32, f32, f32, vp, sz, vp]
     L.paged_sparse_decode_attention.restype = None
+    L.paged_sparse_decode_attention_noalloc.argtypes = [P, P, P, P, P, P, P, P, f32, i32, f32, f32, vp]
+    L.paged_sparse_decode_attention_noalloc.restype = None
     L.paged_decode_attention.argtypes = [P, P, P, P, P, P, P, f32, i32, f32, f32, vp, sz, vp]
     L.paged_decode_attention.restype = None
     L.spd_decode_workspace_bytes.argtypes = [ctypes.c_int64] * 5 + [i32]
@@ -159,6 +162,18 @@ def paged_sparse_decode_attention(q, k_cache, v_cache, block_table, seq_lens, re
         _desc(q, "q"), _desc(k_cache, "k_cache"), _desc(v_cache, "v_cache"), _desc(block_table, "block_table"),
         _desc(seq_lens, "seq_lens"), _desc(req_idx, "req_idx"), _desc(topk_idx, "topk_idx"), _desc(out, "out"),
         float(sm_scale), int(block_size), float(k_scale), float(v_scale), ws_ptr, ws_bytes, _stream(stream))
+    _check()
+
+
+def paged_sparse_decode_attention_noalloc(q, k_cache, v_cache, block_table, seq_lens, req_idx, topk_idx, out,
+                                          sm_scale, block_size, k_scale, v_scale, stream=None) -> None:
+    """Stage 3 for callers that cannot allocate: no workspace argument, the
+    library's built-in 16 MiB scratch is used instead (see include/spd.h for
+    its limit and its sharing rules)."""
+    lib.paged_sparse_decode_attention_noalloc(
+        _desc(q, "q"), _desc(k_cache, "k_cache"), _desc(v_cache, "v_cache"), _desc(block_table, "block_table"),
+        _desc(seq_lens, "seq_lens"), _desc(req_idx, "req_idx"), _desc(topk_idx, "topk_idx"), _desc(out, "out"),
+        float(sm_scale), int(block_size), float(k_scale), float(v_scale), _stream(stream))
     _check()
 
 

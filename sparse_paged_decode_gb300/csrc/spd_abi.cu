@@ -12,6 +12,7 @@
 
 #include <algorithm>
 #include <initializer_list>
+#include <mutex>
 
 #include "spd_internal.cuh"
 #include "spd_dispatch.h"
@@ -295,6 +296,45 @@ bool attention(const spd_tensor *q, const spd_tensor *k, const spd_tensor *v, co
 }  // namespace
 }  // namespace spd
 
+// ============================================ attention with built-in scratch
+//
+// Scratch for paged_sparse_decode_attention_noalloc: a fixed device array
+// that belongs to the library, so the caller never has to provide (or
+// allocate) a workspace.  It is created with the library's device code on each
+// GPU where the entry point is used and stays until the process exits.
+static constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace spd {
+namespace {
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[256] = {};
+
+// Device address of g_noalloc_scratch on the current device.  The name is
+// only a host-side stand-in for the array, so the address is looked up with
+// cudaGetSymbolAddress, once per device and with that device current.
+void *noalloc_scratch() {
+    int dev = 0;
+    if (!check_cuda(cudaGetDevice(&dev), "paged_sparse_decode_attention_noalloc: cudaGetDevice")) return nullptr;
+    if (dev < 0 || dev >= 256) {
+        fail(SPD_ERR_UNSUPPORTED, "paged_sparse_decode_attention_noalloc: device ordinal %d out of range", dev);
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        if (!check_cuda(cudaGetSymbolAddress(&p, g_noalloc_scratch),
+                        "paged_sparse_decode_attention_noalloc: cudaGetSymbolAddress"))
+            return nullptr;
+        g_noalloc_ptr[dev] = p;
+    }
+    return g_noalloc_ptr[dev];
+}
+
+}  // namespace
+}  // namespace spd
+
 // ======================================================================= ABI
 
 extern "C" {
@@ -325,6 +365,37 @@ void paged_sparse_decode_attention(const spd_tensor *q, const spd_tensor *k_cach
     spd::attention(q, k_cache, v_cache, block_table, seq_lens, req_idx, topk_idx, out, sm_scale, block_size,
                    k_scale, v_scale, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream),
                    "paged_sparse_decode_attention");
+}
+
+void paged_sparse_decode_attention_noalloc(const spd_tensor *q, const spd_tensor *k_cache,
+                                           const spd_tensor *v_cache, const spd_tensor *block_table,
+                                           const spd_tensor *seq_lens, const spd_tensor *req_idx,
+                                           const spd_tensor *topk_idx, const spd_tensor *out, float sm_scale,
+                                           int32_t block_size, float k_scale, float v_scale, spd_stream_t stream) {
+    spd::set_ok();
+    if (topk_idx == nullptr) {
+        spd::fail(SPD_ERR_INVALID_ARGUMENT, "topk_idx is NULL");
+        return;
+    }
+    if (q != nullptr && k_cache != nullptr && block_table != nullptr && q->ndim == 3 && k_cache->ndim == 3 &&
+        block_table->ndim == 2) {
+        const size_t need = spd_decode_workspace_bytes(q->shape[0], q->shape[1], k_cache->shape[1], q->shape[2],
+                                                       block_table->shape[1], block_size);
+        if (need > kNoAllocScratchBytes) {
+            spd::fail(SPD_ERR_UNSUPPORTED,
+                      "paged_sparse_decode_attention_noalloc: this shape needs %zu bytes of scratch, more than the "
+                      "%zu-byte scratch built into the library; use paged_sparse_decode_attention with a workspace",
+                      need, kNoAllocScratchBytes);
+            return;
+        }
+    }
+    void *ws = spd::noalloc_scratch();
+    if (ws == nullptr) return;
+    // everything the kernels need to start from zero (the per-pair merge
+    // counters, the status word) is written by this call's planner kernel
+    spd::attention(q, k_cache, v_cache, block_table, seq_lens, req_idx, topk_idx, out, sm_scale, block_size,
+                   k_scale, v_scale, ws, kNoAllocScratchBytes, reinterpret_cast<cudaStream_t>(stream),
+                   "paged_sparse_decode_attention_noalloc");
 }
 
 void paged_decode_attention(const spd_tensor *q, const spd_tensor *k_cache, const spd_tensor *v_cache,

@@ -58,21 +58,17 @@ constexpr int kNMax = 64;             // query rows per group (padded)
 constexpr int kMaxEntries = kPlanMaxNB;
 constexpr float kRaise = 6.0f;        // log2 headroom before the offset is raised (p <= 64)
 constexpr int kD = 128;
-constexpr int kTerms = 3;             // E4M3 terms per query element (12 significant bits)
+constexpr int kTerms = kQueryTerms;   // E4M3 terms per query element (12 significant bits)
 constexpr int kStride = kD + kPartialStride;
 
 struct TcArgs {
-    const void *q;
-    int64_t q_s0, q_s1, q_s2;
     const int32_t *ri;
     int64_t ri_s0;
     const int32_t *sl;
     int64_t sl_s0;
     __nv_bfloat16 *out;
     int64_t o_s0, o_s1, o_s2;
-    int32_t q_dt;
-    int32_t Hkv, G, R, NB;
-    float zscale;  // sm_scale * k_scale * log2(e)
+    int32_t T, Hq, Hkv, G, R, NB, gmax;
     float v_scale;
     char *ws;
     PlanLayout lay;
@@ -86,7 +82,9 @@ struct __align__(16) Shared {
     float red[4][kNMax];  // cross-warp reduction scratch
     uint64_t kv_full[kStages], kv_empty[kStages];
     uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2];
-    uint64_t q_full;
+    uint64_t q_full, q_empty, merge_bar;
+    uint64_t unit_full[4], unit_empty[4];  // ring of unit records, producer -> MMA, softmax
+    PlanUnit ring[4];
     uint32_t tmem_base;
     int abort;
     int combine;
@@ -110,7 +108,6 @@ constexpr int kOffP = kOffV16 + 2 * kV16Tile;
 constexpr int kOffShared = kOffP + 2 * kP16Tile;
 constexpr int kSmemBytes = kOffShared + static_cast<int>(sizeof(Shared)) + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-static_assert(kNMax * kD * 4 <= 2 * kP16Tile, "query staging fits in the P buffers");
 
 __device__ __forceinline__ int pow2_width(int n) { return n <= 16 ? 16 : n <= 32 ? 32 : 64; }
 
@@ -128,22 +125,6 @@ __device__ __forceinline__ bool wait_or_abort(Shared &sh, uint64_t *bar, uint32_
     *reinterpret_cast<volatile int *>(&sh.abort) = 1;
     atomicOr(status, 1);
     return false;
-}
-
-// x rounded to 3 fraction bits (4 significant bits), half away from zero:
-// exactly representable in E4M3 whenever |x| lies in its normal range.
-__device__ __forceinline__ float round4(float x) {
-    return __uint_as_float((__float_as_uint(x) + 0x00080000u) & 0xFFF00000u);
-}
-
-__device__ __forceinline__ PlanUnit load_unit(const PlanUnit *units, int u, int n_units) {
-    PlanUnit un{};
-    if (u < n_units) un = units[u];
-    return un;
-}
-
-__device__ __forceinline__ uint32_t pack4(uint16_t a, uint16_t b) {
-    return static_cast<uint32_t>(a) | (static_cast<uint32_t>(b) << 16);
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -169,112 +150,70 @@ struct Soft {
     int tok, lane, sw, st_id;
 };
 
-// Queries of the unit's group into the three E4M3 term buffers (B operand of
-// Q K^T): rows staged through shared memory with coalesced loads, then per
-// row a power-of-two scale into [128, 256) and x = t0 + t1 + t2, each term
-// the 4-significant-bit rounding of what the previous ones left.
-__device__ __noinline__ void prep_queries(const Soft &c, const TcArgs &a, const PlanUnit &un) {
+// The last unit of a split pair to finish merges all of them: the units'
+// partial rows are pulled into the idle f16 V / P buffers with bulk copies
+// (one wait for all of them), then per row the weights 2^(m_k - max m) and
+// every output element's weighted sum.
+__device__ __noinline__ void merge_partials(const Soft &c, const TcArgs &a, const PlanUnit &un,
+                                            uint32_t &merge_uses) {
     Shared &sh = *c.sh;
-    const int rows = un.nt * a.G;
-    float *stage = reinterpret_cast<float *>(c.smem + kOffP);  // [rows][128]; the P buffers are idle here
-    for (int r0 = 0; r0 < rows; r0 += 8) {
-        float v[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int row = r0 + k;
-            v[k] = 0.f;
-            if (row < rows) {
-                const int j = row / a.G, g = row % a.G;
-                v[k] = load_float(a.q, a.q_dt,
-                                  (un.t0 + j) * a.q_s0 + (un.h * a.G + g) * a.q_s1 + c.st_id * a.q_s2);
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            if (r0 + k < rows) stage[(r0 + k) * kD + c.st_id] = v[k];
-    }
-    named_sync();
-    uint8_t *qt = c.smem + kOffQ;
-    for (int row = c.sw; row < kNMax; row += 4) {
-        float x[4] = {0.f, 0.f, 0.f, 0.f};
-        if (row < rows) {
-            const float4 v = *reinterpret_cast<const float4 *>(stage + row * kD + c.lane * 4);
-            x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-        }
-        const float amax = warp_max(fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))));
-        float scale = 1.f;
-        if (amax > 0.f && amax < INFINITY) {
-            int ex;
-            frexpf(amax, &ex);
-            scale = ldexpf(1.f, 8 - ex);  // amax * scale in [128, 256)
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) x[e] *= scale;
-        const uint32_t off = tc::swz_offset(row, c.lane * 4, 128);
-#pragma unroll
-        for (int term = 0; term < kTerms; ++term) {
-            float t[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                t[e] = round4(x[e]);
-                x[e] -= t[e];
-            }
-            *reinterpret_cast<uint32_t *>(qt + term * kQBytes + off) =
-                pack4(tc::f32x2_to_e4m3x2(t[1], t[0]), tc::f32x2_to_e4m3x2(t[3], t[2]));
-        }
-        if (c.lane == 0) sh.cfac[row] = (row < rows) ? a.zscale / scale : 0.f;
-    }
-}
-
-// The last unit of a split pair to finish merges all of them: per-row weights
-// 2^(m_k - max m) into the (idle) P buffers, then every output element sums
-// its units' partials with all loads of a batch in flight together.
-__device__ __noinline__ void merge_partials(const Soft &c, const TcArgs &a, const PlanUnit &un) {
-    Shared &sh = *c.sh;
-    const int rows = un.nt * a.G;
-    const int ns = un.n_split;
-    float *wgt = reinterpret_cast<float *>(c.smem + kOffP);  // [ns][rows]
+    constexpr int kRowBytes = kStride * 4;
+    constexpr int kStageBytes = 2 * kV16Tile + 2 * kP16Tile;
+    const int rows = un.nt * a.G, ns = un.n_split;
+    uint8_t *stage = c.smem + kOffV16;
+    int R = rows;
+    while (R > 1 && ns * R * (kRowBytes + 4) > kStageBytes) R = (R + 1) / 2;
     const float *pbase = c.partials + static_cast<int64_t>(un.part_base) * kStride;
-    __threadfence();
-    for (int r = c.st_id; r < rows; r += kSoftThreads) {
-        float mstar = -INFINITY;
-        for (int k = 0; k < ns; ++k)
-            mstar = fmaxf(mstar, __ldcg(pbase + static_cast<int64_t>(k * rows + r) * kStride + kD));
-        float den = 0.f;
-        for (int k = 0; k < ns; ++k) {
-            const float *prow = pbase + static_cast<int64_t>(k * rows + r) * kStride;
-            const float mk = __ldcg(prow + kD);
-            const float w = (mk == -INFINITY) ? 0.f : tc::ex2(mk - mstar);
-            wgt[k * rows + r] = w;
-            den += w * __ldcg(prow + kD + 1);
-        }
-        sh.den[r] = den;
-    }
-    named_sync();
+    const float vs = a.v_scale * 256.f;
     const int d = c.tok;
-    for (int r0 = 0; r0 < rows; r0 += 8) {
-        float acc[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-        for (int k = 0; k < ns; ++k) {
-            float v[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                v[j] = (r0 + j < rows) ? __ldcg(pbase + static_cast<int64_t>(k * rows + r0 + j) * kStride + d) : 0.f;
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (r0 + j < rows) acc[j] += wgt[k * rows + r0 + j] * v[j];
+    for (int r0 = 0; r0 < rows; r0 += R) {
+        const int nr = min(R, rows - r0);
+        float *wts = reinterpret_cast<float *>(stage + ns * nr * kRowBytes);
+        if (c.st_id == 0) {
+            tc::fence_proxy_async_global();
+            tc::mbar_arrive_expect_tx(&sh.merge_bar, ns * nr * kRowBytes);
+            for (int k = 0; k < ns; ++k)
+                tc::bulk_load(stage + k * nr * kRowBytes, pbase + static_cast<int64_t>(k * rows + r0) * kStride,
+                              nr * kRowBytes, &sh.merge_bar);
         }
+        wait_or_abort(sh, &sh.merge_bar, merge_uses & 1, c.status);
+        ++merge_uses;
+        const float *st = reinterpret_cast<const float *>(stage);
+        // weights 2^(m_k - max_k m) and the normaliser, one row per thread
+        for (int r = c.st_id; r < nr; r += kSoftThreads) {
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            int k = 0;
+            for (; k + 4 <= ns; k += 4)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int r = r0 + j;
-            if (r < rows) {
-                const float den = sh.den[r];
-                const float val = (den > 0.f) ? acc[j] * (a.v_scale * 256.f) / den : 0.f;
-                const int t = un.t0 + r / a.G, g = r % a.G;
-                a.out[t * a.o_s0 + (un.h * a.G + g) * a.o_s1 + d * a.o_s2] = __float2bfloat16_rn(val);
+                for (int j = 0; j < 4; ++j) m4[j] = fmaxf(m4[j], st[((k + j) * nr + r) * kStride + kD]);
+            for (; k < ns; ++k) m4[0] = fmaxf(m4[0], st[(k * nr + r) * kStride + kD]);
+            const float mstar = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            float den = 0.f;
+            for (k = 0; k < ns; ++k) {
+                const float mk = st[(k * nr + r) * kStride + kD];
+                const float w = (mk == -INFINITY) ? 0.f : tc::ex2(mk - mstar);
+                wts[k * nr + r] = w;
+                den += w * st[(k * nr + r) * kStride + kD + 1];
             }
+            sh.den[r] = den;
         }
+        named_sync();
+        // each thread one d of every row; four independent partial sums
+        for (int r = 0; r < nr; ++r) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            int k = 0;
+            for (; k + 4 <= ns; k += 4)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    acc[j] = fmaf(wts[(k + j) * nr + r], st[((k + j) * nr + r) * kStride + d], acc[j]);
+            for (; k < ns; ++k) acc[0] = fmaf(wts[k * nr + r], st[(k * nr + r) * kStride + d], acc[0]);
+            const float den = sh.den[r];
+            const float sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+            const float val = (den > 0.f) ? sum * vs / den : 0.f;
+            const int t = un.t0 + (r0 + r) / a.G, g = (r0 + r) % a.G;
+            a.out[t * a.o_s0 + (un.h * a.G + g) * a.o_s1 + d * a.o_s2] = __float2bfloat16_rn(val);
+        }
+        named_sync();  // the stage is reused by the next chunk
     }
 }
 
@@ -477,18 +416,45 @@ __device__ __forceinline__ bool unit_body(const Soft &c, const TcArgs &a, const 
                 }
             }
         }
-        __threadfence();
+        tc::fence_proxy_async_global();  // the merge reads partials with bulk copies
         named_sync();
-        if (c.st_id == 0) sh.combine = (atomicAdd(&c.counters[un.pair], 1) == un.n_split - 1);
-        named_sync();
-        if (sh.combine) merge_partials(c, a, un);
     }
     return true;
 }
 
+// A split unit takes a ticket on its pair's counter once its partial is
+// written; whether it was the pair's last unit is looked at only after the
+// next unit (so the atomic's round trip is hidden), and the last one merges.
+struct PendingMerge {
+    PlanUnit un;
+    int ticket;  // thread st_id 0 only
+};
+
+__device__ __forceinline__ void take_ticket(const Soft &c, const PlanUnit &un, PendingMerge &pm) {
+    pm.un = un;
+    if (c.st_id == 0) {
+        __threadfence();  // the CTA's partial writes (ordered by the barrier) before the ticket
+        pm.ticket = atomicAdd(&c.counters[un.pair], 1);
+    }
+}
+
+__device__ __forceinline__ void resolve_ticket(const Soft &c, const TcArgs &a, PendingMerge &pm,
+                                               uint32_t &merge_uses) {
+    Shared &sh = *c.sh;
+    if (pm.un.pair < 0) return;
+    if (c.st_id == 0) {
+        sh.combine = (pm.ticket == pm.un.n_split - 1);
+        if (sh.combine) __threadfence();  // the other units' partials before the merge reads them
+    }
+    named_sync();
+    if (sh.combine) merge_partials(c, a, pm.un, merge_uses);
+    named_sync();
+    pm.un.pair = -1;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                    const TcArgs a) {
+                    const __grid_constant__ CUtensorMap tmap_q, const TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Shared &sh = *reinterpret_cast<Shared *>(smem + kOffShared);
@@ -510,7 +476,13 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
             tc::mbar_init(&sh.p_full[i], kSoftThreads);
             tc::mbar_init(&sh.pv_done[i], 1);
         }
-        tc::mbar_init(&sh.q_full, kSoftThreads);
+        tc::mbar_init(&sh.q_full, 1);
+        tc::mbar_init(&sh.q_empty, 1);
+        tc::mbar_init(&sh.merge_bar, 1);
+        for (int i = 0; i < 4; ++i) {
+            tc::mbar_init(&sh.unit_full[i], 1);
+            tc::mbar_init(&sh.unit_empty[i], 1 + kSoftThreads);
+        }
         sh.abort = 0;
         tc::fence_mbar_init();
     }
@@ -528,13 +500,41 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         if (lane == 0) {
             tc::prefetch_tmap(&tmap_k);
             tc::prefetch_tmap(&tmap_v);
+            tc::prefetch_tmap(&tmap_q);
             const uint64_t policy = tc::policy_evict_first();
-            uint32_t lb = 0;  // blocks loaded by this CTA
-            int u = blockIdx.x;
-            PlanUnit un = load_unit(units, u, n_units);
-            while (u < n_units && !aborted(sh)) {
-                const int u_next = u + gridDim.x;
-                const PlanUnit un_next = load_unit(units, u_next, n_units);
+            const uint32_t qbox = static_cast<uint32_t>(a.G * a.gmax * 128);
+            // Units are claimed from the global work counter (largest first
+            // as the plan orders them) and handed to the MMA and softmax roles
+            // through a 4-slot ring; claims run two units ahead so a record has
+            // arrived by the time it is published.
+            auto claim = [&]() -> PlanUnit {
+                PlanUnit x{};
+                x.pair = -1;
+                const int uu = atomicAdd(&hdr->next_unit, 1);
+                if (uu < n_units) x = units[uu];
+                return x;
+            };
+            auto publish = [&](uint32_t k, const PlanUnit &x) {
+                const int slot = k & 3;
+                if (k >= 4) wait_or_abort(sh, &sh.unit_empty[slot], ((k >> 2) - 1) & 1, &hdr->status);
+                sh.ring[slot] = x;
+                tc::mbar_arrive(&sh.unit_full[slot]);
+            };
+            uint32_t lb = 0, uc = 0;  // blocks and units loaded by this CTA
+            PlanUnit un = claim();
+            publish(0, un);
+            PlanUnit un_next = claim();
+            while (!aborted(sh)) {
+                publish(uc + 1, un_next);
+                const PlanUnit un_after = claim();  // in flight while this unit's loads are issued
+                if (un.pair < 0) break;
+                // the group's query terms, once the previous unit's last Q K^T is done
+                if (uc > 0 && !wait_or_abort(sh, &sh.q_empty, (uc - 1) & 1, &hdr->status)) break;
+                tc::mbar_arrive_expect_tx(&sh.q_full, kTerms * qbox);
+                for (int term = 0; term < kTerms; ++term)
+                    tc::tma_load_3d(smem + kOffQ + term * kQBytes, &tmap_q, &sh.q_full, 0, un.h * a.G,
+                                    term * a.T + un.t0, policy);
+                ++uc;
                 PlanEntry e_next{};
                 if (un.count > 0) e_next = lists[un.entry];
                 bool ok = true;
@@ -551,8 +551,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
                     tc::tma_load_3d(smem + kOffV + st * kTile, &tmap_v, &sh.kv_full[st], 0, un.h, e.page * 128, policy);
                 }
                 if (!ok) break;
-                u = u_next;
                 un = un_next;
+                un_next = un_after;
             }
             // let every issued copy land before the CTA may exit
             const uint32_t first = lb > kStages ? lb - kStages : 0;
@@ -566,11 +566,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
             const uint32_t sQ = tc::smem_u32(smem + kOffQ);
             const uint32_t sV16 = tc::smem_u32(smem + kOffV16);
             const uint32_t sP = tc::smem_u32(smem + kOffP);
-            int u = blockIdx.x;
-            PlanUnit un = load_unit(units, u, n_units);
-            while (u < n_units && !aborted(sh)) {
-                const int u_next = u + gridDim.x;
-                const PlanUnit un_next = load_unit(units, u_next, n_units);
+            while (!aborted(sh)) {
+                const int slot = uc & 3;
+                if (!wait_or_abort(sh, &sh.unit_full[slot], (uc >> 2) & 1, &hdr->status)) break;
+                const PlanUnit un = sh.ring[slot];
+                if (un.pair < 0) break;
                 const int n = pow2_width(un.nt * a.G);
                 const uint32_t idesc_qk = tc::idesc_m128(n, false, false);  // E4M3 x E4M3, both K-major
                 const uint32_t idesc_pv = tc::idesc_m128(n, true, true);    // F16 x F16, both MN-major
@@ -596,9 +596,13 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
                     return true;
                 };
                 bool ok = un.count == 0 || issue_qk(gb);
+                if (un.count <= 1) tc::mma_commit(&sh.q_empty);  // the unit's last Q K^T is issued
                 for (int i = 0; ok && i < un.count; ++i) {
                     const uint32_t b = gb + i;
-                    if (i + 1 < un.count && !issue_qk(b + 1)) { ok = false; break; }
+                    if (i + 1 < un.count) {
+                        if (!issue_qk(b + 1)) { ok = false; break; }
+                        if (i + 2 == un.count) tc::mma_commit(&sh.q_empty);
+                    }
                     const int sb = b & 1;
                     if (!wait_or_abort(sh, &sh.p_full[sb], (b >> 1) & 1, &hdr->status)) { ok = false; break; }
                     tc::tc_fence_after();
@@ -614,10 +618,9 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
                     tc::mma_commit(&sh.pv_done[sb]);
                 }
                 gb += un.count;
+                tc::mbar_arrive(&sh.unit_empty[slot]);
                 ++uc;
                 if (!ok) break;
-                u = u_next;
-                un = un_next;
             }
             if (gb > 0) tc::mbar_wait(&sh.pv_done[(gb - 1) & 1], ((gb - 1) >> 1) & 1);
         }
@@ -642,26 +645,49 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         c.tS0 = tmem_S0;
         c.tS1 = tmem_S1;
         c.tO = tmem_O;
-        uint32_t gb = 0;
+        uint32_t gb = 0, merge_uses = 0;
         bool stop = false;
+        const float *cfac = reinterpret_cast<const float *>(a.ws + a.lay.cfac);
 
-        int u = blockIdx.x;
-        PlanUnit un = load_unit(units, u, n_units);
-        while (u < n_units && !stop) {
-            const int u_next = u + gridDim.x;
-            const PlanUnit un_next = load_unit(units, u_next, n_units);
-            for (int i = c.st_id; i < un.count; i += kSoftThreads) sh.ent[i] = lists[un.entry + i];
-            if (c.st_id < 16) {
-                int r;
-                sh.Lj[c.st_id] = (c.st_id < un.nt) ? static_cast<int>(token_limit(a.ri, a.ri_s0, a.sl, a.sl_s0,
-                                                                                  un.t0 + c.st_id, a.R, a.NB, &r))
-                                                    : 0;
+        // per-unit metadata is loaded one unit ahead into registers: up to two
+        // list entries, one key limit and one logit factor per thread
+        PlanEntry pe0{}, pe1{};
+        int pL = 0;
+        float pcf = 0.f;
+        auto prefetch = [&](const PlanUnit &x) {
+            pe0 = (c.st_id < x.count) ? lists[x.entry + c.st_id] : PlanEntry{};
+            pe1 = (c.st_id + kSoftThreads < x.count) ? lists[x.entry + c.st_id + kSoftThreads] : PlanEntry{};
+            int r;
+            pL = (c.st_id < x.nt)
+                     ? static_cast<int>(token_limit(a.ri, a.ri_s0, a.sl, a.sl_s0, x.t0 + c.st_id, a.R, a.NB, &r))
+                     : 0;
+            pcf = (c.st_id < x.nt * a.G)
+                      ? cfac[static_cast<int64_t>(x.t0 + c.st_id / a.G) * a.Hq + x.h * a.G + c.st_id % a.G]
+                      : 0.f;
+        };
+        uint32_t uc = 0;
+        PendingMerge pending{};
+        pending.un.pair = -1;
+        PlanUnit un{};
+        un.pair = -1;
+        if (wait_or_abort(sh, &sh.unit_full[0], 0, c.status)) un = sh.ring[0];
+        if (un.pair >= 0) prefetch(un);
+        while (un.pair >= 0 && !stop) {
+            // the next unit's record (published by the producer before it issues
+            // this unit's loads) and its metadata, loaded during this unit
+            PlanUnit un_next{};
+            un_next.pair = -1;
+            if (wait_or_abort(sh, &sh.unit_full[(uc + 1) & 3], ((uc + 1) >> 2) & 1, c.status))
+                un_next = sh.ring[(uc + 1) & 3];
+            if (c.st_id < un.count) sh.ent[c.st_id] = pe0;
+            if (c.st_id + kSoftThreads < un.count) sh.ent[c.st_id + kSoftThreads] = pe1;
+            if (c.st_id < 16) sh.Lj[c.st_id] = pL;
+            if (c.st_id < kNMax) {
+                sh.cfac[c.st_id] = pcf;
+                sh.m_run[c.st_id] = -INFINITY;
             }
-            if (c.st_id < kNMax) sh.m_run[c.st_id] = -INFINITY;
-            prep_queries(c, a, un);
-            tc::fence_proxy_async();
             named_sync();
-            tc::mbar_arrive(&sh.q_full);
+            if (un_next.pair >= 0) prefetch(un_next);
 
             const int nch = pow2_width(un.nt * a.G) / 16;
             bool ok;
@@ -670,14 +696,18 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
             else ok = unit_body<4>(c, a, un, gb);
             if (!ok) break;
             gb += un.count;
+            resolve_ticket(c, a, pending, merge_uses);
+            if (un.part_row >= 0) take_ticket(c, un, pending);
+            tc::mbar_arrive(&sh.unit_empty[uc & 3]);
             // unit-level abort decision, uniform over the four warps
             if (lane == 0) sh.unit_vote[c.sw] = aborted(sh) ? 1 : 0;
             named_sync();
             stop = (sh.unit_vote[0] | sh.unit_vote[1] | sh.unit_vote[2] | sh.unit_vote[3]) != 0;
             named_sync();
-            u = u_next;
             un = un_next;
+            ++uc;
         }
+        if (!stop) resolve_ticket(c, a, pending, merge_uses);
     }
 
     tc::tc_fence_before();
@@ -709,6 +739,21 @@ bool make_tmap(CUtensorMap *m, const uint8_t *base, int64_t slots, int64_t hkv, 
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(hkv), static_cast<cuuint64_t>(slots)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(s1), static_cast<cuuint64_t>(s0)};
     cuuint32_t box[3] = {kD, 1, 128};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor map of the query terms qterms[term][t][hq][128 bytes]: box = the
+// gmax rows x G heads of one group for one term, 128-byte swizzle.
+bool make_tmap_q(CUtensorMap *m, const uint8_t *base, int64_t T, int64_t hq, int g, int gmax) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(hq),
+                          static_cast<cuuint64_t>(kTerms * T)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(hq * kD)};
+    cuuint32_t box[3] = {kD, static_cast<cuuint32_t>(g), static_cast<cuuint32_t>(gmax)};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -770,21 +815,29 @@ cudaError_t launch_attention_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cu
     p.units_per_cta = 4;
     p.ws = static_cast<char *>(ws);
     p.lay = lay;
-    cudaError_t e = launch_plan(p, stream);
+    p.q = a.q; p.q_s0 = a.q_s0; p.q_s1 = a.q_s1; p.q_s2 = a.q_s2;
+    p.q_dt = a.q_dt;
+    p.Hq = a.Hq;
+    p.zscale = a.sm_scale * a.k_scale * 1.4426950408889634f;
+
+    CUtensorMap tq;
+    if (!make_tmap_q(&tq, reinterpret_cast<const uint8_t *>(p.ws + lay.qterms), a.T, a.Hq, G, p.gmax))
+        return cudaSuccess;
+
+    const int64_t q_rows = static_cast<int64_t>(a.T) * a.Hq;
+    const int conv_ctas = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(dev.sms - 1, (q_rows + 31) / 32)));
+    cudaError_t e = launch_prepare(p, conv_ctas, stream);
     if (e != cudaSuccess) return e;
 
     TcArgs t{};
-    t.q = a.q; t.q_s0 = a.q_s0; t.q_s1 = a.q_s1; t.q_s2 = a.q_s2;
     t.ri = a.ri; t.ri_s0 = a.ri_s0;
     t.sl = a.sl; t.sl_s0 = a.sl_s0;
     t.out = a.out; t.o_s0 = a.o_s0; t.o_s1 = a.o_s1; t.o_s2 = a.o_s2;
-    t.q_dt = a.q_dt;
-    t.Hkv = a.Hkv; t.G = G; t.R = a.R; t.NB = a.NB;
-    t.zscale = a.sm_scale * a.k_scale * 1.4426950408889634f;
+    t.T = a.T; t.Hq = a.Hq; t.Hkv = a.Hkv; t.G = G; t.R = a.R; t.NB = a.NB; t.gmax = p.gmax;
     t.v_scale = a.v_scale;
     t.ws = static_cast<char *>(ws);
     t.lay = lay;
-    attention_tc_kernel<<<dev.sms, kThreads, kSmemBytes, stream>>>(tk, tv, t);
+    attention_tc_kernel<<<dev.sms, kThreads, kSmemBytes, stream>>>(tk, tv, tq, t);
     e = cudaGetLastError();
     if (e == cudaSuccess) *used = true;
     return e;

@@ -1,6 +1,7 @@
 // plan.cu -- the one-CTA device planner of the tensor-core decode attention
 // (see plan.cuh for what it builds).
 #include "plan.cuh"
+#include "tc_ptx.cuh"
 
 namespace spd {
 namespace {
@@ -67,7 +68,54 @@ __device__ int block_excl_max(int v, int *scratch) {
 // per-warp mask word for each block of the page table
 constexpr size_t kPlanSmem = sizeof(int) * 2 * kPlanMaxT + sizeof(uint32_t) * kWarps * kPlanMaxNB;
 
-__global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanArgs a) {
+// Query rows -> three E4M3 terms each (one warp per row, 4 elements a lane).
+__device__ void convert_queries(const PlanArgs &a) {
+    const int lane = threadIdx.x & 31;
+    const int warps = kWarps * (gridDim.x - 1);
+    const int64_t n_rows = static_cast<int64_t>(a.T) * a.Hq;
+    uint8_t *qt = reinterpret_cast<uint8_t *>(a.ws + a.lay.qterms);
+    float *cf = reinterpret_cast<float *>(a.ws + a.lay.cfac);
+    for (int64_t row = (blockIdx.x - 1) * kWarps + (threadIdx.x >> 5); row < n_rows; row += warps) {
+        const int64_t t = row / a.Hq, hq = row % a.Hq;
+        float x[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[e] = load_float(a.q, a.q_dt, t * a.q_s0 + hq * a.q_s1 + (lane * 4 + e) * a.q_s2);
+        float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+        float scale = 1.f;
+        if (amax > 0.f && amax < INFINITY) {
+            int ex;
+            frexpf(amax, &ex);
+            scale = ldexpf(1.f, 8 - ex);  // amax * scale in [128, 256)
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[e] *= scale;
+#pragma unroll
+        for (int term = 0; term < kQueryTerms; ++term) {
+            float v[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                v[e] = tc::round4(x[e]);
+                x[e] -= v[e];
+            }
+            *reinterpret_cast<uint32_t *>(qt + (term * n_rows + row) * 128 + lane * 4) =
+                tc::pack2x16(tc::f32x2_to_e4m3x2(v[1], v[0]), tc::f32x2_to_e4m3x2(v[3], v[2]));
+        }
+        if (lane == 0) cf[row] = a.zscale / scale;
+    }
+}
+
+__device__ void plan_body(const PlanArgs &a);
+
+__global__ void __launch_bounds__(kPlanThreads, 1) prepare_kernel(PlanArgs a) {
+    if (blockIdx.x == 0)
+        plan_body(a);
+    else
+        convert_queries(a);
+}
+
+__device__ void plan_body(const PlanArgs &a) {
     extern __shared__ int plan_smem[];
     int *s_r = plan_smem;
     int *s_L = plan_smem + kPlanMaxT;
@@ -258,22 +306,23 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanArgs a) {
         hdr->chunk = chunk;
         hdr->partial_rows = tot_rows;
         hdr->gmax = a.gmax;
+        hdr->next_unit = 0;
     }
 }
 
 }  // namespace
 
-cudaError_t launch_plan(const PlanArgs &a, cudaStream_t stream) {
+cudaError_t launch_prepare(const PlanArgs &a, int conv_ctas, cudaStream_t stream) {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (!attr_set[dev & 63]) {
-        cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(prepare_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(kPlanSmem));
         if (e != cudaSuccess) return e;
         attr_set[dev & 63] = true;
     }
-    plan_kernel<<<1, kPlanThreads, kPlanSmem, stream>>>(a);
+    prepare_kernel<<<1 + conv_ctas, kPlanThreads, kPlanSmem, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -27,7 +27,8 @@ struct PlanHeader {
     int32_t chunk;         // blocks per unit
     int32_t partial_rows;  // partial rows in use
     int32_t gmax;
-    int32_t reserved[57];
+    int32_t next_unit;     // work counter of the attention kernel (units claimed so far)
+    int32_t reserved[56];
 };
 static_assert(sizeof(PlanHeader) == 256, "header is one 256-byte line");
 
@@ -70,10 +71,11 @@ constexpr int kPlanMaxT = 4096;   // query rows the one-CTA planner handles
 constexpr int kPlanMaxNB = 256;   // page-table capacity of the fast path
 constexpr int kUnitExtra = 8192;
 constexpr int kPartialStride = 4; // floats after the D output values: max, sum, pad
+constexpr int kQueryTerms = 3;    // E4M3 terms per query element (12 significant bits)
 
 // Byte layout of the workspace for capacities (T, Hq, Hkv, D, NB).
 struct PlanLayout {
-    size_t header, groups, pairs, lists, units, counters, partials, total;
+    size_t header, groups, pairs, lists, units, counters, partials, qterms, cfac, total;
     int64_t unit_cap, rows_cap, pair_cap;
 
     __host__ __device__ static size_t align(size_t x) { return (x + 255) / 256 * 256; }
@@ -92,6 +94,8 @@ struct PlanLayout {
         units = off;    off += align(sizeof(PlanUnit) * (size_t)unit_cap);
         counters = off; off += align(sizeof(int32_t) * (size_t)(pair_cap > 0 ? pair_cap : 1));
         partials = off; off += align(sizeof(float) * (size_t)rows_cap * (size_t)(D + kPartialStride));
+        qterms = off;   off += align((size_t)kQueryTerms * (size_t)(T > 0 ? T : 1) * (size_t)Hq * (size_t)D);
+        cfac = off;     off += align(sizeof(float) * (size_t)(T > 0 ? T : 1) * (size_t)Hq);
         total = off;
     }
 };
@@ -111,8 +115,16 @@ struct PlanArgs {
     int32_t units_per_cta;
     char *ws;
     PlanLayout lay;
+    // query conversion (the other CTAs of the prepare launch)
+    const void *q;
+    int64_t q_s0, q_s1, q_s2;
+    int32_t q_dt, Hq;
+    float zscale;  // sm_scale * k_scale * log2(e)
 };
 
-cudaError_t launch_plan(const PlanArgs &a, cudaStream_t stream);
+// One launch: CTA 0 builds the plan; the other CTAs write each query row as
+// three E4M3 terms (qterms[term][t][hq][d], with the row scaled by a power of
+// two into [128, 256)) and its logit factor cfac[t][hq] = zscale / scale.
+cudaError_t launch_prepare(const PlanArgs &a, int conv_ctas, cudaStream_t stream);
 
 }  // namespace spd

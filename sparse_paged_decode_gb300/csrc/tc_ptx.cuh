@@ -14,6 +14,7 @@ namespace spd {
 namespace tc {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // give up on a barrier after 2 s
+constexpr uint32_t kSuspendHintNs = 20000;          // longest sleep inside one try_wait
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
@@ -45,14 +46,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+// Test for completion of the phase with the given parity; while it is not
+// complete the thread may sleep (up to the hint, in ns) instead of spinning,
+// so a waiting warp leaves its issue slots to the warps doing work.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return done != 0;
 }
@@ -62,9 +66,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 1;; ++i) {
+    for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
     }
 }
 
@@ -88,6 +92,21 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
+}
+
+// 1-D bulk copy global -> shared (size a multiple of 16, both addresses
+// 16-byte aligned), completing on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Order generic-proxy global writes / reads against async-proxy (bulk copy)
+// accesses of global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // Order this thread's generic-proxy shared-memory writes before later
@@ -239,6 +258,16 @@ __device__ __forceinline__ void e4m3x2_to_f32x2(uint16_t v, float &hi, float &lo
 __device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
     const __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// x rounded to 3 fraction bits (4 significant bits), half away from zero:
+// exactly representable in E4M3 whenever |x| lies in its normal range.
+__device__ __forceinline__ float round4(float x) {
+    return __uint_as_float((__float_as_uint(x) + 0x00080000u) & 0xFFF00000u);
+}
+
+__device__ __forceinline__ uint32_t pack2x16(uint16_t lo, uint16_t hi) {
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
 __device__ __forceinline__ float ex2(float x) {

@@ -249,6 +249,16 @@ SPD_API uint64_t spd_launch_count(void);
 SPD_API int spd_set_attention_kernel(int policy);
 
 /*
+ * Diagnostics: kernel selection per stage on this thread's subsequent calls.
+ * stage 1 = msa_block_score, 2 = msa_select_topk, 3 = the attention calls
+ * (the same setting as spd_set_attention_kernel).  policy 0 (default) picks
+ * the specialised kernel whenever the shapes and layouts allow it, 1 always
+ * the general-layout kernel.  Returns the previous setting, or -1 for an
+ * unknown stage.
+ */
+SPD_API int spd_set_kernel_policy(int stage, int policy);
+
+/*
  * Diagnostics: status word an attention call left in its workspace (0 = ok;
  * bit 0 = a device-side wait timed out and the call's output is not valid).
  * Synchronises with `stream` to read it -- never call it on a hot path.

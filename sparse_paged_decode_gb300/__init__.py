@@ -24,6 +24,7 @@ __all__ = [
     "decode_workspace_bytes",
     "launch_count",
     "set_attention_kernel",
+    "set_kernel_policy",
     "workspace_status",
     "library_path",
 ]

@@ -27,6 +27,7 @@ __all__ = [
     "decode_workspace_bytes",
     "launch_count",
     "set_attention_kernel",
+    "set_kernel_policy",
     "workspace_status",
     "library_path",
     "lib",
@@ -88,6 +89,8 @@ def _load():
     L.spd_last_error.restype = ctypes.c_int
     L.spd_set_attention_kernel.argtypes = [ctypes.c_int]
     L.spd_set_attention_kernel.restype = ctypes.c_int
+    L.spd_set_kernel_policy.argtypes = [ctypes.c_int, ctypes.c_int]
+    L.spd_set_kernel_policy.restype = ctypes.c_int
     L.spd_workspace_status.argtypes = [vp, vp]
     L.spd_workspace_status.restype = ctypes.c_int
     L.spd_launch_count.argtypes = []
@@ -200,6 +203,19 @@ def set_attention_kernel(policy: int) -> int:
     """0 = tensor-core kernel where it applies (default), 1 = general-layout
     kernel always.  Applies to this thread; returns the previous policy."""
     return int(lib.spd_set_attention_kernel(int(policy)))
+
+
+STAGE_SCORE, STAGE_SELECT, STAGE_ATTENTION = 1, 2, 3
+
+
+def set_kernel_policy(stage: int, policy: int) -> int:
+    """Kernel choice of one stage (1 score, 2 select, 3 attention) on this
+    thread: 0 = specialised kernel where it applies (default), 1 =
+    general-layout kernel always.  Returns the previous policy."""
+    old = int(lib.spd_set_kernel_policy(int(stage), int(policy)))
+    if old < 0:
+        raise ValueError("unknown stage %r" % (stage,))
+    return old
 
 
 def workspace_status(workspace, stream=None) -> int:

@@ -43,6 +43,7 @@
 #include "plan.cuh"
 #include "spd_internal.cuh"
 #include "tc_ptx.cuh"
+#include "tmap.cuh"
 
 namespace spd {
 
@@ -718,23 +719,10 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
 
 // ------------------------------------------------------------------ host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (fn == nullptr) {
-        cudaDriverEntryPointQueryResult q;
-        void *p = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
 // Tensor map of a [slots, Hkv, D] E4M3 cache: box = 128 tokens x D bytes of
 // one kv head, 128-byte swizzle.
 bool make_tmap(CUtensorMap *m, const uint8_t *base, int64_t slots, int64_t hkv, int64_t s0, int64_t s1) {
-    auto fn = encode_fn();
+    auto fn = tensor_map_encoder();
     if (fn == nullptr) return false;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(hkv), static_cast<cuuint64_t>(slots)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(s1), static_cast<cuuint64_t>(s0)};
@@ -748,7 +736,7 @@ bool make_tmap(CUtensorMap *m, const uint8_t *base, int64_t slots, int64_t hkv, 
 // Tensor map of the query terms qterms[term][t][hq][128 bytes]: box = the
 // gmax rows x G heads of one group for one term, 128-byte swizzle.
 bool make_tmap_q(CUtensorMap *m, const uint8_t *base, int64_t T, int64_t hq, int g, int gmax) {
-    auto fn = encode_fn();
+    auto fn = tensor_map_encoder();
     if (fn == nullptr) return false;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(hq),
                           static_cast<cuuint64_t>(kTerms * T)};

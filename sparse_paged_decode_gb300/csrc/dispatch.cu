@@ -15,32 +15,42 @@ std::atomic<uint64_t> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
 uint64_t launch_count() { return g_launches.load(std::memory_order_relaxed); }
 
+cudaError_t launch_score_tc(const ScoreArgs &a, cudaStream_t stream, bool *used);
+cudaError_t launch_attention_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cudaStream_t stream, bool *used);
+
+namespace {
+// per stage (index = spd stage code): 0 fastest kernel the shapes allow,
+// 1 the general-layout kernel
+thread_local int g_policy[4] = {0, 0, 0, 0};
+}
+
+int set_kernel_policy(int stage, int policy) {
+    if (stage < 1 || stage > 3) return -1;
+    const int old = g_policy[stage];
+    g_policy[stage] = policy;
+    return old;
+}
+
 cudaError_t dispatch_score(const ScoreArgs &a, cudaStream_t stream) {
     count_launches(1);
+    bool used = false;
+    if (g_policy[1] == 0) {
+        cudaError_t e = launch_score_tc(a, stream, &used);
+        if (e != cudaSuccess || used) return e;
+    }
     return launch_score_generic(a, stream);
 }
 
 cudaError_t dispatch_select(const SelectArgs &a, cudaStream_t stream) {
     count_launches(1);
+    if (g_policy[2] == 0) return launch_select_rank(a, stream);
     return launch_select_generic(a, stream);
-}
-
-cudaError_t launch_attention_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cudaStream_t stream, bool *used);
-
-namespace {
-thread_local int g_attention_policy = 0;
-}
-
-int set_attention_policy(int policy) {
-    const int old = g_attention_policy;
-    g_attention_policy = policy;
-    return old;
 }
 
 cudaError_t dispatch_attention(const AttnArgs &a, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
     bool used = false;
     cudaError_t e = cudaSuccess;
-    if (g_attention_policy == 0) e = launch_attention_tc(a, workspace, workspace_bytes, stream, &used);
+    if (g_policy[3] == 0) e = launch_attention_tc(a, workspace, workspace_bytes, stream, &used);
     if (e != cudaSuccess) return e;
     if (used) {
         count_launches(2);  // planner + attention

@@ -97,6 +97,61 @@ select_generic_kernel(SelectArgs a) {
     for (int k = n_cand + lane; k < a.K; k += 32) a.o[h * a.o_s0 + t * a.o_s1 + k * a.o_s2] = -1;
 }
 
+// The same ranks with the row held once per warp in shared memory (padded to
+// a multiple of 4 with -inf, non-candidates stored as -inf) and compared in
+// registers: each lane owns up to 8 candidates per pass and streams the row
+// as broadcast float4 reads, so a comparison is a few ALU instructions.
+constexpr int kSelectPer = 4;
+
+__global__ void __launch_bounds__(kSelectWarps * 32)
+select_rank_kernel(SelectArgs a, int nb4) {
+    extern __shared__ float4 rows4[];  // [kSelectWarps][nb4]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kSelectWarps + warp;
+    if (row >= a.Hi * a.T) return;
+    const int h = row / a.T, t = row % a.T;
+    float4 *s4 = rows4 + warp * nb4;
+    float *s = reinterpret_cast<float *>(s4);
+    int n_cand = 0;
+    for (int b = lane; b < 4 * nb4; b += 32) {
+        float v = -INFINITY;
+        if (b < a.NB) {
+            v = a.s[h * a.s_s0 + t * a.s_s1 + b * a.s_s2];
+            if (!is_candidate(v)) v = -INFINITY;
+        }
+        n_cand += v != -INFINITY;
+        s[b] = v;
+    }
+    __syncwarp();
+    int32_t *o = a.o + h * a.o_s0 + t * a.o_s1;
+    for (int base = 0; base < a.NB; base += 32 * kSelectPer) {
+        float vi[kSelectPer];
+        int ii[kSelectPer], rank[kSelectPer];
+#pragma unroll
+        for (int p = 0; p < kSelectPer; ++p) {
+            ii[p] = base + p * 32 + lane;
+            vi[p] = ii[p] < a.NB ? s[ii[p]] : -INFINITY;
+            rank[p] = 0;
+        }
+        for (int j4 = 0; j4 < nb4; ++j4) {
+            const float4 v = s4[j4];
+            const float vj[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = 4 * j4 + e;
+#pragma unroll
+                for (int p = 0; p < kSelectPer; ++p)
+                    rank[p] += (vj[e] > vi[p]) | ((vj[e] == vi[p]) & (j < ii[p]));
+            }
+        }
+#pragma unroll
+        for (int p = 0; p < kSelectPer; ++p)
+            if (vi[p] != -INFINITY && rank[p] < a.K) o[rank[p] * a.o_s2] = ii[p];
+    }
+    n_cand = warp_sum(n_cand);
+    for (int k = n_cand + lane; k < a.K; k += 32) o[k * a.o_s2] = -1;
+}
+
 // ------------------------------------------------------------------ stage 3
 // "Kernel ABI" -- attention.decode.  One CTA per (query token t, kv head h)
 // serves the G = Hq/Hkv q heads of that kv head.  Blocks are visited in
@@ -230,6 +285,14 @@ attention_generic_kernel(AttnArgs a) {
 cudaError_t launch_score_generic(const ScoreArgs &a, cudaStream_t stream) {
     dim3 grid(a.T, (a.NB + kScoreWarps - 1) / kScoreWarps, a.Hi);
     score_generic_kernel<<<grid, kScoreWarps * 32, a.Di * sizeof(float), stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_select_rank(const SelectArgs &a, cudaStream_t stream) {
+    const int rows = a.Hi * a.T;
+    const int nb4 = (a.NB + 3) / 4;
+    dim3 grid((rows + kSelectWarps - 1) / kSelectWarps);
+    select_rank_kernel<<<grid, kSelectWarps * 32, kSelectWarps * nb4 * sizeof(float4), stream>>>(a, nb4);
     return cudaGetLastError();
 }
 

@@ -1,0 +1,368 @@
+// score_tc.cu -- the block-max score sheet ("Kernel ABI" --
+// attention.msa_block_score / attention.msa_prefill_block_score) on the
+// sm_103a tensor cores, for bf16 / f16 index tensors with Di a multiple of 64
+// (at most 256).
+//
+// Orientation.  A CTA owns a tile of query lanes -- up to 128 (token, index
+// head) pairs, head fastest -- and a chunk of block ids.  Per block and per
+// run of consecutive lanes that read the same block-table row, one
+// tcgen05.mma kind::f16 (fp32 accumulate, M = 128 query lanes, N = 128 keys
+// of the block, K = Di) leaves that block's dot products in tensor memory
+// with one query lane per TMEM lane.  The block maximum of a lane is then a
+// reduction over its own 128 columns inside one thread: no shuffles, and the
+// key mask (tokens at or beyond the lane's seq_len) is a column bound.
+//
+// Keys are TMA-loaded straight from the paged index cache through the block
+// table (128 tokens x 64 elements per box, 128-byte swizzle), double
+// buffered; the two TMEM accumulators let the epilogue of one block overlap
+// the product of the next.  Cells with no valid key are written -inf up front
+// by the lane's own thread; a timed-out wait (a fault, never expected) leaves
+// NaN in the cells it could not compute.
+#include <math.h>
+
+#include "spd_internal.cuh"
+#include "tc_ptx.cuh"
+#include "tmap.cuh"
+
+namespace spd {
+
+cudaError_t launch_score_tc(const ScoreArgs &a, cudaStream_t stream, bool *used);
+
+namespace {
+
+constexpr int kLanes = 128;       // query lanes per tile (M)
+constexpr int kKeyStages = 2;
+constexpr int kMaxChunk = 8;      // block ids per CTA
+constexpr int kThreadsSc = 192;   // warps 0-3 epilogue (TMEM quadrants), 4 TMA, 5 MMA
+constexpr int kAtom = 128 * 128;  // one 64-element column chunk of 128 rows, bytes
+
+struct ScoreTcArgs {
+    const int32_t *bt;
+    int64_t bt_s0, bt_s1;
+    const int32_t *sl;
+    int64_t sl_s0;
+    const int32_t *ri;
+    int64_t ri_s0;
+    float *out;
+    int64_t o_s0, o_s1, o_s2;
+    int32_t T, Hi, Di, R, NB, tq, chunk;
+    int64_t P;
+    float idx_scale;
+    uint32_t idesc;
+};
+
+struct ScoreShared {
+    uint64_t q_full, k_full[kKeyStages], k_empty[kKeyStages], acc_full[2], acc_empty[2];
+    uint32_t tmem_base;
+    int abort;
+    int n_steps;
+    int warp_starts[4];
+    int lane_r[kLanes];
+    int run_r[kLanes], run_lo[kLanes], run_hi[kLanes], run_lim[kLanes];
+    int step_page[kMaxChunk * kLanes];
+    uint16_t step_run[kMaxChunk * kLanes];
+    uint8_t step_b[kMaxChunk * kLanes];
+};
+
+// All 32 lanes wait; the warp goes on only if every lane saw the phase.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, tc::mbar_wait(bar, parity));
+}
+
+__global__ void __launch_bounds__(kThreadsSc)
+score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                const ScoreTcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int nkc = a.Di / 64;
+    uint8_t *sQ = smem;
+    uint8_t *sK = smem + nkc * kAtom;  // stage s at sK + s * nkc * kAtom
+    ScoreShared &sh = *reinterpret_cast<ScoreShared *>(sK + kKeyStages * nkc * kAtom);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int t0 = blockIdx.x * a.tq;
+    const int b0 = blockIdx.y * a.chunk;
+    const int nb = min(a.chunk, a.NB - b0);
+
+    if (tid == 0) {
+        tc::mbar_init(&sh.q_full, 1);
+        for (int i = 0; i < kKeyStages; ++i) {
+            tc::mbar_init(&sh.k_full[i], 1);
+            tc::mbar_init(&sh.k_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&sh.acc_full[i], 1);
+            tc::mbar_init(&sh.acc_empty[i], kLanes);
+        }
+        sh.abort = 0;
+        sh.n_steps = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 5) tc::tmem_alloc(&sh.tmem_base, 256);  // two 128-column accumulators
+
+    // ---- lanes: (token t, head h) of each TMEM lane and its key limit
+    const bool is_lane = tid < kLanes;
+    const int tl = tid / a.Hi, h = tid % a.Hi, t = t0 + tl;
+    const bool lane_row = is_lane && tl < a.tq && t < a.T;
+    int my_r = -1;
+    int my_lim = 0;
+    if (lane_row) {
+        int r;
+        my_lim = static_cast<int>(token_limit(a.ri, a.ri_s0, a.sl, a.sl_s0, t, a.R, a.NB, &r));
+        if (my_lim > 0) my_r = r;
+    }
+    if (is_lane) sh.lane_r[tid] = my_r;
+    __syncthreads();
+
+    // ---- runs: maximal spans of consecutive lanes with one block-table row
+    const bool start = is_lane && my_r >= 0 && (tid == 0 || sh.lane_r[tid - 1] != my_r);
+    const unsigned starts = __ballot_sync(0xffffffffu, start);
+    if (lane == 0 && warp < 4) sh.warp_starts[warp] = __popc(starts);
+    __syncthreads();
+    int n_runs = 0, run_base = 0;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        if (w < warp) run_base += sh.warp_starts[w];
+        n_runs += sh.warp_starts[w];
+    }
+    const int my_run = my_r >= 0 ? run_base + __popc(starts & ((2u << lane) - 1u)) - 1 : -1;
+    if (start) {
+        sh.run_r[my_run] = my_r;
+        sh.run_lo[my_run] = tid;
+        sh.run_hi[my_run] = 0;
+        sh.run_lim[my_run] = 0;
+    }
+    __syncthreads();
+    if (my_run >= 0) {
+        atomicMax(&sh.run_hi[my_run], tid + 1);
+        atomicMax(&sh.run_lim[my_run], my_lim);
+    }
+    // cells with no valid key: -inf now (the lane's own thread)
+    if (lane_row) {
+        for (int bl = 0; bl < nb; ++bl) {
+            const int b = b0 + bl;
+            bool empty = my_r < 0 || static_cast<int64_t>(b) * kBlock >= my_lim;
+            if (!empty) {
+                const int64_t page = a.bt[my_r * a.bt_s0 + b * a.bt_s1];
+                empty = page < 0 || page >= a.P;
+            }
+            if (empty) a.out[h * a.o_s0 + t * a.o_s1 + b * a.o_s2] = -INFINITY;
+        }
+    }
+    __syncthreads();
+    // ---- steps: (block, run) pairs with a valid page and some valid key
+    for (int idx = tid; idx < nb * n_runs; idx += kThreadsSc) {
+        const int bl = idx / n_runs, j = idx % n_runs;
+        const int b = b0 + bl;
+        if (static_cast<int64_t>(b) * kBlock >= sh.run_lim[j]) continue;
+        const int64_t page = a.bt[sh.run_r[j] * a.bt_s0 + b * a.bt_s1];
+        if (page < 0 || page >= a.P) continue;
+        const int s = atomicAdd(&sh.n_steps, 1);
+        sh.step_page[s] = static_cast<int>(page);
+        sh.step_run[s] = static_cast<uint16_t>(j);
+        sh.step_b[s] = static_cast<uint8_t>(bl);
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const int n_steps = sh.n_steps;
+    const uint32_t tmem = sh.tmem_base;
+
+    if (warp == 4) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0 && n_steps > 0) {
+            tc::prefetch_tmap(&tmap_q);
+            tc::prefetch_tmap(&tmap_k);
+            tc::mbar_arrive_expect_tx(&sh.q_full, static_cast<uint32_t>(nkc * a.tq * a.Hi * 128));
+            for (int c = 0; c < nkc; ++c) tc::tma_load_3d(sQ + c * kAtom, &tmap_q, &sh.q_full, c * 64, 0, t0);
+            int s = 0;
+            for (; s < n_steps; ++s) {
+                const int st = s % kKeyStages;
+                if (s >= kKeyStages && !tc::mbar_wait(&sh.k_empty[st], ((s / kKeyStages) - 1) & 1)) {
+                    *reinterpret_cast<volatile int *>(&sh.abort) = 1;
+                    break;
+                }
+                uint8_t *dst = sK + st * nkc * kAtom;
+                tc::mbar_arrive_expect_tx(&sh.k_full[st], static_cast<uint32_t>(nkc * kAtom));
+                for (int c = 0; c < nkc; ++c)
+                    tc::tma_load_2d(dst + c * kAtom, &tmap_k, &sh.k_full[st], c * 64, sh.step_page[s] * kBlock);
+            }
+            // every issued copy lands before the CTA may exit
+            tc::mbar_wait(&sh.q_full, 0);
+            for (int u = s > kKeyStages ? s - kKeyStages : 0; u < s; ++u)
+                tc::mbar_wait(&sh.k_full[u % kKeyStages], (u / kKeyStages) & 1);
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0 && n_steps > 0) {
+            const uint32_t q_base = tc::smem_u32(sQ), k_base = tc::smem_u32(sK);
+            bool ok = tc::mbar_wait(&sh.q_full, 0);
+            int s = 0;
+            for (; ok && s < n_steps; ++s) {
+                const int st = s % kKeyStages, buf = s & 1;
+                ok = tc::mbar_wait(&sh.k_full[st], (s / kKeyStages) & 1);
+                if (ok && s >= 2) ok = tc::mbar_wait(&sh.acc_empty[buf], ((s >> 1) - 1) & 1);
+                if (!ok) break;
+                tc::tc_fence_after();
+                const uint32_t kb = k_base + st * nkc * kAtom;
+                for (int kc = 0; kc < a.Di / 16; ++kc) {
+                    const uint32_t off = (kc >> 2) * kAtom + (kc & 3) * 32;
+                    tc::mma_f16(tmem + buf * 128, tc::smem_desc(q_base + off, 16, 1024, tc::kSw128),
+                                tc::smem_desc(kb + off, 16, 1024, tc::kSw128), a.idesc, kc > 0);
+                }
+                tc::mma_commit(&sh.k_empty[st]);
+                tc::mma_commit(&sh.acc_full[buf]);
+            }
+            if (!ok) *reinterpret_cast<volatile int *>(&sh.abort) = 1;
+            // the issued products complete before TMEM is released
+            if (s > 0) tc::mbar_wait(&sh.acc_full[(s - 1) & 1], ((s - 1) >> 1) & 1);
+        }
+    } else {
+        // --------------------------------------------------------- epilogue
+        // Each warp reads its TMEM lane quadrant; a lane's block maximum is a
+        // reduction over its own row of 128 key columns.
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        bool ok = true;
+        for (int s = 0; s < n_steps; ++s) {
+            const int buf = s & 1, j = sh.step_run[s];
+            const int b = b0 + sh.step_b[s];
+            const int lo = sh.run_lo[j], hi = sh.run_hi[j];
+            const int lim = my_lim - b * kBlock;
+            const bool mine = tid >= lo && tid < hi && lim > 0;
+            if (ok) ok = warp_wait(&sh.acc_full[buf], (s >> 1) & 1);
+            if (!ok) {
+                if (mine) a.out[h * a.o_s0 + t * a.o_s1 + b * a.o_s2] = NAN;
+                continue;
+            }
+            tc::tc_fence_after();
+            if (hi > warp * 32 && lo < warp * 32 + 32) {
+                float best = -INFINITY;
+                const uint32_t base = tmem + buf * 128 + lane_base;
+#pragma unroll
+                for (int c0 = 0; c0 < 128; c0 += 32) {
+                    float v0[16], v1[16];
+                    tc::tmem_ld16(base + c0, v0);
+                    tc::tmem_ld16(base + c0 + 16, v1);
+                    tc::tmem_wait_ld();
+                    if (lim >= 128) {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) best = fmaxf(best, fmaxf(v0[k], v1[k]));
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            if (c0 + k < lim) best = fmaxf(best, v0[k]);
+                            if (c0 + 16 + k < lim) best = fmaxf(best, v1[k]);
+                        }
+                    }
+                }
+                if (mine)
+                    a.out[h * a.o_s0 + t * a.o_s1 + b * a.o_s2] = (best == -INFINITY) ? -INFINITY : best * a.idx_scale;
+            }
+            tc::tc_fence_before();
+            tc::mbar_arrive(&sh.acc_empty[buf]);
+        }
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    if (warp == 5) tc::tmem_dealloc(tmem, 256);
+}
+
+bool make_tmap_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
+                  uint32_t box_rows) {
+    auto fn = tensor_map_encoder();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// q_idx [T, Hi, Di] as a 3-D map: box = 64 elements x Hi heads x tq tokens,
+// which lands as tq*Hi rows of 128 bytes (head fastest).
+bool make_tmap_qidx(CUtensorMap *m, const ScoreArgs &a, int tq) {
+    auto fn = tensor_map_encoder();
+    if (fn == nullptr) return false;
+    const uint64_t s1 = a.Hi > 1 ? static_cast<uint64_t>(a.q_s1) * 2 : static_cast<uint64_t>(a.Di) * 2;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(a.Di), static_cast<cuuint64_t>(a.Hi),
+                          static_cast<cuuint64_t>(a.T)};
+    cuuint64_t strides[2] = {s1, static_cast<cuuint64_t>(a.q_s0) * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(a.Hi), static_cast<cuuint32_t>(tq)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(a.q), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct ScoreDevice {
+    int sms = 0;
+    bool attr_set = false;
+};
+
+}  // namespace
+
+// Covers: q_idx and k_idx_cache both bf16 or both f16, Di in {64, 128, 192,
+// 256}, Hi <= 128, innermost strides 1, 16-byte aligned bases and row
+// strides, at most 2^31 cache slots.  Anything else: *used stays false.
+cudaError_t launch_score_tc(const ScoreArgs &a, cudaStream_t stream, bool *used) {
+    *used = false;
+    if (a.q_dt != a.k_dt || (a.q_dt != SPD_BF16 && a.q_dt != SPD_F16)) return cudaSuccess;
+    if (a.Di % 64 != 0 || a.Di > 256 || a.Hi > kLanes || a.Hi < 1) return cudaSuccess;
+    if (a.q_s2 != 1 || a.k_s2 != 1) return cudaSuccess;
+    if ((reinterpret_cast<uintptr_t>(a.q) % 16) || (reinterpret_cast<uintptr_t>(a.k) % 16)) return cudaSuccess;
+    if (a.q_s0 <= 0 || (a.q_s0 * 2) % 16 || a.k_s0 <= 0 || (a.k_s0 * 2) % 16) return cudaSuccess;
+    if (a.Hi > 1 && (a.q_s1 <= 0 || (a.q_s1 * 2) % 16)) return cudaSuccess;
+    if (a.P * kBlock > (int64_t(1) << 31) - 1) return cudaSuccess;
+
+    static ScoreDevice devs[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    ScoreDevice &d = devs[dev & 63];
+    if (d.sms == 0) {
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (d.sms <= 0) d.sms = 1;
+    }
+    const int nkc = a.Di / 64;
+    const int smem = static_cast<int>(1024 + nkc * kAtom * (1 + kKeyStages) + sizeof(ScoreShared));
+    if (!d.attr_set) {
+        const int smem_max = static_cast<int>(1024 + 4 * kAtom * (1 + kKeyStages) + sizeof(ScoreShared));
+        cudaError_t e = cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+        if (e != cudaSuccess) return e;
+        d.attr_set = true;
+    }
+
+    const int tq = kLanes / a.Hi;
+    const int64_t n_tiles = (a.T + tq - 1) / tq;
+    int64_t chunk = (n_tiles * a.NB + 2 * d.sms - 1) / (2 * d.sms);
+    chunk = chunk < 1 ? 1 : chunk > kMaxChunk ? kMaxChunk : chunk;
+    const int64_t n_chunks = (a.NB + chunk - 1) / chunk;
+    if (n_tiles > INT32_MAX) return cudaSuccess;
+
+    CUtensorMap tq_map, tk_map;
+    if (!make_tmap_qidx(&tq_map, a, tq)) return cudaSuccess;
+    if (!make_tmap_2d(&tk_map, a.k, static_cast<uint64_t>(a.Di), static_cast<uint64_t>(a.P * kBlock),
+                      static_cast<uint64_t>(a.k_s0) * 2, kBlock))
+        return cudaSuccess;
+
+    ScoreTcArgs t{};
+    t.bt = a.bt; t.bt_s0 = a.bt_s0; t.bt_s1 = a.bt_s1;
+    t.sl = a.sl; t.sl_s0 = a.sl_s0;
+    t.ri = a.ri; t.ri_s0 = a.ri_s0;
+    t.out = a.out; t.o_s0 = a.o_s0; t.o_s1 = a.o_s1; t.o_s2 = a.o_s2;
+    t.T = a.T; t.Hi = a.Hi; t.Di = a.Di; t.R = a.R; t.NB = a.NB;
+    t.tq = tq;
+    t.chunk = static_cast<int32_t>(chunk);
+    t.P = a.P;
+    t.idx_scale = a.idx_scale;
+    t.idesc = tc::idesc_f16_m128(128, a.q_dt == SPD_BF16);
+    dim3 grid(static_cast<unsigned>(n_tiles), static_cast<unsigned>(n_chunks));
+    score_tc_kernel<<<grid, kThreadsSc, smem, stream>>>(tq_map, tk_map, t);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) *used = true;
+    return e;
+}
+
+}  // namespace spd

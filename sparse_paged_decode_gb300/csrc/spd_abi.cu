@@ -423,7 +423,9 @@ int spd_last_error(char *msg, size_t cap) {
 
 uint64_t spd_launch_count(void) { return spd::launch_count(); }
 
-int spd_set_attention_kernel(int policy) { return spd::set_attention_policy(policy); }
+int spd_set_attention_kernel(int policy) { return spd::set_kernel_policy(3, policy); }
+
+int spd_set_kernel_policy(int stage, int policy) { return spd::set_kernel_policy(stage, policy); }
 
 int spd_workspace_status(const void *workspace, spd_stream_t stream) {
     return spd::workspace_status(workspace, reinterpret_cast<cudaStream_t>(stream));

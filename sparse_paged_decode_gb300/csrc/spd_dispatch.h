@@ -16,9 +16,9 @@ cudaError_t dispatch_attention(const AttnArgs &a, void *workspace, size_t worksp
 void count_launches(int n);
 uint64_t launch_count();
 
-// Attention kernel policy (spd_set_attention_kernel) and the status word of a
-// workspace (spd_workspace_status).
-int set_attention_policy(int policy);
+// Kernel policy of a stage (1 score, 2 select, 3 attention; spd_set_kernel_policy)
+// and the status word of a workspace (spd_workspace_status).
+int set_kernel_policy(int stage, int policy);
 int workspace_status(const void *workspace, cudaStream_t stream);
 
 // Workspace bytes for the attention calls (capacities only).

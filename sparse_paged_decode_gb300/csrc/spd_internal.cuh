@@ -77,6 +77,7 @@ struct AttnArgs {
 
 cudaError_t launch_score_generic(const ScoreArgs &a, cudaStream_t stream);
 cudaError_t launch_select_generic(const SelectArgs &a, cudaStream_t stream);
+cudaError_t launch_select_rank(const SelectArgs &a, cudaStream_t stream);
 cudaError_t launch_attention_generic(const AttnArgs &a, cudaStream_t stream);
 
 // ------------------------------------------------------------- device helpers

@@ -88,6 +88,24 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, uint64_
         : "memory");
 }
 
+// 3-D tiled load without a cache hint.
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, uint64_t *bar, int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+// 2-D tiled load of one box into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, uint64_t *bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+        : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -212,6 +230,14 @@ __host__ __device__ constexpr uint32_t idesc_m128(uint32_t n, bool a_mn, bool b_
            | (static_cast<uint32_t>(b_mn) << 16)  // B major
            | ((n >> 3) << 17)                     // N / 8
            | ((128u >> 4) << 24);                 // M / 16
+}
+
+// Instruction descriptor of kind::f16 with fp32 accumulate, M = 128, the
+// given N, both operands K-major and of one type: bf16 (format code 1) or
+// f16 (0).
+__host__ __device__ constexpr uint32_t idesc_f16_m128(uint32_t n, bool bf16) {
+    return (1u << 4) | (static_cast<uint32_t>(bf16) << 7) | (static_cast<uint32_t>(bf16) << 10) |
+           ((n >> 3) << 17) | ((128u >> 4) << 24);
 }
 
 // Byte offset of element (row, col) of a row-major tile of `width` bytes per

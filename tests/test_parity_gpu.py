@@ -150,10 +150,11 @@ SMALL = {
 @pytest.fixture(params=[0, 1], ids=["auto_kernel", "general_kernel"])
 def kernel_policy(request, spd):
     """Run a test through the default kernel choice and through the
-    general-layout kernel."""
-    old = spd.set_attention_kernel(request.param)
+    general-layout kernels, for every stage."""
+    old = [spd.set_kernel_policy(stage, request.param) for stage in (1, 2, 3)]
     yield request.param
-    spd.set_attention_kernel(old)
+    for stage, o in zip((1, 2, 3), old):
+        spd.set_kernel_policy(stage, o)
 
 
 @pytest.mark.parametrize("name", sorted(SMALL))

@@ -7,38 +7,42 @@
 //  * Work.  A device planner (plan.cu) groups the query rows of one request
 //    that sit together (draft tokens of a verification row), unions the blocks
 //    they selected per kv head, and cuts each (group, kv head) block list into
-//    units.  A persistent grid walks the units; a pair cut into several units
-//    merges its partials in the last unit to finish (an atomic counter, no
-//    waiting on other CTAs).
+//    units.  A persistent grid claims units from a work counter; a pair cut
+//    into several units merges its partials in the last unit to finish (an
+//    atomic ticket, no waiting on other CTAs).
 //
-//  * Staging.  Warp 0 streams each selected page's K and V tile (128 tokens x
-//    128 bytes of one kv head) with TMA into a ring of shared-memory stages,
-//    128-byte swizzled, straight from the paged cache through the block table.
+//  * Roles (12 warps).  Warp 0 streams each selected page's K and V tile
+//    (128 tokens x 128 bytes of one kv head) with TMA into a ring of stages,
+//    straight from the paged cache through the block table.  Warp 1 issues
+//    every tcgen05.mma.  Warps 2-3 widen V from E4M3 to f16.  Warps 4-7 and
+//    8-11 are two softmax groups that take alternate blocks of a unit, each
+//    with its own accumulators, and combine them at the unit's end.
 //
-//  * Contractions.  Warp 1 issues tcgen05.mma kind::f8f6f4 with fp32
-//    accumulation in tensor memory.  Keys lie on the 128 TMEM lanes and the
-//    group's query rows (rows x q heads, padded to N = 16/32/64) on columns:
-//        S^T[tok][n]  = K[tok][:] . Qs[n][:]          (A = K tile, K-major)
-//        O^T[d][n]   += V^T[d][tok] . P[tok][n]        (A = V tile, MN-major)
-//    The E4M3 K/V bytes feed the tensor core unconverted.  Queries and
-//    probabilities are split into two E4M3 terms, x = hi + lo with
-//    hi = e4m3(x) and lo = e4m3(x - hi), accumulated along the contraction
-//    (about 8 significant bits, like bf16), so no operand is converted from
-//    FP8 and no precision below bf16 is lost.  Each query row is scaled by a
-//    power of two into E4M3 range first; the factor comes out with the
-//    softmax scale.
+//  * Contractions.  Keys lie on the 128 TMEM lanes and the group's query rows
+//    (rows x q heads, padded to N = 16/32/64) on columns:
+//        S^T[tok][n]  = K[tok][:] . Qs[n][:]      kind::f8f6f4, E4M3 K as read
+//        O^T[d][n]   += V^T[d][tok] . P[tok][n]    kind::f16, f16 V and P
+//    Queries enter as E4M3 terms (q = t0 + t1 (+ t2), each row scaled by a
+//    power of two into E4M3 range, the factor folded into the logit scale).
+//    Two terms hold a bf16 query exactly (4 + 4 significant bits); with at
+//    least 8 q heads per kv head they are stacked along N, so one product
+//    per k-step reads the K tile once and the softmax adds the two halves of
+//    S.  Other query types take three terms accumulated into the same
+//    columns.  V is widened to f16 exactly (cvt.rn.f16x2.e4m3x2).
+//    Probabilities are f16 (normal down to 2^-14, so tiny weights survive);
+//    their row sums accumulate per thread and are reduced once per unit.
 //
-//  * Softmax.  Warps 2-5 own the 128 token lanes of S and the 128 d lanes of
-//    O.  The exponent offset per query row is a running maximum that is only
-//    raised when a logit exceeds it by more than 2^6 (then O is rescaled in
-//    tensor memory): most blocks need no cross-lane reduction.  The row sums
-//    accumulate per thread and are reduced once per unit.  Probabilities are
-//    written to shared memory as the B operand of the next PV product.
+//  * Softmax.  A group owns the 128 token lanes of its S and the 128 d lanes
+//    of its O.  Its exponent offset per query row is a running maximum raised
+//    only when a logit exceeds it by more than 2^6 (then O and L are rescaled
+//    in tensor memory): most blocks need no cross-lane reduction.
 //
-// Synchronisation uses mbarriers between the roles, every wait bounded
-// (a timeout sets bit 0 of the workspace status word and the CTA winds down).
+// Synchronisation uses mbarriers between the roles, every wait bounded (a
+// timeout sets bit 0 of the workspace status word and the CTA winds down).
 #include <cuda.h>
 #include <cudaTypedefs.h>
+
+#include <algorithm>
 
 #include "plan.cuh"
 #include "spd_internal.cuh"
@@ -51,8 +55,11 @@ cudaError_t launch_attention_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cu
 
 namespace {
 
-constexpr int kThreads = 192;         // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
-constexpr int kSoftThreads = 128;
+constexpr int kThreads = 512;         // 16 warps, roles above
+constexpr int kWarpSoft = 4;          // first softmax warp
+constexpr int kSoftThreads = 128;     // one softmax group
+constexpr int kConvThreads = 128;     // warps 12-15
+constexpr int kWarpConv = 12;         // first V-widening warp
 constexpr int kStages = 3;
 constexpr int kTile = 128 * 128;      // bytes of one K or V tile
 constexpr int kNMax = 64;             // query rows per group (padded)
@@ -62,6 +69,12 @@ constexpr int kD = 128;
 constexpr int kTerms = kQueryTerms;   // E4M3 terms per query element (12 significant bits)
 constexpr int kStride = kD + kPartialStride;
 
+// tensor memory columns (512 allocated): S of softmax group w at
+// kColS + w * kSCols (N columns, or 2N when the query terms are stacked), O
+// at kColO + w * kNMax
+constexpr uint32_t kSCols = 2 * kNMax;
+constexpr uint32_t kColS = 0, kColO = 2 * kSCols;
+
 struct TcArgs {
     const int32_t *ri;
     int64_t ri_s0;
@@ -70,45 +83,59 @@ struct TcArgs {
     __nv_bfloat16 *out;
     int64_t o_s0, o_s1, o_s2;
     int32_t T, Hq, Hkv, G, R, NB, gmax;
+    int32_t stacked;  // 1: two query terms stacked along N (loaded per token), 0: three accumulated
     float v_scale;
     char *ws;
     PlanLayout lay;
 };
 
 struct __align__(16) Shared {
-    float m_run[kNMax];   // running exponent offset per query row (log2 units)
-    float cfac[kNMax];    // logit factor per query row
-    float alpha[kNMax];   // rescale factor of the last offset raise
-    float den[kNMax];     // merge: normaliser per row
-    float red[4][kNMax];  // cross-warp reduction scratch
+    float m_run[2][kNMax];   // running exponent offset per group and query row (log2 units)
+    float cfac[kNMax];       // logit factor per query row
+    float alpha[2][kNMax];   // rescale factor of a group's last offset raise
+    float red[2][4][kNMax];  // cross-warp reduction scratch per group (block maxima)
+    float lsum[2][4][kNMax]; // per-warp row sums of each group at the unit's end
     uint64_t kv_full[kStages], kv_empty[kStages];
-    uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2];
-    uint64_t q_full, q_empty, merge_bar;
-    uint64_t unit_full[4], unit_empty[4];  // ring of unit records, producer -> MMA, softmax
+    uint64_t s_full[2], s_empty[2], p_full[2], v_full[2], pv_done[2];
+    uint64_t q_full, q_empty, drain[3];
+    uint64_t unit_full[4], unit_empty[4];  // ring of unit records, producer -> everyone
     PlanUnit ring[4];
     uint32_t tmem_base;
     int abort;
     int combine;
-    int rescale;
-    int vote[2][4];
-    int unit_vote[4];
+    int rescale[2];
+    int vote[2][2][4];
+    int unit_vote[8];
     int Lj[16];                  // key limit of each group row
     PlanEntry ent[kMaxEntries];  // the unit's block list
+    uint8_t nvalid[4][kMaxEntries];  // per V-widening warp: tokens of each block valid for some row
+    float2 fac[kNMax];               // unit end: weights of the two groups' O per column
+    int64_t orow[kNMax];             // unit end: first element of each column's output row
 };
 
 // dynamic shared memory: E4M3 K and V stages, query terms, f16 V and P tiles
-// (double buffered), Shared
+// (one per softmax group), Shared
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kStages * kTile;
 constexpr int kQBytes = kNMax * 128;
 constexpr int kOffQ = kOffV + kStages * kTile;
-constexpr int kV16Tile = 128 * kD * 2;   // [2 d-halves][128 tokens][64 d] f16
+constexpr int kV16Tile = 128 * kD * 2;     // [2 d-halves][128 tokens][64 d] f16
 constexpr int kP16Tile = 128 * kNMax * 2;  // [128 tokens][N] f16
 constexpr int kOffV16 = kOffQ + kTerms * kQBytes;
 constexpr int kOffP = kOffV16 + 2 * kV16Tile;
 constexpr int kOffShared = kOffP + 2 * kP16Tile;
 constexpr int kSmemBytes = kOffShared + static_cast<int>(sizeof(Shared)) + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+// a unit record is released by the Q K^T issuer, the two P V issuers, both
+// softmax groups and the V-widening warps
+constexpr uint32_t kUnitArrivals = 3 + 2 * kSoftThreads + kConvThreads;
+
+// Registers: the launch gives 128 per thread (512 x 128 = 65536); warps 0-3
+// (TMA, the MMA issuers) drop to 56, the V-widening warps to 72, and the two
+// softmax groups rise to 192: 128 x 56 + 128 x 72 + 256 x 192 = 65536.
+constexpr uint32_t kRegsIssue = 56, kRegsConv = 72, kRegsSoft = 192;
+static_assert(128 * kRegsIssue + 128 * kRegsConv + 256 * kRegsSoft <= kThreads * 128, "register split");
 
 __device__ __forceinline__ int pow2_width(int n) { return n <= 16 ? 16 : n <= 32 ? 32 : 64; }
 
@@ -117,27 +144,29 @@ __device__ __forceinline__ tc::Swizzle p_swizzle(int n) {
     return n == 16 ? tc::kSw32 : n == 32 ? tc::kSw64 : tc::kSw128;
 }
 
-__device__ __forceinline__ void named_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kSoftThreads) : "memory"); }
+// named barriers: 1 + w = softmax group w, 3 = both groups
+__device__ __forceinline__ void group_sync(int w) { asm volatile("bar.sync %0, 128;" ::"r"(1 + w) : "memory"); }
+__device__ __forceinline__ void soft_sync() { asm volatile("bar.sync 3, 256;" ::: "memory"); }
 
 __device__ __forceinline__ bool aborted(Shared &sh) { return *reinterpret_cast<volatile int *>(&sh.abort) != 0; }
 
-__device__ __forceinline__ bool wait_or_abort(Shared &sh, uint64_t *bar, uint32_t parity, int32_t *status) {
-    if (tc::mbar_wait(bar, parity)) return true;
+__device__ __forceinline__ void set_abort(Shared &sh, int32_t *status) {
     *reinterpret_cast<volatile int *>(&sh.abort) = 1;
     atomicOr(status, 1);
+}
+
+__device__ __forceinline__ bool wait_or_abort(Shared &sh, uint64_t *bar, uint32_t parity, int32_t *status) {
+    if (tc::mbar_wait(bar, parity)) return true;
+    set_abort(sh, status);
     return false;
 }
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
+// Warp-uniform wait: every lane waits, the warp goes on only if all saw the
+// phase (so a warp-collective tcgen05 access that follows is uniform).
+__device__ __forceinline__ bool warp_wait(Shared &sh, uint64_t *bar, uint32_t parity, int32_t *status) {
+    const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(bar, parity));
+    if (!ok) set_abort(sh, status);
+    return ok;
 }
 
 // What a softmax thread needs besides the kernel arguments.
@@ -147,216 +176,211 @@ struct Soft {
     int32_t *status;
     int32_t *counters;
     float *partials;
-    uint32_t tS0, tS1, tO, lane_base;
-    int tok, lane, sw, st_id;
+    uint32_t tmem, lane_base;
+    int wg;     // softmax group
+    int tok;    // token lane of S, d lane of O
+    int lane;
+    int sw;     // warp within the group
+    int st_id;  // 0..255 over both groups
 };
 
-// The last unit of a split pair to finish merges all of them: the units'
-// partial rows are pulled into the idle f16 V / P buffers with bulk copies
-// (one wait for all of them), then per row the weights 2^(m_k - max m) and
-// every output element's weighted sum.
-__device__ __noinline__ void merge_partials(const Soft &c, const TcArgs &a, const PlanUnit &un,
-                                            uint32_t &merge_uses) {
-    Shared &sh = *c.sh;
-    constexpr int kRowBytes = kStride * 4;
-    constexpr int kStageBytes = 2 * kV16Tile + 2 * kP16Tile;
-    const int rows = un.nt * a.G, ns = un.n_split;
-    uint8_t *stage = c.smem + kOffV16;
-    int R = rows;
-    while (R > 1 && ns * R * (kRowBytes + 4) > kStageBytes) R = (R + 1) / 2;
-    const float *pbase = c.partials + static_cast<int64_t>(un.part_base) * kStride;
-    const float vs = a.v_scale * 256.f;
-    const int d = c.tok;
-    for (int r0 = 0; r0 < rows; r0 += R) {
-        const int nr = min(R, rows - r0);
-        float *wts = reinterpret_cast<float *>(stage + ns * nr * kRowBytes);
-        if (c.st_id == 0) {
-            tc::fence_proxy_async_global();
-            tc::mbar_arrive_expect_tx(&sh.merge_bar, ns * nr * kRowBytes);
-            for (int k = 0; k < ns; ++k)
-                tc::bulk_load(stage + k * nr * kRowBytes, pbase + static_cast<int64_t>(k * rows + r0) * kStride,
-                              nr * kRowBytes, &sh.merge_bar);
-        }
-        wait_or_abort(sh, &sh.merge_bar, merge_uses & 1, c.status);
-        ++merge_uses;
-        const float *st = reinterpret_cast<const float *>(stage);
-        // weights 2^(m_k - max_k m) and the normaliser, one row per thread
-        for (int r = c.st_id; r < nr; r += kSoftThreads) {
-            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            int k = 0;
-            for (; k + 4 <= ns; k += 4)
+// The blocks of one unit that fall to this softmax group (global block
+// index b with b % 2 == group) for N = 16*NCH query columns.  Returns false
+// when the CTA must stop (an abort, decided uniformly within the group).
+// Reduction over the 32 lanes of a warp of 32 per-lane columns, transposed:
+// lane l ends with the reduction of column l (31 shuffles instead of 32 x 5).
+template <bool kMax>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) m4[j] = fmaxf(m4[j], st[((k + j) * nr + r) * kStride + kD]);
-            for (; k < ns; ++k) m4[0] = fmaxf(m4[0], st[(k * nr + r) * kStride + kD]);
-            const float mstar = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-            float den = 0.f;
-            for (k = 0; k < ns; ++k) {
-                const float mk = st[(k * nr + r) * kStride + kD];
-                const float w = (mk == -INFINITY) ? 0.f : tc::ex2(mk - mstar);
-                wts[k * nr + r] = w;
-                den += w * st[(k * nr + r) * kStride + kD + 1];
-            }
-            sh.den[r] = den;
-        }
-        named_sync();
-        // each thread one d of every row; four independent partial sums
-        for (int r = 0; r < nr; ++r) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            int k = 0;
-            for (; k + 4 <= ns; k += 4)
+    for (int o = 16; o >= 1; o >>= 1) {
+        const bool upper = (lane & o) != 0;
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    acc[j] = fmaf(wts[(k + j) * nr + r], st[((k + j) * nr + r) * kStride + d], acc[j]);
-            for (; k < ns; ++k) acc[0] = fmaf(wts[k * nr + r], st[(k * nr + r) * kStride + d], acc[0]);
-            const float den = sh.den[r];
-            const float sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-            const float val = (den > 0.f) ? sum * vs / den : 0.f;
-            const int t = un.t0 + (r0 + r) / a.G, g = (r0 + r) % a.G;
-            a.out[t * a.o_s0 + (un.h * a.G + g) * a.o_s1 + d * a.o_s2] = __float2bfloat16_rn(val);
+        for (int i = 0; i < o; ++i) {
+            const float keep = upper ? v[i + o] : v[i];
+            const float send = upper ? v[i] : v[i + o];
+            const float got = __shfl_xor_sync(0xffffffffu, send, o);
+            v[i] = kMax ? fmaxf(keep, got) : keep + got;
         }
-        named_sync();  // the stage is reused by the next chunk
     }
+    return v[0];
 }
 
-// One unit's blocks and its epilogue for N = 16*NCH query columns.  Returns
-// false when the CTA must stop (an abort, decided uniformly).
-template <int NCH>
-__device__ __forceinline__ bool unit_body(const Soft &c, const TcArgs &a, const PlanUnit &un, uint32_t gb) {
+// This thread's logits of one block, masked (-inf where the column is not
+// valid on this token lane): u[col] = s[col] * cfac[col] - m_run[col] (log2
+// units) with kOffset, s[col] * cfac[col] without.  In stacked mode the second
+// query term's logits (N columns further on) are added first.  Returns the
+// maximum over the columns.
+template <int NCH, bool kOffset>
+__device__ __forceinline__ float load_u(const Soft &c, const TcArgs &a, uint32_t tS, const float *m_run,
+                                        uint64_t colmask, float (&u)[NCH * 16]) {
     constexpr int N = NCH * 16;
     Shared &sh = *c.sh;
-    const int rows = un.nt * a.G;
+#pragma unroll
+    for (int ch = 0; ch < NCH; ++ch) {
+        float v[16];
+        tc::tmem_ld16(tS + ch * 16, v);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) u[ch * 16 + q] = v[q];
+    }
+    if (a.stacked) {
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
+            float v[16];
+            tc::tmem_ld16(tS + N + ch * 16, v);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) u[ch * 16 + q] += v[q];
+        }
+    }
+    tc::tmem_wait_ld();
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int c4 = 0; c4 < N; c4 += 4) {
+        const float4 cf = *reinterpret_cast<const float4 *>(&sh.cfac[c4]);
+        float4 mr = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (kOffset) mr = *reinterpret_cast<const float4 *>(&m_run[c4]);
+        const float cfs[4] = {cf.x, cf.y, cf.z, cf.w}, mrs[4] = {mr.x, mr.y, mr.z, mr.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int col = c4 + q;
+            const float v = kOffset ? fmaf(u[col], cfs[q], -mrs[q]) : u[col] * cfs[q];
+            u[col] = ((colmask >> col) & 1) ? v : -INFINITY;
+            mx[q] = fmaxf(mx[q], u[col]);
+        }
+    }
+    return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+}
+
+template <int NCH>
+__device__ __noinline__ bool unit_blocks(const Soft &c_, const TcArgs &a_, const PlanUnit &un_, uint32_t gb) {
+    // work on copies: the arguments live in memory (the caller passes
+    // references), and every inline-asm memory clobber below would force a
+    // field read through them to be repeated
+    const Soft c = c_;
+    const TcArgs a = a_;
+    const PlanUnit un = un_;
+    constexpr int N = NCH * 16;
+    Shared &sh = *c.sh;
+    const int wg = c.wg;
     const uint64_t gmask = (a.G >= 64) ? ~0ull : ((1ull << a.G) - 1);
+    const uint32_t tS = c.tmem + kColS + wg * kSCols + c.lane_base;
+    const uint32_t tO = c.tmem + kColO + wg * kNMax + c.lane_base;
+    float *m_run = sh.m_run[wg];
+    uint8_t *pb = c.smem + kOffP + wg * kP16Tile;
+    // row sums of this thread's token lane, reduced over the group at the end
     float lsum[N];
 #pragma unroll
     for (int col = 0; col < N; ++col) lsum[col] = 0.f;
+    bool ok = true;
 
-    for (int i = 0; i < un.count; ++i) {
-        const uint32_t b = gb + i;
-        const int sb = b & 1, stg = b % kStages;
+    for (int i = ((gb & 1u) == static_cast<uint32_t>(wg)) ? 0 : 1; i < un.count; i += 2) {
+        const uint32_t b = gb + i;  // b % 2 == wg
+        const uint32_t k = b >> 1;  // this group's block ordinal
         const PlanEntry e = sh.ent[i];
         // columns valid on this token lane: selected by the column's row and
         // below that row's key limit
         uint64_t colmask = 0;
         for (int j = 0; j < un.nt; ++j)
             if (((e.mask >> j) & 1) && c.tok < sh.Lj[j] - e.block * 128) colmask |= gmask << (j * a.G);
-        wait_or_abort(sh, &sh.s_full[sb], (b >> 1) & 1, c.status);
-        tc::tc_fence_after();
-        float s[N];
-        const uint32_t sbase = (sb ? c.tS1 : c.tS0) + c.lane_base;
-#pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) {
-            float v[16];
-            tc::tmem_ld16(sbase + ch * 16, v);
-#pragma unroll
-            for (int k = 0; k < 16; ++k) s[ch * 16 + k] = v[k];
-        }
-        tc::tmem_wait_ld();
-        tc::tc_fence_before();
-        tc::mbar_arrive(&sh.s_empty[sb]);
-
-        bool need = false;
-#pragma unroll
-        for (int c4 = 0; c4 < N; c4 += 4) {
-            const float4 cf = *reinterpret_cast<const float4 *>(&sh.cfac[c4]);
-            const float4 mr = *reinterpret_cast<const float4 *>(&sh.m_run[c4]);
-            const float cfs[4] = {cf.x, cf.y, cf.z, cf.w}, mrs[4] = {mr.x, mr.y, mr.z, mr.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int col = c4 + k;
-                s[col] = ((colmask >> col) & 1) ? s[col] * cfs[k] : -INFINITY;
-                need |= s[col] > mrs[k] + kRaise;
-            }
+        // u = logits relative to the offsets; a column without an offset yet
+        // (m = -inf) gives +inf where valid, which forces a raise
+        float u[N];
+        float umax = -INFINITY;
+        const bool have = warp_wait(sh, &sh.s_full[wg], k & 1, c.status);
+        if (have) {
+            tc::tc_fence_after();
+            umax = load_u<NCH, true>(c, a, tS, m_run, colmask, u);
         }
         // votes alternate between two slots by block parity: a warp can be at
-        // most one block ahead of the slowest reader
-        const int mine = (__any_sync(0xffffffffu, need) ? 1 : 0) | (aborted(sh) ? 2 : 0);
-        if (c.lane == 0) sh.vote[sb][c.sw] = mine;
-        named_sync();
-        const int vote = sh.vote[sb][0] | sh.vote[sb][1] | sh.vote[sb][2] | sh.vote[sb][3];
-        if (vote & 2) return false;
+        // most one block ahead of the slowest reader of its group
+        const int mine = (__any_sync(0xffffffffu, umax > kRaise) ? 1 : 0) | (aborted(sh) ? 2 : 0);
+        if (c.lane == 0) sh.vote[wg][k & 1][c.sw] = mine;
+        group_sync(wg);
+        const int vote = sh.vote[wg][k & 1][0] | sh.vote[wg][k & 1][1] | sh.vote[wg][k & 1][2] | sh.vote[wg][k & 1][3];
+        if (vote & 2) {
+            tc::tc_fence_before();
+            tc::mbar_arrive(&sh.s_empty[wg]);
+            ok = false;
+            break;
+        }
         if (vote & 1) {
-            // raise the offsets to the block maximum; rescale O and the sums
+            // raise: an offset moves to its column's block maximum of
+            // s * cfac where that exceeds it by more than 2^kRaise (or where
+            // the column had none); O and the sums are scaled by 2^(old - new).
+            // S is read again without offsets.
+            load_u<NCH, false>(c, a, tS, m_run, colmask, u);
+            if constexpr (N >= 32) {
+                // in place: u is read again from S below
 #pragma unroll
-            for (int col = 0; col < N; ++col) {
-                const float mx = warp_max(s[col]);
-                if (c.lane == 0) sh.red[c.sw][col] = mx;
+                for (int c0 = 0; c0 < N; c0 += 32) {
+                    const float mx = warp_transpose_reduce<true>(*reinterpret_cast<float(*)[32]>(&u[c0]), c.lane);
+                    sh.red[wg][c.sw][c0 + c.lane] = mx;
+                }
+            } else {
+                float v[32];
+#pragma unroll
+                for (int q = 0; q < 32; ++q) v[q] = (q < N) ? u[q] : -INFINITY;
+                const float mx = warp_transpose_reduce<true>(v, c.lane);
+                if (c.lane < N) sh.red[wg][c.sw][c.lane] = mx;
             }
-            named_sync();
+            group_sync(wg);
             if (c.sw == 0) {
                 bool any = false;
                 for (int col = c.lane; col < N; col += 32) {
-                    const float bm = fmaxf(fmaxf(sh.red[0][col], sh.red[1][col]), fmaxf(sh.red[2][col], sh.red[3][col]));
-                    const float old = sh.m_run[col];
+                    const float bm = fmaxf(fmaxf(sh.red[wg][0][col], sh.red[wg][1][col]),
+                                           fmaxf(sh.red[wg][2][col], sh.red[wg][3][col]));
+                    const float old = m_run[col];
                     float al = 1.f;
-                    if (bm > old) {
+                    if (bm != -INFINITY && (old == -INFINITY || bm > old + kRaise)) {
                         al = (old == -INFINITY) ? 0.f : tc::ex2(old - bm);
                         any |= old != -INFINITY;
-                        sh.m_run[col] = bm;
+                        m_run[col] = bm;
                     }
-                    sh.alpha[col] = al;
+                    sh.alpha[wg][col] = al;
                 }
                 any = __any_sync(0xffffffffu, any);
-                if (c.lane == 0) sh.rescale = any;
+                if (c.lane == 0) sh.rescale[wg] = any;
             }
-            named_sync();
+            group_sync(wg);
 #pragma unroll
-            for (int col = 0; col < N; ++col) lsum[col] *= sh.alpha[col];
-            if (sh.rescale && i > 0) {
-                // O holds blocks 0..i-1 of this unit: wait for the last PV
-                wait_or_abort(sh, &sh.pv_done[(b - 1) & 1], ((b - 1) >> 1) & 1, c.status);
-                tc::tc_fence_after();
-                for (int ch = 0; ch < NCH; ++ch) {
-                    float v[16];
-                    tc::tmem_ld16(c.tO + c.lane_base + ch * 16, v);
-                    tc::tmem_wait_ld();
+            for (int col = 0; col < N; ++col) lsum[col] *= sh.alpha[wg][col];
+            if (sh.rescale[wg] && i >= 2) {
+                // O holds this group's earlier blocks of the unit: wait for
+                // its last product, then scale it in place
+                if (warp_wait(sh, &sh.pv_done[wg], (k - 1) & 1, c.status)) {
+                    tc::tc_fence_after();
+#pragma unroll 1
+                    for (int ch = 0; ch < NCH; ++ch) {
+                        float v[16];
+                        tc::tmem_ld16(tO + ch * 16, v);
+                        tc::tmem_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) v[k] *= sh.alpha[ch * 16 + k];
-                    tc::tmem_st16(c.tO + c.lane_base + ch * 16, v);
+                        for (int q = 0; q < 16; ++q) v[q] *= sh.alpha[wg][ch * 16 + q];
+                        tc::tmem_st16(tO + ch * 16, v);
+                        tc::tmem_wait_st();
+                    }
                 }
-                tc::tmem_wait_st();
-                tc::tc_fence_before();
             }
-        }
-
-        // V and P buffers sb were read by the PV of block b-2
-        if (b >= 2) wait_or_abort(sh, &sh.pv_done[sb], ((b >> 1) - 1) & 1, c.status);
-        // this token's V row: E4M3 (128-byte swizzled TMA tile) -> f16 * 2^-8
-        // (two 64-d halves, 128-byte swizzle), the A operand of P V; the E4M3
-        // stage is then free for the next TMA load
-        wait_or_abort(sh, &sh.kv_full[stg], (b / kStages) & 1, c.status);
-        {
-            const uint8_t *vsrc = c.smem + kOffV + stg * kTile + c.tok * 128;
-            uint8_t *vdst = c.smem + kOffV16 + sb * kV16Tile + c.tok * 128;
-            const int sw8 = c.tok & 7;
+            // the logits relative to the new offsets (a column whose offset is
+            // still unset is masked throughout: u = -inf)
+            load_u<NCH, true>(c, a, tS, m_run, colmask, u);
 #pragma unroll
-            for (int cc = 0; cc < 8; ++cc) {
-                const uint4 x = *reinterpret_cast<const uint4 *>(vsrc + ((cc ^ sw8) << 4));
-                uint32_t f[8];
-                tc::e4m3x4_to_f16x4_scaled(x.x, f[0], f[1]);
-                tc::e4m3x4_to_f16x4_scaled(x.y, f[2], f[3]);
-                tc::e4m3x4_to_f16x4_scaled(x.z, f[4], f[5]);
-                tc::e4m3x4_to_f16x4_scaled(x.w, f[6], f[7]);
-                uint8_t *half = vdst + (cc >> 2) * (128 * 128);
-                *reinterpret_cast<uint4 *>(half + ((((2 * cc) & 7) ^ sw8) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
-                *reinterpret_cast<uint4 *>(half + ((((2 * cc + 1) & 7) ^ sw8) << 4)) = make_uint4(f[4], f[5], f[6], f[7]);
-            }
+            for (int col = 0; col < N; ++col)
+                if (m_run[col] == -INFINITY) u[col] = -INFINITY;
         }
-        tc::fence_proxy_async();
-        tc::mbar_arrive(&sh.kv_empty[stg]);
-        // probabilities p = 2^(s - offset) <= 64 in f16 (11-bit significand,
-        // normal down to 2^-14), the B operand of P V
-        uint8_t *pb = c.smem + kOffP + sb * kP16Tile;
+        tc::tc_fence_before();
+        tc::mbar_arrive(&sh.s_empty[wg]);
+
+        // this group's P tile was read by the product of its previous block
+        if (b >= 2) wait_or_abort(sh, &sh.pv_done[wg], (k - 1) & 1, c.status);
+        // probabilities p = 2^u <= 64 in f16 (11-bit significand, normal down
+        // to 2^-14), the B operand of P V; masked columns have u = -inf, p = 0
 #pragma unroll
         for (int c8 = 0; c8 < N; c8 += 8) {
-            const float4 m0 = *reinterpret_cast<const float4 *>(&sh.m_run[c8]);
-            const float4 m1 = *reinterpret_cast<const float4 *>(&sh.m_run[c8 + 4]);
-            const float mr[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
             float p[8];
 #pragma unroll
-            for (int e2 = 0; e2 < 8; ++e2) {
-                const int col = c8 + e2;
-                p[e2] = (s[col] == -INFINITY) ? 0.f : tc::ex2(s[col] - mr[e2]);
-                lsum[col] += p[e2];
+            for (int q = 0; q < 8; ++q) {
+                p[q] = tc::ex2(u[c8 + q]);
+                lsum[c8 + q] += p[q];
             }
             uint4 w;
             w.x = tc::f32x2_to_f16x2(p[0], p[1]);
@@ -366,61 +390,170 @@ __device__ __forceinline__ bool unit_body(const Soft &c, const TcArgs &a, const 
             *reinterpret_cast<uint4 *>(pb + tc::swz_offset(c.tok, c8 * 2, 2 * N)) = w;
         }
         tc::fence_proxy_async();
-        tc::mbar_arrive(&sh.p_full[sb]);
+        tc::mbar_arrive(&sh.p_full[wg]);
     }
+    // the group's row sums: per warp by a transposed butterfly, per group in
+    // shared memory (added up by the unit's end)
+#pragma unroll
+    for (int c0 = 0; c0 < N; c0 += 32) {
+        float v[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) v[q] = (c0 + q < N) ? lsum[c0 + q] : 0.f;
+        const float tot = warp_transpose_reduce<false>(v, c.lane);
+        if (c0 + c.lane < N) sh.lsum[wg][c.sw][c0 + c.lane] = tot;
+    }
+    return ok;
+}
 
-    // ---- epilogue: row sums over the 128 token lanes, then O (d lane = tok)
-#pragma unroll
-    for (int col = 0; col < N; ++col) {
-        const float v = warp_sum(lsum[col]);
-        if (c.lane == 0) sh.red[c.sw][col] = v;
+// End of a unit, both groups: combine the two groups' (offset, O, sum) per
+// query column and write the normalised output, or the unit's partial when
+// its pair is split.  One thread per column first works out the column's two
+// weights and its output row; then group w takes columns [w N/2, (w+1) N/2),
+// each thread its d lane.
+template <int NCH>
+__device__ __noinline__ void unit_finish(const Soft &c_, const TcArgs &a_, const PlanUnit &un_, uint32_t gb,
+                                         bool ok) {
+    // work on copies: the arguments live in memory (the caller passes
+    // references), and every inline-asm memory clobber below would force a
+    // field read through them to be repeated
+    const Soft c = c_;
+    const TcArgs a = a_;
+    const PlanUnit un = un_;
+    constexpr int N = NCH * 16, HALF = N / 2;
+    Shared &sh = *c.sh;
+    const int rows = un.nt * a.G;
+    // blocks of the unit per group: group (gb % 2) has the even positions
+    const int first = static_cast<int>(gb & 1u);
+    const int n_first = (un.count + 1) / 2, n_second = un.count / 2;
+    const int mine = (c.wg == first) ? n_first : n_second;
+    if (ok && mine > 0) {
+        const uint32_t last = gb + ((c.wg == first) ? 2 * (n_first - 1) : 2 * n_second - 1);
+        warp_wait(sh, &sh.pv_done[c.wg], (last >> 1) & 1, c.status);
     }
-    float o[N];
-#pragma unroll
-    for (int col = 0; col < N; ++col) o[col] = 0.f;
-    if (un.count > 0) {
-        const uint32_t last = gb + un.count - 1;
-        wait_or_abort(sh, &sh.pv_done[last & 1], (last >> 1) & 1, c.status);
-        tc::tc_fence_after();
-#pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) {
-            float v[16];
-            tc::tmem_ld16(c.tO + c.lane_base + ch * 16, v);
-#pragma unroll
-            for (int k = 0; k < 16; ++k) o[ch * 16 + k] = v[k];
-        }
-        tc::tmem_wait_ld();
-        tc::tc_fence_before();
-    }
-    named_sync();
-    const int d = c.tok;
-    if (un.part_row < 0) {
-#pragma unroll
-        for (int col = 0; col < N; ++col) {
-            if (col < rows) {
-                const float l = sh.red[0][col] + sh.red[1][col] + sh.red[2][col] + sh.red[3][col];
-                const float val = (l > 0.f) ? o[col] * (a.v_scale * 256.f) / l : 0.f;
+    tc::tc_fence_before();
+    soft_sync();  // both groups' products are complete and their offsets final
+    tc::tc_fence_after();
+    if (c.st_id < N) {
+        const int col = c.st_id;
+        const bool has0 = (first == 0 ? n_first : n_second) > 0, has1 = (first == 1 ? n_first : n_second) > 0;
+        const float m0 = has0 ? sh.m_run[0][col] : -INFINITY;
+        const float m1 = has1 ? sh.m_run[1][col] : -INFINITY;
+        const float m = fmaxf(m0, m1);
+        float w0 = 0.f, w1 = 0.f;
+        if (m0 != -INFINITY) w0 = tc::ex2(m0 - m);
+        if (m1 != -INFINITY) w1 = tc::ex2(m1 - m);
+        const float l0 = (sh.lsum[0][0][col] + sh.lsum[0][1][col]) + (sh.lsum[0][2][col] + sh.lsum[0][3][col]);
+        const float l1 = (sh.lsum[1][0][col] + sh.lsum[1][1][col]) + (sh.lsum[1][2][col] + sh.lsum[1][3][col]);
+        const float l = w0 * l0 + w1 * l1;
+        int64_t off = -1;  // first element of the column's output (or partial) row; -1 for padding
+        if (col < rows) {
+            if (un.part_row < 0) {
+                const float inv = (l > 0.f) ? a.v_scale / l : 0.f;
+                w0 *= inv;
+                w1 *= inv;
                 const int t = un.t0 + col / a.G, g = col % a.G;
-                a.out[t * a.o_s0 + (un.h * a.G + g) * a.o_s1 + d * a.o_s2] = __float2bfloat16_rn(val);
+                off = t * a.o_s0 + (un.h * a.G + g) * a.o_s1;
+            } else {
+                // partial of a split pair: unnormalised O, offset and sum
+                off = static_cast<int64_t>(un.part_row + col) * kStride;
+                c.partials[off + kD] = m;
+                c.partials[off + kD + 1] = l;
             }
         }
-    } else {
-        // partial of a split pair: unnormalised O, offset and sum per row
+        sh.fac[col] = make_float2(w0, w1);
+        sh.orow[col] = off;
+    }
+    soft_sync();
+    const int d = c.tok;
+    const uint32_t base = c.tmem + c.lane_base;
+#pragma unroll 1
+    for (int cc = 0; cc < HALF; cc += 8) {
+        const int col0 = c.wg * HALF + cc;
+        float o0[8], o1[8];
+        tc::tmem_ld8(base + kColO + col0, o0);
+        tc::tmem_ld8(base + kColO + kNMax + col0, o1);
+        tc::tmem_wait_ld();
 #pragma unroll
-        for (int col = 0; col < N; ++col) {
-            if (col < rows) {
-                float *prow = c.partials + static_cast<int64_t>(un.part_row + col) * kStride;
-                prow[d] = o[col];
-                if (d == 0) {
-                    prow[kD] = sh.m_run[col];
-                    prow[kD + 1] = sh.red[0][col] + sh.red[1][col] + sh.red[2][col] + sh.red[3][col];
+        for (int q = 0; q < 8; ++q) {
+            const int64_t off = sh.orow[col0 + q];
+            if (off < 0) continue;
+            const float2 f = sh.fac[col0 + q];
+            // a group without blocks in this unit has weight 0 and stale O
+            const float v = ((f.x != 0.f) ? f.x * o0[q] : 0.f) + ((f.y != 0.f) ? f.y * o1[q] : 0.f);
+            if (un.part_row < 0)
+                a.out[off + d * a.o_s2] = __float2bfloat16_rn(v);
+            else
+                c.partials[off + d] = v;
+        }
+    }
+    tc::tc_fence_before();
+    soft_sync();  // O may now be overwritten by the next unit's products
+}
+
+// The last unit of a split pair to finish merges all of them, both softmax
+// groups together, one warp per output row: every lane reads each partial's
+// (offset, sum) -- the same address across the warp -- and four of its d
+// values, eight partials at a time with an online maximum, so a row costs
+// one round trip to L2 per eight partials.  Partials are read with
+// ld.global.cg: other CTAs wrote them during this launch.
+__device__ __noinline__ void merge_partials(const Soft &c_, const TcArgs &a_, const PlanUnit &un_) {
+    // work on copies: the arguments live in memory (the caller passes
+    // references), and every inline-asm memory clobber below would force a
+    // field read through them to be repeated
+    const Soft c = c_;
+    const TcArgs a = a_;
+    const PlanUnit un = un_;
+    const int rows = un.nt * a.G, ns = un.n_split;
+    const int warp8 = c.st_id >> 5;  // 0..7 over both groups
+    const float *pbase = c.partials + static_cast<int64_t>(un.part_base) * kStride;
+    const int64_t kstep = static_cast<int64_t>(rows) * kStride;
+    const int d4 = c.lane * 4;
+    for (int r = warp8; r < rows; r += 8) {
+        const float *row = pbase + static_cast<int64_t>(r) * kStride;
+        float m = -INFINITY, den = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k0 = 0; k0 < ns; k0 += 8) {
+            float2 ml[8];
+            float4 o[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (k0 + j < ns) {
+                    ml[j] = __ldcg(reinterpret_cast<const float2 *>(row + (k0 + j) * kstep + kD));
+                    o[j] = __ldcg(reinterpret_cast<const float4 *>(row + (k0 + j) * kstep + d4));
+                } else {
+                    ml[j] = make_float2(-INFINITY, 0.f);
+                    o[j] = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
+            float mc = m;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) mc = fmaxf(mc, ml[j].x);
+            if (mc == -INFINITY) continue;
+            const float sc = (m == -INFINITY) ? 0.f : tc::ex2(m - mc);
+            den *= sc;
+            acc.x *= sc;
+            acc.y *= sc;
+            acc.z *= sc;
+            acc.w *= sc;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float w = (ml[j].x == -INFINITY) ? 0.f : tc::ex2(ml[j].x - mc);
+                den = fmaf(w, ml[j].y, den);
+                acc.x = fmaf(w, o[j].x, acc.x);
+                acc.y = fmaf(w, o[j].y, acc.y);
+                acc.z = fmaf(w, o[j].z, acc.z);
+                acc.w = fmaf(w, o[j].w, acc.w);
+            }
+            m = mc;
         }
-        tc::fence_proxy_async_global();  // the merge reads partials with bulk copies
-        named_sync();
+        const float inv = (den > 0.f) ? a.v_scale / den : 0.f;
+        const int t = un.t0 + r / a.G, g = r % a.G;
+        __nv_bfloat16 *dst = a.out + t * a.o_s0 + (un.h * a.G + g) * a.o_s1;
+        dst[(d4 + 0) * a.o_s2] = __float2bfloat16_rn(acc.x * inv);
+        dst[(d4 + 1) * a.o_s2] = __float2bfloat16_rn(acc.y * inv);
+        dst[(d4 + 2) * a.o_s2] = __float2bfloat16_rn(acc.z * inv);
+        dst[(d4 + 3) * a.o_s2] = __float2bfloat16_rn(acc.w * inv);
     }
-    return true;
 }
 
 // A split unit takes a ticket on its pair's counter once its partial is
@@ -439,17 +572,16 @@ __device__ __forceinline__ void take_ticket(const Soft &c, const PlanUnit &un, P
     }
 }
 
-__device__ __forceinline__ void resolve_ticket(const Soft &c, const TcArgs &a, PendingMerge &pm,
-                                               uint32_t &merge_uses) {
+__device__ __forceinline__ void resolve_ticket(const Soft &c, const TcArgs &a, PendingMerge &pm) {
     Shared &sh = *c.sh;
     if (pm.un.pair < 0) return;
     if (c.st_id == 0) {
         sh.combine = (pm.ticket == pm.un.n_split - 1);
         if (sh.combine) __threadfence();  // the other units' partials before the merge reads them
     }
-    named_sync();
-    if (sh.combine) merge_partials(c, a, pm.un, merge_uses);
-    named_sync();
+    soft_sync();
+    if (sh.combine) merge_partials(c, a, pm.un);
+    soft_sync();
     pm.un.pair = -1;
 }
 
@@ -469,31 +601,32 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             tc::mbar_init(&sh.kv_full[i], 1);
-            tc::mbar_init(&sh.kv_empty[i], kSoftThreads);
+            tc::mbar_init(&sh.kv_empty[i], kConvThreads + 1);  // V widened + Q K^T done
         }
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&sh.s_full[i], 1);
             tc::mbar_init(&sh.s_empty[i], kSoftThreads);
             tc::mbar_init(&sh.p_full[i], kSoftThreads);
+            tc::mbar_init(&sh.v_full[i], kConvThreads);
             tc::mbar_init(&sh.pv_done[i], 1);
         }
         tc::mbar_init(&sh.q_full, 1);
         tc::mbar_init(&sh.q_empty, 1);
-        tc::mbar_init(&sh.merge_bar, 1);
+        for (int i = 0; i < 3; ++i) tc::mbar_init(&sh.drain[i], 1);
         for (int i = 0; i < 4; ++i) {
             tc::mbar_init(&sh.unit_full[i], 1);
-            tc::mbar_init(&sh.unit_empty[i], 1 + kSoftThreads);
+            tc::mbar_init(&sh.unit_empty[i], kUnitArrivals);
         }
         sh.abort = 0;
         tc::fence_mbar_init();
     }
-    if (warp == 1) tc::tmem_alloc(&sh.tmem_base, 4 * kNMax);  // S[2], O  (256 columns)
+    if (warp == 1) tc::tmem_alloc(&sh.tmem_base, 512);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
-    const uint32_t tmem_S0 = tmem, tmem_S1 = tmem + kNMax, tmem_O = tmem + 2 * kNMax;
-
+    if (warp < kWarpSoft) {
+    tc::regs_dec<kRegsIssue>();
     if (warp == 0) {
         // ------------------------------------------------------- TMA producer
         // Metadata is software-pipelined: the next unit record and the next
@@ -503,11 +636,12 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
             tc::prefetch_tmap(&tmap_v);
             tc::prefetch_tmap(&tmap_q);
             const uint64_t policy = tc::policy_evict_first();
-            const uint32_t qbox = static_cast<uint32_t>(a.G * a.gmax * 128);
-            // Units are claimed from the global work counter (largest first
-            // as the plan orders them) and handed to the MMA and softmax roles
-            // through a 4-slot ring; claims run two units ahead so a record has
-            // arrived by the time it is published.
+            const uint32_t qbox = static_cast<uint32_t>(a.G * a.gmax * 128);  // one term of a group
+            const uint32_t qrow = static_cast<uint32_t>(a.G * 128);            // one term of one token
+            // Units are claimed from the global work counter (in plan order)
+            // and handed to the other roles through a 4-slot ring; claims run
+            // two units ahead so a record has arrived by the time it is
+            // published.
             auto claim = [&]() -> PlanUnit {
                 PlanUnit x{};
                 x.pair = -1;
@@ -531,10 +665,21 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
                 if (un.pair < 0) break;
                 // the group's query terms, once the previous unit's last Q K^T is done
                 if (uc > 0 && !wait_or_abort(sh, &sh.q_empty, (uc - 1) & 1, &hdr->status)) break;
-                tc::mbar_arrive_expect_tx(&sh.q_full, kTerms * qbox);
-                for (int term = 0; term < kTerms; ++term)
-                    tc::tma_load_3d(smem + kOffQ + term * kQBytes, &tmap_q, &sh.q_full, 0, un.h * a.G,
-                                    term * a.T + un.t0, policy);
+                if (a.stacked) {
+                    // term t of token j at rows t*N + j*G (1 KiB aligned: G >= 8)
+                    const int n = pow2_width(un.nt * a.G);
+                    tc::mbar_arrive_expect_tx(&sh.q_full, 2 * un.nt * qrow);
+                    for (int term = 0; term < 2; ++term)
+                        for (int j = 0; j < un.nt; ++j)
+                            tc::tma_load_3d(smem + kOffQ + (term * n + j * a.G) * 128, &tmap_q, &sh.q_full, 0,
+                                            un.h * a.G, term * a.T + un.t0 + j, policy);
+                } else {
+                    // term t of the group at rows t*64
+                    tc::mbar_arrive_expect_tx(&sh.q_full, kTerms * qbox);
+                    for (int term = 0; term < kTerms; ++term)
+                        tc::tma_load_3d(smem + kOffQ + term * kQBytes, &tmap_q, &sh.q_full, 0, un.h * a.G,
+                                        term * a.T + un.t0, policy);
+                }
                 ++uc;
                 PlanEntry e_next{};
                 if (un.count > 0) e_next = lists[un.entry];
@@ -556,108 +701,227 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
                 un_next = un_after;
             }
             // let every issued copy land before the CTA may exit
+            if (uc > 0) tc::mbar_wait(&sh.q_full, (uc - 1) & 1);
             const uint32_t first = lb > kStages ? lb - kStages : 0;
             for (uint32_t b = first; b < lb; ++b) tc::mbar_wait(&sh.kv_full[b % kStages], (b / kStages) & 1);
         }
     } else if (warp == 1) {
-        // ----------------------------------------------------------- MMA issuer
+        // -------------------------------------------------------- Q K^T issuer
+        // A tcgen05.mma costs its issuing thread over a hundred cycles however
+        // small the tile, so the products are spread over three threads in
+        // different warps: this one issues every Q K^T, warps 2 and 3 the P V
+        // of one softmax group each.  Descriptors are built once and advanced
+        // by their 16-byte address field.
         if (lane == 0) {
             uint32_t gb = 0, uc = 0;
-            const uint32_t sK = tc::smem_u32(smem + kOffK), sV = tc::smem_u32(smem + kOffV);
-            const uint32_t sQ = tc::smem_u32(smem + kOffQ);
-            const uint32_t sV16 = tc::smem_u32(smem + kOffV16);
-            const uint32_t sP = tc::smem_u32(smem + kOffP);
+            const uint64_t dK0 = tc::smem_desc(tc::smem_u32(smem + kOffK), 16, 1024, tc::kSw128);
+            const uint64_t dQ0 = tc::smem_desc(tc::smem_u32(smem + kOffQ), 16, 1024, tc::kSw128);
+            int32_t *status = &hdr->status;
             while (!aborted(sh)) {
                 const int slot = uc & 3;
-                if (!wait_or_abort(sh, &sh.unit_full[slot], (uc >> 2) & 1, &hdr->status)) break;
+                if (!wait_or_abort(sh, &sh.unit_full[slot], (uc >> 2) & 1, status)) break;
                 const PlanUnit un = sh.ring[slot];
                 if (un.pair < 0) break;
                 const int n = pow2_width(un.nt * a.G);
-                const uint32_t idesc_qk = tc::idesc_m128(n, false, false);  // E4M3 x E4M3, both K-major
-                const uint32_t idesc_pv = tc::idesc_m128(n, true, true);    // F16 x F16, both MN-major
-                const tc::Swizzle psw = p_swizzle(n);
-                const uint32_t prow = 2 * n;  // bytes per token row of the P tile
-                if (!wait_or_abort(sh, &sh.q_full, uc & 1, &hdr->status)) break;
+                // E4M3 x E4M3, both K-major; stacked terms give 2n columns
+                const uint32_t idesc_qk = tc::idesc_m128(a.stacked ? 2 * n : n, false, false);
+                if (!wait_or_abort(sh, &sh.q_full, uc & 1, status)) break;
                 tc::tc_fence_after();
-                auto issue_qk = [&](uint32_t b) {
-                    const int st = b % kStages, sb = b & 1;
-                    if (!wait_or_abort(sh, &sh.kv_full[st], (b / kStages) & 1, &hdr->status)) return false;
-                    if (b >= 2 && !wait_or_abort(sh, &sh.s_empty[sb], ((b >> 1) - 1) & 1, &hdr->status)) return false;
-                    tc::tc_fence_after();
-                    const uint32_t d = sb ? tmem_S1 : tmem_S0;
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        const uint64_t ad = tc::smem_desc(sK + st * kTile + ks * 32, 16, 1024, tc::kSw128);
-#pragma unroll
-                        for (int term = 0; term < kTerms; ++term)
-                            tc::mma_f8(d, ad, tc::smem_desc(sQ + term * kQBytes + ks * 32, 16, 1024, tc::kSw128),
-                                       idesc_qk, ks > 0 || term > 0);
-                    }
-                    tc::mma_commit(&sh.s_full[sb]);
-                    return true;
-                };
-                bool ok = un.count == 0 || issue_qk(gb);
-                if (un.count <= 1) tc::mma_commit(&sh.q_empty);  // the unit's last Q K^T is issued
-                for (int i = 0; ok && i < un.count; ++i) {
+                if (un.count == 0) tc::mma_commit(&sh.q_empty);
+                bool ok = true;
+                for (int i = 0; i < un.count; ++i) {
                     const uint32_t b = gb + i;
-                    if (i + 1 < un.count) {
-                        if (!issue_qk(b + 1)) { ok = false; break; }
-                        if (i + 2 == un.count) tc::mma_commit(&sh.q_empty);
-                    }
-                    const int sb = b & 1;
-                    if (!wait_or_abort(sh, &sh.p_full[sb], (b >> 1) & 1, &hdr->status)) { ok = false; break; }
+                    const int st = b % kStages, w = b & 1;
+                    ok = wait_or_abort(sh, &sh.kv_full[st], (b / kStages) & 1, status);
+                    // S buffer w was read by the group's previous block
+                    if (ok && b >= 2) ok = wait_or_abort(sh, &sh.s_empty[w], ((b >> 1) - 1) & 1, status);
+                    if (!ok) break;
                     tc::tc_fence_after();
-                    // O^T[d][n] += V^T[d][tok] P[tok][n]: f16 V (two 64-d atoms, 16 KiB
-                    // apart) and P, 16 tokens per instruction
-                    const uint32_t vb = sV16 + sb * kV16Tile, pb = sP + sb * kP16Tile;
+                    const uint32_t d = tmem + kColS + w * kSCols;
+                    const uint64_t dk = dK0 + ((st * kTile) >> 4);
+                    if (a.stacked) {
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint64_t ad = tc::smem_desc(vb + ks * 16 * 128, 128 * 128, 1024, tc::kSw128);
-                        const uint64_t bd = tc::smem_desc(pb + ks * 16 * prow, 4096, 8 * prow, psw);
-                        tc::mma_f16(tmem_O, ad, bd, idesc_pv, i > 0 || ks > 0);
+                        for (int ks = 0; ks < 4; ++ks) tc::mma_f8(d, dk + 2 * ks, dQ0 + 2 * ks, idesc_qk, ks > 0);
+                    } else {
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+                            for (int term = 0; term < kTerms; ++term)
+                                tc::mma_f8(d, dk + 2 * ks, dQ0 + ((term * kQBytes) >> 4) + 2 * ks, idesc_qk,
+                                           ks > 0 || term > 0);
                     }
-                    tc::mma_commit(&sh.pv_done[sb]);
+                    tc::mma_commit(&sh.s_full[w]);
+                    tc::mma_commit(&sh.kv_empty[st]);
+                    if (i + 1 == un.count) tc::mma_commit(&sh.q_empty);  // the unit's last Q K^T
                 }
                 gb += un.count;
                 tc::mbar_arrive(&sh.unit_empty[slot]);
                 ++uc;
                 if (!ok) break;
             }
-            if (gb > 0) tc::mbar_wait(&sh.pv_done[(gb - 1) & 1], ((gb - 1) >> 1) & 1);
+            // every issued product completes before tensor memory is released
+            tc::mma_commit(&sh.drain[0]);
+            tc::mbar_wait(&sh.drain[0], 0);
         }
     } else {
+        // ------------------------------------------------ P V issuers (2, 3)
+        // O^T[d][n] += V^T[d][tok] P[tok][n] for the blocks of softmax group
+        // w = warp - 2: f16 V (two 64-d atoms, 16 KiB apart) and P, 16 tokens
+        // per instruction; the group's first block of a unit overwrites.
+        if (lane == 0) {
+            const int w = warp - 2;
+            uint32_t gb = 0, uc = 0;
+            const uint64_t dV = tc::smem_desc(tc::smem_u32(smem + kOffV16 + w * kV16Tile), 128 * 128, 1024, tc::kSw128);
+            const uint32_t tO = tmem + kColO + w * kNMax;
+            int32_t *status = &hdr->status;
+            while (!aborted(sh)) {
+                const int slot = uc & 3;
+                if (!wait_or_abort(sh, &sh.unit_full[slot], (uc >> 2) & 1, status)) break;
+                const PlanUnit un = sh.ring[slot];
+                if (un.pair < 0) break;
+                const int n = pow2_width(un.nt * a.G);
+                const uint32_t idesc_pv = tc::idesc_m128(n, true, true);  // F16 x F16, both MN-major
+                const uint32_t prow = 2 * n;                              // bytes per token row of the P tile
+                const uint64_t dP =
+                    tc::smem_desc(tc::smem_u32(smem + kOffP + w * kP16Tile), 4096, 8 * prow, p_swizzle(n));
+                bool ok = true;
+                for (int i = ((gb & 1u) == static_cast<uint32_t>(w)) ? 0 : 1; i < un.count; i += 2) {
+                    const uint32_t k = (gb + i) >> 1;
+                    ok = wait_or_abort(sh, &sh.p_full[w], k & 1, status) &&
+                         wait_or_abort(sh, &sh.v_full[w], k & 1, status);
+                    if (!ok) break;
+                    tc::tc_fence_after();
+                    const bool acc = i >= 2;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc::mma_f16(tO, dV + ((ks * 16 * 128) >> 4), dP + ((ks * 16 * prow) >> 4), idesc_pv,
+                                    acc || ks > 0);
+                    tc::mma_commit(&sh.pv_done[w]);
+                }
+                gb += un.count;
+                tc::mbar_arrive(&sh.unit_empty[slot]);
+                ++uc;
+                if (!ok) break;
+            }
+            tc::mma_commit(&sh.drain[1 + w]);
+            tc::mbar_wait(&sh.drain[1 + w], 0);
+        }
+    }
+    } else if (warp >= kWarpConv) {
+        tc::regs_dec<kRegsConv>();
+        // ------------------------------------------------------- V widening
+        // E4M3 V rows (128-byte swizzled TMA tile) -> f16 in two 64-d halves
+        // with 128-byte swizzle, the A operand of P V, one token row per
+        // thread; the E4M3 stage is released once the Q K^T of the same block
+        // is done too.
+        const int ct = threadIdx.x - kWarpConv * 32;
+        uint8_t *nvalid = sh.nvalid[ct >> 5];
+        uint32_t gb = 0, uc = 0;
+        for (;;) {
+            const int slot = uc & 3;
+            if (!wait_or_abort(sh, &sh.unit_full[slot], (uc >> 2) & 1, &hdr->status)) break;
+            const PlanUnit un = sh.ring[slot];
+            if (un.pair < 0) break;
+            // tokens of each block valid for some row of the unit (each warp
+            // its own copy); the rest -- slots no request owns may hold any
+            // code, NaN included -- are written as zeros
+            int my_lim = 0;
+            if (lane < un.nt) {
+                int r;
+                my_lim = static_cast<int>(token_limit(a.ri, a.ri_s0, a.sl, a.sl_s0, un.t0 + lane, a.R, a.NB, &r));
+            }
+            for (int i0 = 0; i0 < un.count; i0 += 32) {
+                const int i = i0 + lane;
+                PlanEntry e{};
+                if (i < un.count) e = lists[un.entry + i];
+                int m = 0;
+                for (int j = 0; j < un.nt; ++j) {
+                    const int lj = __shfl_sync(0xffffffffu, my_lim, j);
+                    if ((e.mask >> j) & 1) m = max(m, lj);
+                }
+                if (i < un.count) nvalid[i] = static_cast<uint8_t>(min(128, max(0, m - e.block * 128)));
+            }
+            __syncwarp();
+            bool ok = true;
+            for (int i = 0; i < un.count; ++i) {
+                const uint32_t b = gb + i;
+                const int stg = b % kStages, vb = b & 1;
+                ok = wait_or_abort(sh, &sh.kv_full[stg], (b / kStages) & 1, &hdr->status);
+                // the f16 tile vb was read by the product of block b-2
+                if (ok && b >= 2) ok = wait_or_abort(sh, &sh.pv_done[vb], ((b >> 1) - 1) & 1, &hdr->status);
+                if (!ok) break;
+                const int lim = nvalid[i];
+                const int tok = ct;
+                const uint8_t *vsrc = smem + kOffV + stg * kTile + tok * 128;
+                uint8_t *vdst = smem + kOffV16 + vb * kV16Tile + tok * 128;
+                const int sw8 = tok & 7;
+                // a d-half (64 values: 4 source chunks) at a time, its
+                // loads issued together
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint4 x[4];
+                    if (tok < lim) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            x[q] = *reinterpret_cast<const uint4 *>(vsrc + (((4 * hh + q) ^ sw8) << 4));
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) x[q] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    uint8_t *half = vdst + hh * (128 * 128);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t f[8];
+                        tc::e4m3x4_to_f16x4(x[q].x, f[0], f[1]);
+                        tc::e4m3x4_to_f16x4(x[q].y, f[2], f[3]);
+                        tc::e4m3x4_to_f16x4(x[q].z, f[4], f[5]);
+                        tc::e4m3x4_to_f16x4(x[q].w, f[6], f[7]);
+                        *reinterpret_cast<uint4 *>(half + (((2 * q) ^ sw8) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
+                        *reinterpret_cast<uint4 *>(half + (((2 * q + 1) ^ sw8) << 4)) =
+                            make_uint4(f[4], f[5], f[6], f[7]);
+                    }
+                }
+                tc::fence_proxy_async();
+                tc::mbar_arrive(&sh.kv_empty[stg]);
+                tc::mbar_arrive(&sh.v_full[vb]);
+            }
+            if (!ok) break;
+            __syncwarp();  // the counts are rewritten for the next unit
+            gb += un.count;
+            tc::mbar_arrive(&sh.unit_empty[slot]);
+            ++uc;
+        }
+    } else {
+        tc::regs_inc<kRegsSoft>();
         // ------------------------------------------------ softmax / epilogue
-        // The four softmax warps meet at named barriers, so they leave their
+        // The eight softmax warps meet at named barriers, so they leave their
         // loops only together: an abort (a timed-out wait anywhere in the
-        // CTA) is folded into the per-block vote and acted on after it.
-        // Between barriers a timed-out wait only records the abort.
+        // CTA) is folded into the per-block vote of each group and into a
+        // unit-level vote of both, and acted on after it.
         Soft c;
         c.sh = &sh;
         c.smem = smem;
         c.status = &hdr->status;
         c.counters = reinterpret_cast<int32_t *>(a.ws + a.lay.counters);
         c.partials = reinterpret_cast<float *>(a.ws + a.lay.partials);
-        c.st_id = threadIdx.x - 64;
+        c.st_id = threadIdx.x - kWarpSoft * 32;
+        c.wg = (warp - kWarpSoft) >> 2;
         c.lane = lane;
-        c.sw = warp - 2;
-        const int quad = warp & 3;                 // TMEM lane quadrant
-        c.tok = quad * 32 + lane;                  // token lane of S, d lane of O
-        c.lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        c.tS0 = tmem_S0;
-        c.tS1 = tmem_S1;
-        c.tO = tmem_O;
-        uint32_t gb = 0, merge_uses = 0;
+        c.sw = warp & 3;                          // TMEM lane quadrant
+        c.tok = c.sw * 32 + lane;                 // token lane of S, d lane of O
+        c.lane_base = static_cast<uint32_t>(c.sw * 32) << 16;
+        c.tmem = tmem;
+        uint32_t gb = 0;
         bool stop = false;
         const float *cfac = reinterpret_cast<const float *>(a.ws + a.lay.cfac);
 
-        // per-unit metadata is loaded one unit ahead into registers: up to two
-        // list entries, one key limit and one logit factor per thread
-        PlanEntry pe0{}, pe1{};
+        // per-unit metadata is loaded one unit ahead into registers: one list
+        // entry, one key limit and one logit factor per thread
+        PlanEntry pe{};
         int pL = 0;
         float pcf = 0.f;
         auto prefetch = [&](const PlanUnit &x) {
-            pe0 = (c.st_id < x.count) ? lists[x.entry + c.st_id] : PlanEntry{};
-            pe1 = (c.st_id + kSoftThreads < x.count) ? lists[x.entry + c.st_id + kSoftThreads] : PlanEntry{};
+            pe = (c.st_id < x.count) ? lists[x.entry + c.st_id] : PlanEntry{};
             int r;
             pL = (c.st_id < x.nt)
                      ? static_cast<int>(token_limit(a.ri, a.ri_s0, a.sl, a.sl_s0, x.t0 + c.st_id, a.R, a.NB, &r))
@@ -680,41 +944,49 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
             un_next.pair = -1;
             if (wait_or_abort(sh, &sh.unit_full[(uc + 1) & 3], ((uc + 1) >> 2) & 1, c.status))
                 un_next = sh.ring[(uc + 1) & 3];
-            if (c.st_id < un.count) sh.ent[c.st_id] = pe0;
-            if (c.st_id + kSoftThreads < un.count) sh.ent[c.st_id + kSoftThreads] = pe1;
+            if (c.st_id < un.count) sh.ent[c.st_id] = pe;
             if (c.st_id < 16) sh.Lj[c.st_id] = pL;
-            if (c.st_id < kNMax) {
-                sh.cfac[c.st_id] = pcf;
-                sh.m_run[c.st_id] = -INFINITY;
-            }
-            named_sync();
+            if (c.st_id < kNMax) sh.cfac[c.st_id] = pcf;
+            if (c.st_id < 2 * kNMax) sh.m_run[c.st_id / kNMax][c.st_id % kNMax] = -INFINITY;
+            soft_sync();
             if (un_next.pair >= 0) prefetch(un_next);
 
             const int nch = pow2_width(un.nt * a.G) / 16;
             bool ok;
-            if (nch == 1) ok = unit_body<1>(c, a, un, gb);
-            else if (nch == 2) ok = unit_body<2>(c, a, un, gb);
-            else ok = unit_body<4>(c, a, un, gb);
-            if (!ok) break;
+            if (nch == 1) {
+                ok = unit_blocks<1>(c, a, un, gb);
+                unit_finish<1>(c, a, un, gb, ok);
+            } else if (nch == 2) {
+                ok = unit_blocks<2>(c, a, un, gb);
+                unit_finish<2>(c, a, un, gb, ok);
+            } else {
+                ok = unit_blocks<4>(c, a, un, gb);
+                unit_finish<4>(c, a, un, gb, ok);
+            }
             gb += un.count;
-            resolve_ticket(c, a, pending, merge_uses);
-            if (un.part_row >= 0) take_ticket(c, un, pending);
+            // unit-level abort decision, uniform over both groups
+            if (lane == 0) sh.unit_vote[warp - kWarpSoft] = (aborted(sh) || !ok) ? 1 : 0;
+            soft_sync();
+            int any = 0;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) any |= sh.unit_vote[w];
+            stop = any != 0;
+            soft_sync();
+            if (!stop) {
+                resolve_ticket(c, a, pending);
+                if (un.part_row >= 0) take_ticket(c, un, pending);
+            }
             tc::mbar_arrive(&sh.unit_empty[uc & 3]);
-            // unit-level abort decision, uniform over the four warps
-            if (lane == 0) sh.unit_vote[c.sw] = aborted(sh) ? 1 : 0;
-            named_sync();
-            stop = (sh.unit_vote[0] | sh.unit_vote[1] | sh.unit_vote[2] | sh.unit_vote[3]) != 0;
-            named_sync();
             un = un_next;
             ++uc;
         }
-        if (!stop) resolve_ticket(c, a, pending, merge_uses);
+        if (!stop) resolve_ticket(c, a, pending);
     }
 
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (warp == 1) tc::tmem_dealloc(tmem, 4 * kNMax);
+    if (warp == 1) tc::tmem_dealloc(tmem, 512);
 }
 
 // ------------------------------------------------------------------ host side
@@ -733,15 +1005,16 @@ bool make_tmap(CUtensorMap *m, const uint8_t *base, int64_t slots, int64_t hkv, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Tensor map of the query terms qterms[term][t][hq][128 bytes]: box = the
-// gmax rows x G heads of one group for one term, 128-byte swizzle.
-bool make_tmap_q(CUtensorMap *m, const uint8_t *base, int64_t T, int64_t hq, int g, int gmax) {
+// Tensor map of the query terms qterms[term][t][hq][128 bytes]: box = G heads
+// x box_rows tokens of one term (a whole group, or one token when the terms
+// are stacked), 128-byte swizzle.
+bool make_tmap_q(CUtensorMap *m, const uint8_t *base, int64_t T, int64_t hq, int g, int box_rows) {
     auto fn = tensor_map_encoder();
     if (fn == nullptr) return false;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(hq),
                           static_cast<cuuint64_t>(kTerms * T)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(hq * kD)};
-    cuuint32_t box[3] = {kD, static_cast<cuuint32_t>(g), static_cast<cuuint32_t>(gmax)};
+    cuuint32_t box[3] = {kD, static_cast<cuuint32_t>(g), static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -800,7 +1073,6 @@ cudaError_t launch_attention_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cu
     p.gmax = std::min(16, kNMax / G);
     p.P = a.P;
     p.num_ctas = dev.sms;
-    p.units_per_cta = 4;
     p.ws = static_cast<char *>(ws);
     p.lay = lay;
     p.q = a.q; p.q_s0 = a.q_s0; p.q_s1 = a.q_s1; p.q_s2 = a.q_s2;
@@ -809,7 +1081,10 @@ cudaError_t launch_attention_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cu
     p.zscale = a.sm_scale * a.k_scale * 1.4426950408889634f;
 
     CUtensorMap tq;
-    if (!make_tmap_q(&tq, reinterpret_cast<const uint8_t *>(p.ws + lay.qterms), a.T, a.Hq, G, p.gmax))
+    // bf16 queries are exact in two E4M3 terms; with G >= 8 a token's G rows
+    // are 1 KiB, so the terms can be stacked token by token
+    const bool stacked = a.q_dt == SPD_BF16 && G >= 8;
+    if (!make_tmap_q(&tq, reinterpret_cast<const uint8_t *>(p.ws + lay.qterms), a.T, a.Hq, G, stacked ? 1 : p.gmax))
         return cudaSuccess;
 
     const int64_t q_rows = static_cast<int64_t>(a.T) * a.Hq;
@@ -822,6 +1097,7 @@ cudaError_t launch_attention_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cu
     t.sl = a.sl; t.sl_s0 = a.sl_s0;
     t.out = a.out; t.o_s0 = a.o_s0; t.o_s1 = a.o_s1; t.o_s2 = a.o_s2;
     t.T = a.T; t.Hq = a.Hq; t.Hkv = a.Hkv; t.G = G; t.R = a.R; t.NB = a.NB; t.gmax = p.gmax;
+    t.stacked = stacked ? 1 : 0;
     t.v_scale = a.v_scale;
     t.ws = static_cast<char *>(ws);
     t.lay = lay;

@@ -121,7 +121,6 @@ __device__ void plan_body(const PlanArgs &a) {
     int *s_L = plan_smem + kPlanMaxT;
     uint32_t *s_mask_all = reinterpret_cast<uint32_t *>(plan_smem + 2 * kPlanMaxT);
     __shared__ int scratch[32];
-    __shared__ int s_chunk;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     PlanHeader *hdr = reinterpret_cast<PlanHeader *>(a.ws + a.lay.header);
@@ -235,18 +234,17 @@ __device__ void plan_body(const PlanArgs &a) {
     __syncthreads();
     __threadfence_block();
 
-    // ---- chunk size: about units_per_cta units per CTA, within the unit and
-    // partial-row capacities of the workspace
+    // ---- units.  Chunk c = total blocks / CTAs (at least 4): each pair's
+    // list is cut into full chunks of c blocks and a remainder.  The unit
+    // table holds the full chunks first (pair order), then the remainders
+    // and unsplit pairs by decreasing size, so the dynamic scheduler claims
+    // the longest work first.
     int blocks_local = 0;
     for (int p = tid; p < n_pairs; p += kPlanThreads) blocks_local += pairs[p].n_blocks;
     int total_blocks;
     block_excl_sum(blocks_local, &total_blocks, scratch);
-    if (tid == 0) {
-        const int target = max(1, a.num_ctas * a.units_per_cta);
-        s_chunk = max(4, (total_blocks + target - 1) / target);
-    }
-    __syncthreads();
-    int chunk = s_chunk;
+    int chunk = max(4, (total_blocks + a.num_ctas - 1) / max(1, a.num_ctas));
+    int *hist = reinterpret_cast<int *>(s_mask_all);  // [chunk + 1] remainder-size bins (mask words are done)
     for (int attempt = 0; attempt < 24; ++attempt) {
         int nu = 0, rows = 0;
         for (int p = tid; p < n_pairs; p += kPlanThreads) {
@@ -261,30 +259,46 @@ __device__ void plan_body(const PlanArgs &a) {
         if (tot_u <= a.lay.unit_cap && tot_rows <= a.lay.rows_cap) break;
         chunk *= 2;
     }
-
-    // ---- unit table
-    int nu = 0, rows = 0;
+    chunk = min(chunk, kPlanMaxNB);
+    for (int i = tid; i <= chunk; i += kPlanThreads) hist[i] = 0;
+    __syncthreads();
+    // full chunks, split rows and the size of each pair's last unit
+    int n_full = 0, rows = 0;
     for (int p = tid; p < n_pairs; p += kPlanThreads) {
         const int n = pairs[p].n_blocks;
         const int u = max(1, (n + chunk - 1) / chunk);
-        nu += u;
+        const int last = n - (u - 1) * chunk;  // 1..chunk, or 0 for an empty pair
+        n_full += (last == chunk) ? u : u - 1;
         if (u > 1) rows += u * groups[p / a.Hkv].nt * a.G;
+        if (last < chunk) atomicAdd(&hist[last], 1);
     }
-    int tot_u, tot_rows;
-    int u_off = block_excl_sum(nu, &tot_u, scratch);
+    int tot_full, tot_rows;
+    int f_off = block_excl_sum(n_full, &tot_full, scratch);
     int r_off = block_excl_sum(rows, &tot_rows, scratch);
+    // bins in decreasing size: start of bin s = tot_full + units in bins > s
+    // (thread i holds bin chunk-1-i; chunk <= 256 < kPlanThreads)
+    {
+        const int bin = chunk - 1 - tid;
+        const int n = (bin >= 0) ? hist[bin] : 0;
+        int n_rem;
+        const int before = block_excl_sum(n, &n_rem, scratch);
+        if (bin >= 0) hist[bin] = tot_full + before;
+        if (tid == 0) hist[chunk] = tot_full + n_rem;  // total units
+    }
+    __syncthreads();
+    const int tot_u = hist[chunk];
     for (int p = tid; p < n_pairs; p += kPlanThreads) {
         const int n = pairs[p].n_blocks;
         const int u = max(1, (n + chunk - 1) / chunk);
+        const int last = n - (u - 1) * chunk;
         const PlanGroup gr = groups[p / a.Hkv];
         const int rows_per_unit = gr.nt * a.G;
-        pairs[p].unit0 = u_off;
+        pairs[p].unit0 = f_off;
         pairs[p].n_units = u;
         for (int c = 0; c < u; ++c) {
             PlanUnit un;
-            const int first = static_cast<int>((static_cast<int64_t>(n) * c) / u);
-            un.entry = pairs[p].list + first;
-            un.count = static_cast<int>((static_cast<int64_t>(n) * (c + 1)) / u) - first;
+            un.entry = pairs[p].list + c * chunk;
+            un.count = (c + 1 < u) ? chunk : last;
             un.part_row = (u > 1) ? r_off + c * rows_per_unit : -1;
             un.pair = p;
             un.t0 = gr.t0;
@@ -292,9 +306,9 @@ __device__ void plan_body(const PlanArgs &a) {
             un.h = static_cast<int16_t>(p % a.Hkv);
             un.part_base = (u > 1) ? r_off : -1;
             un.n_split = u;
-            units[u_off + c] = un;
+            const int slot = (un.count == chunk) ? f_off++ : atomicAdd(&hist[un.count], 1);
+            units[slot] = un;
         }
-        u_off += u;
         if (u > 1) r_off += u * rows_per_unit;
         counters[p] = 0;
     }

@@ -10,7 +10,10 @@
 //          dropped here)
 //   unit   a contiguous chunk of a pair's block list: the work item of one CTA;
 //          a pair split over several units leaves per-unit partials (running
-//          max, sum, unnormalised output) that the last unit to finish merges
+//          max, sum, unnormalised output) that the last unit to finish merges.
+//          Units are full chunks of `chunk` blocks plus one remainder per
+//          pair; the table lists the full chunks first, then the remainders by
+//          decreasing size (longest work is claimed first)
 #pragma once
 
 #include <stdint.h>
@@ -42,7 +45,7 @@ struct PlanGroup {
 struct PlanPair {
     int32_t list;      // offset of its block list (entries)
     int32_t n_blocks;
-    int32_t unit0;     // first unit
+    int32_t unit0;     // first full-chunk unit in the unit table
     int32_t n_units;
 };
 
@@ -112,7 +115,6 @@ struct PlanArgs {
     int32_t T, R, NB, K, Hkv, G, gmax;
     int64_t P;
     int32_t num_ctas;
-    int32_t units_per_cta;
     char *ws;
     PlanLayout lay;
     // query conversion (the other CTAs of the prepare launch)

@@ -14,7 +14,6 @@ namespace spd {
 namespace tc {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // give up on a barrier after 2 s
-constexpr uint32_t kSuspendHintNs = 20000;          // longest sleep inside one try_wait
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
@@ -46,17 +45,42 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
-// Test for completion of the phase with the given parity; while it is not
-// complete the thread may sleep (up to the hint, in ns) instead of spinning,
-// so a waiting warp leaves its issue slots to the warps doing work.
+// Test for completion of the phase with the given parity, waiting a short,
+// implementation-defined time inside the instruction before giving up.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Like mbar_try_wait with a caller-chosen suspend hint (ns).
+__device__ __forceinline__ bool mbar_try_wait_for(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0;
+}
+
+// Non-blocking test for completion of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return done != 0;
 }
@@ -67,7 +91,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
         if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
     }
 }
@@ -144,6 +170,18 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
+// Per-warpgroup register budget (all 128 threads of the warpgroup execute
+// it).  The budgets of a CTA's warpgroups must add up to at most what the
+// launch gave it (threads x registers per thread).
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -191,6 +229,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
         : "memory");
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 8 consecutive 32-bit columns of this thread's TMEM lane (warp-collective).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
@@ -259,16 +308,16 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float hi, float lo) {
     return r;
 }
 
-// Four E4M3 bytes -> four f16 values scaled by 2^-8, exactly, by moving bits:
-// an E4M3 code s.eeee.mmm becomes the f16 s.0eeee.mmm0000000, whose value is
-// the E4M3 value times 2^-8 for normal and subnormal codes alike (the f16
-// exponent bias is 8 more than E4M3's).  Returns {bytes 0,1} and {bytes 2,3}
-// as f16x2 words, low byte in the low half.
-__device__ __forceinline__ void e4m3x4_to_f16x4_scaled(uint32_t x, uint32_t &lo, uint32_t &hi) {
-    const uint32_t w0 = __byte_perm(x, 0u, 0x4140);  // [b0, 0, b1, 0]
-    const uint32_t w1 = __byte_perm(x, 0u, 0x4342);  // [b2, 0, b3, 0]
-    lo = (w0 + (w0 & 0x00800080u)) << 7;
-    hi = (w1 + (w1 & 0x00800080u)) << 7;
+// Four E4M3 bytes -> four f16 values (exact: every E4M3 value, subnormals
+// included, is an f16 normal).  Returns {bytes 0,1} and {bytes 2,3} as f16x2
+// words, the lower byte in the lower half.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t x, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 a, b;\n\t"
+        "mov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(x));
 }
 
 // Packed E4M3x2 -> two fp32 (exact).

@@ -71,9 +71,11 @@ constexpr int kStride = kD + kPartialStride;
 
 // tensor memory columns (512 allocated): S of softmax group w at
 // kColS + w * kSCols (N columns, or 2N when the query terms are stacked), O
-// at kColO + w * kNMax
+// at kColO + w * kNMax, and the per-lane row sums L (each thread its token
+// lane, added up over the lanes at the unit's end) at kColL + w * kNMax
 constexpr uint32_t kSCols = 2 * kNMax;
-constexpr uint32_t kColS = 0, kColO = 2 * kSCols;
+constexpr uint32_t kColS = 0, kColO = 2 * kSCols, kColL = kColO + 2 * kNMax;
+static_assert(kColL + 2 * kNMax <= 512, "tensor memory columns");
 
 struct TcArgs {
     const int32_t *ri;
@@ -91,13 +93,18 @@ struct TcArgs {
 
 struct __align__(16) Shared {
     float m_run[2][kNMax];   // running exponent offset per group and query row (log2 units)
-    float cfac[kNMax];       // logit factor per query row
+    float cfac[2][kNMax];    // logit factor per query row (double-buffered by unit)
     float alpha[2][kNMax];   // rescale factor of a group's last offset raise
-    float red[2][4][kNMax];  // cross-warp reduction scratch per group (block maxima)
-    float lsum[2][4][kNMax]; // per-warp row sums of each group at the unit's end
+    // per group: per-warp block maxima during the blocks (a raise), per-warp
+    // row sums at the unit's end (the two uses never overlap)
+    union {
+        float red[2][4][kNMax];
+        float lsum[2][4][kNMax];
+    };
     uint64_t kv_full[kStages], kv_empty[kStages];
     uint64_t s_full[2], s_empty[2], p_full[2], v_full[2], pv_done[2];
     uint64_t q_full, q_empty, drain[3];
+    uint64_t meta_full[2], meta_empty[2];  // unit metadata buffers: V-widening warp 0 -> softmax
     uint64_t unit_full[4], unit_empty[4];  // ring of unit records, producer -> everyone
     PlanUnit ring[4];
     uint32_t tmem_base;
@@ -106,11 +113,9 @@ struct __align__(16) Shared {
     int rescale[2];
     int vote[2][2][4];
     int unit_vote[8];
-    int Lj[16];                  // key limit of each group row
-    PlanEntry ent[kMaxEntries];  // the unit's block list
+    int Lj[2][16];                  // key limit of each group row (double-buffered by unit)
+    PlanEntry ent[2][kMaxEntries];  // the unit's block list (double-buffered by unit)
     uint8_t nvalid[4][kMaxEntries];  // per V-widening warp: tokens of each block valid for some row
-    float2 fac[kNMax];               // unit end: weights of the two groups' O per column
-    int64_t orow[kNMax];             // unit end: first element of each column's output row
 };
 
 // dynamic shared memory: E4M3 K and V stages, query terms, f16 V and P tiles
@@ -182,17 +187,55 @@ struct Soft {
     int lane;
     int sw;     // warp within the group
     int st_id;  // 0..255 over both groups
+    int mb;     // metadata buffer of the current unit
 };
 
-// The blocks of one unit that fall to this softmax group (global block
-// index b with b % 2 == group) for N = 16*NCH query columns.  Returns false
-// when the CTA must stop (an abort, decided uniformly within the group).
-// Reduction over the 32 lanes of a warp of 32 per-lane columns, transposed:
-// lane l ends with the reduction of column l (31 shuffles instead of 32 x 5).
-template <bool kMax>
-__device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane) {
+// One 16-column chunk of this thread's logits of a block, masked (-inf
+// where the column is not valid on this token lane): u[q] = s * cfac - m_run
+// (log2 units) with kOffset, s * cfac without.  In stacked mode the second
+// query term's logits (N columns further on) are added first.  Returns the
+// chunk's maximum.
+template <bool kOffset>
+__device__ __forceinline__ float load_chunk(const Shared &sh, int mb, bool stacked, int n, uint32_t tS,
+                                            const float *m_run, uint32_t bits, int c0, float (&u)[16]) {
+    tc::tmem_ld16(tS + c0, u);
+    if (stacked) {
+        float v[16];
+        tc::tmem_ld16(tS + n + c0, v);
+        tc::tmem_wait_ld();
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
+        for (int q = 0; q < 16; ++q) u[q] += v[q];
+    } else {
+        tc::tmem_wait_ld();
+    }
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int c4 = 0; c4 < 16; c4 += 4) {
+        const float4 cf = *reinterpret_cast<const float4 *>(&sh.cfac[mb][c0 + c4]);
+        float4 mr = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (kOffset) mr = *reinterpret_cast<const float4 *>(&m_run[c0 + c4]);
+        const float cfs[4] = {cf.x, cf.y, cf.z, cf.w}, mrs[4] = {mr.x, mr.y, mr.z, mr.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float v = kOffset ? fmaf(u[c4 + q], cfs[q], -mrs[q]) : u[c4 + q] * cfs[q];
+            u[c4 + q] = ((bits >> (c4 + q)) & 1) ? v : -INFINITY;
+            mx[q] = fmaxf(mx[q], u[c4 + q]);
+        }
+    }
+    return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+}
+
+// Reduction over the 32 lanes of a warp of 16 per-lane columns, transposed:
+// lanes l and l+16 end with the reduction of column l & 15.
+template <bool kMax>
+__device__ __forceinline__ float warp_transpose_reduce16(float (&v)[16], int lane) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float got = __shfl_xor_sync(0xffffffffu, v[i], 16);
+        v[i] = kMax ? fmaxf(v[i], got) : v[i] + got;
+    }
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) {
         const bool upper = (lane & o) != 0;
 #pragma unroll
         for (int i = 0; i < o; ++i) {
@@ -205,90 +248,46 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane)
     return v[0];
 }
 
-// This thread's logits of one block, masked (-inf where the column is not
-// valid on this token lane): u[col] = s[col] * cfac[col] - m_run[col] (log2
-// units) with kOffset, s[col] * cfac[col] without.  In stacked mode the second
-// query term's logits (N columns further on) are added first.  Returns the
-// maximum over the columns.
-template <int NCH, bool kOffset>
-__device__ __forceinline__ float load_u(const Soft &c, const TcArgs &a, uint32_t tS, const float *m_run,
-                                        uint64_t colmask, float (&u)[NCH * 16]) {
-    constexpr int N = NCH * 16;
+// The blocks of one unit that fall to this softmax group (global block index
+// b with b % 2 == group), N = 16 * nch query columns processed 16 at a time:
+// a first pass over S finds whether an offset must be raised (a vote of the
+// group), a second computes the probabilities.  Returns false when the CTA
+// must stop (an abort, decided uniformly within the group).
+__device__ __forceinline__ bool unit_blocks(const Soft &c, const TcArgs &a, const PlanUnit &un, uint32_t gb) {
     Shared &sh = *c.sh;
-#pragma unroll
-    for (int ch = 0; ch < NCH; ++ch) {
-        float v[16];
-        tc::tmem_ld16(tS + ch * 16, v);
-#pragma unroll
-        for (int q = 0; q < 16; ++q) u[ch * 16 + q] = v[q];
-    }
-    if (a.stacked) {
-#pragma unroll
-        for (int ch = 0; ch < NCH; ++ch) {
-            float v[16];
-            tc::tmem_ld16(tS + N + ch * 16, v);
-#pragma unroll
-            for (int q = 0; q < 16; ++q) u[ch * 16 + q] += v[q];
-        }
-    }
-    tc::tmem_wait_ld();
-    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-    for (int c4 = 0; c4 < N; c4 += 4) {
-        const float4 cf = *reinterpret_cast<const float4 *>(&sh.cfac[c4]);
-        float4 mr = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (kOffset) mr = *reinterpret_cast<const float4 *>(&m_run[c4]);
-        const float cfs[4] = {cf.x, cf.y, cf.z, cf.w}, mrs[4] = {mr.x, mr.y, mr.z, mr.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int col = c4 + q;
-            const float v = kOffset ? fmaf(u[col], cfs[q], -mrs[q]) : u[col] * cfs[q];
-            u[col] = ((colmask >> col) & 1) ? v : -INFINITY;
-            mx[q] = fmaxf(mx[q], u[col]);
-        }
-    }
-    return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-}
-
-template <int NCH>
-__device__ __noinline__ bool unit_blocks(const Soft &c_, const TcArgs &a_, const PlanUnit &un_, uint32_t gb) {
-    // work on copies: the arguments live in memory (the caller passes
-    // references), and every inline-asm memory clobber below would force a
-    // field read through them to be repeated
-    const Soft c = c_;
-    const TcArgs a = a_;
-    const PlanUnit un = un_;
-    constexpr int N = NCH * 16;
-    Shared &sh = *c.sh;
-    const int wg = c.wg;
+    const int wg = c.wg, mb = c.mb;
+    const int n = pow2_width(un.nt * a.G), nch = n / 16;
+    const bool stacked = a.stacked != 0;
     const uint64_t gmask = (a.G >= 64) ? ~0ull : ((1ull << a.G) - 1);
     const uint32_t tS = c.tmem + kColS + wg * kSCols + c.lane_base;
     const uint32_t tO = c.tmem + kColO + wg * kNMax + c.lane_base;
+    const uint32_t tL = c.tmem + kColL + wg * kNMax + c.lane_base;
     float *m_run = sh.m_run[wg];
     uint8_t *pb = c.smem + kOffP + wg * kP16Tile;
-    // row sums of this thread's token lane, reduced over the group at the end
-    float lsum[N];
-#pragma unroll
-    for (int col = 0; col < N; ++col) lsum[col] = 0.f;
     bool ok = true;
+    int mine_blocks = 0;
 
     for (int i = ((gb & 1u) == static_cast<uint32_t>(wg)) ? 0 : 1; i < un.count; i += 2) {
         const uint32_t b = gb + i;  // b % 2 == wg
         const uint32_t k = b >> 1;  // this group's block ordinal
-        const PlanEntry e = sh.ent[i];
+        const PlanEntry e = sh.ent[mb][i];
         // columns valid on this token lane: selected by the column's row and
         // below that row's key limit
         uint64_t colmask = 0;
         for (int j = 0; j < un.nt; ++j)
-            if (((e.mask >> j) & 1) && c.tok < sh.Lj[j] - e.block * 128) colmask |= gmask << (j * a.G);
-        // u = logits relative to the offsets; a column without an offset yet
-        // (m = -inf) gives +inf where valid, which forces a raise
-        float u[N];
+            if (((e.mask >> j) & 1) && c.tok < sh.Lj[mb][j] - e.block * 128) colmask |= gmask << (j * a.G);
+        // pass 1: the largest logit relative to the offsets; a column without
+        // an offset yet (m = -inf) gives +inf where valid, forcing a raise
         float umax = -INFINITY;
         const bool have = warp_wait(sh, &sh.s_full[wg], k & 1, c.status);
         if (have) {
             tc::tc_fence_after();
-            umax = load_u<NCH, true>(c, a, tS, m_run, colmask, u);
+#pragma unroll 1
+            for (int ch = 0; ch < nch; ++ch) {
+                float u[16];
+                umax = fmaxf(umax, load_chunk<true>(sh, mb, stacked, n, tS, m_run,
+                                                    static_cast<uint32_t>(colmask >> (16 * ch)), 16 * ch, u));
+            }
         }
         // votes alternate between two slots by block parity: a warp can be at
         // most one block ahead of the slowest reader of its group
@@ -305,27 +304,19 @@ __device__ __noinline__ bool unit_blocks(const Soft &c_, const TcArgs &a_, const
         if (vote & 1) {
             // raise: an offset moves to its column's block maximum of
             // s * cfac where that exceeds it by more than 2^kRaise (or where
-            // the column had none); O and the sums are scaled by 2^(old - new).
-            // S is read again without offsets.
-            load_u<NCH, false>(c, a, tS, m_run, colmask, u);
-            if constexpr (N >= 32) {
-                // in place: u is read again from S below
-#pragma unroll
-                for (int c0 = 0; c0 < N; c0 += 32) {
-                    const float mx = warp_transpose_reduce<true>(*reinterpret_cast<float(*)[32]>(&u[c0]), c.lane);
-                    sh.red[wg][c.sw][c0 + c.lane] = mx;
-                }
-            } else {
-                float v[32];
-#pragma unroll
-                for (int q = 0; q < 32; ++q) v[q] = (q < N) ? u[q] : -INFINITY;
-                const float mx = warp_transpose_reduce<true>(v, c.lane);
-                if (c.lane < N) sh.red[wg][c.sw][c.lane] = mx;
+            // the column had none); O and L are scaled by 2^(old - new)
+#pragma unroll 1
+            for (int ch = 0; ch < nch; ++ch) {
+                float u[16];
+                load_chunk<false>(sh, mb, stacked, n, tS, m_run, static_cast<uint32_t>(colmask >> (16 * ch)), 16 * ch,
+                                  u);
+                const float mx = warp_transpose_reduce16<true>(u, c.lane);
+                if (c.lane < 16) sh.red[wg][c.sw][16 * ch + c.lane] = mx;
             }
             group_sync(wg);
             if (c.sw == 0) {
                 bool any = false;
-                for (int col = c.lane; col < N; col += 32) {
+                for (int col = c.lane; col < n; col += 32) {
                     const float bm = fmaxf(fmaxf(sh.red[wg][0][col], sh.red[wg][1][col]),
                                            fmaxf(sh.red[wg][2][col], sh.red[wg][3][col]));
                     const float old = m_run[col];
@@ -341,66 +332,83 @@ __device__ __noinline__ bool unit_blocks(const Soft &c_, const TcArgs &a_, const
                 if (c.lane == 0) sh.rescale[wg] = any;
             }
             group_sync(wg);
-#pragma unroll
-            for (int col = 0; col < N; ++col) lsum[col] *= sh.alpha[wg][col];
             if (sh.rescale[wg] && i >= 2) {
-                // O holds this group's earlier blocks of the unit: wait for
-                // its last product, then scale it in place
+                // O and L hold this group's earlier blocks of the unit: wait
+                // for its last product, then scale both in place
                 if (warp_wait(sh, &sh.pv_done[wg], (k - 1) & 1, c.status)) {
                     tc::tc_fence_after();
 #pragma unroll 1
-                    for (int ch = 0; ch < NCH; ++ch) {
+                    for (int ch = 0; ch < 2 * nch; ++ch) {
+                        const int cc = (ch % nch) * 16;
+                        const uint32_t addr = (ch < nch ? tO : tL) + cc;
                         float v[16];
-                        tc::tmem_ld16(tO + ch * 16, v);
+                        tc::tmem_ld16(addr, v);
                         tc::tmem_wait_ld();
 #pragma unroll
-                        for (int q = 0; q < 16; ++q) v[q] *= sh.alpha[wg][ch * 16 + q];
-                        tc::tmem_st16(tO + ch * 16, v);
+                        for (int q = 0; q < 16; ++q) v[q] *= sh.alpha[wg][cc + q];
+                        tc::tmem_st16(addr, v);
                         tc::tmem_wait_st();
                     }
                 }
             }
-            // the logits relative to the new offsets (a column whose offset is
-            // still unset is masked throughout: u = -inf)
-            load_u<NCH, true>(c, a, tS, m_run, colmask, u);
-#pragma unroll
-            for (int col = 0; col < N; ++col)
-                if (m_run[col] == -INFINITY) u[col] = -INFINITY;
         }
-        tc::tc_fence_before();
-        tc::mbar_arrive(&sh.s_empty[wg]);
 
         // this group's P tile was read by the product of its previous block
         if (b >= 2) wait_or_abort(sh, &sh.pv_done[wg], (k - 1) & 1, c.status);
-        // probabilities p = 2^u <= 64 in f16 (11-bit significand, normal down
-        // to 2^-14), the B operand of P V; masked columns have u = -inf, p = 0
+        // pass 2: probabilities p = 2^u <= 64 in f16 (11-bit significand,
+        // normal down to 2^-14), the B operand of P V; masked columns have
+        // u = -inf, p = 0.  A column whose offset is still unset is masked
+        // throughout.  The lane's row sums in L gain p (the group's first
+        // block of the unit sets them).
+        const bool first = i < 2;
+#pragma unroll 1
+        for (int ch = 0; ch < nch; ++ch) {
+            const int c0 = 16 * ch;
+            float u[16];
+            if (have)
+                load_chunk<true>(sh, mb, stacked, n, tS, m_run, static_cast<uint32_t>(colmask >> c0), c0, u);
+            float l[16];
+            if (!first) tc::tmem_ld16(tL + c0, l);
+            float p[16];
 #pragma unroll
-        for (int c8 = 0; c8 < N; c8 += 8) {
-            float p[8];
+            for (int q = 0; q < 16; ++q) p[q] = (have && m_run[c0 + q] != -INFINITY) ? tc::ex2(u[q]) : 0.f;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                p[q] = tc::ex2(u[c8 + q]);
-                lsum[c8 + q] += p[q];
+            for (int h = 0; h < 2; ++h) {
+                uint4 w;
+                w.x = tc::f32x2_to_f16x2(p[8 * h + 0], p[8 * h + 1]);
+                w.y = tc::f32x2_to_f16x2(p[8 * h + 2], p[8 * h + 3]);
+                w.z = tc::f32x2_to_f16x2(p[8 * h + 4], p[8 * h + 5]);
+                w.w = tc::f32x2_to_f16x2(p[8 * h + 6], p[8 * h + 7]);
+                *reinterpret_cast<uint4 *>(pb + tc::swz_offset(c.tok, (c0 + 8 * h) * 2, 2 * n)) = w;
             }
-            uint4 w;
-            w.x = tc::f32x2_to_f16x2(p[0], p[1]);
-            w.y = tc::f32x2_to_f16x2(p[2], p[3]);
-            w.z = tc::f32x2_to_f16x2(p[4], p[5]);
-            w.w = tc::f32x2_to_f16x2(p[6], p[7]);
-            *reinterpret_cast<uint4 *>(pb + tc::swz_offset(c.tok, c8 * 2, 2 * N)) = w;
+            if (!first) {
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 16; ++q) p[q] += l[q];
+            }
+            tc::tmem_st16(tL + c0, p);
         }
+        tc::tmem_wait_st();
+        tc::tc_fence_before();
+        tc::mbar_arrive(&sh.s_empty[wg]);
         tc::fence_proxy_async();
         tc::mbar_arrive(&sh.p_full[wg]);
+        ++mine_blocks;
     }
-    // the group's row sums: per warp by a transposed butterfly, per group in
-    // shared memory (added up by the unit's end)
+    // the group's row sums: the lanes' L per warp by a transposed butterfly,
+    // per group in shared memory (added up by the unit's end)
+#pragma unroll 1
+    for (int ch = 0; ch < nch; ++ch) {
+        float v[16];
+        if (mine_blocks > 0) {
+            tc::tmem_ld16(tL + 16 * ch, v);
+            tc::tmem_wait_ld();
+        } else {
 #pragma unroll
-    for (int c0 = 0; c0 < N; c0 += 32) {
-        float v[32];
-#pragma unroll
-        for (int q = 0; q < 32; ++q) v[q] = (c0 + q < N) ? lsum[c0 + q] : 0.f;
-        const float tot = warp_transpose_reduce<false>(v, c.lane);
-        if (c0 + c.lane < N) sh.lsum[wg][c.sw][c0 + c.lane] = tot;
+            for (int q = 0; q < 16; ++q) v[q] = 0.f;
+        }
+        const float tot = warp_transpose_reduce16<false>(v, c.lane);
+        if (c.lane < 16) sh.lsum[wg][c.sw][16 * ch + c.lane] = tot;
     }
     return ok;
 }
@@ -410,17 +418,10 @@ __device__ __noinline__ bool unit_blocks(const Soft &c_, const TcArgs &a_, const
 // its pair is split.  One thread per column first works out the column's two
 // weights and its output row; then group w takes columns [w N/2, (w+1) N/2),
 // each thread its d lane.
-template <int NCH>
-__device__ __noinline__ void unit_finish(const Soft &c_, const TcArgs &a_, const PlanUnit &un_, uint32_t gb,
-                                         bool ok) {
-    // work on copies: the arguments live in memory (the caller passes
-    // references), and every inline-asm memory clobber below would force a
-    // field read through them to be repeated
-    const Soft c = c_;
-    const TcArgs a = a_;
-    const PlanUnit un = un_;
-    constexpr int N = NCH * 16, HALF = N / 2;
+__device__ __forceinline__ void unit_finish(const Soft &c, const TcArgs &a, const PlanUnit &un, uint32_t gb,
+                                            bool ok) {
     Shared &sh = *c.sh;
+    const int n = pow2_width(un.nt * a.G), half = n / 2;
     const int rows = un.nt * a.G;
     // blocks of the unit per group: group (gb % 2) has the even positions
     const int first = static_cast<int>(gb & 1u);
@@ -433,7 +434,11 @@ __device__ __noinline__ void unit_finish(const Soft &c_, const TcArgs &a_, const
     tc::tc_fence_before();
     soft_sync();  // both groups' products are complete and their offsets final
     tc::tc_fence_after();
-    if (c.st_id < N) {
+    // per-column weights and output rows, in the P tiles (every product of
+    // the unit is done; the next unit's probabilities come after this call)
+    float2 *fac = reinterpret_cast<float2 *>(c.smem + kOffP);
+    int64_t *orow = reinterpret_cast<int64_t *>(c.smem + kOffP + kNMax * sizeof(float2));
+    if (c.st_id < n) {
         const int col = c.st_id;
         const bool has0 = (first == 0 ? n_first : n_second) > 0, has1 = (first == 1 ? n_first : n_second) > 0;
         const float m0 = has0 ? sh.m_run[0][col] : -INFINITY;
@@ -460,24 +465,24 @@ __device__ __noinline__ void unit_finish(const Soft &c_, const TcArgs &a_, const
                 c.partials[off + kD + 1] = l;
             }
         }
-        sh.fac[col] = make_float2(w0, w1);
-        sh.orow[col] = off;
+        fac[col] = make_float2(w0, w1);
+        orow[col] = off;
     }
     soft_sync();
     const int d = c.tok;
     const uint32_t base = c.tmem + c.lane_base;
 #pragma unroll 1
-    for (int cc = 0; cc < HALF; cc += 8) {
-        const int col0 = c.wg * HALF + cc;
+    for (int cc = 0; cc < half; cc += 8) {
+        const int col0 = c.wg * half + cc;
         float o0[8], o1[8];
         tc::tmem_ld8(base + kColO + col0, o0);
         tc::tmem_ld8(base + kColO + kNMax + col0, o1);
         tc::tmem_wait_ld();
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            const int64_t off = sh.orow[col0 + q];
+            const int64_t off = orow[col0 + q];
             if (off < 0) continue;
-            const float2 f = sh.fac[col0 + q];
+            const float2 f = fac[col0 + q];
             // a group without blocks in this unit has weight 0 and stale O
             const float v = ((f.x != 0.f) ? f.x * o0[q] : 0.f) + ((f.y != 0.f) ? f.y * o1[q] : 0.f);
             if (un.part_row < 0)
@@ -491,68 +496,85 @@ __device__ __noinline__ void unit_finish(const Soft &c_, const TcArgs &a_, const
 }
 
 // The last unit of a split pair to finish merges all of them, both softmax
-// groups together, one warp per output row: every lane reads each partial's
-// (offset, sum) -- the same address across the warp -- and four of its d
-// values, eight partials at a time with an online maximum, so a row costs
-// one round trip to L2 per eight partials.  Partials are read with
+// groups together: warp w (of 8) takes output rows w, w+8, w+16, w+24 at
+// once, every lane four of their d values.  Each lane reads each partial's
+// (offset, sum) -- the same address across the warp -- and its d values,
+// four partials of four rows per round with an online maximum, so a round of
+// sixteen rows costs one round trip to L2.  Partials are read with
 // ld.global.cg: other CTAs wrote them during this launch.
-__device__ __noinline__ void merge_partials(const Soft &c_, const TcArgs &a_, const PlanUnit &un_) {
-    // work on copies: the arguments live in memory (the caller passes
-    // references), and every inline-asm memory clobber below would force a
-    // field read through them to be repeated
+__device__ __forceinline__ void merge_partials(const Soft &c_, const TcArgs &a_, const PlanUnit &un_) {
     const Soft c = c_;
     const TcArgs a = a_;
     const PlanUnit un = un_;
+    constexpr int kRows = 4, kParts = 4;
     const int rows = un.nt * a.G, ns = un.n_split;
     const int warp8 = c.st_id >> 5;  // 0..7 over both groups
     const float *pbase = c.partials + static_cast<int64_t>(un.part_base) * kStride;
     const int64_t kstep = static_cast<int64_t>(rows) * kStride;
     const int d4 = c.lane * 4;
-    for (int r = warp8; r < rows; r += 8) {
-        const float *row = pbase + static_cast<int64_t>(r) * kStride;
-        float m = -INFINITY, den = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int k0 = 0; k0 < ns; k0 += 8) {
-            float2 ml[8];
-            float4 o[8];
+    for (int r0 = warp8; r0 < rows; r0 += 8 * kRows) {
+        float m[kRows], den[kRows];
+        float4 acc[kRows];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (k0 + j < ns) {
-                    ml[j] = __ldcg(reinterpret_cast<const float2 *>(row + (k0 + j) * kstep + kD));
-                    o[j] = __ldcg(reinterpret_cast<const float4 *>(row + (k0 + j) * kstep + d4));
-                } else {
-                    ml[j] = make_float2(-INFINITY, 0.f);
-                    o[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < kRows; ++j) {
+            m[j] = -INFINITY;
+            den[j] = 0.f;
+            acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        for (int k0 = 0; k0 < ns; k0 += kParts) {
+            float2 ml[kRows][kParts];
+            float4 o[kRows][kParts];
+#pragma unroll
+            for (int j = 0; j < kRows; ++j) {
+                const int r = r0 + 8 * j;
+                const float *row = pbase + static_cast<int64_t>(r) * kStride;
+#pragma unroll
+                for (int q = 0; q < kParts; ++q) {
+                    if (r < rows && k0 + q < ns) {
+                        ml[j][q] = __ldcg(reinterpret_cast<const float2 *>(row + (k0 + q) * kstep + kD));
+                        o[j][q] = __ldcg(reinterpret_cast<const float4 *>(row + (k0 + q) * kstep + d4));
+                    } else {
+                        ml[j][q] = make_float2(-INFINITY, 0.f);
+                        o[j][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
                 }
             }
-            float mc = m;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) mc = fmaxf(mc, ml[j].x);
-            if (mc == -INFINITY) continue;
-            const float sc = (m == -INFINITY) ? 0.f : tc::ex2(m - mc);
-            den *= sc;
-            acc.x *= sc;
-            acc.y *= sc;
-            acc.z *= sc;
-            acc.w *= sc;
+            for (int j = 0; j < kRows; ++j) {
+                float mc = m[j];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float w = (ml[j].x == -INFINITY) ? 0.f : tc::ex2(ml[j].x - mc);
-                den = fmaf(w, ml[j].y, den);
-                acc.x = fmaf(w, o[j].x, acc.x);
-                acc.y = fmaf(w, o[j].y, acc.y);
-                acc.z = fmaf(w, o[j].z, acc.z);
-                acc.w = fmaf(w, o[j].w, acc.w);
+                for (int q = 0; q < kParts; ++q) mc = fmaxf(mc, ml[j][q].x);
+                if (mc == -INFINITY) continue;
+                const float sc = (m[j] == -INFINITY) ? 0.f : tc::ex2(m[j] - mc);
+                den[j] *= sc;
+                acc[j].x *= sc;
+                acc[j].y *= sc;
+                acc[j].z *= sc;
+                acc[j].w *= sc;
+#pragma unroll
+                for (int q = 0; q < kParts; ++q) {
+                    const float w = (ml[j][q].x == -INFINITY) ? 0.f : tc::ex2(ml[j][q].x - mc);
+                    den[j] = fmaf(w, ml[j][q].y, den[j]);
+                    acc[j].x = fmaf(w, o[j][q].x, acc[j].x);
+                    acc[j].y = fmaf(w, o[j][q].y, acc[j].y);
+                    acc[j].z = fmaf(w, o[j][q].z, acc[j].z);
+                    acc[j].w = fmaf(w, o[j][q].w, acc[j].w);
+                }
+                m[j] = mc;
             }
-            m = mc;
         }
-        const float inv = (den > 0.f) ? a.v_scale / den : 0.f;
-        const int t = un.t0 + r / a.G, g = r % a.G;
-        __nv_bfloat16 *dst = a.out + t * a.o_s0 + (un.h * a.G + g) * a.o_s1;
-        dst[(d4 + 0) * a.o_s2] = __float2bfloat16_rn(acc.x * inv);
-        dst[(d4 + 1) * a.o_s2] = __float2bfloat16_rn(acc.y * inv);
-        dst[(d4 + 2) * a.o_s2] = __float2bfloat16_rn(acc.z * inv);
-        dst[(d4 + 3) * a.o_s2] = __float2bfloat16_rn(acc.w * inv);
+#pragma unroll
+        for (int j = 0; j < kRows; ++j) {
+            const int r = r0 + 8 * j;
+            if (r >= rows) continue;
+            const float inv = (den[j] > 0.f) ? a.v_scale / den[j] : 0.f;
+            const int t = un.t0 + r / a.G, g = r % a.G;
+            __nv_bfloat16 *dst = a.out + t * a.o_s0 + (un.h * a.G + g) * a.o_s1;
+            dst[(d4 + 0) * a.o_s2] = __float2bfloat16_rn(acc[j].x * inv);
+            dst[(d4 + 1) * a.o_s2] = __float2bfloat16_rn(acc[j].y * inv);
+            dst[(d4 + 2) * a.o_s2] = __float2bfloat16_rn(acc[j].z * inv);
+            dst[(d4 + 3) * a.o_s2] = __float2bfloat16_rn(acc[j].w * inv);
+        }
     }
 }
 
@@ -587,7 +609,7 @@ __device__ __forceinline__ void resolve_ticket(const Soft &c, const TcArgs &a, P
 
 __global__ void __launch_bounds__(kThreads, 1)
 attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                    const __grid_constant__ CUtensorMap tmap_q, const TcArgs a) {
+                    const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Shared &sh = *reinterpret_cast<Shared *>(smem + kOffShared);
@@ -613,6 +635,10 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         tc::mbar_init(&sh.q_full, 1);
         tc::mbar_init(&sh.q_empty, 1);
         for (int i = 0; i < 3; ++i) tc::mbar_init(&sh.drain[i], 1);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&sh.meta_full[i], 32);
+            tc::mbar_init(&sh.meta_empty[i], 2 * kSoftThreads);
+        }
         for (int i = 0; i < 4; ++i) {
             tc::mbar_init(&sh.unit_full[i], 1);
             tc::mbar_init(&sh.unit_empty[i], kUnitArrivals);
@@ -815,13 +841,20 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         // thread; the E4M3 stage is released once the Q K^T of the same block
         // is done too.
         const int ct = threadIdx.x - kWarpConv * 32;
-        uint8_t *nvalid = sh.nvalid[ct >> 5];
+        const int cw = ct >> 5;
+        uint8_t *nvalid = sh.nvalid[cw];
+        const float *cfac_g = reinterpret_cast<const float *>(a.ws + a.lay.cfac);
         uint32_t gb = 0, uc = 0;
         for (;;) {
             const int slot = uc & 3;
             if (!wait_or_abort(sh, &sh.unit_full[slot], (uc >> 2) & 1, &hdr->status)) break;
             const PlanUnit un = sh.ring[slot];
             if (un.pair < 0) break;
+            // warp 0 also stages the unit's metadata for the softmax groups:
+            // block list, key limit per row, logit factor per query column
+            const int mb = uc & 1;
+            if (cw == 0 && uc >= 2 && !wait_or_abort(sh, &sh.meta_empty[mb], ((uc >> 1) - 1) & 1, &hdr->status))
+                break;
             // tokens of each block valid for some row of the unit (each warp
             // its own copy); the rest -- slots no request owns may hold any
             // code, NaN included -- are written as zeros
@@ -839,7 +872,18 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
                     const int lj = __shfl_sync(0xffffffffu, my_lim, j);
                     if ((e.mask >> j) & 1) m = max(m, lj);
                 }
-                if (i < un.count) nvalid[i] = static_cast<uint8_t>(min(128, max(0, m - e.block * 128)));
+                if (i < un.count) {
+                    nvalid[i] = static_cast<uint8_t>(min(128, max(0, m - e.block * 128)));
+                    if (cw == 0) sh.ent[mb][i] = e;
+                }
+            }
+            if (cw == 0) {
+                if (lane < 16) sh.Lj[mb][lane] = (lane < un.nt) ? my_lim : 0;
+                for (int r = lane; r < kNMax; r += 32)
+                    sh.cfac[mb][r] = (r < un.nt * a.G)
+                                         ? cfac_g[static_cast<int64_t>(un.t0 + r / a.G) * a.Hq + un.h * a.G + r % a.G]
+                                         : 0.f;
+                tc::mbar_arrive(&sh.meta_full[mb]);
             }
             __syncwarp();
             bool ok = true;
@@ -911,76 +955,47 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         c.tok = c.sw * 32 + lane;                 // token lane of S, d lane of O
         c.lane_base = static_cast<uint32_t>(c.sw * 32) << 16;
         c.tmem = tmem;
-        uint32_t gb = 0;
-        bool stop = false;
-        const float *cfac = reinterpret_cast<const float *>(a.ws + a.lay.cfac);
-
-        // per-unit metadata is loaded one unit ahead into registers: one list
-        // entry, one key limit and one logit factor per thread
-        PlanEntry pe{};
-        int pL = 0;
-        float pcf = 0.f;
-        auto prefetch = [&](const PlanUnit &x) {
-            pe = (c.st_id < x.count) ? lists[x.entry + c.st_id] : PlanEntry{};
-            int r;
-            pL = (c.st_id < x.nt)
-                     ? static_cast<int>(token_limit(a.ri, a.ri_s0, a.sl, a.sl_s0, x.t0 + c.st_id, a.R, a.NB, &r))
-                     : 0;
-            pcf = (c.st_id < x.nt * a.G)
-                      ? cfac[static_cast<int64_t>(x.t0 + c.st_id / a.G) * a.Hq + x.h * a.G + c.st_id % a.G]
-                      : 0.f;
-        };
-        uint32_t uc = 0;
+        uint32_t gb = 0, uc = 0;
         PendingMerge pending{};
         pending.un.pair = -1;
+        // uniform decisions of both groups: bit 0 abort, bit 1 no more units
+        auto vote = [&](int mine) -> int {
+            if (lane == 0) sh.unit_vote[warp - kWarpSoft] = mine;
+            soft_sync();
+            int all = 0;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) all |= sh.unit_vote[w];
+            soft_sync();
+            return all;
+        };
         PlanUnit un{};
         un.pair = -1;
         if (wait_or_abort(sh, &sh.unit_full[0], 0, c.status)) un = sh.ring[0];
-        if (un.pair >= 0) prefetch(un);
-        while (un.pair >= 0 && !stop) {
-            // the next unit's record (published by the producer before it issues
-            // this unit's loads) and its metadata, loaded during this unit
-            PlanUnit un_next{};
-            un_next.pair = -1;
-            if (wait_or_abort(sh, &sh.unit_full[(uc + 1) & 3], ((uc + 1) >> 2) & 1, c.status))
-                un_next = sh.ring[(uc + 1) & 3];
-            if (c.st_id < un.count) sh.ent[c.st_id] = pe;
-            if (c.st_id < 16) sh.Lj[c.st_id] = pL;
-            if (c.st_id < kNMax) sh.cfac[c.st_id] = pcf;
+        int state = vote((aborted(sh) ? 1 : 0) | (un.pair < 0 ? 2 : 0));
+        while (state == 0) {
+            c.mb = uc & 1;
+            wait_or_abort(sh, &sh.meta_full[c.mb], (uc >> 1) & 1, c.status);  // a timeout shows in the votes
             if (c.st_id < 2 * kNMax) sh.m_run[c.st_id / kNMax][c.st_id % kNMax] = -INFINITY;
             soft_sync();
-            if (un_next.pair >= 0) prefetch(un_next);
-
-            const int nch = pow2_width(un.nt * a.G) / 16;
-            bool ok;
-            if (nch == 1) {
-                ok = unit_blocks<1>(c, a, un, gb);
-                unit_finish<1>(c, a, un, gb, ok);
-            } else if (nch == 2) {
-                ok = unit_blocks<2>(c, a, un, gb);
-                unit_finish<2>(c, a, un, gb, ok);
-            } else {
-                ok = unit_blocks<4>(c, a, un, gb);
-                unit_finish<4>(c, a, un, gb, ok);
-            }
+            const bool ok = unit_blocks(c, a, un, gb);
+            unit_finish(c, a, un, gb, ok);
+            tc::mbar_arrive(&sh.meta_empty[c.mb]);
             gb += un.count;
-            // unit-level abort decision, uniform over both groups
-            if (lane == 0) sh.unit_vote[warp - kWarpSoft] = (aborted(sh) || !ok) ? 1 : 0;
-            soft_sync();
-            int any = 0;
-#pragma unroll
-            for (int w = 0; w < 8; ++w) any |= sh.unit_vote[w];
-            stop = any != 0;
-            soft_sync();
-            if (!stop) {
+            // the next unit's record (published before this unit's loads)
+            PlanUnit nx{};
+            nx.pair = -1;
+            if (wait_or_abort(sh, &sh.unit_full[(uc + 1) & 3], ((uc + 1) >> 2) & 1, c.status))
+                nx = sh.ring[(uc + 1) & 3];
+            state = vote(((aborted(sh) || !ok) ? 1 : 0) | (nx.pair < 0 ? 2 : 0));
+            if (!(state & 1)) {
                 resolve_ticket(c, a, pending);
                 if (un.part_row >= 0) take_ticket(c, un, pending);
+                if (state & 2) resolve_ticket(c, a, pending);
             }
             tc::mbar_arrive(&sh.unit_empty[uc & 3]);
-            un = un_next;
+            un = nx;
             ++uc;
         }
-        if (!stop) resolve_ticket(c, a, pending);
     }
 
     tc::tc_fence_before();

@@ -11,31 +11,35 @@
 //    into several units merges its partials in the last unit to finish (an
 //    atomic ticket, no waiting on other CTAs).
 //
-//  * Roles (12 warps).  Warp 0 streams each selected page's K and V tile
+//  * Roles (16 warps).  Warp 0 streams each selected page's K and V tile
 //    (128 tokens x 128 bytes of one kv head) with TMA into a ring of stages,
-//    straight from the paged cache through the block table.  Warp 1 issues
-//    every tcgen05.mma.  Warps 2-3 widen V from E4M3 to f16.  Warps 4-7 and
+//    straight from the paged cache through the block table.  Warps 4-7 and
 //    8-11 are two softmax groups that take alternate blocks of a unit, each
-//    with its own accumulators, and combine them at the unit's end.
+//    with its own accumulators, and combine them at the unit's end.  Warp 1
+//    issues every Q K^T, warps 2 and 3 the P V of one group each (an MMA
+//    costs its issuing thread over a hundred cycles however small the tile,
+//    so the issue is spread over three threads).  Warps 12-15 widen V.
 //
 //  * Contractions.  Keys lie on the 128 TMEM lanes and the group's query rows
 //    (rows x q heads, padded to N = 16/32/64) on columns:
 //        S^T[tok][n]  = K[tok][:] . Qs[n][:]      kind::f8f6f4, E4M3 K as read
 //        O^T[d][n]   += V^T[d][tok] . P[tok][n]    kind::f16, f16 V and P
 //    Queries enter as E4M3 terms (q = t0 + t1 (+ t2), each row scaled by a
-//    power of two into E4M3 range, the factor folded into the logit scale).
-//    Two terms hold a bf16 query exactly (4 + 4 significant bits); with at
-//    least 8 q heads per kv head they are stacked along N, so one product
-//    per k-step reads the K tile once and the softmax adds the two halves of
-//    S.  Other query types take three terms accumulated into the same
-//    columns.  V is widened to f16 exactly (cvt.rn.f16x2.e4m3x2).
-//    Probabilities are f16 (normal down to 2^-14, so tiny weights survive);
-//    their row sums accumulate per thread and are reduced once per unit.
+//    power of two into E4M3 range, the factor folded into the logit scale):
+//    two terms hold a bf16 query exactly (4 + 4 significant bits), other
+//    query types take three.  Two terms of a narrow group are stacked along
+//    N (one product per k-step, the softmax adds the halves); otherwise the
+//    terms accumulate into the same columns.  V is
+//    widened to f16 exactly (cvt.rn.f16x2.e4m3x2).  Probabilities are f16
+//    (normal down to 2^-14, so tiny weights survive).
 //
 //  * Softmax.  A group owns the 128 token lanes of its S and the 128 d lanes
-//    of its O.  Its exponent offset per query row is a running maximum raised
-//    only when a logit exceeds it by more than 2^6 (then O and L are rescaled
-//    in tensor memory): most blocks need no cross-lane reduction.
+//    of its O.  A thread reads its lane's logits of a block from tensor
+//    memory in one batch; its row sums stay in registers and are reduced
+//    over the lanes once per unit.  The exponent offset per query row is a
+//    running maximum raised only when a logit exceeds it by more than 2^6
+//    (then O is rescaled in tensor memory): most blocks need no cross-lane
+//    reduction.
 //
 // Synchronisation uses mbarriers between the roles, every wait bounded (a
 // timeout sets bit 0 of the workspace status word and the CTA winds down).
@@ -69,13 +73,13 @@ constexpr int kD = 128;
 constexpr int kTerms = kQueryTerms;   // E4M3 terms per query element (12 significant bits)
 constexpr int kStride = kD + kPartialStride;
 
-// tensor memory columns (512 allocated): S of softmax group w at
-// kColS + w * kSCols (N columns, or 2N when the query terms are stacked), O
-// at kColO + w * kNMax, and the per-lane row sums L (each thread its token
-// lane, added up over the lanes at the unit's end) at kColL + w * kNMax
-constexpr uint32_t kSCols = 2 * kNMax;
-constexpr uint32_t kColS = 0, kColO = 2 * kSCols, kColL = kColO + 2 * kNMax;
-static_assert(kColL + 2 * kNMax <= 512, "tensor memory columns");
+// tensor memory columns (512 allocated): two S buffers per softmax group
+// (the group's k-th block uses buffer k % 2) at kColS + (2 w + k % 2) * kNMax,
+// O of group w at kColO + w * kNMax
+constexpr uint32_t kSCols = kNMax;
+constexpr uint32_t kColS = 0, kColO = 4 * kSCols;
+constexpr uint32_t kTmemCols = 512;
+static_assert(kColO + 2 * kNMax <= kTmemCols, "tensor memory columns");
 
 struct TcArgs {
     const int32_t *ri;
@@ -85,7 +89,8 @@ struct TcArgs {
     __nv_bfloat16 *out;
     int64_t o_s0, o_s1, o_s2;
     int32_t T, Hq, Hkv, G, R, NB, gmax;
-    int32_t stacked;  // 1: two query terms stacked along N (loaded per token), 0: three accumulated
+    int32_t terms;      // E4M3 query terms: 2 for bf16 queries (exact), 3 otherwise
+    int32_t per_token;  // query terms loaded token by token (G >= 8), else one box per group
     float v_scale;
     char *ws;
     PlanLayout lay;
@@ -102,7 +107,8 @@ struct __align__(16) Shared {
         float lsum[2][4][kNMax];
     };
     uint64_t kv_full[kStages], kv_empty[kStages];
-    uint64_t s_full[2], s_empty[2], p_full[2], v_full[2], pv_done[2];
+    uint64_t s_full[2][2], s_empty[2][2];  // [group][S buffer]
+    uint64_t p_full[2], v_full[2], pv_done[2];
     uint64_t q_full, q_empty, drain[3];
     uint64_t meta_full[2], meta_empty[2];  // unit metadata buffers: V-widening warp 0 -> softmax
     uint64_t unit_full[4], unit_empty[4];  // ring of unit records, producer -> everyone
@@ -132,17 +138,25 @@ constexpr int kOffShared = kOffP + 2 * kP16Tile;
 constexpr int kSmemBytes = kOffShared + static_cast<int>(sizeof(Shared)) + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
-// a unit record is released by the Q K^T issuer, the two P V issuers, both
-// softmax groups and the V-widening warps
+// a unit record is released by the three MMA issuers, both softmax groups and
+// the V-widening warps
 constexpr uint32_t kUnitArrivals = 3 + 2 * kSoftThreads + kConvThreads;
 
 // Registers: the launch gives 128 per thread (512 x 128 = 65536); warps 0-3
-// (TMA, the MMA issuers) drop to 56, the V-widening warps to 72, and the two
-// softmax groups rise to 192: 128 x 56 + 128 x 72 + 256 x 192 = 65536.
-constexpr uint32_t kRegsIssue = 56, kRegsConv = 72, kRegsSoft = 192;
+// (TMA, the MMA issuers, one idle warp) and the V-widening warps drop to 64,
+// and the two softmax groups rise to 192: 256 x 64 + 256 x 192 = 65536.
+constexpr uint32_t kRegsIssue = 64, kRegsConv = 64, kRegsSoft = 192;
 static_assert(128 * kRegsIssue + 128 * kRegsConv + 256 * kRegsSoft <= kThreads * 128, "register split");
 
 __device__ __forceinline__ int pow2_width(int n) { return n <= 16 ? 16 : n <= 32 ? 32 : 64; }
+
+// Two query terms of a group of width n are stacked along N (one Q K^T per
+// k-step, 2n logit columns that the softmax adds) when they fit one S buffer
+// and the terms are loaded token by token; otherwise the terms accumulate
+// into the same n columns.
+__device__ __forceinline__ bool stacked_terms(int terms, int per_token, int n) {
+    return terms == 2 && per_token && n <= 32;
+}
 
 // swizzle of an f16 [tokens][n] tile whose rows are 2n bytes
 __device__ __forceinline__ tc::Swizzle p_swizzle(int n) {
@@ -190,41 +204,6 @@ struct Soft {
     int mb;     // metadata buffer of the current unit
 };
 
-// One 16-column chunk of this thread's logits of a block, masked (-inf
-// where the column is not valid on this token lane): u[q] = s * cfac - m_run
-// (log2 units) with kOffset, s * cfac without.  In stacked mode the second
-// query term's logits (N columns further on) are added first.  Returns the
-// chunk's maximum.
-template <bool kOffset>
-__device__ __forceinline__ float load_chunk(const Shared &sh, int mb, bool stacked, int n, uint32_t tS,
-                                            const float *m_run, uint32_t bits, int c0, float (&u)[16]) {
-    tc::tmem_ld16(tS + c0, u);
-    if (stacked) {
-        float v[16];
-        tc::tmem_ld16(tS + n + c0, v);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int q = 0; q < 16; ++q) u[q] += v[q];
-    } else {
-        tc::tmem_wait_ld();
-    }
-    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-    for (int c4 = 0; c4 < 16; c4 += 4) {
-        const float4 cf = *reinterpret_cast<const float4 *>(&sh.cfac[mb][c0 + c4]);
-        float4 mr = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (kOffset) mr = *reinterpret_cast<const float4 *>(&m_run[c0 + c4]);
-        const float cfs[4] = {cf.x, cf.y, cf.z, cf.w}, mrs[4] = {mr.x, mr.y, mr.z, mr.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float v = kOffset ? fmaf(u[c4 + q], cfs[q], -mrs[q]) : u[c4 + q] * cfs[q];
-            u[c4 + q] = ((bits >> (c4 + q)) & 1) ? v : -INFINITY;
-            mx[q] = fmaxf(mx[q], u[c4 + q]);
-        }
-    }
-    return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-}
-
 // Reduction over the 32 lanes of a warp of 16 per-lane columns, transposed:
 // lanes l and l+16 end with the reduction of column l & 15.
 template <bool kMax>
@@ -248,24 +227,65 @@ __device__ __forceinline__ float warp_transpose_reduce16(float (&v)[16], int lan
     return v[0];
 }
 
+// This thread's logits of one block (its token lane, N = 16 * nch columns)
+// read from S in one batch and masked (-inf where the column is not valid on
+// the lane): u = s * cfac - m_run (log2 units) with kOffset, s * cfac
+// without.  Returns the maximum over the columns.
+template <bool kOffset>
+__device__ __forceinline__ float load_u(const Shared &sh, int mb, int nch, bool stacked, uint32_t tS,
+                                        const float *m_run, uint64_t colmask, float (&u)[kNMax]) {
+    // stacked: the second term's logits follow in chunks nch..2nch-1
+    const int nld = stacked ? 2 * nch : nch;
+#pragma unroll
+    for (int ch = 0; ch < kNMax / 16; ++ch)
+        if (ch < nld) tc::tmem_ld16(tS + 16 * ch, *reinterpret_cast<float(*)[16]>(&u[16 * ch]));
+    tc::tmem_wait_ld();
+    if (stacked) {  // n = 16 or 32 (compile-time indices keep u in registers)
+        if (nch == 1) {
+#pragma unroll
+            for (int col = 0; col < 16; ++col) u[col] += u[16 + col];
+        } else {
+#pragma unroll
+            for (int col = 0; col < 32; ++col) u[col] += u[32 + col];
+        }
+    }
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int c4 = 0; c4 < kNMax; c4 += 4) {
+        if (c4 < 16 * nch) {
+            const float4 cf = *reinterpret_cast<const float4 *>(&sh.cfac[mb][c4]);
+            float4 mr = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (kOffset) mr = *reinterpret_cast<const float4 *>(&m_run[c4]);
+            const float cfs[4] = {cf.x, cf.y, cf.z, cf.w}, mrs[4] = {mr.x, mr.y, mr.z, mr.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int col = c4 + q;
+                const float v = kOffset ? fmaf(u[col], cfs[q], -mrs[q]) : u[col] * cfs[q];
+                u[col] = ((colmask >> col) & 1) ? v : -INFINITY;
+                mx[q] = fmaxf(mx[q], u[col]);
+            }
+        }
+    }
+    return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+}
+
 // The blocks of one unit that fall to this softmax group (global block index
-// b with b % 2 == group), N = 16 * nch query columns processed 16 at a time:
-// a first pass over S finds whether an offset must be raised (a vote of the
-// group), a second computes the probabilities.  Returns false when the CTA
-// must stop (an abort, decided uniformly within the group).
+// b with b % 2 == group), N = 16 * nch query columns.  Returns false when the
+// CTA must stop (an abort, decided uniformly within the group).
 __device__ __forceinline__ bool unit_blocks(const Soft &c, const TcArgs &a, const PlanUnit &un, uint32_t gb) {
     Shared &sh = *c.sh;
     const int wg = c.wg, mb = c.mb;
     const int n = pow2_width(un.nt * a.G), nch = n / 16;
-    const bool stacked = a.stacked != 0;
+    const bool stacked = stacked_terms(a.terms, a.per_token, n);
     const uint64_t gmask = (a.G >= 64) ? ~0ull : ((1ull << a.G) - 1);
-    const uint32_t tS = c.tmem + kColS + wg * kSCols + c.lane_base;
     const uint32_t tO = c.tmem + kColO + wg * kNMax + c.lane_base;
-    const uint32_t tL = c.tmem + kColL + wg * kNMax + c.lane_base;
     float *m_run = sh.m_run[wg];
     uint8_t *pb = c.smem + kOffP + wg * kP16Tile;
+    // row sums of this thread's token lane, reduced over the group at the end
+    float lsum[kNMax];
+#pragma unroll
+    for (int col = 0; col < kNMax; ++col) lsum[col] = 0.f;
     bool ok = true;
-    int mine_blocks = 0;
 
     for (int i = ((gb & 1u) == static_cast<uint32_t>(wg)) ? 0 : 1; i < un.count; i += 2) {
         const uint32_t b = gb + i;  // b % 2 == wg
@@ -276,18 +296,16 @@ __device__ __forceinline__ bool unit_blocks(const Soft &c, const TcArgs &a, cons
         uint64_t colmask = 0;
         for (int j = 0; j < un.nt; ++j)
             if (((e.mask >> j) & 1) && c.tok < sh.Lj[mb][j] - e.block * 128) colmask |= gmask << (j * a.G);
-        // pass 1: the largest logit relative to the offsets; a column without
-        // an offset yet (m = -inf) gives +inf where valid, forcing a raise
+        // logits relative to the offsets; a column without an offset yet
+        // (m = -inf) gives +inf where valid, which forces a raise
+        float u[kNMax];
         float umax = -INFINITY;
-        const bool have = warp_wait(sh, &sh.s_full[wg], k & 1, c.status);
+        const int sb = k & 1;  // S buffer of this block
+        const uint32_t tS = c.tmem + kColS + (2 * wg + sb) * kSCols + c.lane_base;
+        const bool have = warp_wait(sh, &sh.s_full[wg][sb], (k >> 1) & 1, c.status);
         if (have) {
             tc::tc_fence_after();
-#pragma unroll 1
-            for (int ch = 0; ch < nch; ++ch) {
-                float u[16];
-                umax = fmaxf(umax, load_chunk<true>(sh, mb, stacked, n, tS, m_run,
-                                                    static_cast<uint32_t>(colmask >> (16 * ch)), 16 * ch, u));
-            }
+            umax = load_u<true>(sh, mb, nch, stacked, tS, m_run, colmask, u);
         }
         // votes alternate between two slots by block parity: a warp can be at
         // most one block ahead of the slowest reader of its group
@@ -297,21 +315,25 @@ __device__ __forceinline__ bool unit_blocks(const Soft &c, const TcArgs &a, cons
         const int vote = sh.vote[wg][k & 1][0] | sh.vote[wg][k & 1][1] | sh.vote[wg][k & 1][2] | sh.vote[wg][k & 1][3];
         if (vote & 2) {
             tc::tc_fence_before();
-            tc::mbar_arrive(&sh.s_empty[wg]);
+            tc::mbar_arrive(&sh.s_empty[wg][sb]);
             ok = false;
             break;
         }
         if (vote & 1) {
             // raise: an offset moves to its column's block maximum of
             // s * cfac where that exceeds it by more than 2^kRaise (or where
-            // the column had none); O and L are scaled by 2^(old - new)
-#pragma unroll 1
-            for (int ch = 0; ch < nch; ++ch) {
-                float u[16];
-                load_chunk<false>(sh, mb, stacked, n, tS, m_run, static_cast<uint32_t>(colmask >> (16 * ch)), 16 * ch,
-                                  u);
-                const float mx = warp_transpose_reduce16<true>(u, c.lane);
-                if (c.lane < 16) sh.red[wg][c.sw][16 * ch + c.lane] = mx;
+            // the column had none); O and the sums are scaled by
+            // 2^(old - new).  S is read again without offsets.
+            load_u<false>(sh, mb, nch, stacked, tS, m_run, colmask, u);
+#pragma unroll
+            for (int ch = 0; ch < kNMax / 16; ++ch) {
+                if (ch < nch) {
+                    float v[16];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) v[q] = u[16 * ch + q];
+                    const float mx = warp_transpose_reduce16<true>(v, c.lane);
+                    if (c.lane < 16) sh.red[wg][c.sw][16 * ch + c.lane] = mx;
+                }
             }
             group_sync(wg);
             if (c.sw == 0) {
@@ -332,83 +354,72 @@ __device__ __forceinline__ bool unit_blocks(const Soft &c, const TcArgs &a, cons
                 if (c.lane == 0) sh.rescale[wg] = any;
             }
             group_sync(wg);
+#pragma unroll
+            for (int col = 0; col < kNMax; ++col) {
+                if (col < n) {
+                    lsum[col] *= sh.alpha[wg][col];
+                    // relative to the new offsets (a still unset offset means
+                    // the column is masked throughout)
+                    const float m = m_run[col];
+                    u[col] = (u[col] == -INFINITY || m == -INFINITY) ? -INFINITY : u[col] - m;
+                }
+            }
             if (sh.rescale[wg] && i >= 2) {
-                // O and L hold this group's earlier blocks of the unit: wait
-                // for its last product, then scale both in place
+                // O holds this group's earlier blocks of the unit: wait for
+                // its last product, then scale it in place
                 if (warp_wait(sh, &sh.pv_done[wg], (k - 1) & 1, c.status)) {
                     tc::tc_fence_after();
 #pragma unroll 1
-                    for (int ch = 0; ch < 2 * nch; ++ch) {
-                        const int cc = (ch % nch) * 16;
-                        const uint32_t addr = (ch < nch ? tO : tL) + cc;
+                    for (int ch = 0; ch < nch; ++ch) {
                         float v[16];
-                        tc::tmem_ld16(addr, v);
+                        tc::tmem_ld16(tO + 16 * ch, v);
                         tc::tmem_wait_ld();
 #pragma unroll
-                        for (int q = 0; q < 16; ++q) v[q] *= sh.alpha[wg][cc + q];
-                        tc::tmem_st16(addr, v);
+                        for (int q = 0; q < 16; ++q) v[q] *= sh.alpha[wg][16 * ch + q];
+                        tc::tmem_st16(tO + 16 * ch, v);
                         tc::tmem_wait_st();
                     }
                 }
             }
         }
+        tc::tc_fence_before();
+        tc::mbar_arrive(&sh.s_empty[wg][sb]);
 
         // this group's P tile was read by the product of its previous block
         if (b >= 2) wait_or_abort(sh, &sh.pv_done[wg], (k - 1) & 1, c.status);
-        // pass 2: probabilities p = 2^u <= 64 in f16 (11-bit significand,
-        // normal down to 2^-14), the B operand of P V; masked columns have
-        // u = -inf, p = 0.  A column whose offset is still unset is masked
-        // throughout.  The lane's row sums in L gain p (the group's first
-        // block of the unit sets them).
-        const bool first = i < 2;
-#pragma unroll 1
-        for (int ch = 0; ch < nch; ++ch) {
-            const int c0 = 16 * ch;
-            float u[16];
-            if (have)
-                load_chunk<true>(sh, mb, stacked, n, tS, m_run, static_cast<uint32_t>(colmask >> c0), c0, u);
-            float l[16];
-            if (!first) tc::tmem_ld16(tL + c0, l);
-            float p[16];
+        // probabilities p = 2^u <= 64 in f16 (11-bit significand, normal down
+        // to 2^-14), the B operand of P V; masked columns have u = -inf, p = 0
 #pragma unroll
-            for (int q = 0; q < 16; ++q) p[q] = (have && m_run[c0 + q] != -INFINITY) ? tc::ex2(u[q]) : 0.f;
+        for (int c8 = 0; c8 < kNMax; c8 += 8) {
+            if (c8 < n) {
+                float p[8];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+                for (int q = 0; q < 8; ++q) {
+                    p[q] = have ? tc::ex2(u[c8 + q]) : 0.f;
+                    lsum[c8 + q] += p[q];
+                }
                 uint4 w;
-                w.x = tc::f32x2_to_f16x2(p[8 * h + 0], p[8 * h + 1]);
-                w.y = tc::f32x2_to_f16x2(p[8 * h + 2], p[8 * h + 3]);
-                w.z = tc::f32x2_to_f16x2(p[8 * h + 4], p[8 * h + 5]);
-                w.w = tc::f32x2_to_f16x2(p[8 * h + 6], p[8 * h + 7]);
-                *reinterpret_cast<uint4 *>(pb + tc::swz_offset(c.tok, (c0 + 8 * h) * 2, 2 * n)) = w;
+                w.x = tc::f32x2_to_f16x2(p[0], p[1]);
+                w.y = tc::f32x2_to_f16x2(p[2], p[3]);
+                w.z = tc::f32x2_to_f16x2(p[4], p[5]);
+                w.w = tc::f32x2_to_f16x2(p[6], p[7]);
+                *reinterpret_cast<uint4 *>(pb + tc::swz_offset(c.tok, c8 * 2, 2 * n)) = w;
             }
-            if (!first) {
-                tc::tmem_wait_ld();
-#pragma unroll
-                for (int q = 0; q < 16; ++q) p[q] += l[q];
-            }
-            tc::tmem_st16(tL + c0, p);
         }
-        tc::tmem_wait_st();
-        tc::tc_fence_before();
-        tc::mbar_arrive(&sh.s_empty[wg]);
         tc::fence_proxy_async();
         tc::mbar_arrive(&sh.p_full[wg]);
-        ++mine_blocks;
     }
-    // the group's row sums: the lanes' L per warp by a transposed butterfly,
-    // per group in shared memory (added up by the unit's end)
-#pragma unroll 1
-    for (int ch = 0; ch < nch; ++ch) {
-        float v[16];
-        if (mine_blocks > 0) {
-            tc::tmem_ld16(tL + 16 * ch, v);
-            tc::tmem_wait_ld();
-        } else {
+    // the group's row sums: per warp by a transposed butterfly, per group in
+    // shared memory (added up by the unit's end)
 #pragma unroll
-            for (int q = 0; q < 16; ++q) v[q] = 0.f;
+    for (int ch = 0; ch < kNMax / 16; ++ch) {
+        if (ch < nch) {
+            float v[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) v[q] = lsum[16 * ch + q];
+            const float tot = warp_transpose_reduce16<false>(v, c.lane);
+            if (c.lane < 16) sh.lsum[wg][c.sw][16 * ch + c.lane] = tot;
         }
-        const float tot = warp_transpose_reduce16<false>(v, c.lane);
-        if (c.lane < 16) sh.lsum[wg][c.sw][16 * ch + c.lane] = tot;
     }
     return ok;
 }
@@ -626,8 +637,10 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
             tc::mbar_init(&sh.kv_empty[i], kConvThreads + 1);  // V widened + Q K^T done
         }
         for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(&sh.s_full[i], 1);
-            tc::mbar_init(&sh.s_empty[i], kSoftThreads);
+            for (int j = 0; j < 2; ++j) {
+                tc::mbar_init(&sh.s_full[i][j], 1);
+                tc::mbar_init(&sh.s_empty[i][j], kSoftThreads);
+            }
             tc::mbar_init(&sh.p_full[i], kSoftThreads);
             tc::mbar_init(&sh.v_full[i], kConvThreads);
             tc::mbar_init(&sh.pv_done[i], 1);
@@ -646,7 +659,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         sh.abort = 0;
         tc::fence_mbar_init();
     }
-    if (warp == 1) tc::tmem_alloc(&sh.tmem_base, 512);
+    if (warp == 1) tc::tmem_alloc(&sh.tmem_base, kTmemCols);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
@@ -663,7 +676,6 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
             tc::prefetch_tmap(&tmap_q);
             const uint64_t policy = tc::policy_evict_first();
             const uint32_t qbox = static_cast<uint32_t>(a.G * a.gmax * 128);  // one term of a group
-            const uint32_t qrow = static_cast<uint32_t>(a.G * 128);            // one term of one token
             // Units are claimed from the global work counter (in plan order)
             // and handed to the other roles through a 4-slot ring; claims run
             // two units ahead so a record has arrived by the time it is
@@ -691,18 +703,20 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
                 if (un.pair < 0) break;
                 // the group's query terms, once the previous unit's last Q K^T is done
                 if (uc > 0 && !wait_or_abort(sh, &sh.q_empty, (uc - 1) & 1, &hdr->status)) break;
-                if (a.stacked) {
-                    // term t of token j at rows t*N + j*G (1 KiB aligned: G >= 8)
+                if (a.per_token) {
+                    // term t of token j at rows t*N + j*G when stacked, else
+                    // t*64 + j*G (G >= 8: 1 KiB aligned)
                     const int n = pow2_width(un.nt * a.G);
-                    tc::mbar_arrive_expect_tx(&sh.q_full, 2 * un.nt * qrow);
-                    for (int term = 0; term < 2; ++term)
+                    const int tstride = stacked_terms(a.terms, a.per_token, n) ? n : kNMax;
+                    tc::mbar_arrive_expect_tx(&sh.q_full, a.terms * un.nt * a.G * 128);
+                    for (int term = 0; term < a.terms; ++term)
                         for (int j = 0; j < un.nt; ++j)
-                            tc::tma_load_3d(smem + kOffQ + (term * n + j * a.G) * 128, &tmap_q, &sh.q_full, 0,
+                            tc::tma_load_3d(smem + kOffQ + (term * tstride + j * a.G) * 128, &tmap_q, &sh.q_full, 0,
                                             un.h * a.G, term * a.T + un.t0 + j, policy);
                 } else {
                     // term t of the group at rows t*64
-                    tc::mbar_arrive_expect_tx(&sh.q_full, kTerms * qbox);
-                    for (int term = 0; term < kTerms; ++term)
+                    tc::mbar_arrive_expect_tx(&sh.q_full, a.terms * qbox);
+                    for (int term = 0; term < a.terms; ++term)
                         tc::tma_load_3d(smem + kOffQ + term * kQBytes, &tmap_q, &sh.q_full, 0, un.h * a.G,
                                         term * a.T + un.t0, policy);
                 }
@@ -733,11 +747,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         }
     } else if (warp == 1) {
         // -------------------------------------------------------- Q K^T issuer
-        // A tcgen05.mma costs its issuing thread over a hundred cycles however
-        // small the tile, so the products are spread over three threads in
-        // different warps: this one issues every Q K^T, warps 2 and 3 the P V
-        // of one softmax group each.  Descriptors are built once and advanced
-        // by their 16-byte address field.
+        // An MMA costs its issuing thread over a hundred cycles however small
+        // the tile, so the products are spread over three threads in
+        // different warps: this one issues every Q K^T (block order), warps 2
+        // and 3 the P V of one softmax group each.  Descriptors are built once
+        // and advanced by their 16-byte address field.
         if (lane == 0) {
             uint32_t gb = 0, uc = 0;
             const uint64_t dK0 = tc::smem_desc(tc::smem_u32(smem + kOffK), 16, 1024, tc::kSw128);
@@ -749,34 +763,37 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
                 const PlanUnit un = sh.ring[slot];
                 if (un.pair < 0) break;
                 const int n = pow2_width(un.nt * a.G);
-                // E4M3 x E4M3, both K-major; stacked terms give 2n columns
-                const uint32_t idesc_qk = tc::idesc_m128(a.stacked ? 2 * n : n, false, false);
+                const bool stacked = stacked_terms(a.terms, a.per_token, n);
+                // E4M3 x E4M3, both K-major
+                const uint32_t idesc_qk = tc::idesc_m128(stacked ? 2 * n : n, false, false);
+                const int tstride = ((a.per_token && stacked) ? n : kNMax) * 128;  // bytes between query terms
                 if (!wait_or_abort(sh, &sh.q_full, uc & 1, status)) break;
                 tc::tc_fence_after();
                 if (un.count == 0) tc::mma_commit(&sh.q_empty);
                 bool ok = true;
                 for (int i = 0; i < un.count; ++i) {
                     const uint32_t b = gb + i;
-                    const int st = b % kStages, w = b & 1;
+                    const int w = b & 1;
+                    const uint32_t k = b >> 1;  // the group's block ordinal
+                    const int st = b % kStages, sb = k & 1;
                     ok = wait_or_abort(sh, &sh.kv_full[st], (b / kStages) & 1, status);
-                    // S buffer w was read by the group's previous block
-                    if (ok && b >= 2) ok = wait_or_abort(sh, &sh.s_empty[w], ((b >> 1) - 1) & 1, status);
+                    // S buffer sb of group w was read by the group's block before last
+                    if (ok && k >= 2) ok = wait_or_abort(sh, &sh.s_empty[w][sb], ((k >> 1) - 1) & 1, status);
                     if (!ok) break;
                     tc::tc_fence_after();
-                    const uint32_t d = tmem + kColS + w * kSCols;
+                    const uint32_t tS = tmem + kColS + (2 * w + sb) * kSCols;
                     const uint64_t dk = dK0 + ((st * kTile) >> 4);
-                    if (a.stacked) {
+                    if (stacked) {
 #pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) tc::mma_f8(d, dk + 2 * ks, dQ0 + 2 * ks, idesc_qk, ks > 0);
+                        for (int ks = 0; ks < 4; ++ks) tc::mma_f8(tS, dk + 2 * ks, dQ0 + 2 * ks, idesc_qk, ks > 0);
                     } else {
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks)
-#pragma unroll
-                            for (int term = 0; term < kTerms; ++term)
-                                tc::mma_f8(d, dk + 2 * ks, dQ0 + ((term * kQBytes) >> 4) + 2 * ks, idesc_qk,
+                            for (int term = 0; term < a.terms; ++term)
+                                tc::mma_f8(tS, dk + 2 * ks, dQ0 + ((term * tstride) >> 4) + 2 * ks, idesc_qk,
                                            ks > 0 || term > 0);
                     }
-                    tc::mma_commit(&sh.s_full[w]);
+                    tc::mma_commit(&sh.s_full[w][sb]);
                     tc::mma_commit(&sh.kv_empty[st]);
                     if (i + 1 == un.count) tc::mma_commit(&sh.q_empty);  // the unit's last Q K^T
                 }
@@ -790,14 +807,15 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
             tc::mbar_wait(&sh.drain[0], 0);
         }
     } else {
-        // ------------------------------------------------ P V issuers (2, 3)
+        // ---------------------------------------------- P V issuers (warps 2, 3)
         // O^T[d][n] += V^T[d][tok] P[tok][n] for the blocks of softmax group
         // w = warp - 2: f16 V (two 64-d atoms, 16 KiB apart) and P, 16 tokens
         // per instruction; the group's first block of a unit overwrites.
         if (lane == 0) {
             const int w = warp - 2;
             uint32_t gb = 0, uc = 0;
-            const uint64_t dV = tc::smem_desc(tc::smem_u32(smem + kOffV16 + w * kV16Tile), 128 * 128, 1024, tc::kSw128);
+            const uint64_t dV =
+                tc::smem_desc(tc::smem_u32(smem + kOffV16 + w * kV16Tile), 128 * 128, 1024, tc::kSw128);
             const uint32_t tO = tmem + kColO + w * kNMax;
             int32_t *status = &hdr->status;
             while (!aborted(sh)) {
@@ -1001,7 +1019,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (warp == 1) tc::tmem_dealloc(tmem, 512);
+    if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
 // ------------------------------------------------------------------ host side
@@ -1021,8 +1039,8 @@ bool make_tmap(CUtensorMap *m, const uint8_t *base, int64_t slots, int64_t hkv, 
 }
 
 // Tensor map of the query terms qterms[term][t][hq][128 bytes]: box = G heads
-// x box_rows tokens of one term (a whole group, or one token when the terms
-// are stacked), 128-byte swizzle.
+// x box_rows tokens (one token, or a whole group) of one term, 128-byte
+// swizzle.
 bool make_tmap_q(CUtensorMap *m, const uint8_t *base, int64_t T, int64_t hq, int g, int box_rows) {
     auto fn = tensor_map_encoder();
     if (fn == nullptr) return false;
@@ -1096,10 +1114,11 @@ cudaError_t launch_attention_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cu
     p.zscale = a.sm_scale * a.k_scale * 1.4426950408889634f;
 
     CUtensorMap tq;
-    // bf16 queries are exact in two E4M3 terms; with G >= 8 a token's G rows
-    // are 1 KiB, so the terms can be stacked token by token
-    const bool stacked = a.q_dt == SPD_BF16 && G >= 8;
-    if (!make_tmap_q(&tq, reinterpret_cast<const uint8_t *>(p.ws + lay.qterms), a.T, a.Hq, G, stacked ? 1 : p.gmax))
+    // with G >= 8 a token's G query rows are 1 KiB, so terms can be loaded
+    // (and stacked) token by token
+    const bool per_token = G >= 8;
+    if (!make_tmap_q(&tq, reinterpret_cast<const uint8_t *>(p.ws + lay.qterms), a.T, a.Hq, G,
+                     per_token ? 1 : p.gmax))
         return cudaSuccess;
 
     const int64_t q_rows = static_cast<int64_t>(a.T) * a.Hq;
@@ -1112,7 +1131,8 @@ cudaError_t launch_attention_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cu
     t.sl = a.sl; t.sl_s0 = a.sl_s0;
     t.out = a.out; t.o_s0 = a.o_s0; t.o_s1 = a.o_s1; t.o_s2 = a.o_s2;
     t.T = a.T; t.Hq = a.Hq; t.Hkv = a.Hkv; t.G = G; t.R = a.R; t.NB = a.NB; t.gmax = p.gmax;
-    t.stacked = stacked ? 1 : 0;
+    t.terms = (a.q_dt == SPD_BF16) ? 2 : kTerms;  // bf16 queries are exact in two E4M3 terms
+    t.per_token = per_token ? 1 : 0;
     t.v_scale = a.v_scale;
     t.ws = static_cast<char *>(ws);
     t.lay = lay;

@@ -354,10 +354,10 @@ def run_gpu(args, rank, world, local_rank):
     return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3/f16 mma, f32 accumulate", "data": "synthetic",
         "config": workload_desc(w),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "kernel": "paged attention launch",
+                     "traffic": traffic, "kernel": "paged attention call (planner + attention kernels)",
                      "algorithmic_bytes_per_launch": abytes,
                      "mean_launch_us": attn_mean_s * 1e6, "peak_source": peak_src},
         "cpu_baseline": cpu,

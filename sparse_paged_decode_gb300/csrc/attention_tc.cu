@@ -100,6 +100,7 @@ struct __align__(16) Shared {
     float m_run[2][kNMax];   // running exponent offset per group and query row (log2 units)
     float cfac[2][kNMax];    // logit factor per query row (double-buffered by unit)
     float alpha[2][kNMax];   // rescale factor of a group's last offset raise
+    float delta[2][kNMax];   // change of each offset in that raise
     // per group: per-warp block maxima during the blocks (a raise), per-warp
     // row sums at the unit's end (the two uses never overlap)
     union {
@@ -229,11 +230,11 @@ __device__ __forceinline__ float warp_transpose_reduce16(float (&v)[16], int lan
 
 // This thread's logits of one block (its token lane, N = 16 * nch columns)
 // read from S in one batch and masked (-inf where the column is not valid on
-// the lane): u = s * cfac - m_run (log2 units) with kOffset, s * cfac
-// without.  Returns the maximum over the columns.
-template <bool kOffset>
-__device__ __forceinline__ float load_u(const Shared &sh, int mb, int nch, bool stacked, uint32_t tS,
-                                        const float *m_run, uint64_t colmask, float (&u)[kNMax]) {
+// the lane): u = s * cfac - m (log2 units), m the column's offset or 0 while
+// it has none.  Returns whether some column needs a raise: a logit more than
+// 2^kRaise above its offset, or a valid logit in a column without one.
+__device__ __forceinline__ bool load_u(const Shared &sh, int mb, int nch, bool stacked, uint32_t tS,
+                                       const float *m_run, uint64_t colmask, float (&u)[kNMax]) {
     // stacked: the second term's logits follow in chunks nch..2nch-1
     const int nld = stacked ? 2 * nch : nch;
 #pragma unroll
@@ -249,24 +250,24 @@ __device__ __forceinline__ float load_u(const Shared &sh, int mb, int nch, bool 
             for (int col = 0; col < 32; ++col) u[col] += u[32 + col];
         }
     }
-    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    bool need[4] = {false, false, false, false};
 #pragma unroll
     for (int c4 = 0; c4 < kNMax; c4 += 4) {
         if (c4 < 16 * nch) {
             const float4 cf = *reinterpret_cast<const float4 *>(&sh.cfac[mb][c4]);
-            float4 mr = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (kOffset) mr = *reinterpret_cast<const float4 *>(&m_run[c4]);
+            const float4 mr = *reinterpret_cast<const float4 *>(&m_run[c4]);
             const float cfs[4] = {cf.x, cf.y, cf.z, cf.w}, mrs[4] = {mr.x, mr.y, mr.z, mr.w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int col = c4 + q;
-                const float v = kOffset ? fmaf(u[col], cfs[q], -mrs[q]) : u[col] * cfs[q];
+                const bool unset = mrs[q] == -INFINITY;
+                const float v = fmaf(u[col], cfs[q], unset ? 0.f : -mrs[q]);
                 u[col] = ((colmask >> col) & 1) ? v : -INFINITY;
-                mx[q] = fmaxf(mx[q], u[col]);
+                need[q] |= u[col] > (unset ? -INFINITY : kRaise);
             }
         }
     }
-    return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    return need[0] | need[1] | need[2] | need[3];
 }
 
 // The blocks of one unit that fall to this softmax group (global block index
@@ -297,19 +298,21 @@ __device__ __forceinline__ bool unit_blocks(const Soft &c, const TcArgs &a, cons
         for (int j = 0; j < un.nt; ++j)
             if (((e.mask >> j) & 1) && c.tok < sh.Lj[mb][j] - e.block * 128) colmask |= gmask << (j * a.G);
         // logits relative to the offsets; a column without an offset yet
-        // (m = -inf) gives +inf where valid, which forces a raise
+        // (m = -inf) gives +inf where valid, which forces a raise.  The
+        // group's first block of the unit has no offsets at all: it reads
+        // s * cfac directly and always takes the raise path.
         float u[kNMax];
-        float umax = -INFINITY;
+        bool need = false;
         const int sb = k & 1;  // S buffer of this block
         const uint32_t tS = c.tmem + kColS + (2 * wg + sb) * kSCols + c.lane_base;
         const bool have = warp_wait(sh, &sh.s_full[wg][sb], (k >> 1) & 1, c.status);
         if (have) {
             tc::tc_fence_after();
-            umax = load_u<true>(sh, mb, nch, stacked, tS, m_run, colmask, u);
+            need = load_u(sh, mb, nch, stacked, tS, m_run, colmask, u);
         }
         // votes alternate between two slots by block parity: a warp can be at
         // most one block ahead of the slowest reader of its group
-        const int mine = (__any_sync(0xffffffffu, umax > kRaise) ? 1 : 0) | (aborted(sh) ? 2 : 0);
+        const int mine = (__any_sync(0xffffffffu, need) ? 1 : 0) | (aborted(sh) ? 2 : 0);
         if (c.lane == 0) sh.vote[wg][k & 1][c.sw] = mine;
         group_sync(wg);
         const int vote = sh.vote[wg][k & 1][0] | sh.vote[wg][k & 1][1] | sh.vote[wg][k & 1][2] | sh.vote[wg][k & 1][3];
@@ -323,8 +326,9 @@ __device__ __forceinline__ bool unit_blocks(const Soft &c, const TcArgs &a, cons
             // raise: an offset moves to its column's block maximum of
             // s * cfac where that exceeds it by more than 2^kRaise (or where
             // the column had none); O and the sums are scaled by
-            // 2^(old - new).  S is read again without offsets.
-            load_u<false>(sh, mb, nch, stacked, tS, m_run, colmask, u);
+            // 2^(old - new), and u shifts by the change of its offset.  The
+            // block maxima come from u (u + m is s * cfac with m the column's
+            // offset, 0 while unset).
 #pragma unroll
             for (int ch = 0; ch < kNMax / 16; ++ch) {
                 if (ch < nch) {
@@ -339,16 +343,20 @@ __device__ __forceinline__ bool unit_blocks(const Soft &c, const TcArgs &a, cons
             if (c.sw == 0) {
                 bool any = false;
                 for (int col = c.lane; col < n; col += 32) {
-                    const float bm = fmaxf(fmaxf(sh.red[wg][0][col], sh.red[wg][1][col]),
+                    const float bu = fmaxf(fmaxf(sh.red[wg][0][col], sh.red[wg][1][col]),
                                            fmaxf(sh.red[wg][2][col], sh.red[wg][3][col]));
                     const float old = m_run[col];
-                    float al = 1.f;
-                    if (bm != -INFINITY && (old == -INFINITY || bm > old + kRaise)) {
+                    const float meff = (old == -INFINITY) ? 0.f : old;
+                    float al = 1.f, delta = 0.f;
+                    if (bu != -INFINITY && (old == -INFINITY || bu > kRaise)) {
+                        const float bm = meff + bu;
                         al = (old == -INFINITY) ? 0.f : tc::ex2(old - bm);
                         any |= old != -INFINITY;
                         m_run[col] = bm;
+                        delta = bu;
                     }
                     sh.alpha[wg][col] = al;
+                    sh.delta[wg][col] = delta;
                 }
                 any = __any_sync(0xffffffffu, any);
                 if (c.lane == 0) sh.rescale[wg] = any;
@@ -358,10 +366,7 @@ __device__ __forceinline__ bool unit_blocks(const Soft &c, const TcArgs &a, cons
             for (int col = 0; col < kNMax; ++col) {
                 if (col < n) {
                     lsum[col] *= sh.alpha[wg][col];
-                    // relative to the new offsets (a still unset offset means
-                    // the column is masked throughout)
-                    const float m = m_run[col];
-                    u[col] = (u[col] == -INFINITY || m == -INFINITY) ? -INFINITY : u[col] - m;
+                    u[col] -= sh.delta[wg][col];  // -inf stays -inf
                 }
             }
             if (sh.rescale[wg] && i >= 2) {
@@ -507,17 +512,17 @@ __device__ __forceinline__ void unit_finish(const Soft &c, const TcArgs &a, cons
 }
 
 // The last unit of a split pair to finish merges all of them, both softmax
-// groups together: warp w (of 8) takes output rows w, w+8, w+16, w+24 at
-// once, every lane four of their d values.  Each lane reads each partial's
-// (offset, sum) -- the same address across the warp -- and its d values,
-// four partials of four rows per round with an online maximum, so a round of
-// sixteen rows costs one round trip to L2.  Partials are read with
+// groups together: warp w (of 8) takes output rows w and w+8 at once (then
+// w+16, w+24, ...), every lane four of their d values.  Each lane reads each
+// partial's (offset, sum) -- the same address across the warp -- and its d
+// values, four partials of two rows per round with an online maximum, so a
+// round costs one round trip to L2.  Partials are read with
 // ld.global.cg: other CTAs wrote them during this launch.
 __device__ __forceinline__ void merge_partials(const Soft &c_, const TcArgs &a_, const PlanUnit &un_) {
     const Soft c = c_;
     const TcArgs a = a_;
     const PlanUnit un = un_;
-    constexpr int kRows = 4, kParts = 4;
+    constexpr int kRows = 2, kParts = 4;
     const int rows = un.nt * a.G, ns = un.n_split;
     const int warp8 = c.st_id >> 5;  // 0..7 over both groups
     const float *pbase = c.partials + static_cast<int64_t>(un.part_base) * kStride;
@@ -676,10 +681,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
             tc::prefetch_tmap(&tmap_q);
             const uint64_t policy = tc::policy_evict_first();
             const uint32_t qbox = static_cast<uint32_t>(a.G * a.gmax * 128);  // one term of a group
-            // Units are claimed from the global work counter (in plan order)
-            // and handed to the other roles through a 4-slot ring; claims run
-            // two units ahead so a record has arrived by the time it is
-            // published.
+            // Units are claimed from the global work counter (in plan order,
+            // longest first) and handed to the other roles through a 4-slot
+            // ring.  The next unit is claimed only once this unit's loads are
+            // all issued, so no CTA holds work it cannot start while others
+            // run out; the claim's round trip overlaps the draining stages.
             auto claim = [&]() -> PlanUnit {
                 PlanUnit x{};
                 x.pair = -1;
@@ -696,11 +702,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
             uint32_t lb = 0, uc = 0;  // blocks and units loaded by this CTA
             PlanUnit un = claim();
             publish(0, un);
-            PlanUnit un_next = claim();
-            while (!aborted(sh)) {
-                publish(uc + 1, un_next);
-                const PlanUnit un_after = claim();  // in flight while this unit's loads are issued
-                if (un.pair < 0) break;
+            while (!aborted(sh) && un.pair >= 0) {
                 // the group's query terms, once the previous unit's last Q K^T is done
                 if (uc > 0 && !wait_or_abort(sh, &sh.q_empty, (uc - 1) & 1, &hdr->status)) break;
                 if (a.per_token) {
@@ -737,8 +739,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
                     tc::tma_load_3d(smem + kOffV + st * kTile, &tmap_v, &sh.kv_full[st], 0, un.h, e.page * 128, policy);
                 }
                 if (!ok) break;
-                un = un_next;
-                un_next = un_after;
+                un = claim();
+                publish(uc, un);
             }
             // let every issued copy land before the CTA may exit
             if (uc > 0) tc::mbar_wait(&sh.q_full, (uc - 1) & 1);

@@ -234,8 +234,9 @@ __device__ void plan_body(const PlanArgs &a) {
     __syncthreads();
     __threadfence_block();
 
-    // ---- units.  Chunk c = total blocks / CTAs (at least 4): each pair's
-    // list is cut into full chunks of c blocks and a remainder.  The unit
+    // ---- units.  Chunk c = total blocks / CTAs (at least 4; a little more
+    // when that fits every unit in one wave): each pair's list is cut into
+    // full chunks of c blocks and a remainder.  The unit
     // table holds the full chunks first (pair order), then the remainders
     // and unsplit pairs by decreasing size, so the dynamic scheduler claims
     // the longest work first.
@@ -244,6 +245,26 @@ __device__ void plan_body(const PlanArgs &a) {
     int total_blocks;
     block_excl_sum(blocks_local, &total_blocks, scratch);
     int chunk = max(4, (total_blocks + a.num_ctas - 1) / max(1, a.num_ctas));
+    // One wave when it costs little: the warps try chunk, chunk+1, ... (up to
+    // a quarter more) at once and the smallest whose unit count fits the grid
+    // is taken -- every CTA then runs one unit, instead of a few CTAs running
+    // a second one after everybody else.
+    {
+        __shared__ int s_best;
+        if (tid == 0) s_best = 0x7fffffff;
+        __syncthreads();
+        const int c = chunk + warp;
+        if (c <= kPlanMaxNB && 4 * c <= 5 * chunk + 4) {
+            int cnt = 0;
+            for (int p = lane; p < n_pairs; p += 32) cnt += max(1, (pairs[p].n_blocks + c - 1) / c);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(kFull, cnt, o);
+            if (lane == 0 && cnt <= a.num_ctas) atomicMin(&s_best, c);
+        }
+        __syncthreads();
+        if (s_best != 0x7fffffff) chunk = s_best;
+        __syncthreads();
+    }
     int *hist = reinterpret_cast<int *>(s_mask_all);  // [chunk + 1] remainder-size bins (mask words are done)
     for (int attempt = 0; attempt < 24; ++attempt) {
         int nu = 0, rows = 0;

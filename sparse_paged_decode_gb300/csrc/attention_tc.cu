@@ -634,8 +634,9 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
     PlanHeader *hdr = reinterpret_cast<PlanHeader *>(a.ws + a.lay.header);
     const PlanEntry *lists = reinterpret_cast<const PlanEntry *>(a.ws + a.lay.lists);
     const PlanUnit *units = reinterpret_cast<const PlanUnit *>(a.ws + a.lay.units);
-    const int n_units = hdr->n_units;
 
+    // prologue (barriers, tensor memory, descriptor prefetch) overlaps the
+    // planner; global memory is touched only after pdl_wait
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             tc::mbar_init(&sh.kv_full[i], 1);
@@ -665,6 +666,13 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         tc::fence_mbar_init();
     }
     if (warp == 1) tc::tmem_alloc(&sh.tmem_base, kTmemCols);
+    if (threadIdx.x == 32) {
+        tc::prefetch_tmap(&tmap_k);
+        tc::prefetch_tmap(&tmap_v);
+        tc::prefetch_tmap(&tmap_q);
+    }
+    tc::pdl_wait();
+    tc::pdl_trigger();
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
@@ -676,9 +684,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         // Metadata is software-pipelined: the next unit record and the next
         // list entry are loaded one step ahead of their use.
         if (lane == 0) {
-            tc::prefetch_tmap(&tmap_k);
-            tc::prefetch_tmap(&tmap_v);
-            tc::prefetch_tmap(&tmap_q);
+            const int n_units = hdr->n_units;
             const uint64_t policy = tc::policy_evict_first();
             const uint32_t qbox = static_cast<uint32_t>(a.G * a.gmax * 128);  // one term of a group
             // Units are claimed from the global work counter (in plan order,
@@ -1114,6 +1120,7 @@ cudaError_t launch_attention_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cu
     p.q_dt = a.q_dt;
     p.Hq = a.Hq;
     p.zscale = a.sm_scale * a.k_scale * 1.4426950408889634f;
+    if (!plan_configure(&p)) return cudaSuccess;
 
     CUtensorMap tq;
     // with G >= 8 a token's G query rows are 1 KiB, so terms can be loaded
@@ -1124,7 +1131,8 @@ cudaError_t launch_attention_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cu
         return cudaSuccess;
 
     const int64_t q_rows = static_cast<int64_t>(a.T) * a.Hq;
-    const int conv_ctas = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(dev.sms - 1, (q_rows + 31) / 32)));
+    // query conversion: 64 rows per CTA (four per warp), up to two CTAs per SM
+    const int conv_ctas = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(2 * dev.sms - 1, (q_rows + 63) / 64)));
     cudaError_t e = launch_prepare(p, conv_ctas, stream);
     if (e != cudaSuccess) return e;
 
@@ -1138,8 +1146,17 @@ cudaError_t launch_attention_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cu
     t.v_scale = a.v_scale;
     t.ws = static_cast<char *>(ws);
     t.lay = lay;
-    attention_tc_kernel<<<dev.sms, kThreads, kSmemBytes, stream>>>(tk, tv, tq, t);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(dev.sms);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, attention_tc_kernel, tk, tv, tq, t);
     if (e == cudaSuccess) *used = true;
     return e;
 }

@@ -106,6 +106,9 @@ constexpr int kSelectPer = 4;
 __global__ void __launch_bounds__(kSelectWarps * 32)
 select_rank_kernel(SelectArgs a, int nb4) {
     extern __shared__ float4 rows4[];  // [kSelectWarps][nb4]
+    // launched with programmatic stream serialisation (see launch_select_rank)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row = blockIdx.x * kSelectWarps + warp;
     if (row >= a.Hi * a.T) return;
@@ -292,8 +295,19 @@ cudaError_t launch_select_rank(const SelectArgs &a, cudaStream_t stream) {
     const int rows = a.Hi * a.T;
     const int nb4 = (a.NB + 3) / 4;
     dim3 grid((rows + kSelectWarps - 1) / kSelectWarps);
-    select_rank_kernel<<<grid, kSelectWarps * 32, kSelectWarps * nb4 * sizeof(float4), stream>>>(a, nb4);
-    return cudaGetLastError();
+    // programmatic stream serialisation: the kernel may be scheduled while
+    // the score kernel drains and waits for it before reading the sheet
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kSelectWarps * 32);
+    cfg.dynamicSmemBytes = kSelectWarps * nb4 * sizeof(float4);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, select_rank_kernel, a, nb4);
 }
 
 cudaError_t launch_select_generic(const SelectArgs &a, cudaStream_t stream) {

@@ -1,19 +1,24 @@
 // plan.cuh -- the work plan of the tensor-core decode attention, built on the
-// device by one CTA from req_idx / seq_lens / topk_idx (no host reads, so the
-// call stays graph safe), and its layout inside the caller's workspace.
+// device from req_idx / seq_lens / topk_idx (no host reads, so the call stays
+// graph safe), and its layout inside the caller's workspace.
 //
 //   group  a run of consecutive query rows of one request (at most gmax rows):
 //          the draft tokens of a verification row, which share every K/V page
 //   pair   (group, kv head): its block list is the union of the blocks its
 //          rows selected, ascending, each with the mask of rows that selected
 //          it and its page id (blocks whose page lies outside the pool are
-//          dropped here)
+//          dropped here).  When every kv head shares one selection the list
+//          is built once per group.
 //   unit   a contiguous chunk of a pair's block list: the work item of one CTA;
 //          a pair split over several units leaves per-unit partials (running
 //          max, sum, unnormalised output) that the last unit to finish merges.
 //          Units are full chunks of `chunk` blocks plus one remainder per
 //          pair; the table lists the full chunks first, then the remainders by
 //          decreasing size (longest work is claimed first)
+//
+// Two launches build it: the list kernel (one warp per list) writes the block
+// lists, their lengths and the group starts; the unit kernel cuts the lists
+// into the unit table on one CTA while its other CTAs convert the queries.
 #pragma once
 
 #include <stdint.h>
@@ -35,20 +40,6 @@ struct PlanHeader {
 };
 static_assert(sizeof(PlanHeader) == 256, "header is one 256-byte line");
 
-struct PlanGroup {
-    int32_t t0;  // first query row
-    int32_t nt;  // rows in the group
-    int32_t r;   // block_table row (valid only when some row has keys)
-    int32_t pad;
-};
-
-struct PlanPair {
-    int32_t list;      // offset of its block list (entries)
-    int32_t n_blocks;
-    int32_t unit0;     // first full-chunk unit in the unit table
-    int32_t n_units;
-};
-
 struct PlanEntry {
     int32_t page;
     uint16_t block;
@@ -69,7 +60,7 @@ struct PlanUnit {
 };
 static_assert(sizeof(PlanUnit) == 32, "unit record is 32 bytes");
 
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 512;
 constexpr int kPlanMaxT = 4096;   // query rows the one-CTA planner handles
 constexpr int kPlanMaxNB = 256;   // page-table capacity of the fast path
 constexpr int kUnitExtra = 8192;
@@ -78,7 +69,7 @@ constexpr int kQueryTerms = 3;    // E4M3 terms per query element (12 significan
 
 // Byte layout of the workspace for capacities (T, Hq, Hkv, D, NB).
 struct PlanLayout {
-    size_t header, groups, pairs, lists, units, counters, partials, qterms, cfac, total;
+    size_t header, gstart, lcount, lists, units, counters, partials, qterms, cfac, total;
     int64_t unit_cap, rows_cap, pair_cap;
 
     __host__ __device__ static size_t align(size_t x) { return (x + 255) / 256 * 256; }
@@ -91,8 +82,8 @@ struct PlanLayout {
         rows_cap = 2 * T * Hq + 16384;
         size_t off = 0;
         header = off;   off += align(sizeof(PlanHeader));
-        groups = off;   off += align(sizeof(PlanGroup) * (size_t)(T > 0 ? T : 1));
-        pairs = off;    off += align(sizeof(PlanPair) * (size_t)(pair_cap > 0 ? pair_cap : 1));
+        gstart = off;   off += align(sizeof(int32_t) * (size_t)(T + 1));
+        lcount = off;   off += align(sizeof(int32_t) * (size_t)(pair_cap > 0 ? pair_cap : 1));
         lists = off;    off += align(sizeof(PlanEntry) * (size_t)(pair_cap > 0 ? pair_cap : 1) * (size_t)NB);
         units = off;    off += align(sizeof(PlanUnit) * (size_t)unit_cap);
         counters = off; off += align(sizeof(int32_t) * (size_t)(pair_cap > 0 ? pair_cap : 1));
@@ -113,6 +104,8 @@ struct PlanArgs {
     const int32_t *tk;  // nullptr: dense
     int64_t tk_s0, tk_s1, tk_s2;
     int32_t T, R, NB, K, Hkv, G, gmax;
+    int32_t heads_built;  // block lists per group: 1 when every kv head shares the selection, else Hkv
+    int32_t list_ctas;    // CTAs of the list kernel
     int64_t P;
     int32_t num_ctas;
     char *ws;
@@ -124,9 +117,17 @@ struct PlanArgs {
     float zscale;  // sm_scale * k_scale * log2(e)
 };
 
-// One launch: CTA 0 builds the plan; the other CTAs write each query row as
-// three E4M3 terms (qterms[term][t][hq][d], with the row scaled by a power of
-// two into [128, 256)) and its logit factor cfac[t][hq] = zscale / scale.
+// Fills heads_built and list_ctas for the call; false when the planner's
+// shared memory cannot hold its per-row state (the fast path is then not
+// taken).
+bool plan_configure(PlanArgs *a);
+
+// The two launches (programmatic stream serialisation: each waits for the
+// previous kernel of the stream before touching memory and lets the next one
+// start its prologue early).  The unit kernel's CTAs from 1 on write each
+// query row as E4M3 terms (qterms[term][t][hq][d], with the row scaled by a
+// power of two into [128, 256); two terms for bf16 queries, three otherwise)
+// and its logit factor cfac[t][hq] = zscale / scale.
 cudaError_t launch_prepare(const PlanArgs &a, int conv_ctas, cudaStream_t stream);
 
 }  // namespace spd

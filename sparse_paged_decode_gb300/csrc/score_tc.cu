@@ -98,6 +98,10 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         tc::fence_mbar_init();
     }
     if (warp == 5) tc::tmem_alloc(&sh.tmem_base, 256);  // two 128-column accumulators
+    // launched with programmatic stream serialisation: global memory only
+    // after the previous kernel of the stream is done
+    tc::pdl_wait();
+    tc::pdl_trigger();
 
     // ---- lanes: (token t, head h) of each TMEM lane and its key limit
     const bool is_lane = tid < kLanes;
@@ -359,8 +363,17 @@ cudaError_t launch_score_tc(const ScoreArgs &a, cudaStream_t stream, bool *used)
     t.idx_scale = a.idx_scale;
     t.idesc = tc::idesc_f16_m128(128, a.q_dt == SPD_BF16);
     dim3 grid(static_cast<unsigned>(n_tiles), static_cast<unsigned>(n_chunks));
-    score_tc_kernel<<<grid, kThreadsSc, smem, stream>>>(tq_map, tk_map, t);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreadsSc);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, score_tc_kernel, tq_map, tk_map, t);
     if (e == cudaSuccess) *used = true;
     return e;
 }

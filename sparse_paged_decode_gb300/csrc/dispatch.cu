@@ -53,7 +53,7 @@ cudaError_t dispatch_attention(const AttnArgs &a, void *workspace, size_t worksp
     if (g_policy[3] == 0) e = launch_attention_tc(a, workspace, workspace_bytes, stream, &used);
     if (e != cudaSuccess) return e;
     if (used) {
-        count_launches(2);  // planner + attention
+        count_launches(3);  // list and unit planner kernels + attention
         return cudaSuccess;
     }
     count_launches(1);

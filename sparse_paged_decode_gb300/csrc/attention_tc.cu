@@ -228,6 +228,30 @@ __device__ __forceinline__ float warp_transpose_reduce16(float (&v)[16], int lan
     return v[0];
 }
 
+// Copy of columns [16 ch, 16 ch + 16) of a per-thread column array (the
+// switch keeps every index compile-time, so the array stays in registers and
+// a loop over chunks can stay rolled).
+__device__ __forceinline__ void chunk16(const float (&x)[kNMax], int ch, float (&v)[16]) {
+    switch (ch) {
+        case 0:
+#pragma unroll
+            for (int q = 0; q < 16; ++q) v[q] = x[q];
+            break;
+        case 1:
+#pragma unroll
+            for (int q = 0; q < 16; ++q) v[q] = x[16 + q];
+            break;
+        case 2:
+#pragma unroll
+            for (int q = 0; q < 16; ++q) v[q] = x[32 + q];
+            break;
+        default:
+#pragma unroll
+            for (int q = 0; q < 16; ++q) v[q] = x[48 + q];
+            break;
+    }
+}
+
 // This thread's logits of one block (its token lane, N = 16 * nch columns)
 // read from S in one batch and masked (-inf where the column is not valid on
 // the lane): u = s * cfac - m (log2 units), m the column's offset or 0 while
@@ -329,15 +353,12 @@ __device__ __forceinline__ bool unit_blocks(const Soft &c, const TcArgs &a, cons
             // 2^(old - new), and u shifts by the change of its offset.  The
             // block maxima come from u (u + m is s * cfac with m the column's
             // offset, 0 while unset).
-#pragma unroll
-            for (int ch = 0; ch < kNMax / 16; ++ch) {
-                if (ch < nch) {
-                    float v[16];
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) v[q] = u[16 * ch + q];
-                    const float mx = warp_transpose_reduce16<true>(v, c.lane);
-                    if (c.lane < 16) sh.red[wg][c.sw][16 * ch + c.lane] = mx;
-                }
+#pragma unroll 1
+            for (int ch = 0; ch < nch; ++ch) {
+                float v[16];
+                chunk16(u, ch, v);
+                const float mx = warp_transpose_reduce16<true>(v, c.lane);
+                if (c.lane < 16) sh.red[wg][c.sw][16 * ch + c.lane] = mx;
             }
             group_sync(wg);
             if (c.sw == 0) {
@@ -417,14 +438,12 @@ __device__ __forceinline__ bool unit_blocks(const Soft &c, const TcArgs &a, cons
     // the group's row sums: per warp by a transposed butterfly, per group in
     // shared memory (added up by the unit's end)
 #pragma unroll
-    for (int ch = 0; ch < kNMax / 16; ++ch) {
-        if (ch < nch) {
-            float v[16];
-#pragma unroll
-            for (int q = 0; q < 16; ++q) v[q] = lsum[16 * ch + q];
-            const float tot = warp_transpose_reduce16<false>(v, c.lane);
-            if (c.lane < 16) sh.lsum[wg][c.sw][16 * ch + c.lane] = tot;
-        }
+#pragma unroll 1
+    for (int ch = 0; ch < nch; ++ch) {
+        float v[16];
+        chunk16(lsum, ch, v);
+        const float tot = warp_transpose_reduce16<false>(v, c.lane);
+        if (c.lane < 16) sh.lsum[wg][c.sw][16 * ch + c.lane] = tot;
     }
     return ok;
 }

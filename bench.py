@@ -12,8 +12,10 @@ HBM bandwidth against the measured peak, the end-to-end rate through the same
 calls with host buffers, and the CPU oracle's rate on a bounded sample.
 
 Timing: CUDA events on the launching stream around each step; between timed
-steps a 256 MiB buffer is rewritten to flush the 129 MB L2 (outside the
-events); W warm-up steps first.  Under torchrun each rank runs its own batch
+steps a 256 MiB buffer is rewritten to flush the 129 MB L2, then a second
+256 MiB buffer is read so that the flush's dirty lines are written back
+before the step rather than during it (both outside the events); W warm-up
+steps first.  Under torchrun each rank runs its own batch
 (different seed) with no data exchange: weak scaling, max time over ranks.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
@@ -65,7 +67,8 @@ def workload_desc(w):
         "block_size": w.block_size, "page_table_blocks": w.NB, "pool_pages": w.P, "top_k": w.K,
         "kv_dtype": "e4m3 (static scalar scales)", "q_dtype": str(w.q.dtype).replace("torch.", ""),
         "index_dtype": str(w.q_idx.dtype).replace("torch.", "") if w.q_idx is not None else None,
-        "l2": "flushed between timed steps (256 MiB rewrite, outside the events)",
+        "l2": "flushed between timed steps (256 MiB rewrite, then a 256 MiB read that cleans the dirty lines; "
+              "outside the events)",
     }
 
 
@@ -217,6 +220,15 @@ def run_gpu(args, rank, world, local_rank):
     out = torch.empty((T, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
     ws = torch.empty(spd.decode_workspace_bytes(T, w.Hq, w.Hkv, w.D, NB), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    clean = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    clean_sum = torch.empty((), dtype=torch.int64, device=dev)
+
+    def flush_l2(i):
+        # rewrite 256 MiB (evicts every input), then read another 256 MiB so
+        # the rewrite's dirty lines are written back here, not in the step
+        flush.fill_(i & 0xFF)
+        torch.sum(clean, 0, dtype=torch.int64, out=clean_sum)
+
     stream = torch.cuda.current_stream(dev)
     dense = w.dense
 
@@ -281,7 +293,7 @@ def run_gpu(args, rank, world, local_rank):
     launches_per_step = spd.launch_count() - n0
     launches0 = spd.launch_count()
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+        flush_l2(i)
         starts[i].record(stream)
         if graph is not None:
             graph.replay()
@@ -296,7 +308,7 @@ def run_gpu(args, rank, world, local_rank):
         # the attention call's device time: its own graph replayed between
         # events on the same stream, L2 flushed before each
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)
+            flush_l2(i)
             attn[i][0].record(stream)
             graph_attn.replay()
             attn[i][1].record(stream)
@@ -317,7 +329,7 @@ def run_gpu(args, rank, world, local_rank):
     d2h = host_out.numel() * host_out.element_size()
     e2e_ms = []
     for i in range(args.warmup + args.steps):
-        flush.fill_(i & 0xFF)
+        flush_l2(i)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for k, t in host_in.items():

@@ -31,7 +31,7 @@ cudaError_t launch_score_tc(const ScoreArgs &a, cudaStream_t stream, bool *used)
 namespace {
 
 constexpr int kLanes = 128;       // query lanes per tile (M)
-constexpr int kKeyStages = 2;
+constexpr int kMaxStages = 4;     // key stages: 4 for Di <= 128, else 2 (shared-memory budget)
 constexpr int kMaxChunk = 8;      // block ids per CTA
 constexpr int kThreadsSc = 192;   // warps 0-3 epilogue (TMEM quadrants), 4 TMA, 5 MMA
 constexpr int kAtom = 128 * 128;  // one 64-element column chunk of 128 rows, bytes
@@ -52,7 +52,7 @@ struct ScoreTcArgs {
 };
 
 struct ScoreShared {
-    uint64_t q_full, k_full[kKeyStages], k_empty[kKeyStages], acc_full[2], acc_empty[2];
+    uint64_t q_full, k_full[kMaxStages], k_empty[kMaxStages], acc_full[4], acc_empty[4];
     uint32_t tmem_base;
     int abort;
     int n_steps;
@@ -62,7 +62,14 @@ struct ScoreShared {
     int step_page[kMaxChunk * kLanes];
     uint16_t step_run[kMaxChunk * kLanes];
     uint8_t step_b[kMaxChunk * kLanes];
+    uint32_t run_ok[kMaxChunk][kLanes / 32];  // bit j of word: run j has a valid page for that block
 };
+
+__host__ __device__ inline int key_stages(int nkc) { return nkc <= 2 ? 4 : 2; }
+
+// 128-column TMEM accumulators: four when the shared memory keeps the CTA
+// alone on its SM (Di >= 128), so no other CTA waits for tensor memory.
+__device__ __forceinline__ int acc_count(int nkc) { return nkc >= 2 ? 4 : 2; }
 
 // All 32 lanes wait; the warp goes on only if every lane saw the phase.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
@@ -77,7 +84,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     const int nkc = a.Di / 64;
     uint8_t *sQ = smem;
     uint8_t *sK = smem + nkc * kAtom;  // stage s at sK + s * nkc * kAtom
-    ScoreShared &sh = *reinterpret_cast<ScoreShared *>(sK + kKeyStages * nkc * kAtom);
+    const int n_stages = key_stages(nkc);
+    ScoreShared &sh = *reinterpret_cast<ScoreShared *>(sK + n_stages * nkc * kAtom);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t0 = blockIdx.x * a.tq;
     const int b0 = blockIdx.y * a.chunk;
@@ -85,11 +93,11 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 
     if (tid == 0) {
         tc::mbar_init(&sh.q_full, 1);
-        for (int i = 0; i < kKeyStages; ++i) {
+        for (int i = 0; i < kMaxStages; ++i) {
             tc::mbar_init(&sh.k_full[i], 1);
             tc::mbar_init(&sh.k_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 4; ++i) {
             tc::mbar_init(&sh.acc_full[i], 1);
             tc::mbar_init(&sh.acc_empty[i], kLanes);
         }
@@ -97,7 +105,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         sh.n_steps = 0;
         tc::fence_mbar_init();
     }
-    if (warp == 5) tc::tmem_alloc(&sh.tmem_base, 256);  // two 128-column accumulators
+    const int n_acc = acc_count(nkc);
+    if (warp == 5) tc::tmem_alloc(&sh.tmem_base, 128 * n_acc);
     // launched with programmatic stream serialisation: global memory only
     // after the previous kernel of the stream is done
     tc::pdl_wait();
@@ -140,30 +149,31 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         atomicMax(&sh.run_hi[my_run], tid + 1);
         atomicMax(&sh.run_lim[my_run], my_lim);
     }
-    // cells with no valid key: -inf now (the lane's own thread)
-    if (lane_row) {
-        for (int bl = 0; bl < nb; ++bl) {
-            const int b = b0 + bl;
-            bool empty = my_r < 0 || static_cast<int64_t>(b) * kBlock >= my_lim;
-            if (!empty) {
-                const int64_t page = a.bt[my_r * a.bt_s0 + b * a.bt_s1];
-                empty = page < 0 || page >= a.P;
-            }
-            if (empty) a.out[h * a.o_s0 + t * a.o_s1 + b * a.o_s2] = -INFINITY;
-        }
-    }
-    __syncthreads();
     // ---- steps: (block, run) pairs with a valid page and some valid key
+    // (the page table is read once, here)
+    for (int i = tid; i < kMaxChunk * (kLanes / 32); i += kThreadsSc) (&sh.run_ok[0][0])[i] = 0u;
+    __syncthreads();
     for (int idx = tid; idx < nb * n_runs; idx += kThreadsSc) {
         const int bl = idx / n_runs, j = idx % n_runs;
         const int b = b0 + bl;
         if (static_cast<int64_t>(b) * kBlock >= sh.run_lim[j]) continue;
         const int64_t page = a.bt[sh.run_r[j] * a.bt_s0 + b * a.bt_s1];
         if (page < 0 || page >= a.P) continue;
+        atomicOr(&sh.run_ok[bl][j >> 5], 1u << (j & 31));
         const int s = atomicAdd(&sh.n_steps, 1);
         sh.step_page[s] = static_cast<int>(page);
         sh.step_run[s] = static_cast<uint16_t>(j);
         sh.step_b[s] = static_cast<uint8_t>(bl);
+    }
+    __syncthreads();
+    // cells with no valid key: -inf now (the lane's own thread)
+    if (lane_row) {
+        for (int bl = 0; bl < nb; ++bl) {
+            const int b = b0 + bl;
+            bool empty = my_r < 0 || static_cast<int64_t>(b) * kBlock >= my_lim;
+            if (!empty) empty = !((sh.run_ok[bl][my_run >> 5] >> (my_run & 31)) & 1u);
+            if (empty) a.out[h * a.o_s0 + t * a.o_s1 + b * a.o_s2] = -INFINITY;
+        }
     }
     tc::tc_fence_before();
     __syncthreads();
@@ -180,8 +190,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             for (int c = 0; c < nkc; ++c) tc::tma_load_3d(sQ + c * kAtom, &tmap_q, &sh.q_full, c * 64, 0, t0);
             int s = 0;
             for (; s < n_steps; ++s) {
-                const int st = s % kKeyStages;
-                if (s >= kKeyStages && !tc::mbar_wait(&sh.k_empty[st], ((s / kKeyStages) - 1) & 1)) {
+                const int st = s % n_stages;
+                if (s >= n_stages && !tc::mbar_wait(&sh.k_empty[st], ((s / n_stages) - 1) & 1)) {
                     *reinterpret_cast<volatile int *>(&sh.abort) = 1;
                     break;
                 }
@@ -192,8 +202,8 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             }
             // every issued copy lands before the CTA may exit
             tc::mbar_wait(&sh.q_full, 0);
-            for (int u = s > kKeyStages ? s - kKeyStages : 0; u < s; ++u)
-                tc::mbar_wait(&sh.k_full[u % kKeyStages], (u / kKeyStages) & 1);
+            for (int u = s > n_stages ? s - n_stages : 0; u < s; ++u)
+                tc::mbar_wait(&sh.k_full[u % n_stages], (u / n_stages) & 1);
         }
     } else if (warp == 5) {
         // ------------------------------------------------------- MMA issuer
@@ -202,9 +212,9 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             bool ok = tc::mbar_wait(&sh.q_full, 0);
             int s = 0;
             for (; ok && s < n_steps; ++s) {
-                const int st = s % kKeyStages, buf = s & 1;
-                ok = tc::mbar_wait(&sh.k_full[st], (s / kKeyStages) & 1);
-                if (ok && s >= 2) ok = tc::mbar_wait(&sh.acc_empty[buf], ((s >> 1) - 1) & 1);
+                const int st = s % n_stages, buf = s % n_acc;
+                ok = tc::mbar_wait(&sh.k_full[st], (s / n_stages) & 1);
+                if (ok && s >= n_acc) ok = tc::mbar_wait(&sh.acc_empty[buf], ((s / n_acc) - 1) & 1);
                 if (!ok) break;
                 tc::tc_fence_after();
                 const uint32_t kb = k_base + st * nkc * kAtom;
@@ -218,7 +228,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             }
             if (!ok) *reinterpret_cast<volatile int *>(&sh.abort) = 1;
             // the issued products complete before TMEM is released
-            if (s > 0) tc::mbar_wait(&sh.acc_full[(s - 1) & 1], ((s - 1) >> 1) & 1);
+            if (s > 0) tc::mbar_wait(&sh.acc_full[(s - 1) % n_acc], ((s - 1) / n_acc) & 1);
         }
     } else {
         // --------------------------------------------------------- epilogue
@@ -227,12 +237,12 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
         bool ok = true;
         for (int s = 0; s < n_steps; ++s) {
-            const int buf = s & 1, j = sh.step_run[s];
+            const int buf = s % n_acc, j = sh.step_run[s];
             const int b = b0 + sh.step_b[s];
             const int lo = sh.run_lo[j], hi = sh.run_hi[j];
             const int lim = my_lim - b * kBlock;
             const bool mine = tid >= lo && tid < hi && lim > 0;
-            if (ok) ok = warp_wait(&sh.acc_full[buf], (s >> 1) & 1);
+            if (ok) ok = warp_wait(&sh.acc_full[buf], (s / n_acc) & 1);
             if (!ok) {
                 if (mine) a.out[h * a.o_s0 + t * a.o_s1 + b * a.o_s2] = NAN;
                 continue;
@@ -241,20 +251,22 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             if (hi > warp * 32 && lo < warp * 32 + 32) {
                 float best = -INFINITY;
                 const uint32_t base = tmem + buf * 128 + lane_base;
+                // 64 columns per tensor-memory round trip
 #pragma unroll
-                for (int c0 = 0; c0 < 128; c0 += 32) {
-                    float v0[16], v1[16];
-                    tc::tmem_ld16(base + c0, v0);
-                    tc::tmem_ld16(base + c0 + 16, v1);
+                for (int c0 = 0; c0 < 128; c0 += 64) {
+                    float v[4][16];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) tc::tmem_ld16(base + c0 + 16 * q, v[q]);
                     tc::tmem_wait_ld();
-                    if (lim >= 128) {
 #pragma unroll
-                        for (int k = 0; k < 16; ++k) best = fmaxf(best, fmaxf(v0[k], v1[k]));
-                    } else {
+                    for (int q = 0; q < 4; ++q) {
+                        if (lim >= 128) {
 #pragma unroll
-                        for (int k = 0; k < 16; ++k) {
-                            if (c0 + k < lim) best = fmaxf(best, v0[k]);
-                            if (c0 + 16 + k < lim) best = fmaxf(best, v1[k]);
+                            for (int k = 0; k < 16; ++k) best = fmaxf(best, v[q][k]);
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < 16; ++k)
+                                if (c0 + 16 * q + k < lim) best = fmaxf(best, v[q][k]);
                         }
                     }
                 }
@@ -269,7 +281,7 @@ score_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (warp == 5) tc::tmem_dealloc(tmem, 256);
+    if (warp == 5) tc::tmem_dealloc(tmem, 128 * n_acc);
 }
 
 bool make_tmap_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint64_t row_bytes,
@@ -330,9 +342,13 @@ cudaError_t launch_score_tc(const ScoreArgs &a, cudaStream_t stream, bool *used)
         if (d.sms <= 0) d.sms = 1;
     }
     const int nkc = a.Di / 64;
-    const int smem = static_cast<int>(1024 + nkc * kAtom * (1 + kKeyStages) + sizeof(ScoreShared));
+    const int smem = static_cast<int>(1024 + nkc * kAtom * (1 + key_stages(nkc)) + sizeof(ScoreShared));
     if (!d.attr_set) {
-        const int smem_max = static_cast<int>(1024 + 4 * kAtom * (1 + kKeyStages) + sizeof(ScoreShared));
+        int smem_max = 0;
+        for (int c = 1; c <= 4; ++c) {
+            const int bytes = static_cast<int>(1024 + c * kAtom * (1 + key_stages(c)) + sizeof(ScoreShared));
+            smem_max = bytes > smem_max ? bytes : smem_max;
+        }
         cudaError_t e = cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
         if (e != cudaSuccess) return e;
         d.attr_set = true;

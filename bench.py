@@ -381,7 +381,8 @@ def run_gpu(args, rank, world, local_rank):
         "config": workload_desc(w),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic,
-                     "kernel": "paged attention call (list, unit and attention kernels; graph replay)",
+                     "kernel": "paged attention call (list, unit and attention kernels; %s)"
+                               % ("graph replay" if graph is not None else "direct launches"),
                      "algorithmic_bytes_per_launch": abytes,
                      "mean_launch_us": attn_mean_s * 1e6, "peak_source": peak_src},
         "cpu_baseline": cpu,

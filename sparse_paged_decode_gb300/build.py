@@ -42,7 +42,10 @@ def _stamp() -> str:
         with open(path, "rb") as f:
             h.update(os.path.basename(path).encode())
             h.update(f.read())
-    h.update(" ".join(ARCH + NVCC_FLAGS).encode())
+    # flags with the checkout's own paths made relative: the same sources
+    # stamp the same on every machine
+    flags = [os.path.relpath(f, ROOT) if f.startswith(ROOT) else f for f in ARCH + NVCC_FLAGS]
+    h.update(" ".join(flags).encode())
     return h.hexdigest()
 
 

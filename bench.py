@@ -214,6 +214,24 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     w = W.config(args.config, seed=1000 + args.config + 97 * rank)
     g = w.to(dev)
+    # the step's per-call inputs live in one device buffer (each tensor a
+    # 256-byte aligned view), so the end-to-end run stages them with a
+    # single host-to-device copy
+    in_names = [k for k in ("q", "q_idx", "block_table", "seq_lens", "req_idx") if getattr(w, k) is not None]
+    offs, total_in = {}, 0
+    for k in in_names:
+        t = getattr(w, k)
+        offs[k] = total_in
+        total_in += (t.numel() * t.element_size() + 255) // 256 * 256
+    dev_pack = torch.zeros(total_in, dtype=torch.uint8, device=dev)
+    host_pack = torch.zeros(total_in, dtype=torch.uint8).pin_memory()
+    for k in in_names:
+        t = getattr(w, k).contiguous()
+        nb = t.numel() * t.element_size()
+        host_pack[offs[k]:offs[k] + nb].copy_(t.view(-1).view(torch.uint8))
+        view = dev_pack[offs[k]:offs[k] + nb].view(t.dtype).view(t.shape)
+        view.copy_(getattr(g, k))
+        setattr(g, k, view)
     T, NB, K = w.T, w.NB, max(w.K, 1)
     scores = torch.empty((w.Hi, T, NB), device=dev)
     topk = torch.empty((w.Hi, T, K), dtype=torch.int32, device=dev)
@@ -320,20 +338,18 @@ def run_gpu(args, rank, world, local_rank):
     total_ms = sum(step_ms)
 
     # end to end through the same calls with host buffers: the step's inputs
-    # (queries, index queries, page table, seq_lens, req_idx) copied in from
-    # pinned memory, the attention output copied back; caches stay resident
-    host_in = {k: getattr(w, k).pin_memory() for k in ("q", "q_idx", "block_table", "seq_lens", "req_idx")
-               if getattr(w, k) is not None}
+    # (queries, index queries, page table, seq_lens, req_idx), packed in one
+    # pinned buffer, copied in with one transfer, the attention output copied
+    # back; caches stay resident
     host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    h2d = total_in
     d2h = host_out.numel() * host_out.element_size()
     e2e_ms = []
     for i in range(args.warmup + args.steps):
         flush_l2(i)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for k, t in host_in.items():
-            getattr(g, k).copy_(t, non_blocking=True)
+        dev_pack.copy_(host_pack, non_blocking=True)
         if graph is not None:
             graph.replay()
         else:

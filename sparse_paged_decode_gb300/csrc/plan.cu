@@ -1,5 +1,5 @@
 // plan.cu -- the device planner of the tensor-core decode attention and the
-// query conversion that shares its first launch (see plan.cuh for what the
+// query conversion that shares its unit launch (see plan.cuh for what the
 // plan holds).
 //
 // The planner is latency-bound work on few SMs, so it is laid out for few

@@ -191,6 +191,20 @@ def test_per_head_selection_and_bad_metadata(spd, orc):
     full_check(spd, orc, w, per_head_topk=True)
 
 
+def test_many_rows_planner_rounds(spd, orc):
+    """More query rows than one planner round (512) and more lists than one
+    list CTA's warps, with per-kv-head selection: the group scan carries run
+    starts and group counts across rounds, and lists spread over CTAs."""
+    rng = np.random.default_rng(404)
+    n_req = 170
+    toks = rng.choice([1, 2, 3, 4, 8], size=n_req).tolist()
+    lengths = rng.integers(1, 500, size=n_req).tolist()
+    w = W.make_decode("rows", lengths=lengths, tokens_per_request=toks, Hq=16, Hkv=2, D=128, Di=64, NB=4,
+                      P=4 * n_req + 8, K=2, seed=404)
+    assert w.T > 512
+    full_check(spd, orc, w, per_head_topk=True)
+
+
 def test_duplicate_and_out_of_range_ids(spd, orc):
     w = W.make_decode("dup", lengths=[1000, 600], tokens_per_request=[2, 1], Hq=16, Hkv=2, D=128, Di=128, NB=8,
                       P=20, K=4, seed=5)

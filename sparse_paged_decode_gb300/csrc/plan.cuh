@@ -110,7 +110,7 @@ struct PlanArgs {
     int32_t num_ctas;
     char *ws;
     PlanLayout lay;
-    // query conversion (the other CTAs of the prepare launch)
+    // query conversion (the other CTAs of the unit launch)
     const void *q;
     int64_t q_s0, q_s1, q_s2;
     int32_t q_dt, Hq;

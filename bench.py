@@ -58,6 +58,23 @@ def measured_peaks():
     return 6800.0, "fallback 6.8 TB/s"
 
 
+def measured_bf16_peak():
+    """Dense bf16 tensor peak in TFLOP/s (burst: the score kernel is timed alone)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    return 1900.0, "fallback 1.9 PFLOP/s"
+
+
+def score_flops(w):
+    """Algorithmic FLOPs of one score call: every query token against every
+    key it may see (below its seq_len), Di multiply-adds each, per index head."""
+    lim = np.minimum(np.maximum(w.seq_lens.numpy().astype(np.int64), 0), w.NB * BS)
+    return float(2 * int(lim.sum()) * w.Di * w.Hi)
+
+
 def workload_desc(w):
     return {
         "workload": "cfg%s: %s" % (w.name[-1], W.CONFIG_NAMES.get(int(w.name[-1]), w.name)),
@@ -65,7 +82,8 @@ def workload_desc(w):
         "tokens_per_request": w.tokens_per_request, "request_lengths": w.request_lengths,
         "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.D, "index_heads": w.Hi, "index_dim": w.Di,
         "block_size": w.block_size, "page_table_blocks": w.NB, "pool_pages": w.P, "top_k": w.K,
-        "kv_dtype": "e4m3 (static scalar scales)", "q_dtype": str(w.q.dtype).replace("torch.", ""),
+        "kv_dtype": "e4m3 (static scalar scales)" if w.k_cache is not None else None,
+        "q_dtype": str(w.q.dtype).replace("torch.", "") if w.q is not None else None,
         "index_dtype": str(w.q_idx.dtype).replace("torch.", "") if w.q_idx is not None else None,
         "l2": "flushed between timed steps (256 MiB rewrite, then a 256 MiB read that cleans the dirty lines; "
               "outside the events)",
@@ -170,6 +188,11 @@ def oracle_rate(w, budget_s=12.0, max_rows=None):
         s = o.block_score(w.q_idx[idx], w.k_idx_cache, w.block_table, w.req_idx[idx], w.seq_lens[idx],
                           float(np.float32(w.idx_scale)))
         tk = o.select_topk(s, w.K)
+        if w.q is None:  # prefill score-to-selection: no attention stage
+            done += 1
+            if time.perf_counter() - t0 >= budget_s or (max_rows and done >= max_rows):
+                break
+            continue
         o.paged_attention(w.q[idx], w.k_cache, w.v_cache, w.block_table, w.req_idx[idx], w.seq_lens[idx], tk,
                           float(np.float32(w.sm_scale)), float(np.float32(w.k_scale)), float(np.float32(w.v_scale)))
         done += 1
@@ -235,8 +258,11 @@ def run_gpu(args, rank, world, local_rank):
     T, NB, K = w.T, w.NB, max(w.K, 1)
     scores = torch.empty((w.Hi, T, NB), device=dev)
     topk = torch.empty((w.Hi, T, K), dtype=torch.int32, device=dev)
-    out = torch.empty((T, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(spd.decode_workspace_bytes(T, w.Hq, w.Hkv, w.D, NB), dtype=torch.uint8, device=dev)
+    prefill = w.q is None  # cfg4: score-to-selection only, no attention stage
+    out = ws = None
+    if not prefill:
+        out = torch.empty((T, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(spd.decode_workspace_bytes(T, w.Hq, w.Hkv, w.D, NB), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     clean = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     clean_sum = torch.empty((), dtype=torch.int64, device=dev)
@@ -259,10 +285,25 @@ def run_gpu(args, rank, world, local_rank):
                                               gg.req_idx, topk.expand(w.Hkv, -1, -1), out, gg.sm_scale, BS,
                                               gg.k_scale, gg.v_scale, ws)
 
+    def score_call(gg):
+        spd.msa_block_score(gg.q_idx, gg.k_idx_cache, gg.block_table, gg.seq_lens, gg.req_idx, BS, scores,
+                            gg.idx_scale)
+
+    # the call the roofline is taken on: the attention call for decode, the
+    # score call for prefill
+    timed = score_call if prefill else attention
+
     def step(gg, evs=None):
+        if prefill:
+            if evs is not None:
+                evs[0].record(stream)
+            score_call(gg)
+            if evs is not None:
+                evs[1].record(stream)
+            spd.msa_select_topk(scores, topk)
+            return
         if not dense:
-            spd.msa_block_score(gg.q_idx, gg.k_idx_cache, gg.block_table, gg.seq_lens, gg.req_idx, BS, scores,
-                                gg.idx_scale)
+            score_call(gg)
             spd.msa_select_topk(scores, topk)
         if evs is not None:
             evs[0].record(stream)
@@ -289,10 +330,11 @@ def run_gpu(args, rank, world, local_rank):
         with torch.cuda.graph(graph, stream=side):
             step(g)
         torch.cuda.synchronize(dev)
-        # the attention call alone (its three kernels), for the roofline
+        # the attention call alone (its three kernels; the score call for
+        # prefill), for the roofline
         graph_attn = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph_attn, stream=side):
-            attention(g)
+            timed(g)
         torch.cuda.synchronize(dev)
 
     sampler = ClockSampler(local_rank) if rank == 0 else None
@@ -339,9 +381,10 @@ def run_gpu(args, rank, world, local_rank):
 
     # end to end through the same calls with host buffers: the step's inputs
     # (queries, index queries, page table, seq_lens, req_idx), packed in one
-    # pinned buffer, copied in with one transfer, the attention output copied
-    # back; caches stay resident
-    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    # pinned buffer, copied in with one transfer, the attention output (the
+    # top-k ids for prefill) copied back; caches stay resident
+    result = topk if prefill else out
+    host_out = torch.empty(result.shape, dtype=result.dtype).pin_memory()
     h2d = total_in
     d2h = host_out.numel() * host_out.element_size()
     e2e_ms = []
@@ -354,7 +397,7 @@ def run_gpu(args, rank, world, local_rank):
             graph.replay()
         else:
             step(g)
-        host_out.copy_(out, non_blocking=True)
+        host_out.copy_(result, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         if i >= args.warmup:
@@ -373,10 +416,7 @@ def run_gpu(args, rank, world, local_rank):
     value = rows * args.steps / (total_ms / 1e3)
     e2e_value = rows * args.steps / (e2e_total / 1e3)
     topk_np = None if dense else topk.cpu().numpy()
-    abytes = attention_bytes(w, topk_np)
     attn_mean_s = statistics.mean(attn_ms) / 1e3
-    achieved = abytes / attn_mean_s / 1e9
-    peak, peak_src = measured_peaks()
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "attention_traffic.json")
     if os.path.exists(tpath):
@@ -384,23 +424,41 @@ def run_gpu(args, rank, world, local_rank):
             tj = json.load(f)
         if tj.get("config") == args.config and tj.get("kernel_stamp") == _kernel_stamp():
             traffic = tj.get("traffic_bytes_per_launch")
+    if prefill:
+        # the score call is a contraction: tensor-bound against the bf16 peak
+        flops = score_flops(w)
+        achieved = flops / attn_mean_s / 1e12
+        peak, peak_src = measured_bf16_peak()
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": None,
+                    "kernel": "score call (score_tc_kernel; %s)" % ("graph replay" if graph is not None
+                                                                      else "direct launches"),
+                    "algorithmic_flops_per_launch": flops, "mean_launch_us": attn_mean_s * 1e6,
+                    "peak_source": peak_src}
+    else:
+        abytes = attention_bytes(w, topk_np)
+        achieved = abytes / attn_mean_s / 1e9
+        peak, peak_src = measured_peaks()
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                    "traffic": traffic,
+                    "kernel": "paged attention call (list, unit and attention kernels; %s)"
+                              % ("graph replay" if graph is not None else "direct launches"),
+                    "algorithmic_bytes_per_launch": abytes,
+                    "mean_launch_us": attn_mean_s * 1e6, "peak_source": peak_src}
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         rate, n, dt = oracle_rate(W.config(args.config, seed=1000 + args.config), budget_s=args.cpu_seconds)
         cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": "%d query rows of this workload through the oracle's three stages "
-                         "(single-threaded C, fp64), %.1f s" % (n, dt)}
+               "sample": "%d query rows of this workload through the oracle's %s "
+                         "(single-threaded C, fp64), %.1f s" % (n, "score and select stages" if prefill
+                                                               else "three stages", dt)}
     return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3/f16 mma, f32 accumulate", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 mma, f32 accumulate" if prefill else "e4m3/f16 mma, f32 accumulate", "data": "synthetic",
         "config": workload_desc(w),
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic,
-                     "kernel": "paged attention call (list, unit and attention kernels; %s)"
-                               % ("graph replay" if graph is not None else "direct launches"),
-                     "algorithmic_bytes_per_launch": abytes,
-                     "mean_launch_us": attn_mean_s * 1e6, "peak_source": peak_src},
+        "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
@@ -425,7 +483,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=2, choices=[2, 3, 5],
+    ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5],
                     help="workload (2 = EAGLE-style verification decode, the metric's workload)")
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

@@ -253,8 +253,10 @@ SPD_API int spd_set_attention_kernel(int policy);
  * stage 1 = msa_block_score, 2 = msa_select_topk, 3 = the attention calls
  * (the same setting as spd_set_attention_kernel).  policy 0 (default) picks
  * the specialised kernel whenever the shapes and layouts allow it, 1 always
- * the general-layout kernel.  Returns the previous setting, or -1 for an
- * unknown stage.
+ * the general-layout kernel; for stage 2, policy 2 picks the shared-memory
+ * rank kernel (the default sorts rows of up to 256 blocks in registers and
+ * ranks longer ones).  All give identical selections.  Returns the previous
+ * setting, or -1 for an unknown stage.
  */
 SPD_API int spd_set_kernel_policy(int stage, int policy);
 

@@ -20,7 +20,7 @@ cudaError_t launch_attention_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cu
 
 namespace {
 // per stage (index = spd stage code): 0 fastest kernel the shapes allow,
-// 1 the general-layout kernel
+// 1 the general-layout kernel, 2 (selection only) the rank kernel
 thread_local int g_policy[4] = {0, 0, 0, 0};
 }
 
@@ -43,7 +43,8 @@ cudaError_t dispatch_score(const ScoreArgs &a, cudaStream_t stream) {
 
 cudaError_t dispatch_select(const SelectArgs &a, cudaStream_t stream) {
     count_launches(1);
-    if (g_policy[2] == 0) return launch_select_rank(a, stream);
+    if (g_policy[2] == 0) return launch_select_fast(a, stream);
+    if (g_policy[2] == 2) return launch_select_rank(a, stream);
     return launch_select_generic(a, stream);
 }
 

@@ -155,6 +155,84 @@ select_rank_kernel(SelectArgs a, int nb4) {
     for (int k = n_cand + lane; k < a.K; k += 32) o[k * a.o_s2] = -1;
 }
 
+// Top-k by sorting, for rows of at most 256 blocks.  Each score becomes a
+// 64-bit key ordered by score (descending), then block id (ascending) -- the
+// order the ranks above count in -- with non-candidates after every
+// candidate; one warp sorts the row's 32E keys with a bitonic network, E
+// keys per lane (lane l holds keys lE .. lE+E-1: partners E or more apart
+// are exchanged by shuffles, nearer ones inside the lane).  The first K keys
+// are the selection in output order.  About 28 (E = 4) to 36 (E = 8)
+// exchange steps of a few instructions per key replace the NB^2 comparisons
+// of the rank kernel.
+constexpr uint64_t kNoKey = ~0ull;
+
+__device__ __forceinline__ uint64_t order_key(float v, uint32_t b) {
+    if (!is_candidate(v)) return kNoKey;
+    if (v == 0.f) v = 0.f;  // -0 and +0 are equal scores
+    uint32_t u = __float_as_uint(v);
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);  // increasing in v
+    return (static_cast<uint64_t>(~u) << 32) | b;      // decreasing in v, then increasing in b
+}
+
+template <int E>
+__device__ __forceinline__ void warp_bitonic_sort(uint64_t (&x)[E], int lane) {
+    constexpr int M = 32 * E;
+#pragma unroll
+    for (int k = 2; k <= M; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            if (j >= E) {
+                const int lj = j / E;
+                const bool lower = (lane & lj) == 0;  // this lane holds the lower index of each pair
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const bool up = ((lane * E + e) & k) == 0;
+                    const uint64_t y = __shfl_xor_sync(0xffffffffu, x[e], lj);
+                    const bool lt = x[e] < y;
+                    x[e] = (lower == up) ? (lt ? x[e] : y) : (lt ? y : x[e]);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    if (e & j) continue;
+                    const bool up = ((lane * E + e) & k) == 0;
+                    const uint64_t p = x[e], q = x[e + j];
+                    const bool swap = up ? (q < p) : (p < q);
+                    x[e] = swap ? q : p;
+                    x[e + j] = swap ? p : q;
+                }
+            }
+        }
+    }
+}
+
+template <int E>
+__global__ void __launch_bounds__(kSelectWarps * 32)
+select_sort_kernel(SelectArgs a) {
+    // launched with programmatic stream serialisation (see launch_select_fast)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kSelectWarps + warp;
+    if (row >= a.Hi * a.T) return;
+    const int h = row / a.T, t = row % a.T;
+    const float *s = a.s + h * a.s_s0 + t * a.s_s1;
+    uint64_t key[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const int b = lane * E + e;
+        key[e] = (b < a.NB) ? order_key(s[b * a.s_s2], static_cast<uint32_t>(b)) : kNoKey;
+    }
+    warp_bitonic_sort<E>(key, lane);
+    int32_t *o = a.o + h * a.o_s0 + t * a.o_s1;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const int i = lane * E + e;
+        if (i < a.K) o[i * a.o_s2] = (key[e] == kNoKey) ? -1 : static_cast<int32_t>(static_cast<uint32_t>(key[e]));
+    }
+    for (int i = 32 * E + lane; i < a.K; i += 32) o[i * a.o_s2] = -1;
+}
+
 // ------------------------------------------------------------------ stage 3
 // "Kernel ABI" -- attention.decode.  One CTA per (query token t, kv head h)
 // serves the G = Hq/Hkv q heads of that kv head.  Blocks are visited in
@@ -289,6 +367,26 @@ cudaError_t launch_score_generic(const ScoreArgs &a, cudaStream_t stream) {
     dim3 grid(a.T, (a.NB + kScoreWarps - 1) / kScoreWarps, a.Hi);
     score_generic_kernel<<<grid, kScoreWarps * 32, a.Di * sizeof(float), stream>>>(a);
     return cudaGetLastError();
+}
+
+cudaError_t launch_select_fast(const SelectArgs &a, cudaStream_t stream) {
+    if (a.NB > 256) return launch_select_rank(a, stream);
+    const int rows = a.Hi * a.T;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((rows + kSelectWarps - 1) / kSelectWarps);
+    cfg.blockDim = dim3(kSelectWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    // programmatic stream serialisation, as for the rank kernel
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (a.NB <= 32) return cudaLaunchKernelEx(&cfg, select_sort_kernel<1>, a);
+    if (a.NB <= 64) return cudaLaunchKernelEx(&cfg, select_sort_kernel<2>, a);
+    if (a.NB <= 128) return cudaLaunchKernelEx(&cfg, select_sort_kernel<4>, a);
+    return cudaLaunchKernelEx(&cfg, select_sort_kernel<8>, a);
 }
 
 cudaError_t launch_select_rank(const SelectArgs &a, cudaStream_t stream) {

@@ -78,6 +78,7 @@ struct AttnArgs {
 cudaError_t launch_score_generic(const ScoreArgs &a, cudaStream_t stream);
 cudaError_t launch_select_generic(const SelectArgs &a, cudaStream_t stream);
 cudaError_t launch_select_rank(const SelectArgs &a, cudaStream_t stream);
+cudaError_t launch_select_fast(const SelectArgs &a, cudaStream_t stream);  // sort for NB <= 256, else rank
 cudaError_t launch_attention_generic(const AttnArgs &a, cudaStream_t stream);
 
 // ------------------------------------------------------------- device helpers

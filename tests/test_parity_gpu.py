@@ -178,6 +178,57 @@ def test_cfg1_tiny(spd, orc):
     full_check(spd, orc, W.config(1))
 
 
+SELECT_SHAPES = [(1, 1), (5, 3), (31, 16), (32, 32), (33, 7), (64, 64), (100, 16), (128, 32), (128, 64),
+                 (129, 32), (200, 50), (256, 128), (256, 300), (257, 16), (300, 64)]
+
+
+def edge_score_rows(rng, T, NB):
+    """Score rows that stress the ordering: random values, heavy ties, signed
+    zeros, NaN / -inf (not candidates), +inf, rows with fewer candidates than
+    K and rows with none."""
+    s = rng.standard_normal((T, NB)).astype(np.float32)
+    for t in range(T):
+        kind = t % 8
+        if kind == 1:
+            s[t] = rng.choice(np.array([-1.0, 0.0, 1.0, 2.0], np.float32), NB)
+        elif kind == 2:
+            s[t] = rng.choice(np.array([0.0, -0.0, -np.inf, 0.5], np.float32), NB)
+        elif kind == 3:
+            s[t, rng.random(NB) < 0.3] = np.nan
+        elif kind == 4:
+            s[t, rng.random(NB) < 0.2] = np.inf
+        elif kind == 5:
+            s[t] = rng.choice(np.array([np.nan, -np.inf], np.float32), NB)
+        elif kind == 6:
+            s[t] = 0.25
+        elif kind == 7:
+            s[t, rng.random(NB) < 0.9] = -np.inf
+    return s
+
+
+@pytest.mark.parametrize("NB,K", SELECT_SHAPES)
+def test_select_kernels_agree_on_edge_rows(spd, orc, NB, K):
+    """Top-k ("attention.msa_select_topk"): every selection kernel (register
+    sort, shared-memory ranks, general layout) gives the oracle's ids exactly
+    -- ties to the lower block id, -0 equal to +0, NaN and -inf never
+    selected, -1 padding -- on contiguous and strided sheets."""
+    rng = np.random.default_rng(NB * 1000 + K)
+    Hi, T = 2, 16
+    sheet = np.stack([edge_score_rows(rng, T, NB) for _ in range(Hi)])
+    ref = orc.select_topk(sheet, K)
+    dense = torch.from_numpy(sheet).to(DEV)
+    wide = torch.full((Hi, T, 2 * NB), 77.0, device=DEV)
+    wide[:, :, ::2] = dense
+    for scores in (dense, wide[:, :, ::2]):
+        for policy in (0, 2, 1):
+            old = spd.set_kernel_policy(2, policy)
+            try:
+                got = gpu_topk(spd, scores, K).cpu().numpy()
+            finally:
+                spd.set_kernel_policy(2, old)
+            assert np.array_equal(got, ref), f"policy {policy}, stride {scores.stride()}"
+
+
 def test_per_head_selection_and_bad_metadata(spd, orc):
     w = W.make_decode("meta", lengths=[900, 300, 1700], tokens_per_request=[2, 3, 4], Hq=32, Hkv=4, D=128,
                       Di=128, NB=16, P=48, K=6, seed=77)

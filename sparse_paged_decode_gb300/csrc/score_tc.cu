@@ -31,7 +31,7 @@ cudaError_t launch_score_tc(const ScoreArgs &a, cudaStream_t stream, bool *used)
 namespace {
 
 constexpr int kLanes = 128;       // query lanes per tile (M)
-constexpr int kMaxStages = 4;     // key stages: 4 for Di <= 128, else 2 (shared-memory budget)
+constexpr int kMaxStages = 4;     // key stages: 4 for Di = 64, else 2 (shared-memory budget)
 constexpr int kMaxChunk = 8;      // block ids per CTA
 constexpr int kThreadsSc = 192;   // warps 0-3 epilogue (TMEM quadrants), 4 TMA, 5 MMA
 constexpr int kAtom = 128 * 128;  // one 64-element column chunk of 128 rows, bytes
@@ -65,11 +65,13 @@ struct ScoreShared {
     uint32_t run_ok[kMaxChunk][kLanes / 32];  // bit j of word: run j has a valid page for that block
 };
 
-__host__ __device__ inline int key_stages(int nkc) { return nkc <= 2 ? 4 : 2; }
-
-// 128-column TMEM accumulators: four when the shared memory keeps the CTA
-// alone on its SM (Di >= 128), so no other CTA waits for tensor memory.
-__device__ __forceinline__ int acc_count(int nkc) { return nkc >= 2 ? 4 : 2; }
+// Key stages and 128-column TMEM accumulators per CTA.  Up to Di = 128 a CTA
+// takes at most ~110 KB of shared memory and 256 TMEM columns, so two CTAs
+// share an SM: one's prologue (lane limits, page table, first loads)
+// overlaps the other's products.  Wider keys keep the CTA alone on its SM,
+// with four accumulators.
+__host__ __device__ inline int key_stages(int nkc) { return nkc <= 1 ? 4 : 2; }
+__device__ __forceinline__ int acc_count(int nkc) { return nkc >= 3 ? 4 : 2; }
 
 // All 32 lanes wait; the warp goes on only if every lane saw the phase.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {

@@ -47,6 +47,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 
 #include "plan.cuh"
 #include "spd_internal.cuh"
@@ -1098,6 +1099,22 @@ DeviceInfo &device_info() {
     return d;
 }
 
+// Query rows of one request that share a unit (a group).  A group reads each
+// block of the union of its rows' selections once, but the softmax cost of a
+// block grows with the group's width: 16 columns cost about half of 32 or 64
+// (measured).  Dense calls and groups no wider than 16 columns always group.
+// For sparse calls whose groups would be wider, the union of g independent
+// K-of-NB selections is expected to hold NB (1 - (1 - K/NB)^g) blocks; when
+// twice that exceeds the g K blocks the rows would read one by one (little
+// overlap), each row is a group of its own.
+int group_rows(const AttnArgs &a, int G) {
+    const int g = std::min(16, kNMax / G);
+    if (a.tk == nullptr || g * G <= 16 || a.K >= a.NB || a.NB <= 0) return g;
+    const double keep = 1.0 - static_cast<double>(a.K) / a.NB;
+    const double uni = a.NB * (1.0 - std::pow(keep, g));
+    return (2.0 * uni > static_cast<double>(g) * a.K) ? 1 : g;
+}
+
 }  // namespace
 
 // The fast path covers: head dim 128, E4M3 caches whose rows are 16-byte
@@ -1130,7 +1147,7 @@ cudaError_t launch_attention_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cu
     p.bt = a.bt; p.bt_s0 = a.bt_s0; p.bt_s1 = a.bt_s1;
     p.tk = a.tk; p.tk_s0 = a.tk_s0; p.tk_s1 = a.tk_s1; p.tk_s2 = a.tk_s2;
     p.T = a.T; p.R = a.R; p.NB = a.NB; p.K = a.K; p.Hkv = a.Hkv; p.G = G;
-    p.gmax = std::min(16, kNMax / G);
+    p.gmax = group_rows(a, G);
     p.P = a.P;
     p.num_ctas = dev.sms;
     p.ws = static_cast<char *>(ws);

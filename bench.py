@@ -473,7 +473,7 @@ def _kernel_stamp():
     try:
         from sparse_paged_decode_gb300 import build as b
 
-        return b._stamp()[:16]
+        return b._stamp(b.ATTENTION_SOURCES)[:16]
     except Exception:  # pragma: no cover
         return None
 

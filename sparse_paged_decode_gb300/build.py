@@ -36,9 +36,19 @@ def _sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-def _stamp() -> str:
+# sources of the sparse/dense attention call (planner kernels and the
+# tensor-core attention kernel): what a DRAM-traffic capture of that call
+# depends on
+ATTENTION_SOURCES = ("attention_tc.cu", "plan.cu", "plan.cuh", "spd_internal.cuh", "tc_ptx.cuh", "tmap.cuh")
+
+
+def _stamp(names=None) -> str:
+    """Hash of the sources (all of them, or the named files of csrc) and the
+    compiler flags."""
     h = hashlib.sha256()
-    for path in sorted(glob.glob(os.path.join(CSRC, "*")) + [os.path.join(INCLUDE, "spd.h")]):
+    paths = (sorted(glob.glob(os.path.join(CSRC, "*")) + [os.path.join(INCLUDE, "spd.h")]) if names is None
+             else [os.path.join(CSRC, n) for n in sorted(names)])
+    for path in paths:
         with open(path, "rb") as f:
             h.update(os.path.basename(path).encode())
             h.update(f.read())

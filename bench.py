@@ -202,6 +202,30 @@ def oracle_rate(w, budget_s=12.0, max_rows=None):
     return done / dt, done, dt
 
 
+# ------------------------------------------------------------ replicas
+# The path has no exchange step: N ranks run N independent batches (weak
+# scaling).  These are the only places the ranks meet.
+
+def batch_seed(config, rank):
+    """Seed of a rank's synthetic batch: every rank gets its own inputs."""
+    return 1000 + config + 97 * rank
+
+
+def max_over_ranks(values, world, device):
+    """Element-wise maximum of per-rank timings (the slowest rank sets the
+    job's time)."""
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_rate(rows_per_rank, world, steps, total_ms):
+    """Whole-job throughput: the query rows all ranks processed over the
+    slowest rank's time."""
+    return rows_per_rank * world * steps / (total_ms / 1e3)
+
+
 # --------------------------------------------------------------------- arms
 
 def run_reference(args, rank, world):
@@ -235,7 +259,7 @@ def run_gpu(args, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = W.config(args.config, seed=1000 + args.config + 97 * rank)
+    w = W.config(args.config, seed=batch_seed(args.config, rank))
     g = w.to(dev)
     # the step's per-call inputs live in one device buffer (each tensor a
     # 256-byte aligned view), so the end-to-end run stages them with a
@@ -405,16 +429,12 @@ def run_gpu(args, rank, world, local_rank):
     clocks = sampler.stop() if sampler else None
 
     # max over ranks
-    t_max = torch.tensor([total_ms, sum(e2e_ms)], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t_max, op=torch.distributed.ReduceOp.MAX)
-    total_ms, e2e_total = float(t_max[0]), float(t_max[1])
+    total_ms, e2e_total = max_over_ranks([total_ms, sum(e2e_ms)], world, dev)
     if rank != 0:
         return None
 
-    rows = w.n_valid_tokens * world
-    value = rows * args.steps / (total_ms / 1e3)
-    e2e_value = rows * args.steps / (e2e_total / 1e3)
+    value = job_rate(w.n_valid_tokens, world, args.steps, total_ms)
+    e2e_value = job_rate(w.n_valid_tokens, world, args.steps, e2e_total)
     topk_np = None if dense else topk.cpu().numpy()
     attn_mean_s = statistics.mean(attn_ms) / 1e3
     traffic = None

@@ -99,7 +99,10 @@ typedef enum {
  *   b whose page id is outside the pool).
  *
  * q_idx        [T, Hi, Di]  f32 | bf16 | f16   query index heads
- * k_idx_cache  [P*128, 1, Di] same dtype as q_idx; one index key head
+ * k_idx_cache  [P*128, 1, Di] same dtype as q_idx, or e4m3 (an FP8 index
+ *              cache: its values enter as the E4M3 numbers they encode; a
+ *              static scalar dequantisation scale is folded into idx_scale
+ *              by the caller); one index key head
  * block_table  [R, NB] i32  page id of each logical block
  * seq_lens     [T] i32      valid keys of each query token (prefill: position + 1)
  * req_idx      [T] i32      block_table row of each query token

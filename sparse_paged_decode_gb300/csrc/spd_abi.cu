@@ -167,11 +167,12 @@ bool block_score(const spd_tensor *q, const spd_tensor *k, const spd_tensor *bt,
                  const spd_tensor *ri, int32_t block_size, const spd_tensor *out, float idx_scale,
                  cudaStream_t stream) {
     if (!check_desc(q, "q_idx", 3, {SPD_F32, SPD_BF16, SPD_F16})) return false;
-    if (!check_desc(k, "k_idx_cache", 3, {SPD_F32, SPD_BF16, SPD_F16})) return false;
+    if (!check_desc(k, "k_idx_cache", 3, {SPD_F32, SPD_BF16, SPD_F16, SPD_E4M3})) return false;
     if (!check_desc(out, "scores", 3, {SPD_F32})) return false;
     const int64_t T = q->shape[0], Hi = q->shape[1], Di = q->shape[2];
     if (!check_paging(bt, sl, ri, T, block_size)) return false;
-    if (k->dtype != q->dtype) return fail(SPD_ERR_UNSUPPORTED, "k_idx_cache dtype must match q_idx");
+    if (k->dtype != q->dtype && k->dtype != SPD_E4M3)
+        return fail(SPD_ERR_UNSUPPORTED, "k_idx_cache dtype must match q_idx (or be e4m3)");
     if (k->shape[1] != 1) return fail(SPD_ERR_UNSUPPORTED, "k_idx_cache must have one index key head");
     if (k->shape[2] != Di) return fail(SPD_ERR_INVALID_ARGUMENT, "k_idx_cache head dim != q_idx head dim");
     if (k->shape[0] % kBlock != 0) return fail(SPD_ERR_INVALID_ARGUMENT, "k_idx_cache slots not a whole number of pages");

@@ -83,16 +83,17 @@ cudaError_t launch_attention_generic(const AttnArgs &a, cudaStream_t stream);
 
 // ------------------------------------------------------------- device helpers
 
-__device__ __forceinline__ float load_float(const void *base, int dt, int64_t off) {
-    if (dt == SPD_F32) return static_cast<const float *>(base)[off];
-    if (dt == SPD_BF16) return __bfloat162float(static_cast<const __nv_bfloat16 *>(base)[off]);
-    return __half2float(static_cast<const __half *>(base)[off]);
-}
-
 __device__ __forceinline__ float e4m3_to_float(uint8_t code) {
     __nv_fp8_e4m3 v;
     v.__x = code;
     return static_cast<float>(v);
+}
+
+__device__ __forceinline__ float load_float(const void *base, int dt, int64_t off) {
+    if (dt == SPD_F32) return static_cast<const float *>(base)[off];
+    if (dt == SPD_BF16) return __bfloat162float(static_cast<const __nv_bfloat16 *>(base)[off]);
+    if (dt == SPD_E4M3) return e4m3_to_float(static_cast<const uint8_t *>(base)[off]);
+    return __half2float(static_cast<const __half *>(base)[off]);
 }
 
 // seq_len of query token t clipped to [0, NB*128]; 0 when its request row is

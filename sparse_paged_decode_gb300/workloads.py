@@ -231,6 +231,17 @@ CONFIG_NAMES = {
 }
 
 
+def with_fp8_index(w: Workload) -> Workload:
+    """The same batch with its index cache stored as FP8-E4M3 under a static
+    scalar scale max|x|/448; the scale is folded into idx_scale, as a caller
+    of msa_block_score does for an FP8 index cache."""
+    out = Workload(**{k: getattr(w, k) for k in w.__dataclass_fields__})
+    codes, scale = _to_e4m3(w.k_idx_cache.float())
+    out.k_idx_cache = codes
+    out.idx_scale = w.idx_scale * scale
+    return out
+
+
 def config(cfg: int, seed: Optional[int] = None) -> Workload:
     """The five benchmark configurations, full size."""
     seed = 1000 + cfg if seed is None else seed

@@ -151,6 +151,9 @@ def test_score_and_select_rejections(spd):
     assert score(bs=256) == SPD_ERR_UNSUPPORTED
     assert score(kk=Fake((256, 2, 32), BF16)) == SPD_ERR_UNSUPPORTED  # two index key heads
     assert score(kk=Fake((256, 1, 32), F32)) == SPD_ERR_UNSUPPORTED  # dtype mismatch
+    # an E4M3 index cache goes with any query dtype (validation passes; the launch needs a GPU)
+    assert score(kk=Fake((256, 1, 32), E4M3)) in (SPD_OK, SPD_ERR_CUDA)
+    assert score(qq=Fake((3, 1, 32), F32), kk=Fake((256, 1, 32), E4M3)) in (SPD_OK, SPD_ERR_CUDA)
     assert score(o=Fake((1, 3, 3), F32)) == SPD_ERR_INVALID_ARGUMENT
     assert score(sll=Fake((2,), I32)) == SPD_ERR_INVALID_ARGUMENT
     # select

@@ -377,6 +377,67 @@ def test_empty_batch(spd):
     torch.cuda.synchronize()
 
 
+# ------------------------------------------------------ FP8 index cache
+
+FP8_INDEX = {
+    # bf16 queries of 128 dims: the tensor-core f8 product
+    "di128": dict(lengths=[1500, 700, 300], tokens_per_request=[4, 2, 1], Di=128, NB=16, P=40, K=4),
+    # 64 dims: the general-layout kernel
+    "di64": dict(lengths=[900, 200], tokens_per_request=[3, 1], Di=64, NB=8, P=16, K=3),
+    # two index heads (64 lanes of tokens per tile)
+    "hi2": dict(lengths=[1300, 600], tokens_per_request=[5, 2], Di=128, Hi=2, NB=16, P=32, K=3),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FP8_INDEX))
+def test_fp8_index_cache(spd, orc, name, kernel_policy):
+    """An FP8-E4M3 index cache (its static scale folded into idx_scale):
+    the score sheet and top-k against the oracle on the same E4M3 codes."""
+    w = W.with_fp8_index(W.make_decode("fp8idx_" + name, Hq=16, Hkv=2, D=128, seed=zlib.crc32(name.encode()) % 1000,
+                                       with_kv=False, **FP8_INDEX[name]))
+    g = w.to(DEV)
+    s = gpu_scores(spd, g)
+    ref = orc.block_score(w.q_idx, w.k_idx_cache, w.block_table, w.req_idx, w.seq_lens, f32(w.idx_scale))
+    check_scores(s.cpu().numpy(), ref, name + " scores")
+    check_topk(gpu_topk(spd, s, w.K).cpu().numpy(), ref, w.K, name + " topk")
+
+
+def test_fp8_index_cache_strided_queries(spd, orc):
+    """Queries viewed inside a wider buffer (16-byte aligned rows) still take
+    the f8 product; the result matches the contiguous call."""
+    w = W.with_fp8_index(W.make_decode("fp8idx_strided", lengths=[1100, 500], tokens_per_request=[3, 3], Hq=16,
+                                       Hkv=2, D=128, Di=128, NB=16, P=24, K=4, seed=77, with_kv=False))
+    g = w.to(DEV)
+    wide = torch.zeros((w.T, 1, 2 * w.Di), dtype=g.q_idx.dtype, device=DEV)
+    wide[:, :, 8:8 + w.Di] = g.q_idx
+    view = wide[:, :, 8:8 + w.Di]
+    T, NB = g.seq_lens.shape[0], g.block_table.shape[1]
+    out = nan_like((1, T, NB), torch.float32, DEV)
+    spd.msa_block_score(view, g.k_idx_cache, g.block_table, g.seq_lens, g.req_idx, BS, out, g.idx_scale)
+    torch.cuda.synchronize()
+    ref = orc.block_score(w.q_idx, w.k_idx_cache, w.block_table, w.req_idx, w.seq_lens, f32(w.idx_scale))
+    check_scores(out.cpu().numpy(), ref, "strided fp8 index scores")
+
+
+def test_fp8_index_cache_cfg2_and_cfg4(spd, orc):
+    """The verification-decode and prefill index shapes with an FP8 index
+    cache: cfg2's whole sheet, sampled cfg4 rows."""
+    w = W.with_fp8_index(W.config(2))
+    g = w.to(DEV)
+    s = gpu_scores(spd, g)
+    ref = orc.block_score(w.q_idx, w.k_idx_cache, w.block_table, w.req_idx, w.seq_lens, f32(w.idx_scale))
+    check_scores(s.cpu().numpy(), ref, "cfg2 fp8 index scores")
+    check_topk(gpu_topk(spd, s, w.K).cpu().numpy(), ref, w.K, "cfg2 fp8 index topk")
+    w = W.with_fp8_index(W.config(4))
+    g = w.to(DEV)
+    s = gpu_scores(spd, g)
+    rows = [0, 1, 511, 512, 2047, w.T - 1]
+    ridx = torch.tensor(rows)
+    ref = orc.block_score(w.q_idx[ridx], w.k_idx_cache, w.block_table, w.req_idx[ridx], w.seq_lens[ridx],
+                          f32(w.idx_scale))
+    check_scores(s.cpu().numpy()[:, rows], ref, "cfg4 fp8 index scores")
+
+
 # --------------------------------------------------------- full-size configs
 
 def test_cfg2_full(spd, orc):

@@ -7,7 +7,8 @@ the oracle disagrees with what the pages and the mathematics fix:
     every code;
   * the block-score sheet against a numpy brute force (gather the request's
     logical keys through the page table, one matrix product, mask, per-block
-    max) and against a hand-worked fixture and a closed-form ramp;
+    max; bf16, fp32 and FP8-E4M3 index caches) and against a hand-worked
+    fixture and a closed-form ramp;
   * top-k against numpy's lexicographic sort, ties and padding included;
   * attention against torch's fp64 ``scaled_dot_product_attention`` with GQA
     expansion on gathered, torch-dequantised keys and values, against a
@@ -180,6 +181,13 @@ def pin_block_score_bruteforce(o):
         got = o.block_score(w.q_idx, w.k_idx_cache, bt, ri, sl, w.idx_scale)
         ref = np_block_score(w.q_idx, w.k_idx_cache, bt, ri, sl, w.idx_scale, w.NB, w.P)
         assert_close(got, ref, what="block score seed %d" % seed)
+    # an FP8-E4M3 index cache: the oracle decodes the codes itself; the brute
+    # force takes torch's decoding of the same codes
+    w = W.with_fp8_index(tiny_decode(14, idx_dtype=torch.bfloat16))
+    got = o.block_score(w.q_idx, w.k_idx_cache, w.block_table, w.req_idx, w.seq_lens, w.idx_scale)
+    ref = np_block_score(w.q_idx, e4m3_to_f64(w.k_idx_cache.view(torch.uint8)), w.block_table, w.req_idx,
+                         w.seq_lens, w.idx_scale, w.NB, w.P)
+    assert_close(got, ref, what="block score, E4M3 index cache")
     # two query index heads sharing the single index key head
     w = tiny_decode(13)
     q2 = torch.randn((w.T, 2, w.Di), generator=torch.Generator().manual_seed(5))

@@ -85,6 +85,8 @@ def workload_desc(w):
         "kv_dtype": "e4m3 (static scalar scales)" if w.k_cache is not None else None,
         "q_dtype": str(w.q.dtype).replace("torch.", "") if w.q is not None else None,
         "index_dtype": str(w.q_idx.dtype).replace("torch.", "") if w.q_idx is not None else None,
+        "index_cache_dtype": (str(w.k_idx_cache.dtype).replace("torch.", "")
+                              if w.k_idx_cache is not None else None),
         "l2": "flushed between timed steps (256 MiB rewrite, then a 256 MiB read that cleans the dirty lines; "
               "outside the events)",
     }
@@ -226,12 +228,19 @@ def job_rate(rows_per_rank, world, steps, total_ms):
     return rows_per_rank * world * steps / (total_ms / 1e3)
 
 
+def make_workload(args, seed):
+    """The configuration's batch; with --index-cache e4m3 its index cache is
+    stored as FP8-E4M3 (scale folded into idx_scale)."""
+    w = W.config(args.config, seed=seed)
+    return W.with_fp8_index(w) if args.index_cache == "e4m3" and w.k_idx_cache is not None else w
+
+
 # --------------------------------------------------------------------- arms
 
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    w = W.config(args.config, seed=1000 + args.config)
+    w = make_workload(args, 1000 + args.config)
     per_step_budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         oracle_rate(w, budget_s=per_step_budget / 4, max_rows=1)
@@ -259,7 +268,7 @@ def run_gpu(args, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = W.config(args.config, seed=batch_seed(args.config, rank))
+    w = make_workload(args, batch_seed(args.config, rank))
     g = w.to(dev)
     # the step's per-call inputs live in one device buffer (each tensor a
     # 256-byte aligned view), so the end-to-end run stages them with a
@@ -467,7 +476,7 @@ def run_gpu(args, rank, world, local_rank):
                     "mean_launch_us": attn_mean_s * 1e6, "peak_source": peak_src}
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        rate, n, dt = oracle_rate(W.config(args.config, seed=1000 + args.config), budget_s=args.cpu_seconds)
+        rate, n, dt = oracle_rate(make_workload(args, 1000 + args.config), budget_s=args.cpu_seconds)
         cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": "%d query rows of this workload through the oracle's %s "
                          "(single-threaded C, fp64), %.1f s" % (n, "score and select stages" if prefill
@@ -509,6 +518,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch each call directly instead of replaying a graph")
+    ap.add_argument("--index-cache", default="native", choices=["native", "e4m3"],
+                    help="index cache as generated (bf16) or stored FP8-E4M3")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

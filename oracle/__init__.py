@@ -102,6 +102,8 @@ class Oracle:
         L.oracle_paged_attention.argtypes = [vp, c_int, i64, i64, i64, vp, vp, i64, i64, vp, i64, i64,
                                              vp, vp, vp, i64, dbl, dbl, dbl, i64, vp]
         L.oracle_paged_attention.restype = c_int
+        L.oracle_sdpa.argtypes = [vp, vp, vp, c_int, i64, i64, i64, i64, i64, dbl, c_int, vp]
+        L.oracle_sdpa.restype = c_int
 
     # -- decoders ----------------------------------------------------------
     def e4m3_value(self, code: int) -> float:
@@ -186,6 +188,25 @@ class Oracle:
                                              int(block_size), _ptr(out))
         if rc:
             raise RuntimeError("oracle_paged_attention failed")
+        return out
+
+    # -- dense attention ---------------------------------------------------
+    def sdpa(self, q, k, v, sm_scale: float, causal: bool) -> np.ndarray:
+        """Dense GQA attention output [T, Hq, D] (fp64); see oracle_sdpa."""
+        qa, qdt = _raw(q, "float")
+        ka, kdt = _raw(k, "float")
+        va, vdt = _raw(v, "float")
+        if not (qdt == kdt == vdt):
+            raise ValueError("oracle: q, k and v must share one dtype")
+        T, Hq, D = qa.shape
+        S, Hkv, Dk = ka.shape
+        if Dk != D or va.shape != ka.shape or Hkv < 1 or Hq % Hkv:
+            raise ValueError("oracle: k/v must be [S, Hkv, D] with Hq divisible by Hkv")
+        out = np.empty((T, Hq, D), dtype=np.float64)
+        rc = self.lib.oracle_sdpa(_ptr(qa), _ptr(ka), _ptr(va), qdt, T, S, Hq, Hkv, D,
+                                  float(sm_scale), int(bool(causal)), _ptr(out))
+        if rc:
+            raise RuntimeError("oracle_sdpa failed")
         return out
 
 

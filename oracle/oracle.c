@@ -28,7 +28,9 @@
  *   - a selection is a set of block ids: negative ids, ids >= the page-table
  *     capacity and repeats select nothing more;
  *   - q head g reads kv head g / (Hq / Hkv);
- *   - a query token with no valid key writes zeros.
+ *   - a query token with no valid key writes zeros;
+ *   - dense attention's causal flag aligns the T query tokens with the last
+ *     T of the S keys (query t reads keys j <= t + S - T).
  *
  * Parity pins: every function below is pinned by the "not gpu" tests
  * (brute force with numpy / torch fp64 SDPA, closed forms, invariants,
@@ -325,6 +327,79 @@ int oracle_paged_attention(const void *q, int q_dtype, int64_t T, int64_t Hq, in
     }
     free(selected);
     free(slots);
+    free(z);
+    return 0;
+}
+
+/* --------------------------------------------------- dense GQA attention */
+
+/*
+ * "Kernel ABI" -- attention.sdpa: scaled dot-product attention of T query
+ * tokens over S keys, with GQA expansion (Hq divisible by Hkv; q head g reads
+ * kv head g / (Hq / Hkv)) and a causal flag.
+ *
+ * Causal reading (the page gives the flag, not its alignment): the T query
+ * tokens are the last T positions of the S-key sequence, so query token t may
+ * read key j iff j <= t + (S - T).  For T == S this is the usual
+ * lower-triangular mask; a query token with no readable key (t + S - T < 0)
+ * writes zeros.  Without the flag every query token reads all S keys.
+ *
+ *   z_j  = sm_scale * sum_d q[t][g][d] * k[j][h][d]
+ *   out[t][g][d] = sum_j exp(z_j - max z) * v[j][h][d] / sum_j exp(z_j - max z)
+ *
+ * over the readable keys in ascending j (two passes: the maximum first, then
+ * both sums).  q, k and v share one element type.
+ * Layouts (contiguous): q [T][Hq][D], k/v [S][Hkv][D], out [T][Hq][D].
+ */
+int oracle_sdpa(const void *q, const void *k, const void *v, int dtype,
+                int64_t T, int64_t S, int64_t Hq, int64_t Hkv, int64_t D,
+                double sm_scale, int causal, double *out)
+{
+    int64_t G = Hq / Hkv;
+    double *z = (double *)malloc(sizeof(double) * (size_t)(S > 0 ? S : 1));
+    if (!z)
+        return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        /* number of readable keys: 0 .. n-1 */
+        int64_t n = S;
+        if (causal) {
+            n = t + (S - T) + 1;
+            if (n < 0)
+                n = 0;
+            if (n > S)
+                n = S;
+        }
+        for (int64_t g = 0; g < Hq; ++g) {
+            int64_t kvh = g / G;
+            double *o = out + (t * Hq + g) * D;
+            for (int64_t d = 0; d < D; ++d)
+                o[d] = 0.0;
+            if (n == 0)
+                continue;
+
+            /* pass 1: logits and their maximum */
+            double zmax = -INFINITY;
+            for (int64_t j = 0; j < n; ++j) {
+                double dot = 0.0;
+                for (int64_t d = 0; d < D; ++d)
+                    dot += load(q, dtype, (t * Hq + g) * D + d) * load(k, dtype, (j * Hkv + kvh) * D + d);
+                z[j] = sm_scale * dot;
+                if (z[j] > zmax)
+                    zmax = z[j];
+            }
+
+            /* pass 2: normaliser and weighted sum of values */
+            double l = 0.0;
+            for (int64_t j = 0; j < n; ++j) {
+                double w = exp(z[j] - zmax);
+                l += w;
+                for (int64_t d = 0; d < D; ++d)
+                    o[d] += w * load(v, dtype, (j * Hkv + kvh) * D + d);
+            }
+            for (int64_t d = 0; d < D; ++d)
+                o[d] /= l;
+        }
+    }
     free(z);
     return 0;
 }

@@ -282,3 +282,52 @@ def stress(seed: int = 1005, rows: int = 64, P: int = 8192, K: int = 64,
     return make_decode("cfg5" if rows == 64 else "stress%d" % rows, lengths=lengths,
                        tokens_per_request=n, Hq=64, Hkv=8, D=128, Di=128, NB=128, P=P, K=K,
                        seed=seed, q_dist="student_t3", padded_tail=padded)
+
+
+# ------------------------------------------------------- dense attention
+
+@dataclass
+class DenseAttention:
+    """Inputs of one dense GQA attention call (CPU tensors): T query tokens
+    over S keys that are not paged."""
+
+    name: str
+    T: int
+    S: int
+    Hq: int
+    Hkv: int
+    D: int
+    causal: bool
+    q: torch.Tensor  # [T, Hq, D]
+    k: torch.Tensor  # [S, Hkv, D]
+    v: torch.Tensor  # [S, Hkv, D]
+    sm_scale: float
+
+    def to(self, device) -> "DenseAttention":
+        out = DenseAttention(**{k: getattr(self, k) for k in self.__dataclass_fields__})
+        for name in ("q", "k", "v"):
+            setattr(out, name, getattr(self, name).to(device))
+        return out
+
+
+def make_dense(name: str, *, T: int, S: int, Hq: int, Hkv: int, D: int, causal: bool, seed: int,
+               dtype: torch.dtype = torch.bfloat16, q_dist: str = "normal") -> DenseAttention:
+    """q, k, v drawn N(0, 1) (q optionally Student-t with 3 degrees of
+    freedom), cast to ``dtype``; ``sm_scale = 1/sqrt(D)``."""
+    g = torch.Generator().manual_seed(seed)
+    q = _student_t3((T, Hq, D), g) if q_dist == "student_t3" else torch.randn((T, Hq, D), generator=g)
+    k = torch.randn((S, Hkv, D), generator=g)
+    v = torch.randn((S, Hkv, D), generator=g)
+    return DenseAttention(name=name, T=T, S=S, Hq=Hq, Hkv=Hkv, D=D, causal=causal, q=q.to(dtype),
+                          k=k.to(dtype), v=v.to(dtype), sm_scale=1.0 / math.sqrt(D))
+
+
+DENSE_NAME = ("dense causal GQA prefill chunk (512 query tokens after a 7680-token prefix, S=8192, "
+              "64/8 heads, D=128, bf16)")
+
+
+def dense_prefill(seed: int = 1006) -> DenseAttention:
+    """Dense-attention workload: one 512-token prefill chunk of a sequence
+    whose first 7680 tokens are already cached (the chunk length and head
+    shape of the prefill and decode configurations above)."""
+    return make_dense("dense_prefill", T=512, S=8192, Hq=64, Hkv=8, D=128, causal=True, seed=seed)

@@ -15,7 +15,13 @@ the oracle disagrees with what the pages and the mathematics fix:
     hand-worked fixture and closed forms (uniform logits -> mean of V, one key
     -> that key's value), and the invariants "selecting every block equals
     dense decode", "a one-block context is that block's softmax", "permuting
-    pool pages changes nothing", "a selection is a set".
+    pool pages changes nothing", "a selection is a set";
+  * dense GQA attention against torch's fp64 ``scaled_dot_product_attention``
+    (explicit bottom-right causal mask, and its own ``is_causal`` flag on a
+    square case), a closed form (two keys give tanh(q/2)), uniform logits,
+    one key, and the invariants "a causal row is non-causal attention over
+    its prefix", "GQA equals MHA on repeated kv heads", "key order does not
+    matter without the flag".
 
 ``test_oracle_pins.py`` runs them on the oracle; ``test_oracle_mutants.py``
 runs them on copies of the oracle with planted mistakes and checks that each
@@ -392,6 +398,108 @@ def pin_attention_invariants(o):
     assert np.allclose(d2, 2 * dense, rtol=1e-14, atol=0)
 
 
+# ---------------------------------------------------------- dense attention
+
+def np_causal_mask(T, S):
+    """[T, S] booleans: query t reads key j iff j <= t + S - T (the query
+    tokens are the last T positions of the key sequence)."""
+    t = np.arange(T)[:, None]
+    j = np.arange(S)[None, :]
+    return j <= t + (S - T)
+
+
+def torch_sdpa_f64(q, k, v, sm_scale, causal):
+    """torch's fp64 ``scaled_dot_product_attention`` with the kv heads
+    repeated for GQA and the causal mask given explicitly; rows with no
+    readable key (which torch leaves NaN) are set to zero."""
+    qf, kf, vf = (x.to(torch.float64) for x in (q, k, v))
+    T, Hq, D = qf.shape
+    S, Hkv, _ = kf.shape
+    G = Hq // Hkv
+    qh = qf.permute(1, 0, 2)
+    kh = kf.repeat_interleave(G, dim=1).permute(1, 0, 2)
+    vh = vf.repeat_interleave(G, dim=1).permute(1, 0, 2)
+    mask = torch.from_numpy(np_causal_mask(T, S)) if causal else torch.ones((T, S), dtype=torch.bool)
+    out = torch.nn.functional.scaled_dot_product_attention(qh, kh, vh, attn_mask=mask, scale=sm_scale)
+    out = out.permute(1, 0, 2).numpy().copy()
+    empty = ~mask.numpy().any(axis=1)
+    out[empty] = 0.0
+    return out
+
+
+def pin_sdpa_vs_torch(o):
+    cases = [  # T, S, Hq, Hkv, D, causal, dtype
+        (5, 9, 4, 2, 8, True, torch.float32),
+        (5, 9, 4, 2, 8, False, torch.bfloat16),
+        (7, 7, 6, 3, 5, True, torch.float16),
+        (9, 4, 4, 1, 16, True, torch.bfloat16),  # T > S: the first rows read nothing
+        (1, 13, 8, 8, 4, True, torch.float32),
+        (3, 0, 2, 1, 4, False, torch.float32),  # no keys at all
+    ]
+    for i, (T, S, Hq, Hkv, D, causal, dt) in enumerate(cases):
+        w = W.make_dense("pin", T=T, S=S, Hq=Hq, Hkv=Hkv, D=D, causal=causal, seed=60 + i, dtype=dt,
+                         q_dist="student_t3" if i % 2 else "normal")
+        got = o.sdpa(w.q, w.k, w.v, w.sm_scale, causal)
+        ref = torch_sdpa_f64(w.q, w.k, w.v, w.sm_scale, causal)
+        assert_close(got, ref, rtol=1e-11, atol=1e-12, what="sdpa case %d" % i)
+    # square causal case against torch's own causal flag (no explicit mask)
+    w = W.make_dense("pin", T=6, S=6, Hq=4, Hkv=2, D=8, causal=True, seed=70, dtype=torch.float32)
+    qf, kf, vf = (x.to(torch.float64) for x in (w.q, w.k, w.v))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        qf.permute(1, 0, 2), kf.repeat_interleave(2, dim=1).permute(1, 0, 2),
+        vf.repeat_interleave(2, dim=1).permute(1, 0, 2), is_causal=True, scale=w.sm_scale)
+    got = o.sdpa(w.q, w.k, w.v, w.sm_scale, True)
+    assert_close(got, ref.permute(1, 0, 2).numpy(), rtol=1e-11, atol=1e-12, what="sdpa is_causal")
+
+
+def pin_sdpa_closed_forms(o):
+    # two keys, one dim: weights e^{q} and 1, values +1 and -1, so the row
+    # that reads both keys is tanh(q / 2); the causal first row reads key 0
+    qv = float(np.float32(math.log(3.0)))
+    q = torch.tensor([[[qv]], [[qv]]], dtype=torch.float32)
+    k = torch.tensor([[[1.0]], [[0.0]]], dtype=torch.float32)
+    v = torch.tensor([[[1.0]], [[-1.0]]], dtype=torch.float32)
+    full = o.sdpa(q, k, v, 1.0, False)
+    assert np.allclose(full[:, 0, 0], math.tanh(qv / 2), rtol=1e-14, atol=1e-15), full
+    causal = o.sdpa(q, k, v, 1.0, True)
+    assert causal[0, 0, 0] == 1.0 and abs(causal[1, 0, 0] - math.tanh(qv / 2)) < 1e-15, causal
+    # q = 0: every row is the mean of the values it may read
+    w = W.make_dense("pin", T=5, S=8, Hq=4, Hkv=2, D=6, causal=True, seed=71, dtype=torch.float32)
+    got = o.sdpa(torch.zeros_like(w.q), w.k, w.v, w.sm_scale, True)
+    vf = w.v.to(torch.float64).numpy()
+    for t in range(5):
+        n = t + 8 - 5 + 1
+        for g in range(4):
+            assert np.allclose(got[t, g], vf[:n, g // 2].mean(axis=0), rtol=1e-13, atol=1e-14), (t, g)
+    # one key: the output is that key's value, exactly
+    got1 = o.sdpa(w.q, w.k[:1], w.v[:1], w.sm_scale, False)
+    for g in range(4):
+        assert np.array_equal(got1[:, g], np.broadcast_to(vf[0, g // 2], (5, 6))), g
+
+
+def pin_sdpa_invariants(o):
+    w = W.make_dense("pin", T=4, S=11, Hq=6, Hkv=2, D=7, causal=True, seed=72, dtype=torch.bfloat16)
+    causal = o.sdpa(w.q, w.k, w.v, w.sm_scale, True)
+    full = o.sdpa(w.q, w.k, w.v, w.sm_scale, False)
+    # causal row t equals non-causal attention over the keys it may read
+    for t in range(4):
+        n = t + 11 - 4 + 1
+        pre = o.sdpa(w.q[t:t + 1], w.k[:n], w.v[:n], w.sm_scale, False)
+        assert np.array_equal(causal[t], pre[0]), t
+    # the last row reads every key under either flag
+    assert np.array_equal(causal[3], full[3])
+    # GQA equals multi-head attention on kv heads repeated explicitly
+    mha = o.sdpa(w.q, w.k.repeat_interleave(3, dim=1), w.v.repeat_interleave(3, dim=1), w.sm_scale, True)
+    assert np.array_equal(mha, causal)
+    # without the flag, permuting the keys (values with them) changes only rounding
+    perm = torch.randperm(11, generator=torch.Generator().manual_seed(5))
+    fp = o.sdpa(w.q, w.k[perm], w.v[perm], w.sm_scale, False)
+    assert_close(fp, full, rtol=1e-12, atol=1e-13, what="key permutation")
+    # scaling V scales the output
+    f2 = o.sdpa(w.q, w.k, (w.v.float() * 2).to(w.v.dtype), w.sm_scale, False)
+    assert np.allclose(f2, 2 * full, rtol=1e-14, atol=0)
+
+
 PINS = [
     pin_e4m3_decoder,
     pin_bf16_decoder,
@@ -405,4 +513,7 @@ PINS = [
     pin_attention_golden,
     pin_attention_closed_forms,
     pin_attention_invariants,
+    pin_sdpa_vs_torch,
+    pin_sdpa_closed_forms,
+    pin_sdpa_invariants,
 ]

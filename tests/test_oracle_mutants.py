@@ -33,6 +33,12 @@ MUTATIONS = [
     ("clip to one block short", "L = NB * bs;", "L = (NB - 1) * bs;"),
     ("dense skips last block", "for (int64_t b = 0; b < NB && L > 0; ++b) {", "for (int64_t b = 0; b + 1 < NB && L > 0; ++b) {"),
     ("no max subtraction guard on empty", "if (n == 0) {", "if (n < 0) {"),
+    ("sdpa causal off by one", "n = t + (S - T) + 1;", "n = t + (S - T);"),
+    ("sdpa causal aligned top-left", "n = t + (S - T) + 1;", "n = t + 1;"),
+    ("sdpa gqa index", "int64_t kvh = g / G;", "int64_t kvh = g % Hkv;"),
+    ("sdpa drops sm_scale", "z[j] = sm_scale * dot;", "z[j] = dot;"),
+    ("sdpa ignores the causal flag", "if (causal) {", "if (0) {"),
+    ("sdpa drops the first value", "o[d] += w * load(v, dtype,", "o[d] += (j > 0) * w * load(v, dtype,"),
 ]
 
 

@@ -18,7 +18,12 @@ before the step rather than during it (both outside the events); W warm-up
 steps first.  Under torchrun each rank runs its own batch
 (different seed) with no data exchange: weak scaling, max time over ranks.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
+With --config dense the step is instead one dense GQA attention call
+(attention_sdpa) on a causal prefill chunk: 512 query tokens after 7680 cached
+tokens, 64 q / 8 kv heads, head dim 128, bf16; its roofline is the call's
+algorithmic FLOPs against the dense bf16 tensor peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C|dense] [--impl reference]
 """
 from __future__ import annotations
 
@@ -43,6 +48,7 @@ from sparse_paged_decode_gb300 import workloads as W  # noqa: E402
 
 METRIC = "decode query-rows/sec and achieved HBM GB/s vs ~8 TB/s (sparse paged decode)"
 UNIT = "query-rows/s"
+DENSE_METRIC = "dense GQA attention query-rows/sec (prefill chunk)"
 BS = 128
 FLUSH_BYTES = 256 << 20
 
@@ -503,6 +509,172 @@ def run_gpu(args, rank, world, local_rank):
     }
 
 
+# ------------------------------------------------- dense attention workload
+
+def dense_flops(w):
+    """Algorithmic FLOPs of one dense attention call: 2 D for the logit and
+    2 D for the weighted value, per (query row, readable key) pair."""
+    n_keys = 0
+    for t in range(w.T):
+        n = t + w.S - w.T + 1 if w.causal else w.S
+        n_keys += max(0, min(w.S, n))
+    return 4 * w.D * w.Hq * n_keys
+
+
+def dense_oracle_rate(w, budget_s=12.0, max_tokens=None):
+    """The oracle on query tokens of the dense workload, one at a time (token
+    t under the causal flag is non-causal attention over its first
+    t + S - T + 1 keys); returns (query tokens/s, tokens timed, seconds)."""
+    import oracle
+
+    o = oracle.default()
+    done, t0 = 0, time.perf_counter()
+    for t in range(w.T - 1, -1, -1):  # the longest rows first: a conservative rate
+        n = t + w.S - w.T + 1 if w.causal else w.S
+        o.sdpa(w.q[t:t + 1], w.k[:max(0, n)], w.v[:max(0, n)], float(np.float32(w.sm_scale)), False)
+        done += 1
+        if time.perf_counter() - t0 >= budget_s or (max_tokens and done >= max_tokens):
+            break
+    dt = time.perf_counter() - t0
+    return done / dt, done, dt
+
+
+def dense_desc(w):
+    return {"workload": W.DENSE_NAME, "query_tokens": w.T, "keys": w.S, "Hq": w.Hq, "Hkv": w.Hkv,
+            "head_dim": w.D, "causal": w.causal, "q_dtype": str(w.q.dtype)[6:], "kv_dtype": str(w.k.dtype)[6:],
+            "out_dtype": "bfloat16",
+            "l2": "flushed between timed steps (256 MiB rewrite, then a 256 MiB read that cleans the dirty "
+                  "lines; outside the events)"}
+
+
+def run_dense_reference(args, rank, world):
+    if rank != 0:
+        return None
+    w = W.dense_prefill()
+    per_step_budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        dense_oracle_rate(w, budget_s=per_step_budget / 4, max_tokens=1)
+    rows, secs = 0, 0.0
+    for _ in range(args.steps):
+        _, n, dt = dense_oracle_rate(w, budget_s=per_step_budget)
+        rows += n
+        secs += dt
+    value = rows / secs
+    return {
+        "impl": "reference", "metric": DENSE_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dense_desc(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "%d query tokens (all heads) of the chunk through the oracle (single-threaded "
+                                   "C, fp64), %.1f s per step" % (rows, per_step_budget)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def run_dense_gpu(args, rank, world, local_rank):
+    import sparse_paged_decode_gb300 as spd
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = W.dense_prefill(seed=1006 + 97 * rank)
+    g = w.to(dev)
+    out = torch.empty((w.T, w.Hq, w.D), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    clean = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    clean_sum = torch.empty((), dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def flush_l2(i):
+        flush.fill_(i & 0xFF)
+        torch.sum(clean, 0, dtype=torch.int64, out=clean_sum)
+
+    def step():
+        spd.attention_sdpa(g.q, g.k, g.v, out, w.sm_scale, w.causal)
+
+    for i in range(args.warmup):
+        flush_l2(i)
+        step()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.25)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    n0 = spd.launch_count()
+    for i in range(args.steps):
+        flush_l2(i)
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    launches = spd.launch_count() - n0
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+
+    # end to end: the chunk's queries and its own 512 keys and values (the
+    # prefix's stay resident, as in a KV cache) copied in from pinned host
+    # memory, the output copied back
+    new = slice(w.S - w.T, w.S)
+    host_q = w.q.contiguous().pin_memory()
+    host_k = w.k[new].contiguous().pin_memory()
+    host_v = w.v[new].contiguous().pin_memory()
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (host_q, host_k, host_v))
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush_l2(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.q.copy_(host_q, non_blocking=True)
+        g.k[new].copy_(host_k, non_blocking=True)
+        g.v[new].copy_(host_v, non_blocking=True)
+        step()
+        host_out.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if i >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    clocks = sampler.stop() if sampler else None
+
+    total_ms, e2e_total = max_over_ranks([sum(step_ms), sum(e2e_ms)], world, dev)
+    if rank != 0:
+        return None
+    value = job_rate(w.T, world, args.steps, total_ms)
+    e2e_value = job_rate(w.T, world, args.steps, e2e_total)
+    flops = dense_flops(w)
+    mean_s = statistics.mean(step_ms) / 1e3
+    achieved = flops / mean_s / 1e12
+    peak, peak_src = measured_bf16_peak()
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        rate, n, dt = dense_oracle_rate(w, budget_s=args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": "%d query tokens (all heads; the longest rows) of the chunk through the oracle "
+                         "(single-threaded C, fp64), %.1f s" % (n, dt)}
+    return {
+        "metric": DENSE_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32 (CUDA-core FMA; bf16 inputs and output)",
+        "data": "synthetic", "config": dense_desc(w),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None, "kernel": "sdpa_kernel (direct launch)",
+                     "algorithmic_flops_per_launch": flops, "mean_launch_us": mean_s * 1e6,
+                     "peak_source": peak_src},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "timed_as": "direct launches per step",
+        "clocks": clocks,
+        "step_ms_median": statistics.median(step_ms),
+    }
+
+
 def _kernel_stamp():
     try:
         from sparse_paged_decode_gb300 import build as b
@@ -517,8 +689,10 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5],
-                    help="workload (2 = EAGLE-style verification decode, the metric's workload)")
+    ap.add_argument("--config", type=lambda c: c if c == "dense" else int(c), default=2,
+                    choices=[2, 3, 4, 5, "dense"],
+                    help="workload (2 = EAGLE-style verification decode, the metric's workload; "
+                         "dense = the dense-attention prefill chunk)")
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -532,16 +706,17 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    dense = args.config == "dense"
     if args.impl == "reference":
         # the oracle arm runs on rank 0 only; other ranks exit without work
-        res = run_reference(args, rank, world)
+        res = (run_dense_reference if dense else run_reference)(args, rank, world)
         if res is not None:
             print(json.dumps(res), flush=True)
         return
     if world > 1:
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group(backend="nccl")
-    res = run_gpu(args, rank, world, local_rank)
+    res = (run_dense_gpu if dense else run_gpu)(args, rank, world, local_rank)
     if res is not None:
         print(json.dumps(res), flush=True)
     if world > 1:

@@ -6,6 +6,8 @@
  *   2. msa_select_topk                top-k block ids per query row
  *   3. paged_sparse_decode_attention  paged GQA attention over the selected blocks
  *      paged_decode_attention         the same over every block (dense decode)
+ * and, beside them, attention_sdpa: dense (not paged) GQA attention with a
+ * causal flag, the prefill-side attention slot of the same boundary.
  *
  * Contract shared by every entry point ("Kernel ABI" -- Core rules; "Slot
  * contract" -- 1. The validator owns the boundary):
@@ -187,6 +189,32 @@ SPD_API void paged_decode_attention(const spd_tensor *q, const spd_tensor *k_cac
                             const spd_tensor *out, float sm_scale, int32_t block_size,
                             float k_scale, float v_scale, void *workspace,
                             size_t workspace_bytes, spd_stream_t stream);
+
+/*
+ * Dense GQA attention with a causal flag.
+ * "Kernel ABI" -- attention.sdpa ("attention(q, k, v, out, sm_scale, causal)":
+ * scaled dot-product attention with GQA/MQA expansion; Hq divisible by Hkv).
+ *
+ *   z_j = sm_scale * (q[t][g] . k[j][h]),  h = g / (Hq / Hkv)
+ *   out[t][g] = sum_j softmax(z)_j * v[j][h]
+ * over the keys j that query token t may read: all S keys, or, when causal
+ * is nonzero, the keys j <= t + S - T (the T query tokens are the last T
+ * positions of the key sequence -- a prefill chunk after S - T cached
+ * tokens; for T == S the usual lower-triangular mask).  A query token that
+ * may read no key (causal with t < T - S, or S == 0) writes zeros.  The page
+ * fixes the flag, not its alignment; this bottom-right alignment is the
+ * reading taken here.
+ *
+ * q    [T, Hq, D]   f32 | bf16 | f16, any strides
+ * k, v [S, Hkv, D]  the dtype of q, any strides (keys are not paged)
+ * out  OUT [T, Hq, D] f32 | bf16 | f16 (rounded to nearest even)
+ * sm_scale finite fp32 scalar
+ * Logits, softmax and accumulation are fp32.  No workspace.
+ * Domain: D in [1, 256], Hq a positive multiple of Hkv, Hkv <= 65535,
+ * T * Hq and S below 2^30.
+ */
+SPD_API void attention_sdpa(const spd_tensor *q, const spd_tensor *k, const spd_tensor *v, const spd_tensor *out,
+                            float sm_scale, int32_t causal, spd_stream_t stream);
 
 /*
  * paged_sparse_decode_attention without a caller-provided workspace.

@@ -7,6 +7,7 @@ CUDA kernel:
   msa_select_topk                 top-k block ids per query row
   paged_sparse_decode_attention   paged GQA attention over the selected blocks
   paged_decode_attention          the same over every block (dense decode)
+  attention_sdpa                  dense (not paged) GQA attention, causal flag
 
 The Python functions of the same names (in :mod:`.binding`) only marshal
 torch tensors into the C ABI; every step runs in the CUDA library.  They
@@ -21,6 +22,7 @@ __all__ = [
     "paged_sparse_decode_attention",
     "paged_decode_attention",
     "paged_sparse_decode_attention_noalloc",
+    "attention_sdpa",
     "decode_workspace_bytes",
     "launch_count",
     "set_attention_kernel",

@@ -24,6 +24,7 @@ __all__ = [
     "paged_sparse_decode_attention",
     "paged_decode_attention",
     "paged_sparse_decode_attention_noalloc",
+    "attention_sdpa",
     "decode_workspace_bytes",
     "launch_count",
     "set_attention_kernel",
@@ -83,6 +84,8 @@ def _load():
     L.paged_sparse_decode_attention_noalloc.restype = None
     L.paged_decode_attention.argtypes = [P, P, P, P, P, P, P, f32, i32, f32, f32, vp, sz, vp]
     L.paged_decode_attention.restype = None
+    L.attention_sdpa.argtypes = [P, P, P, P, f32, i32, vp]
+    L.attention_sdpa.restype = None
     L.spd_decode_workspace_bytes.argtypes = [ctypes.c_int64] * 5 + [i32]
     L.spd_decode_workspace_bytes.restype = sz
     L.spd_last_error.argtypes = [ctypes.c_char_p, sz]
@@ -188,6 +191,14 @@ def paged_decode_attention(q, k_cache, v_cache, block_table, seq_lens, req_idx, 
         _desc(q, "q"), _desc(k_cache, "k_cache"), _desc(v_cache, "v_cache"), _desc(block_table, "block_table"),
         _desc(seq_lens, "seq_lens"), _desc(req_idx, "req_idx"), _desc(out, "out"), float(sm_scale),
         int(block_size), float(k_scale), float(v_scale), ws_ptr, ws_bytes, _stream(stream))
+    _check()
+
+
+def attention_sdpa(q, k, v, out, sm_scale, causal, stream=None) -> None:
+    """Dense GQA attention: fill ``out`` [T, Hq, D] from q [T, Hq, D] and
+    k, v [S, Hkv, D]; with ``causal`` query t reads keys j <= t + S - T."""
+    lib.attention_sdpa(_desc(q, "q"), _desc(k, "k"), _desc(v, "v"), _desc(out, "out"), float(sm_scale),
+                       1 if causal else 0, _stream(stream))
     _check()
 
 

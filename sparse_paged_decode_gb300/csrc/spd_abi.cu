@@ -14,6 +14,7 @@
 #include <initializer_list>
 #include <mutex>
 
+#include "sdpa.cuh"
 #include "spd_internal.cuh"
 #include "spd_dispatch.h"
 
@@ -294,6 +295,47 @@ bool attention(const spd_tensor *q, const spd_tensor *k, const spd_tensor *v, co
     return check_cuda(dispatch_attention(a, ws, ws_bytes, stream), entry);
 }
 
+// ------------------------------------------------------- dense attention
+
+bool sdpa(const spd_tensor *q, const spd_tensor *k, const spd_tensor *v, const spd_tensor *out, float sm_scale,
+          int32_t causal, cudaStream_t stream) {
+    if (!check_desc(q, "q", 3, {SPD_F32, SPD_BF16, SPD_F16})) return false;
+    if (!check_desc(k, "k", 3, {SPD_F32, SPD_BF16, SPD_F16})) return false;
+    if (!check_desc(v, "v", 3, {SPD_F32, SPD_BF16, SPD_F16})) return false;
+    if (!check_desc(out, "out", 3, {SPD_F32, SPD_BF16, SPD_F16})) return false;
+    if (k->dtype != q->dtype || v->dtype != q->dtype)
+        return fail(SPD_ERR_UNSUPPORTED, "k and v must have the dtype of q");
+    const int64_t T = q->shape[0], Hq = q->shape[1], D = q->shape[2];
+    const int64_t S = k->shape[0], Hkv = k->shape[1];
+    for (int i = 0; i < 3; ++i)
+        if (v->shape[i] != k->shape[i]) return fail(SPD_ERR_INVALID_ARGUMENT, "v shape != k shape");
+    if (k->shape[2] != D) return fail(SPD_ERR_INVALID_ARGUMENT, "k head dim != q head dim");
+    if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
+        return fail(SPD_ERR_UNSUPPORTED, "Hq=%lld must be a positive multiple of Hkv=%lld", (long long)Hq,
+                    (long long)Hkv);
+    if (D < 1 || D > kMaxD) return fail(SPD_ERR_UNSUPPORTED, "D=%lld outside [1, %d]", (long long)D, kMaxD);
+    if (Hkv > 65535 || S > INT32_MAX / 2 || T > INT32_MAX / 2 || T * Hq > INT32_MAX / 2)
+        return fail(SPD_ERR_UNSUPPORTED, "too many heads, keys or query rows");
+    if (out->shape[0] != T || out->shape[1] != Hq || out->shape[2] != D)
+        return fail(SPD_ERR_INVALID_ARGUMENT, "out must be [T, Hq, D] like q");
+    if (!check_scalar(sm_scale, "sm_scale")) return false;
+    if (!check_output_layout(out, "out")) return false;
+    if (!check_no_overlap(out, "out", {q, k, v})) return false;
+    if (T == 0) return true;
+
+    SdpaArgs a{};
+    a.q = q->data; a.q_s0 = q->stride[0]; a.q_s1 = q->stride[1]; a.q_s2 = q->stride[2];
+    a.k = k->data; a.k_s0 = k->stride[0]; a.k_s1 = k->stride[1]; a.k_s2 = k->stride[2];
+    a.v = v->data; a.v_s0 = v->stride[0]; a.v_s1 = v->stride[1]; a.v_s2 = v->stride[2];
+    a.out = out->data; a.o_s0 = out->stride[0]; a.o_s1 = out->stride[1]; a.o_s2 = out->stride[2];
+    a.in_dt = q->dtype; a.out_dt = out->dtype;
+    a.T = (int32_t)T; a.S = (int32_t)S; a.Hq = (int32_t)Hq; a.Hkv = (int32_t)Hkv; a.D = (int32_t)D;
+    a.causal = causal != 0;
+    a.sm_scale = sm_scale;
+    count_launches(1);
+    return check_cuda(launch_sdpa(a, stream), "attention_sdpa launch");
+}
+
 }  // namespace
 }  // namespace spd
 
@@ -407,6 +449,12 @@ void paged_decode_attention(const spd_tensor *q, const spd_tensor *k_cache, cons
     spd::attention(q, k_cache, v_cache, block_table, seq_lens, req_idx, nullptr, out, sm_scale, block_size,
                    k_scale, v_scale, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream),
                    "paged_decode_attention");
+}
+
+void attention_sdpa(const spd_tensor *q, const spd_tensor *k, const spd_tensor *v, const spd_tensor *out,
+                    float sm_scale, int32_t causal, spd_stream_t stream) {
+    spd::set_ok();
+    spd::sdpa(q, k, v, out, sm_scale, causal, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t spd_decode_workspace_bytes(int64_t T, int64_t Hq, int64_t Hkv, int64_t D, int64_t NB, int32_t block_size) {

@@ -122,6 +122,36 @@ def test_attention_rejections(spd):
     assert attn_call(spd, out=Fake((4, 8, 32), BF16))[0] == SPD_ERR_INVALID_ARGUMENT
 
 
+def sdpa_call(spd, T=5, S=9, Hq=8, Hkv=2, D=64, dtype=BF16, kv_dtype=None, out=None, sm_scale=0.125,
+              causal=1, v_shape=None):
+    q = Fake((T, Hq, D), dtype)
+    k = Fake((S, Hkv, D), kv_dtype if kv_dtype is not None else dtype)
+    v = Fake(v_shape or (S, Hkv, D), kv_dtype if kv_dtype is not None else dtype)
+    o = out or Fake((T, Hq, D), BF16)
+    spd.lib.attention_sdpa(q.ref(), k.ref(), v.ref(), o.ref(), sm_scale, causal, None)
+    return status(spd)
+
+
+def test_sdpa_validation(spd):
+    for dt in (F32, BF16, F16):
+        code, msg = sdpa_call(spd, dtype=dt)
+        assert code in (SPD_OK, SPD_ERR_CUDA), msg
+    assert sdpa_call(spd, T=0)[0] == SPD_OK  # nothing to write, nothing launched
+    assert sdpa_call(spd, Hq=6, Hkv=4)[0] == SPD_ERR_UNSUPPORTED  # not divisible
+    assert sdpa_call(spd, D=300)[0] == SPD_ERR_UNSUPPORTED
+    assert sdpa_call(spd, dtype=E4M3)[0] == SPD_ERR_UNSUPPORTED
+    assert sdpa_call(spd, kv_dtype=F16)[0] == SPD_ERR_UNSUPPORTED  # k/v dtype != q dtype
+    assert sdpa_call(spd, v_shape=(8, 2, 64))[0] == SPD_ERR_INVALID_ARGUMENT
+    assert sdpa_call(spd, sm_scale=float("inf"))[0] == SPD_ERR_INVALID_ARGUMENT
+    assert sdpa_call(spd, out=Fake((5, 8, 32), BF16))[0] == SPD_ERR_INVALID_ARGUMENT
+    assert sdpa_call(spd, out=Fake((5, 8, 64), BF16, strides=(64, 8, 1)))[0] == SPD_ERR_ALIASING
+    q = Fake((5, 8, 64), BF16)
+    k = Fake((9, 2, 64), BF16)
+    v = Fake((9, 2, 64), BF16)
+    spd.lib.attention_sdpa(q.ref(), k.ref(), v.ref(), Fake((5, 8, 64), BF16, addr=q.d.data).ref(), 0.1, 0, None)
+    assert status(spd)[0] == SPD_ERR_ALIASING
+
+
 def test_output_overlapping_input_rejected(spd):
     q = Fake((2, 1, 32), BF16)
     k = Fake((128, 1, 32), BF16)

@@ -2,7 +2,7 @@
 CPU oracle, through the C ABI.
 
 Outputs are NaN-poisoned before each call and the inputs hashed before and
-after.  Small cases compare every cell; they span several 32-row CTAs and
+after.  Small cases compare every cell; they span several 64-row CTAs and
 64-key tiles with ragged tails, every head-dim specialisation (D up to 32,
 64, 128, 256, and a D that is none of these), group sizes 1 to 16, all input
 and output dtypes, arbitrary strides, and the degenerate cases (no keys,

@@ -104,6 +104,9 @@ class Oracle:
         L.oracle_paged_attention.restype = c_int
         L.oracle_sdpa.argtypes = [vp, vp, vp, c_int, i64, i64, i64, i64, i64, dbl, c_int, vp]
         L.oracle_sdpa.restype = c_int
+        L.oracle_prefill_topk.argtypes = [vp, c_int, i64, i64, i64, vp, c_int, i64, vp, i64, i64,
+                                          vp, vp, vp, vp, vp, i64, i64, i64, i64, dbl, i64, i64, i64, vp, vp]
+        L.oracle_prefill_topk.restype = c_int
 
     # -- decoders ----------------------------------------------------------
     def e4m3_value(self, code: int) -> float:
@@ -208,6 +211,33 @@ class Oracle:
         if rc:
             raise RuntimeError("oracle_sdpa failed")
         return out
+
+    # -- prefill score-to-selection ------------------------------------------
+    def prefill_topk(self, q_idx, k_idx_cache, block_table, slot_ids, cu_seqlens, seq_lens, prefix_lens,
+                     cu_seqblocks_q, block_size_q: int, init_blocks: int, local_blocks: int, scale: float,
+                     n_rows: int, topk: int, block_size: int = 128):
+        """(topk ids [Hi, n_rows, topk] int32, block scores [Hi, n_rows, NB]
+        fp64); see oracle_prefill_topk in oracle.c."""
+        q, qdt = _raw(q_idx, "float")
+        k, kdt = _raw(k_idx_cache, "float")
+        bt, _ = _raw(block_table, "int")
+        arrs = [_raw(x, "int")[0] for x in (slot_ids, cu_seqlens, seq_lens, prefix_lens, cu_seqblocks_q)]
+        T, Hi, Di = q.shape
+        if k.ndim != 3 or k.shape[1] != 1 or k.shape[2] != Di:
+            raise ValueError("oracle: index cache must be [slots, 1, Di]")
+        R, NB = bt.shape
+        B = arrs[0].shape[0]
+        if arrs[1].shape[0] != B + 1 or arrs[4].shape[0] != B + 1:
+            raise ValueError("oracle: cu_seqlens and cu_seqblocks_q need B + 1 entries")
+        out = np.empty((Hi, n_rows, topk), dtype=np.int32)
+        sc = np.empty((Hi, n_rows, NB), dtype=np.float64)
+        rc = self.lib.oracle_prefill_topk(_ptr(q), qdt, T, Hi, Di, _ptr(k), kdt, k.shape[0], _ptr(bt), R, NB,
+                                          *[_ptr(a) for a in arrs], B, int(block_size_q), int(init_blocks),
+                                          int(local_blocks), float(scale), int(block_size), int(n_rows),
+                                          int(topk), _ptr(out), _ptr(sc))
+        if rc:
+            raise RuntimeError("oracle_prefill_topk failed")
+        return out, sc
 
 
 _default: Optional[Oracle] = None

@@ -403,3 +403,140 @@ int oracle_sdpa(const void *q, const void *k, const void *v, int dtype,
     free(z);
     return 0;
 }
+
+/* ------------------------------------ prefill score-to-selection (V2) */
+
+/*
+ * "Kernel ABI" -- attention.msa_prefill_block_score: one call that scores and
+ * selects for a ragged batch of prefill chunks over a paged index cache, per
+ * query head and per query block of block_size_q tokens.
+ *
+ * Sequence b owns query tokens cu_seqlens[b] .. cu_seqlens[b+1]-1 (its chunk,
+ * whose first token sits at position prefix_lens[b]), seq_lens[b] keys in
+ * total, and output rows cu_seqblocks_q[b] + qb for its query blocks qb.
+ * Its keys are read through row slot_ids[b] of the page table.
+ *
+ * Readings (the page states the rule, not the formulas):
+ *   - visibility: query block qb sees the keys at positions up to and
+ *     including prefix_lens[b] + qb * block_size_q (its first token's own
+ *     position), so L = prefix_lens[b] + qb * block_size_q + 1 keys, clipped
+ *     to seq_lens[b] and to the page table; key block kb is visible iff
+ *     kb * block_size < L (nvis = ceil(L / block_size) blocks);
+ *   - score: the block-max of the decode score sheet taken over the query
+ *     block as well: max over the block's tokens t and the keys tau < L of
+ *     key block kb of (q[t][h] . k[slot(tau)]) * scale; -inf if none;
+ *   - policy: the first init_blocks and the last local_blocks visible blocks
+ *     are always selected and come first, in ascending id; the remaining
+ *     cells are filled with the other visible candidate blocks (score neither
+ *     NaN nor -inf) in descending score, ties to the lower id; then -1.
+ *     Ids are logical block ids of the request's key sequence.
+ * Rows that no sequence owns are all -1.  With block_size_q = 1 and no
+ * init/local blocks a row is exactly the decode top-k of one query token
+ * whose seq_len is its position + 1.
+ *
+ * Layouts (contiguous): q [total_q][Hi][Di], k [n_slots][1][Di],
+ * block_table [R][NB], slot_ids/seq_lens/prefix_lens [B],
+ * cu_seqlens/cu_seqblocks_q [B+1], out [Hi][n_rows][topk];
+ * scores (optional) [Hi][n_rows][NB] receives the block scores (-inf for
+ * blocks that are not visible).
+ */
+int oracle_prefill_topk(const void *q, int q_dtype, int64_t total_q, int64_t Hi, int64_t Di,
+                        const void *k, int k_dtype, int64_t n_slots,
+                        const int32_t *block_table, int64_t R, int64_t NB,
+                        const int32_t *slot_ids, const int32_t *cu_seqlens, const int32_t *seq_lens,
+                        const int32_t *prefix_lens, const int32_t *cu_seqblocks_q, int64_t B,
+                        int64_t block_size_q, int64_t init_blocks, int64_t local_blocks,
+                        double scale, int64_t block_size, int64_t n_rows, int64_t topk,
+                        int32_t *out, double *scores)
+{
+    int64_t n_pages = n_slots / block_size;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(NB > 0 ? NB : 1));
+    char *forced = (char *)malloc((size_t)(NB > 0 ? NB : 1));
+    cell_t *cells = (cell_t *)malloc(sizeof(cell_t) * (size_t)(NB > 0 ? NB : 1));
+    if (!s || !forced || !cells) {
+        free(s); free(forced); free(cells);
+        return -1;
+    }
+    for (int64_t i = 0; i < Hi * n_rows * topk; ++i)
+        out[i] = -1;
+    if (scores)
+        for (int64_t i = 0; i < Hi * n_rows * NB; ++i)
+            scores[i] = -INFINITY;
+
+    for (int64_t b = 0; b < B; ++b) {
+        int64_t r = slot_ids[b];
+        for (int64_t qb = 0; qb < (int64_t)cu_seqblocks_q[b + 1] - cu_seqblocks_q[b]; ++qb) {
+            int64_t row = cu_seqblocks_q[b] + qb;
+            if (row < 0 || row >= n_rows)
+                continue;
+
+            /* visible keys and blocks */
+            int64_t L = (int64_t)prefix_lens[b] + qb * block_size_q + 1;
+            if (L > seq_lens[b])
+                L = seq_lens[b];
+            if (L > NB * block_size)
+                L = NB * block_size;
+            if (r < 0 || r >= R || L < 0)
+                L = 0;
+            int64_t nvis = (L + block_size - 1) / block_size;
+
+            /* the query block's tokens */
+            int64_t t0 = (int64_t)cu_seqlens[b] + qb * block_size_q;
+            int64_t t1 = t0 + block_size_q;
+            if (t1 > cu_seqlens[b + 1])
+                t1 = cu_seqlens[b + 1];
+            if (t0 < 0)
+                t0 = 0;
+            if (t1 > total_q)
+                t1 = total_q;
+
+            for (int64_t h = 0; h < Hi; ++h) {
+                /* block scores */
+                for (int64_t kb = 0; kb < NB; ++kb) {
+                    double best = -INFINITY;
+                    int64_t page = kb < nvis ? page_of(block_table, NB, r, kb, n_pages) : -1;
+                    for (int64_t t = t0; t < t1 && page >= 0; ++t) {
+                        for (int64_t tau = kb * block_size; tau < (kb + 1) * block_size && tau < L; ++tau) {
+                            int64_t slot = page * block_size + (tau - kb * block_size);
+                            double dot = 0.0;
+                            for (int64_t d = 0; d < Di; ++d)
+                                dot += load(q, q_dtype, (t * Hi + h) * Di + d) * load(k, k_dtype, slot * Di + d);
+                            double v = dot * scale;
+                            if (v > best)
+                                best = v;
+                        }
+                    }
+                    s[kb] = best;
+                    if (scores)
+                        scores[(h * n_rows + row) * NB + kb] = best;
+                }
+
+                /* policy blocks first, ascending id */
+                int32_t *o = out + (h * n_rows + row) * topk;
+                int64_t n = 0;
+                for (int64_t kb = 0; kb < NB; ++kb) {
+                    forced[kb] = kb < nvis && (kb < init_blocks || kb >= nvis - local_blocks);
+                    if (forced[kb] && n < topk)
+                        o[n++] = (int32_t)kb;
+                }
+
+                /* then the best of the other visible candidates */
+                int64_t m = 0;
+                for (int64_t kb = 0; kb < nvis; ++kb) {
+                    if (forced[kb] || isnan(s[kb]) || s[kb] == -INFINITY)
+                        continue;
+                    cells[m].score = s[kb];
+                    cells[m].block = (int32_t)kb;
+                    ++m;
+                }
+                qsort(cells, (size_t)m, sizeof(cell_t), cell_order);
+                for (int64_t j = 0; j < m && n < topk; ++j)
+                    o[n++] = cells[j].block;
+            }
+        }
+    }
+    free(s);
+    free(forced);
+    free(cells);
+    return 0;
+}

@@ -331,3 +331,90 @@ def dense_prefill(seed: int = 1006) -> DenseAttention:
     whose first 7680 tokens are already cached (the chunk length and head
     shape of the prefill and decode configurations above)."""
     return make_dense("dense_prefill", T=512, S=8192, Hq=64, Hkv=8, D=128, causal=True, seed=seed)
+
+
+# ------------------------------------------- prefill score-to-selection (V2)
+
+@dataclass
+class PrefillBatch:
+    """Inputs of one fused prefill score-to-selection call (CPU tensors):
+    a ragged batch of query chunks over a paged index cache."""
+
+    name: str
+    B: int
+    Hi: int
+    Di: int
+    NB: int
+    P: int
+    topk: int
+    block_size_q: int
+    init_blocks: int
+    local_blocks: int
+    scale: float
+    n_rows: int  # query blocks over the batch (all_seqblock_q)
+    q_idx: torch.Tensor  # [total_q, Hi, Di]
+    k_idx_cache: torch.Tensor  # [P*BS, 1, Di]
+    block_table: torch.Tensor  # int32 [R, NB] (R >= B; rows in shuffled order)
+    slot_ids: torch.Tensor  # int32 [B]: page-table row of each sequence
+    cu_seqlens: torch.Tensor  # int32 [B+1]: query token offsets
+    seq_lens: torch.Tensor  # int32 [B]: keys of each sequence, chunk included
+    prefix_lens: torch.Tensor  # int32 [B]: keys before the chunk
+    cu_seqblocks_q: torch.Tensor  # int32 [B+1]: query block offsets
+
+    def to(self, device) -> "PrefillBatch":
+        out = PrefillBatch(**{k: getattr(self, k) for k in self.__dataclass_fields__})
+        for name in ("q_idx", "k_idx_cache", "block_table", "slot_ids", "cu_seqlens", "seq_lens", "prefix_lens",
+                     "cu_seqblocks_q"):
+            setattr(out, name, getattr(self, name).to(device))
+        return out
+
+
+def make_prefill_batch(name: str, *, offsets: Sequence[int], chunks: Sequence[int], block_size_q: int,
+                       topk: int, init_blocks: int = 0, local_blocks: int = 0, Hi: int = 1, Di: int = 128,
+                       NB: int = 128, P: int = 1024, spare_rows: int = 2, seed: int,
+                       idx_dtype: torch.dtype = torch.bfloat16) -> PrefillBatch:
+    """Sequence b has ``chunks[b]`` query tokens at positions ``offsets[b]`` ..
+    ``offsets[b] + chunks[b] - 1`` and ``offsets[b] + chunks[b]`` keys; its
+    page-table row is drawn from a shuffled table with ``spare_rows`` rows
+    that no sequence owns (their entries point at unowned pages).  Index
+    queries and keys are N(0, 1); unowned index slots hold the finite poison.
+    ``scale = 1/sqrt(Di)``."""
+    g = torch.Generator().manual_seed(seed)
+    B = len(offsets)
+    lengths = [o + c for o, c in zip(offsets, chunks)]
+    table, owned = _pages_for(lengths + [0] * spare_rows, P, NB, g)
+    perm = torch.randperm(B + spare_rows, generator=g)
+    block_table = table[perm].contiguous()
+    slot_ids = torch.argsort(perm)[:B].to(torch.int32)  # row of sequence b in the shuffled table
+    cu = [0]
+    cub = [0]
+    for c in chunks:
+        cu.append(cu[-1] + c)
+        cub.append(cub[-1] + (c + block_size_q - 1) // block_size_q)
+    total_q = cu[-1]
+    n_slots = P * BLOCK_SIZE
+    all_slots = torch.cat([_request_slots(pages, L) for pages, L in zip(owned[:B], lengths)])
+    q_idx = torch.randn((total_q, Hi, Di), generator=g).to(idx_dtype)
+    kidx = torch.full((n_slots, 1, Di), INDEX_POISON, dtype=idx_dtype)
+    kidx.index_copy_(0, all_slots, torch.randn((all_slots.numel(), 1, Di), generator=g).to(idx_dtype))
+    return PrefillBatch(name=name, B=B, Hi=Hi, Di=Di, NB=NB, P=P, topk=topk, block_size_q=block_size_q,
+                        init_blocks=init_blocks, local_blocks=local_blocks, scale=1.0 / math.sqrt(Di),
+                        n_rows=cub[-1], q_idx=q_idx, k_idx_cache=kidx, block_table=block_table,
+                        slot_ids=slot_ids, cu_seqlens=torch.tensor(cu, dtype=torch.int32),
+                        seq_lens=torch.tensor(lengths, dtype=torch.int32),
+                        prefix_lens=torch.tensor(list(offsets), dtype=torch.int32),
+                        cu_seqblocks_q=torch.tensor(cub, dtype=torch.int32))
+
+
+PREFILL_BATCH_NAME = ("batched paged prefill score-to-selection, one call (8 x 512-token chunks at offsets "
+                      "~U[0,15872], Di=128, query blocks of 64 tokens, 1 initial + 2 local blocks, top-32)")
+
+
+def prefill_batch(seed: int = 1004, block_size_q: int = 64, init_blocks: int = 1, local_blocks: int = 2,
+                  topk: int = 32) -> PrefillBatch:
+    """The batched prefill configuration's sequences (same offsets as the
+    per-token score-to-selection workload) as one fused call."""
+    g = torch.Generator().manual_seed(seed + 7919)
+    offsets = torch.randint(0, 15873, (8,), generator=g).tolist()
+    return make_prefill_batch("prefill_batch", offsets=offsets, chunks=[512] * 8, block_size_q=block_size_q,
+                              topk=topk, init_blocks=init_blocks, local_blocks=local_blocks, seed=seed)

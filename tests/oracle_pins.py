@@ -21,7 +21,14 @@ the oracle disagrees with what the pages and the mathematics fix:
     square case), a closed form (two keys give tanh(q/2)), uniform logits,
     one key, and the invariants "a causal row is non-causal attention over
     its prefix", "GQA equals MHA on repeated kv heads", "key order does not
-    matter without the flag".
+    matter without the flag";
+  * the fused prefill score-to-selection against a numpy brute force
+    (gathered keys, one product per sequence, masked maxima, policy blocks,
+    lexicographic sort; bad metadata included), its reduction to the decode
+    score sheet and top-k when query blocks are single tokens, and the
+    invariants "positive scale changes nothing", "page permutation changes
+    nothing", "a wide enough selection takes every visible block, policy
+    blocks first".
 
 ``test_oracle_pins.py`` runs them on the oracle; ``test_oracle_mutants.py``
 runs them on copies of the oracle with planted mistakes and checks that each
@@ -500,6 +507,146 @@ def pin_sdpa_invariants(o):
     assert np.allclose(f2, 2 * full, rtol=1e-14, atol=0)
 
 
+# ----------------------------------------- prefill score-to-selection (V2)
+
+def np_prefill(pb, bt=None, slot_ids=None, seq_lens=None, n_rows=None, topk=None):
+    """Brute force of the fused prefill call with numpy, written from the
+    rule without the oracle's loops: gather each sequence's keys through its
+    page-table row, one matrix product per sequence, mask, reduce each
+    (query block, key block) cell with a max, then the policy blocks and a
+    lexicographic sort.  Returns (ids [Hi, n_rows, topk], scores)."""
+    bt = (pb.block_table if bt is None else bt).numpy()
+    sid = (pb.slot_ids if slot_ids is None else slot_ids).numpy()
+    sl = (pb.seq_lens if seq_lens is None else seq_lens).numpy()
+    cu, cub, pre = pb.cu_seqlens.numpy(), pb.cu_seqblocks_q.numpy(), pb.prefix_lens.numpy()
+    n_rows = pb.n_rows if n_rows is None else n_rows
+    topk = pb.topk if topk is None else topk
+    q = pb.q_idx.to(torch.float64).numpy()
+    k = pb.k_idx_cache.to(torch.float64).numpy()[:, 0, :]
+    R, NB = bt.shape
+    Hi = q.shape[1]
+    ids = np.full((Hi, n_rows, topk), -1, dtype=np.int32)
+    sc = np.full((Hi, n_rows, NB), -np.inf)
+    for b in range(pb.B):
+        r = int(sid[b])
+        for qb in range(int(cub[b + 1] - cub[b])):
+            row = int(cub[b]) + qb
+            if not 0 <= row < n_rows:
+                continue
+            L = min(int(pre[b]) + qb * pb.block_size_q + 1, int(sl[b]), NB * BS)
+            if not 0 <= r < R:
+                L = 0
+            L = max(L, 0)
+            nvis = -(-L // BS)
+            toks = list(range(int(cu[b]) + qb * pb.block_size_q,
+                              min(int(cu[b]) + (qb + 1) * pb.block_size_q, int(cu[b + 1]))))
+            taus = np.arange(L)
+            pages = bt[r, taus // BS] if L else np.zeros(0, dtype=np.int64)
+            ok = (pages >= 0) & (pages < pb.P)
+            slots = pages.astype(np.int64) * BS + taus % BS
+            for h in range(Hi):
+                z = q[toks, h, :] @ k[np.where(ok, slots, 0)].T * pb.scale if toks else np.zeros((0, L))
+                z = np.where(ok[None, :], z, -np.inf)
+                for kb in range(nvis):
+                    cell = z[:, kb * BS:min((kb + 1) * BS, L)]
+                    sc[h, row, kb] = cell.max() if cell.size else -np.inf
+                forced = [kb for kb in range(nvis) if kb < pb.init_blocks or kb >= nvis - pb.local_blocks]
+                rest = np.array([kb for kb in range(nvis) if kb not in forced and np.isfinite(sc[h, row, kb])],
+                                dtype=np.int64)
+                rest = rest[np.lexsort((rest, -sc[h, row, rest]))] if len(rest) else rest
+                sel = (forced + rest.tolist())[:topk]
+                ids[h, row, :len(sel)] = sel
+    return ids, sc
+
+
+def tiny_prefill(seed, **kw):
+    args = dict(offsets=[130, 0, 250], chunks=[5, 1, 9], block_size_q=4, topk=3, init_blocks=1, local_blocks=1,
+                Hi=2, Di=8, NB=4, P=24, seed=seed, idx_dtype=torch.float32)
+    args.update(kw)
+    return W.make_prefill_batch("tiny", **args)
+
+
+def run_prefill(o, pb, bt=None, slot_ids=None, seq_lens=None, n_rows=None, topk=None, scale=None):
+    return o.prefill_topk(pb.q_idx, pb.k_idx_cache, pb.block_table if bt is None else bt,
+                          pb.slot_ids if slot_ids is None else slot_ids, pb.cu_seqlens,
+                          pb.seq_lens if seq_lens is None else seq_lens, pb.prefix_lens, pb.cu_seqblocks_q,
+                          pb.block_size_q, pb.init_blocks, pb.local_blocks, pb.scale if scale is None else scale,
+                          pb.n_rows if n_rows is None else n_rows, pb.topk if topk is None else topk)
+
+
+def pin_prefill_bruteforce(o):
+    cases = [dict(), dict(block_size_q=1, init_blocks=0, local_blocks=0),
+             dict(topk=6), dict(topk=1, init_blocks=2, local_blocks=2),
+             dict(block_size_q=3, idx_dtype=torch.bfloat16, Hi=1, local_blocks=0),
+             dict(offsets=[0, 0, 380], chunks=[130, 7, 4], block_size_q=32, init_blocks=0, local_blocks=2)]
+    for i, kw in enumerate(cases):
+        pb = tiny_prefill(90 + i, **kw)
+        got, gs = run_prefill(o, pb)
+        ref, rs = np_prefill(pb)
+        assert np.array_equal(got, ref), "prefill ids, case %d" % i
+        assert_close(gs, rs, rtol=1e-12, atol=1e-12, what="prefill scores, case %d" % i)
+    # out-of-domain metadata: a sequence outside the table, a page outside
+    # the pool, seq_lens short of the chunk, rows that no sequence owns
+    pb = tiny_prefill(97)
+    bt = pb.block_table.clone()
+    bt[int(pb.slot_ids[2]), 1] = pb.P + 5
+    sid = pb.slot_ids.clone()
+    sid[1] = bt.shape[0] + 3
+    sl = pb.seq_lens.clone()
+    sl[0] = int(pb.prefix_lens[0]) + 2
+    got, gs = run_prefill(o, pb, bt=bt, slot_ids=sid, seq_lens=sl, n_rows=pb.n_rows + 2)
+    ref, rs = np_prefill(pb, bt=bt, slot_ids=sid, seq_lens=sl, n_rows=pb.n_rows + 2)
+    assert np.array_equal(got, ref), "prefill ids, bad metadata"
+    assert np.all(got[:, pb.n_rows:] == -1)
+    assert_close(gs, rs, rtol=1e-12, atol=1e-12, what="prefill scores, bad metadata")
+
+
+def pin_prefill_reduces_to_decode(o):
+    """Query blocks of one token and no policy blocks: each row is the decode
+    top-k of its token with seq_len = position + 1 (the pinned score sheet
+    and selection)."""
+    pb = tiny_prefill(98, block_size_q=1, init_blocks=0, local_blocks=0, topk=3)
+    got, _ = run_prefill(o, pb)
+    cu = pb.cu_seqlens.tolist()
+    ri, sl = [], []
+    for b in range(pb.B):
+        for j in range(cu[b + 1] - cu[b]):
+            ri.append(int(pb.slot_ids[b]))
+            sl.append(int(pb.prefix_lens[b]) + j + 1)
+    s = o.block_score(pb.q_idx, pb.k_idx_cache, pb.block_table, torch.tensor(ri, dtype=torch.int32),
+                      torch.tensor(sl, dtype=torch.int32), pb.scale)
+    assert np.array_equal(got, o.select_topk(s, pb.topk))
+
+
+def pin_prefill_invariants(o):
+    pb = tiny_prefill(99, topk=4, init_blocks=1, local_blocks=1)
+    base, _ = run_prefill(o, pb)
+    # selection does not depend on the (positive) scale
+    assert np.array_equal(run_prefill(o, pb, scale=3.5 * pb.scale)[0], base)
+    # permuting pool pages (and the table with them) changes nothing
+    perm = torch.randperm(pb.P, generator=torch.Generator().manual_seed(3))
+    slots = (perm.to(torch.int64)[:, None] * BS + torch.arange(BS)[None]).reshape(-1)
+    k2 = torch.empty_like(pb.k_idx_cache)
+    k2[slots] = pb.k_idx_cache
+    pb2 = W.PrefillBatch(**{f: getattr(pb, f) for f in pb.__dataclass_fields__})
+    pb2.k_idx_cache = k2
+    pb2.block_table = perm[pb.block_table.to(torch.int64)].to(torch.int32)
+    assert np.array_equal(run_prefill(o, pb2)[0], base)
+    # a selection at least as wide as the visible blocks takes them all, and
+    # the policy blocks always lead
+    wide, _ = run_prefill(o, pb, topk=8)
+    cub, pre = pb.cu_seqblocks_q.tolist(), pb.prefix_lens.tolist()
+    for b in range(pb.B):
+        for qb in range(cub[b + 1] - cub[b]):
+            L = min(pre[b] + qb * pb.block_size_q + 1, int(pb.seq_lens[b]))
+            nvis = -(-L // BS)
+            for h in range(pb.Hi):
+                row = wide[h, cub[b] + qb]
+                assert sorted(row[row >= 0].tolist()) == list(range(nvis)), (b, qb, h, row)
+                forced = sorted({0, nvis - 1})
+                assert row[:len(forced)].tolist() == forced, (b, qb, h, row)
+
+
 PINS = [
     pin_e4m3_decoder,
     pin_bf16_decoder,
@@ -516,4 +663,7 @@ PINS = [
     pin_sdpa_vs_torch,
     pin_sdpa_closed_forms,
     pin_sdpa_invariants,
+    pin_prefill_bruteforce,
+    pin_prefill_reduces_to_decode,
+    pin_prefill_invariants,
 ]

@@ -38,6 +38,17 @@ MUTATIONS = [
     ("sdpa gqa index", "int64_t kvh = g / G;", "int64_t kvh = g % Hkv;"),
     ("sdpa drops sm_scale", "z[j] = sm_scale * dot;", "z[j] = dot;"),
     ("sdpa ignores the causal flag", "if (causal) {", "if (0) {"),
+    ("prefill visibility excludes the own position", "int64_t L = (int64_t)prefix_lens[b] + qb * block_size_q + 1;",
+     "int64_t L = (int64_t)prefix_lens[b] + qb * block_size_q;"),
+    ("prefill visibility through the block end", "int64_t L = (int64_t)prefix_lens[b] + qb * block_size_q + 1;",
+     "int64_t L = (int64_t)prefix_lens[b] + (qb + 1) * block_size_q;"),
+    ("prefill local blocks off by one", "kb >= nvis - local_blocks);", "kb > nvis - local_blocks);"),
+    ("prefill init ignores visibility", "forced[kb] = kb < nvis && (kb < init_blocks || kb >= nvis - local_blocks);",
+     "forced[kb] = kb < init_blocks || (kb < nvis && kb >= nvis - local_blocks);"),
+    ("prefill query block is its first token", "int64_t t1 = t0 + block_size_q;", "int64_t t1 = t0 + 1;"),
+    ("prefill ranks the policy blocks again", "if (forced[kb] || isnan(s[kb]) || s[kb] == -INFINITY)",
+     "if (isnan(s[kb]) || s[kb] == -INFINITY)"),
+    ("prefill ignores slot_ids", "int64_t r = slot_ids[b];", "int64_t r = b;"),
     ("sdpa drops the first value", "o[d] += w * load(v, dtype,", "o[d] += (j > 0) * w * load(v, dtype,"),
 ]
 

@@ -18,12 +18,17 @@ before the step rather than during it (both outside the events); W warm-up
 steps first.  Under torchrun each rank runs its own batch
 (different seed) with no data exchange: weak scaling, max time over ranks.
 
+With --config prefill the step is one fused prefill score-to-selection call
+(msa_prefill_block_score) over the batched prefill sequences (8 x 512-token
+chunks, query blocks of 64 tokens, 1 initial + 2 local blocks, top-32); its
+roofline is the score FLOPs against the dense bf16 tensor peak.
+
 With --config dense the step is instead one dense GQA attention call
 (attention_sdpa) on a causal prefill chunk: 512 query tokens after 7680 cached
 tokens, 64 q / 8 kv heads, head dim 128, bf16; its roofline is the call's
 algorithmic FLOPs against the dense bf16 tensor peak.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C|dense] [--impl reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C|dense|prefill] [--impl reference]
 """
 from __future__ import annotations
 
@@ -49,6 +54,7 @@ from sparse_paged_decode_gb300 import workloads as W  # noqa: E402
 METRIC = "decode query-rows/sec and achieved HBM GB/s vs ~8 TB/s (sparse paged decode)"
 UNIT = "query-rows/s"
 DENSE_METRIC = "dense GQA attention query-rows/sec (prefill chunk)"
+PREFILL_METRIC = "fused prefill score-to-selection query-rows/sec (batched paged prefill)"
 BS = 128
 FLUSH_BYTES = 256 << 20
 
@@ -675,6 +681,195 @@ def run_dense_gpu(args, rank, world, local_rank):
     }
 
 
+# ------------------------------------ fused prefill score-to-selection workload
+
+def prefill_limits(pb):
+    """(tokens, visible keys) of every query block of the batch."""
+    cu, cub, pre, sl = (pb.cu_seqlens.tolist(), pb.cu_seqblocks_q.tolist(), pb.prefix_lens.tolist(),
+                        pb.seq_lens.tolist())
+    out = []
+    for b in range(pb.B):
+        for qb in range(cub[b + 1] - cub[b]):
+            n_tok = max(0, min(pb.block_size_q, cu[b + 1] - cu[b] - qb * pb.block_size_q))
+            L = max(0, min(pre[b] + qb * pb.block_size_q + 1, sl[b], pb.NB * BS))
+            out.append((n_tok, L))
+    return out
+
+
+def prefill_flops(pb):
+    """Algorithmic FLOPs of one fused prefill call: each query token of a
+    query block against each key the block sees, Di multiply-adds, per index
+    head."""
+    return float(2 * pb.Di * pb.Hi * sum(n * L for n, L in prefill_limits(pb)))
+
+
+def prefill_oracle_rate(pb, budget_s=12.0, max_rows=None):
+    """The oracle on the batch's query blocks, one at a time (each as a batch
+    of its own: its tokens, with the block's first position as the prefix),
+    until the budget is spent; returns (query tokens/s, tokens timed, s)."""
+    import oracle
+
+    o = oracle.default()
+    cu, cub, pre = pb.cu_seqlens.tolist(), pb.cu_seqblocks_q.tolist(), pb.prefix_lens.tolist()
+    done, blocks, t0 = 0, 0, time.perf_counter()
+    for b in range(pb.B):
+        for qb in range(cub[b + 1] - cub[b]):
+            lo = cu[b] + qb * pb.block_size_q
+            hi = min(lo + pb.block_size_q, cu[b + 1])
+            o.prefill_topk(pb.q_idx[lo:hi], pb.k_idx_cache, pb.block_table, pb.slot_ids[b:b + 1],
+                           torch.tensor([0, hi - lo], dtype=torch.int32), pb.seq_lens[b:b + 1],
+                           torch.tensor([pre[b] + qb * pb.block_size_q], dtype=torch.int32),
+                           torch.tensor([0, 1], dtype=torch.int32), pb.block_size_q, pb.init_blocks,
+                           pb.local_blocks, float(np.float32(pb.scale)), 1, pb.topk)
+            done += hi - lo
+            blocks += 1
+            if time.perf_counter() - t0 >= budget_s or (max_rows and blocks >= max_rows):
+                dt = time.perf_counter() - t0
+                return done / dt, done, dt
+    dt = time.perf_counter() - t0
+    return done / dt, done, dt
+
+
+def prefill_desc(pb):
+    return {"workload": W.PREFILL_BATCH_NAME, "sequences": pb.B, "query_tokens": int(pb.q_idx.shape[0]),
+            "query_blocks": pb.n_rows, "block_size_q": pb.block_size_q, "init_blocks": pb.init_blocks,
+            "local_blocks": pb.local_blocks, "top_k": pb.topk, "index_heads": pb.Hi, "index_dim": pb.Di,
+            "page_table_blocks": pb.NB, "pool_pages": pb.P, "prefix_lens": pb.prefix_lens.tolist(),
+            "index_dtype": str(pb.q_idx.dtype)[6:],
+            "l2": "flushed between timed steps (256 MiB rewrite, then a 256 MiB read that cleans the dirty "
+                  "lines; outside the events)"}
+
+
+def run_prefill_reference(args, rank, world):
+    if rank != 0:
+        return None
+    pb = W.prefill_batch()
+    per_step_budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        prefill_oracle_rate(pb, budget_s=per_step_budget / 4, max_rows=1)
+    rows, secs = 0, 0.0
+    for _ in range(args.steps):
+        _, n, dt = prefill_oracle_rate(pb, budget_s=per_step_budget)
+        rows += n
+        secs += dt
+    value = rows / secs
+    return {
+        "impl": "reference", "metric": PREFILL_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": prefill_desc(pb),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "%d query tokens (whole query blocks) through the oracle (single-threaded "
+                                   "C, fp64), %.1f s per step" % (rows, per_step_budget)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def run_prefill_gpu(args, rank, world, local_rank):
+    import sparse_paged_decode_gb300 as spd
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    pb = W.prefill_batch(seed=1004 + 97 * rank)
+    g = pb.to(dev)
+    total_q = int(pb.q_idx.shape[0])
+    out = torch.empty((pb.Hi, pb.n_rows, pb.topk), dtype=torch.int32, device=dev)
+    ws = torch.empty(spd.prefill_workspace_bytes(total_q, pb.Hi, pb.NB), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    clean = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    clean_sum = torch.empty((), dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def flush_l2(i):
+        flush.fill_(i & 0xFF)
+        torch.sum(clean, 0, dtype=torch.int64, out=clean_sum)
+
+    def step():
+        spd.msa_prefill_block_score(g.q_idx, g.k_idx_cache, g.block_table, g.slot_ids, g.cu_seqlens, g.seq_lens,
+                                    g.prefix_lens, pb.block_size_q, BS, pb.init_blocks, pb.local_blocks, pb.scale,
+                                    g.cu_seqblocks_q, out, ws)
+
+    for i in range(args.warmup):
+        flush_l2(i)
+        step()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.25)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    n0 = spd.launch_count()
+    for i in range(args.steps):
+        flush_l2(i)
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    launches = spd.launch_count() - n0
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+
+    # end to end: the batch's index queries and metadata copied in from
+    # pinned host memory (the index cache stays resident), the ids copied back
+    per_call = [("q_idx", pb.q_idx), ("slot_ids", pb.slot_ids), ("cu_seqlens", pb.cu_seqlens),
+                ("seq_lens", pb.seq_lens), ("prefix_lens", pb.prefix_lens), ("cu_seqblocks_q", pb.cu_seqblocks_q)]
+    hosts = [(getattr(g, k), t.contiguous().pin_memory()) for k, t in per_call]
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(h.numel() * h.element_size() for _, h in hosts)
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush_l2(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for d, h in hosts:
+            d.copy_(h, non_blocking=True)
+        step()
+        host_out.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if i >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    clocks = sampler.stop() if sampler else None
+
+    total_ms, e2e_total = max_over_ranks([sum(step_ms), sum(e2e_ms)], world, dev)
+    if rank != 0:
+        return None
+    value = job_rate(total_q, world, args.steps, total_ms)
+    e2e_value = job_rate(total_q, world, args.steps, e2e_total)
+    flops = prefill_flops(pb)
+    mean_s = statistics.mean(step_ms) / 1e3
+    achieved = flops / mean_s / 1e12
+    peak, peak_src = measured_bf16_peak()
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        rate, n, dt = prefill_oracle_rate(pb, budget_s=args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": "%d query tokens (whole query blocks) of the batch through the oracle "
+                         "(single-threaded C, fp64), %.1f s" % (n, dt)}
+    return {
+        "metric": PREFILL_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 mma, f32 accumulate", "data": "synthetic",
+        "config": prefill_desc(pb),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "fused prefill call (token limits, score_tc_kernel, selection; direct launch)",
+                     "algorithmic_flops_per_launch": flops, "mean_launch_us": mean_s * 1e6,
+                     "peak_source": peak_src},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "timed_as": "direct launches per step",
+        "clocks": clocks,
+        "step_ms_median": statistics.median(step_ms),
+    }
+
+
 def _kernel_stamp():
     try:
         from sparse_paged_decode_gb300 import build as b
@@ -689,10 +884,11 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=lambda c: c if c == "dense" else int(c), default=2,
-                    choices=[2, 3, 4, 5, "dense"],
+    ap.add_argument("--config", type=lambda c: c if c in ("dense", "prefill") else int(c), default=2,
+                    choices=[2, 3, 4, 5, "dense", "prefill"],
                     help="workload (2 = EAGLE-style verification decode, the metric's workload; "
-                         "dense = the dense-attention prefill chunk)")
+                         "dense = the dense-attention prefill chunk; prefill = the fused prefill "
+                         "score-to-selection call)")
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -706,17 +902,18 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    dense = args.config == "dense"
+    ref_arm = {"dense": run_dense_reference, "prefill": run_prefill_reference}.get(args.config, run_reference)
+    gpu_arm = {"dense": run_dense_gpu, "prefill": run_prefill_gpu}.get(args.config, run_gpu)
     if args.impl == "reference":
         # the oracle arm runs on rank 0 only; other ranks exit without work
-        res = (run_dense_reference if dense else run_reference)(args, rank, world)
+        res = ref_arm(args, rank, world)
         if res is not None:
             print(json.dumps(res), flush=True)
         return
     if world > 1:
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group(backend="nccl")
-    res = (run_dense_gpu if dense else run_gpu)(args, rank, world, local_rank)
+    res = gpu_arm(args, rank, world, local_rank)
     if res is not None:
         print(json.dumps(res), flush=True)
     if world > 1:

@@ -6,8 +6,9 @@
  *   2. msa_select_topk                top-k block ids per query row
  *   3. paged_sparse_decode_attention  paged GQA attention over the selected blocks
  *      paged_decode_attention         the same over every block (dense decode)
- * and, beside them, attention_sdpa: dense (not paged) GQA attention with a
- * causal flag, the prefill-side attention slot of the same boundary.
+ * and, beside them, for prefill: msa_prefill_block_score, the fused
+ * score-to-selection of a ragged batch of chunks per query block, and
+ * attention_sdpa, dense (not paged) GQA attention with a causal flag.
  *
  * Contract shared by every entry point ("Kernel ABI" -- Core rules; "Slot
  * contract" -- 1. The validator owns the boundary):
@@ -189,6 +190,66 @@ SPD_API void paged_decode_attention(const spd_tensor *q, const spd_tensor *k_cac
                             const spd_tensor *out, float sm_scale, int32_t block_size,
                             float k_scale, float v_scale, void *workspace,
                             size_t workspace_bytes, spd_stream_t stream);
+
+/*
+ * Fused prefill score-to-selection for a ragged batch of prefill chunks.
+ * "Kernel ABI" -- attention.msa_prefill_block_score (the V2 call that owns
+ * score production and selection for the full batch: query block qb selects
+ * only blocks visible through prefix_lens[b] + qb * block_size_q; initial and
+ * local blocks follow the supplied policy; ids are logical blocks of the
+ * request's key sequence; unused output cells are -1).
+ *
+ * Sequence b owns query tokens cu_seqlens[b] .. cu_seqlens[b+1]-1, whose
+ * first token sits at key position prefix_lens[b]; it has seq_lens[b] keys
+ * in total, read through row slot_ids[b] of block_table; its query blocks of
+ * block_size_q tokens are output rows cu_seqblocks_q[b] + qb.  For query
+ * block qb and index head h:
+ *   L     = min(prefix_lens[b] + qb * block_size_q + 1, seq_lens[b], NB * 128)
+ *           visible keys (through the block's first token's own position;
+ *           0 if slot_ids[b] is outside the table); nvis = ceil(L / 128)
+ *   S[kb] = max over the block's tokens t and keys tau < L of key block kb of
+ *           (q[t][h] . index_k_cache[slot(tau)][0]) * scale   (kb < nvis)
+ *   row   = the policy blocks (the first init_blocks and the last
+ *           local_blocks visible blocks) in ascending id, then the other
+ *           visible blocks whose S is neither NaN nor -inf in descending S
+ *           (ties to the lower id), truncated to topk, padded with -1.
+ * Output rows that no sequence owns are all -1.  With block_size_q = 1 and
+ * no policy blocks a row is msa_select_topk of msa_block_score for one token
+ * with seq_len = its position + 1.
+ *
+ * q              [total_q, Hi, Di] f32 | bf16 | f16 index queries (Hi heads)
+ * index_k_cache  [P*128, 1, Di] the dtype of q, or e4m3 (values as encoded)
+ * block_table    [R, NB] i32 page ids (stands in for req_to_token)
+ * slot_ids       [B] i32 page-table row of each sequence
+ * cu_seqlens     [B+1] i32 nondecreasing query token offsets
+ * seq_lens       [B] i32, prefix_lens [B] i32
+ * block_size_q >= 1; block_size_k must be 128; init_blocks, local_blocks >= 0
+ * scale          finite and > 0
+ * cu_seqblocks_q [B+1] i32 nondecreasing output row offsets
+ *                (normally cu_seqblocks_q[b+1] - cu_seqblocks_q[b] =
+ *                ceil(chunk_b / block_size_q))
+ * out_topk       OUT [Hi, all_seqblock_q, topk] i32 (topk >= 1 from its shape)
+ * workspace      device scratch of at least spd_prefill_workspace_bytes(
+ *                total_q, Hi, NB) bytes, 256-byte aligned, no initialisation
+ *                needed, not shared by calls that may run concurrently
+ * The pages' max_seqlen_q, max_seqlen_k, topk, max_seqblock_q and
+ * all_seqblock_q arguments are not taken: the launch is sized from the
+ * tensors' shapes, so the call reads no device data on the host.
+ * Domain: Di in [1, 512], Hi <= 65535, NB in [1, 1024].  Accumulation is fp32.
+ */
+SPD_API void msa_prefill_block_score(const spd_tensor *q, const spd_tensor *index_k_cache,
+                                     const spd_tensor *block_table, const spd_tensor *slot_ids,
+                                     const spd_tensor *cu_seqlens, const spd_tensor *seq_lens,
+                                     const spd_tensor *prefix_lens, int32_t block_size_q, int32_t block_size_k,
+                                     int32_t init_blocks, int32_t local_blocks, float scale,
+                                     const spd_tensor *cu_seqblocks_q, const spd_tensor *out_topk,
+                                     void *workspace, size_t workspace_bytes, spd_stream_t stream);
+
+/*
+ * Workspace bytes msa_prefill_block_score needs for total_q query tokens, Hi
+ * index heads and a page table of NB blocks (0 for invalid sizes).
+ */
+SPD_API size_t spd_prefill_workspace_bytes(int64_t total_q, int64_t Hi, int64_t NB);
 
 /*
  * Dense GQA attention with a causal flag.

@@ -7,6 +7,7 @@ CUDA kernel:
   msa_select_topk                 top-k block ids per query row
   paged_sparse_decode_attention   paged GQA attention over the selected blocks
   paged_decode_attention          the same over every block (dense decode)
+  msa_prefill_block_score         fused prefill score-to-selection per query block
   attention_sdpa                  dense (not paged) GQA attention, causal flag
 
 The Python functions of the same names (in :mod:`.binding`) only marshal
@@ -23,6 +24,8 @@ __all__ = [
     "paged_decode_attention",
     "paged_sparse_decode_attention_noalloc",
     "attention_sdpa",
+    "msa_prefill_block_score",
+    "prefill_workspace_bytes",
     "decode_workspace_bytes",
     "launch_count",
     "set_attention_kernel",

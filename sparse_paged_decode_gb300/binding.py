@@ -25,6 +25,8 @@ __all__ = [
     "paged_decode_attention",
     "paged_sparse_decode_attention_noalloc",
     "attention_sdpa",
+    "msa_prefill_block_score",
+    "prefill_workspace_bytes",
     "decode_workspace_bytes",
     "launch_count",
     "set_attention_kernel",
@@ -84,6 +86,10 @@ def _load():
     L.paged_sparse_decode_attention_noalloc.restype = None
     L.paged_decode_attention.argtypes = [P, P, P, P, P, P, P, f32, i32, f32, f32, vp, sz, vp]
     L.paged_decode_attention.restype = None
+    L.msa_prefill_block_score.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, f32, P, P, vp, sz, vp]
+    L.msa_prefill_block_score.restype = None
+    L.spd_prefill_workspace_bytes.argtypes = [ctypes.c_int64] * 3
+    L.spd_prefill_workspace_bytes.restype = sz
     L.attention_sdpa.argtypes = [P, P, P, P, f32, i32, vp]
     L.attention_sdpa.restype = None
     L.spd_decode_workspace_bytes.argtypes = [ctypes.c_int64] * 5 + [i32]
@@ -192,6 +198,29 @@ def paged_decode_attention(q, k_cache, v_cache, block_table, seq_lens, req_idx, 
         _desc(seq_lens, "seq_lens"), _desc(req_idx, "req_idx"), _desc(out, "out"), float(sm_scale),
         int(block_size), float(k_scale), float(v_scale), ws_ptr, ws_bytes, _stream(stream))
     _check()
+
+
+def msa_prefill_block_score(q, index_k_cache, block_table, slot_ids, cu_seqlens, seq_lens, prefix_lens,
+                            block_size_q, block_size_k, init_blocks, local_blocks, scale, cu_seqblocks_q, out_topk,
+                            workspace, stream=None) -> None:
+    """Fused prefill score-to-selection: fill ``out_topk`` [Hi, rows, topk]
+    with the selected key blocks of every query block of a ragged batch.
+
+    ``workspace`` is a CUDA uint8 tensor of at least
+    ``prefill_workspace_bytes(total_q, Hi, NB)`` bytes."""
+    ws_ptr, ws_bytes = _workspace(workspace)
+    lib.msa_prefill_block_score(
+        _desc(q, "q"), _desc(index_k_cache, "index_k_cache"), _desc(block_table, "block_table"),
+        _desc(slot_ids, "slot_ids"), _desc(cu_seqlens, "cu_seqlens"), _desc(seq_lens, "seq_lens"),
+        _desc(prefix_lens, "prefix_lens"), int(block_size_q), int(block_size_k), int(init_blocks),
+        int(local_blocks), float(scale), _desc(cu_seqblocks_q, "cu_seqblocks_q"), _desc(out_topk, "out_topk"),
+        ws_ptr, ws_bytes, _stream(stream))
+    _check()
+
+
+def prefill_workspace_bytes(total_q: int, Hi: int, NB: int) -> int:
+    """Workspace bytes msa_prefill_block_score needs for these sizes."""
+    return int(lib.spd_prefill_workspace_bytes(total_q, Hi, NB))
 
 
 def attention_sdpa(q, k, v, out, sm_scale, causal, stream=None) -> None:

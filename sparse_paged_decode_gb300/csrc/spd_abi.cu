@@ -14,6 +14,7 @@
 #include <initializer_list>
 #include <mutex>
 
+#include "prefill.cuh"
 #include "sdpa.cuh"
 #include "spd_internal.cuh"
 #include "spd_dispatch.h"
@@ -295,6 +296,81 @@ bool attention(const spd_tensor *q, const spd_tensor *k, const spd_tensor *v, co
     return check_cuda(dispatch_attention(a, ws, ws_bytes, stream), entry);
 }
 
+// ------------------------------------------- prefill score-to-selection
+
+bool prefill_block_score(const spd_tensor *q, const spd_tensor *k, const spd_tensor *bt, const spd_tensor *sid,
+                         const spd_tensor *cu_q, const spd_tensor *sl, const spd_tensor *pre, int32_t bsq,
+                         int32_t bsk, int32_t init_blocks, int32_t local_blocks, float scale,
+                         const spd_tensor *cu_b, const spd_tensor *out, void *ws, size_t ws_bytes,
+                         cudaStream_t stream) {
+    if (!check_desc(q, "q", 3, {SPD_F32, SPD_BF16, SPD_F16})) return false;
+    if (!check_desc(k, "index_k_cache", 3, {SPD_F32, SPD_BF16, SPD_F16, SPD_E4M3})) return false;
+    if (!check_desc(bt, "block_table", 2, {SPD_I32})) return false;
+    if (!check_desc(sid, "slot_ids", 1, {SPD_I32})) return false;
+    if (!check_desc(cu_q, "cu_seqlens", 1, {SPD_I32})) return false;
+    if (!check_desc(sl, "seq_lens", 1, {SPD_I32})) return false;
+    if (!check_desc(pre, "prefix_lens", 1, {SPD_I32})) return false;
+    if (!check_desc(cu_b, "cu_seqblocks_q", 1, {SPD_I32})) return false;
+    if (!check_desc(out, "out_topk", 3, {SPD_I32})) return false;
+    const int64_t total_q = q->shape[0], Hi = q->shape[1], Di = q->shape[2];
+    const int64_t B = sid->shape[0], NB = bt->shape[1];
+    const int64_t n_rows = out->shape[1], topk = out->shape[2];
+    if (k->dtype != q->dtype && k->dtype != SPD_E4M3)
+        return fail(SPD_ERR_UNSUPPORTED, "index_k_cache dtype must match q (or be e4m3)");
+    if (k->shape[1] != 1) return fail(SPD_ERR_UNSUPPORTED, "index_k_cache must have one key head");
+    if (k->shape[2] != Di) return fail(SPD_ERR_INVALID_ARGUMENT, "index_k_cache head dim != q head dim");
+    if (k->shape[0] % kBlock != 0) return fail(SPD_ERR_INVALID_ARGUMENT, "index_k_cache slots not a whole number of pages");
+    if (sl->shape[0] != B || pre->shape[0] != B || cu_q->shape[0] != B + 1 || cu_b->shape[0] != B + 1)
+        return fail(SPD_ERR_INVALID_ARGUMENT,
+                    "slot_ids, seq_lens and prefix_lens need B entries, cu_seqlens and cu_seqblocks_q B + 1");
+    if (bsk != kBlock) return fail(SPD_ERR_UNSUPPORTED, "block_size_k must be %d (got %d)", kBlock, bsk);
+    if (bsq < 1) return fail(SPD_ERR_INVALID_ARGUMENT, "block_size_q must be >= 1");
+    if (init_blocks < 0 || local_blocks < 0) return fail(SPD_ERR_INVALID_ARGUMENT, "init/local block counts must be >= 0");
+    if (!(scale > 0.f) || scale == INFINITY) return fail(SPD_ERR_UNSUPPORTED, "scale must be finite and > 0");
+    if (NB < 1 || NB > kMaxNB) return fail(SPD_ERR_UNSUPPORTED, "NB=%lld outside [1, %d]", (long long)NB, kMaxNB);
+    if (Di < 1 || Di > kMaxDi) return fail(SPD_ERR_UNSUPPORTED, "Di=%lld outside [1, %d]", (long long)Di, kMaxDi);
+    if (Hi < 1 || Hi > 65535) return fail(SPD_ERR_UNSUPPORTED, "Hi=%lld outside [1, 65535]", (long long)Hi);
+    if (out->shape[0] != Hi) return fail(SPD_ERR_INVALID_ARGUMENT, "out_topk must be [Hi, rows, topk]");
+    if (topk < 1) return fail(SPD_ERR_INVALID_ARGUMENT, "out_topk needs topk >= 1");
+    if (B > INT32_MAX / 2 || total_q > INT32_MAX / 2 || n_rows > INT32_MAX / 2 || topk > INT32_MAX / 2 ||
+        Hi * total_q * NB > (int64_t(1) << 40))
+        return fail(SPD_ERR_UNSUPPORTED, "batch too large");
+    if (B > 0 && bt->shape[0] < 1) return fail(SPD_ERR_INVALID_ARGUMENT, "block_table has no rows");
+    if (numel(out) > 0 && !check_output_layout(out, "out_topk")) return false;  // an empty output has no cells
+    if (!check_no_overlap(out, "out_topk", {q, k, bt, sid, cu_q, sl, pre, cu_b})) return false;
+    const size_t need = prefill_workspace_bytes(total_q, Hi, NB);
+    if (need > 0 && (ws == nullptr || ws_bytes < need))
+        return fail(SPD_ERR_WORKSPACE, "msa_prefill_block_score: workspace of %zu bytes needed, %zu given", need,
+                    ws_bytes);
+    if (need > 0 && reinterpret_cast<uintptr_t>(ws) % 256 != 0)
+        return fail(SPD_ERR_WORKSPACE, "msa_prefill_block_score: workspace must be 256-byte aligned");
+    if (need > 0 && numel(out) > 0) {
+        uintptr_t olo, ohi;
+        byte_span(out, &olo, &ohi);
+        const uintptr_t wlo = reinterpret_cast<uintptr_t>(ws), whi = wlo + ws_bytes;
+        if (olo < whi && wlo < ohi) return fail(SPD_ERR_ALIASING, "out_topk overlaps the workspace");
+    }
+    if (n_rows == 0) return true;
+
+    PrefillArgs a{};
+    a.q = q->data; a.q_s0 = q->stride[0]; a.q_s1 = q->stride[1]; a.q_s2 = q->stride[2];
+    a.k = k->data; a.k_s0 = k->stride[0]; a.k_s2 = k->stride[2];
+    a.bt = static_cast<const int32_t *>(bt->data); a.bt_s0 = bt->stride[0]; a.bt_s1 = bt->stride[1];
+    a.slot_ids = static_cast<const int32_t *>(sid->data); a.sid_s0 = sid->stride[0];
+    a.cu_q = static_cast<const int32_t *>(cu_q->data); a.cuq_s0 = cu_q->stride[0];
+    a.seq_lens = static_cast<const int32_t *>(sl->data); a.sl_s0 = sl->stride[0];
+    a.prefix = static_cast<const int32_t *>(pre->data); a.pre_s0 = pre->stride[0];
+    a.cu_b = static_cast<const int32_t *>(cu_b->data); a.cub_s0 = cu_b->stride[0];
+    a.out = static_cast<int32_t *>(out->data); a.o_s0 = out->stride[0]; a.o_s1 = out->stride[1]; a.o_s2 = out->stride[2];
+    a.q_dt = q->dtype; a.k_dt = k->dtype;
+    a.total_q = (int32_t)total_q; a.Hi = (int32_t)Hi; a.Di = (int32_t)Di; a.R = (int32_t)bt->shape[0];
+    a.NB = (int32_t)NB; a.B = (int32_t)B; a.n_rows = (int32_t)n_rows; a.topk = (int32_t)topk;
+    a.bsq = bsq; a.init_blocks = init_blocks; a.local_blocks = local_blocks;
+    a.P = k->shape[0] / kBlock;
+    a.scale = scale;
+    return check_cuda(launch_prefill(a, ws, stream), "msa_prefill_block_score launch");
+}
+
 // ------------------------------------------------------- dense attention
 
 bool sdpa(const spd_tensor *q, const spd_tensor *k, const spd_tensor *v, const spd_tensor *out, float sm_scale,
@@ -449,6 +525,23 @@ void paged_decode_attention(const spd_tensor *q, const spd_tensor *k_cache, cons
     spd::attention(q, k_cache, v_cache, block_table, seq_lens, req_idx, nullptr, out, sm_scale, block_size,
                    k_scale, v_scale, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream),
                    "paged_decode_attention");
+}
+
+void msa_prefill_block_score(const spd_tensor *q, const spd_tensor *index_k_cache, const spd_tensor *block_table,
+                             const spd_tensor *slot_ids, const spd_tensor *cu_seqlens, const spd_tensor *seq_lens,
+                             const spd_tensor *prefix_lens, int32_t block_size_q, int32_t block_size_k,
+                             int32_t init_blocks, int32_t local_blocks, float scale,
+                             const spd_tensor *cu_seqblocks_q, const spd_tensor *out_topk, void *workspace,
+                             size_t workspace_bytes, spd_stream_t stream) {
+    spd::set_ok();
+    spd::prefill_block_score(q, index_k_cache, block_table, slot_ids, cu_seqlens, seq_lens, prefix_lens,
+                             block_size_q, block_size_k, init_blocks, local_blocks, scale, cu_seqblocks_q, out_topk,
+                             workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t spd_prefill_workspace_bytes(int64_t total_q, int64_t Hi, int64_t NB) {
+    if (total_q < 0 || Hi < 1 || NB < 1) return 0;
+    return spd::prefill_workspace_bytes(total_q, Hi, NB);
 }
 
 void attention_sdpa(const spd_tensor *q, const spd_tensor *k, const spd_tensor *v, const spd_tensor *out,

@@ -116,3 +116,54 @@ def nan_like(shape, dtype, device):
     if dtype == torch.int32:
         return torch.full(shape, 0x7FFFFFF0, dtype=dtype, device=device)
     return torch.full(shape, float("nan"), dtype=dtype, device=device)
+
+
+def check_prefill_rows(got, ref_ids, ref_scores, n_forced, what="prefill"):
+    """Rows of the fused prefill selection.  ``got``/``ref_ids`` [rows, topk]
+    int; ``ref_scores`` [rows, NB] fp64 oracle block scores; ``n_forced[row]``
+    the number of policy blocks the row leads with.  The policy blocks must
+    match exactly; the rest of each row is held to the top-k rule above
+    (tie clusters of the oracle's scores over the row's other visible
+    candidates, exact padding, distinct ids), the set overlap taken over all
+    rows together."""
+    got = np.asarray(got)
+    ref_ids = np.asarray(ref_ids)
+    s = np.asarray(ref_scores, dtype=np.float64)
+    matched = total = 0
+    for row in range(got.shape[0]):
+        K = got.shape[1]
+        nf = min(int(n_forced[row]), K)
+        assert np.array_equal(got[row, :nf], ref_ids[row, :nf]), (
+            "%s row %d: policy blocks %s, oracle %s" % (what, row, got[row, :nf], ref_ids[row, :nf]))
+        forced = set(ref_ids[row, :nf].tolist())
+        r = s[row].copy()
+        r[list(forced)] = -np.inf
+        # the other candidates (blocks that are not visible score -inf)
+        cand = np.flatnonzero(np.isfinite(r) | np.isposinf(r))
+        order = cand[np.lexsort((cand, -r[cand]))]
+        Kr = K - nf
+        n = min(len(order), Kr)
+        g = got[row, nf:]
+        assert np.all(g[n:] == -1), "%s row %d: padding differs (%s)" % (what, row, g)
+        sel = g[:n]
+        assert np.all(sel >= 0) and len(set(sel.tolist()) | forced) == len(sel) + len(forced), (
+            "%s row %d: bad or repeated ids %s" % (what, row, got[row]))
+        if n == 0:
+            continue
+        vals = r[order]
+        scale = max(np.max(np.abs(vals[np.isfinite(vals)])) if np.any(np.isfinite(vals)) else 1.0, 1e-30)
+        cluster = np.zeros(len(order), dtype=np.int64)
+        for i in range(1, len(order)):
+            gap = abs(vals[i - 1] - vals[i]) / max(abs(vals[i - 1]), 1e-2 * scale)
+            cluster[i] = cluster[i - 1] + (gap > TIE_RTOL)
+        cl_of = {int(b): int(c) for b, c in zip(order, cluster)}
+        for k, b in enumerate(sel):
+            assert int(b) in cl_of, "%s row %d: id %d is not a candidate" % (what, row, b)
+            assert cl_of[int(b)] == cluster[k], (
+                "%s row %d pos %d: got block %d, oracle %d" % (what, row, nf + k, b, order[k]))
+        ref_set = set(order[:Kr].tolist())
+        matched += len(ref_set & set(sel.tolist()))
+        total += len(ref_set)
+    overlap = matched / total if total else 1.0
+    assert overlap >= TOPK_OVERLAP, "%s: overlap %.4f" % (what, overlap)
+    return overlap

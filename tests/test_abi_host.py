@@ -152,6 +152,42 @@ def test_sdpa_validation(spd):
     assert status(spd)[0] == SPD_ERR_ALIASING
 
 
+def prefill_call(spd, total_q=20, Hi=2, Di=64, B=3, NB=4, P=8, rows=7, topk=4, q_dtype=BF16, k_dtype=None,
+                 bsq=4, bsk=128, init=1, local=1, scale=0.125, ws_bytes=None, cu_len=None, out=None):
+    q = Fake((total_q, Hi, Di), q_dtype)
+    k = Fake((P * 128, 1, Di), k_dtype if k_dtype is not None else q_dtype)
+    bt = Fake((B + 1, NB), I32)
+    sid, sl, pre = Fake((B,), I32), Fake((B,), I32), Fake((B,), I32)
+    cu_q = Fake(((B + 1) if cu_len is None else cu_len,), I32)
+    cu_b = Fake((B + 1,), I32)
+    o = out or Fake((Hi, rows, topk), I32)
+    need = spd.lib.spd_prefill_workspace_bytes(total_q, Hi, NB)
+    ws = Fake((need + 256,), E4M3)
+    spd.lib.msa_prefill_block_score(q.ref(), k.ref(), bt.ref(), sid.ref(), cu_q.ref(), sl.ref(), pre.ref(), bsq, bsk,
+                                    init, local, scale, cu_b.ref(), o.ref(), ws.d.data,
+                                    need if ws_bytes is None else ws_bytes, None)
+    return status(spd)
+
+
+def test_prefill_validation(spd):
+    for kd in (None, E4M3):
+        code, msg = prefill_call(spd, k_dtype=kd)
+        assert code in (SPD_OK, SPD_ERR_CUDA), msg
+    assert prefill_call(spd, rows=0)[0] == SPD_OK  # no rows: nothing to write
+    assert prefill_call(spd, bsk=64)[0] == SPD_ERR_UNSUPPORTED
+    assert prefill_call(spd, bsq=0)[0] == SPD_ERR_INVALID_ARGUMENT
+    assert prefill_call(spd, init=-1)[0] == SPD_ERR_INVALID_ARGUMENT
+    assert prefill_call(spd, scale=-0.5)[0] == SPD_ERR_UNSUPPORTED
+    assert prefill_call(spd, NB=2000)[0] == SPD_ERR_UNSUPPORTED
+    assert prefill_call(spd, k_dtype=F16)[0] == SPD_ERR_UNSUPPORTED  # bf16 queries, f16 keys
+    assert prefill_call(spd, cu_len=3)[0] == SPD_ERR_INVALID_ARGUMENT  # cu_seqlens needs B + 1 entries
+    assert prefill_call(spd, topk=0)[0] == SPD_ERR_INVALID_ARGUMENT
+    assert prefill_call(spd, ws_bytes=64)[0] == SPD_ERR_WORKSPACE
+    assert prefill_call(spd, out=Fake((2, 7, 4), I32, strides=(4, 4, 1)))[0] == SPD_ERR_ALIASING
+    assert prefill_call(spd, out=Fake((3, 7, 4), I32))[0] == SPD_ERR_INVALID_ARGUMENT  # Hi mismatch
+    assert spd.lib.spd_prefill_workspace_bytes(4096, 1, 128) >= 4096 * 128 * 4 + 2 * 4096 * 4
+
+
 def test_output_overlapping_input_rejected(spd):
     q = Fake((2, 1, 32), BF16)
     k = Fake((128, 1, 32), BF16)

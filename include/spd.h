@@ -139,9 +139,9 @@ SPD_API void msa_select_topk(const spd_tensor *scores, const spd_tensor *topk_id
 
 /*
  * Stage 3 -- paged sparse GQA decode attention.
- * "Kernel ABI" -- attention.decode: each query row attends exactly the
- * supplied non-negative block ids; -1 entries and tokens at or beyond
- * seq_lens are excluded.  "Kernel ABI" -- attention.sdpa: Hq divisible by
+ * "Kernel ABI" -- attention.decode: a query row reads the given block ids
+ * that are >= 0 and nothing else; a -1 id selects nothing, and keys at
+ * positions >= seq_lens are left out.  "Kernel ABI" -- attention.sdpa: Hq divisible by
  * Hkv; q head g reads kv head g / (Hq / Hkv).  "MiniMax-M3 decode through the
  * ATOM kernel library" -- static scalar K/V scales on FP8 caches.
  *
@@ -193,11 +193,11 @@ SPD_API void paged_decode_attention(const spd_tensor *q, const spd_tensor *k_cac
 
 /*
  * Fused prefill score-to-selection for a ragged batch of prefill chunks.
- * "Kernel ABI" -- attention.msa_prefill_block_score (the V2 call that owns
- * score production and selection for the full batch: query block qb selects
- * only blocks visible through prefix_lens[b] + qb * block_size_q; initial and
- * local blocks follow the supplied policy; ids are logical blocks of the
- * request's key sequence; unused output cells are -1).
+ * "Kernel ABI" -- attention.msa_prefill_block_score (the V2 call: one call
+ * scores and selects for the whole ragged batch; a query block may pick only
+ * key blocks it can see from position prefix_lens[b] + qb * block_size_q;
+ * the init/local arguments fix blocks that are always taken; ids count the
+ * blocks of the request's own key sequence; leftover cells hold -1).
  *
  * Sequence b owns query tokens cu_seqlens[b] .. cu_seqlens[b+1]-1, whose
  * first token sits at key position prefix_lens[b]; it has seq_lens[b] keys
@@ -253,8 +253,9 @@ SPD_API size_t spd_prefill_workspace_bytes(int64_t total_q, int64_t Hi, int64_t 
 
 /*
  * Dense GQA attention with a causal flag.
- * "Kernel ABI" -- attention.sdpa ("attention(q, k, v, out, sm_scale, causal)":
- * scaled dot-product attention with GQA/MQA expansion; Hq divisible by Hkv).
+ * "Kernel ABI" -- attention.sdpa (q, k, v, out, a softmax scale and a
+ * causal flag; softmax attention where each kv head serves Hq / Hkv query
+ * heads, Hq a multiple of Hkv).
  *
  *   z_j = sm_scale * (q[t][g] . k[j][h]),  h = g / (Hq / Hkv)
  *   out[t][g] = sum_j softmax(z)_j * v[j][h]

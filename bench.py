@@ -89,7 +89,7 @@ def score_flops(w):
 
 def workload_desc(w):
     return {
-        "workload": "cfg%s: %s" % (w.name[-1], W.CONFIG_NAMES.get(int(w.name[-1]), w.name)),
+        "workload": next((W.CONFIG_NAMES[k] for k, n in W.WORKLOAD_NAMES.items() if n == w.name), w.name),
         "requests": w.R, "query_rows": w.T, "valid_query_rows": w.n_valid_tokens,
         "tokens_per_request": w.tokens_per_request, "request_lengths": w.request_lengths,
         "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.D, "index_heads": w.Hi, "index_dim": w.Di,
@@ -303,7 +303,7 @@ def run_gpu(args, rank, world, local_rank):
     T, NB, K = w.T, w.NB, max(w.K, 1)
     scores = torch.empty((w.Hi, T, NB), device=dev)
     topk = torch.empty((w.Hi, T, K), dtype=torch.int32, device=dev)
-    prefill = w.q is None  # cfg4: score-to-selection only, no attention stage
+    prefill = w.q is None  # prefill score-to-selection: no attention stage
     out = ws = None
     if not prefill:
         out = torch.empty((T, w.Hq, w.D), dtype=torch.bfloat16, device=dev)

@@ -222,6 +222,7 @@ def make_prefill(name: str, *, offsets: Sequence[int], chunk: int, Di: int = 128
 
 # ----------------------------------------------------------------- configs
 
+# descriptions of the five workloads, by the number bench.py --config takes
 CONFIG_NAMES = {
     1: "tiny sparse decode (B=1, 8/1 heads, D=64, Di=32, L=512, top-2, fp32 inputs)",
     2: "EAGLE-style verification decode (4 rows x 4 tokens, 64/8 heads, D=128, L~U[2048,16384], top-16)",
@@ -229,6 +230,8 @@ CONFIG_NAMES = {
     4: "batched paged prefill score-to-selection (8 x 512 tokens, Di=128, causal, top-32)",
     5: "stress sparse decode (64 rows x {1,4,8,16} tokens, L log-uniform [256,16384], top-64, t3 queries)",
 }
+WORKLOAD_NAMES = {1: "tiny_sparse_decode", 2: "verification_decode", 3: "dense_decode", 4: "prefill_score_select",
+                  5: "stress_decode"}
 
 
 def with_fp8_index(w: Workload) -> Workload:
@@ -246,20 +249,20 @@ def config(cfg: int, seed: Optional[int] = None) -> Workload:
     """The five benchmark configurations, full size."""
     seed = 1000 + cfg if seed is None else seed
     if cfg == 1:
-        return make_decode("cfg1", lengths=[512], tokens_per_request=[1], Hq=8, Hkv=1, D=64,
+        return make_decode("tiny_sparse_decode", lengths=[512], tokens_per_request=[1], Hq=8, Hkv=1, D=64,
                            Hi=1, Di=32, NB=4, P=16, K=2, dtype=torch.float32, seed=seed)
     if cfg == 2:
         g = torch.Generator().manual_seed(seed + 7919)
         lengths = torch.randint(2048, 16385, (4,), generator=g).tolist()
-        return make_decode("cfg2", lengths=lengths, tokens_per_request=[4] * 4, Hq=64, Hkv=8, D=128,
+        return make_decode("verification_decode", lengths=lengths, tokens_per_request=[4] * 4, Hq=64, Hkv=8, D=128,
                            Di=128, NB=128, P=1024, K=16, seed=seed)
     if cfg == 3:
-        return make_decode("cfg3", lengths=[16384] * 16, tokens_per_request=[1] * 16, Hq=64, Hkv=8,
+        return make_decode("dense_decode", lengths=[16384] * 16, tokens_per_request=[1] * 16, Hq=64, Hkv=8,
                            D=128, NB=128, P=2048, K=0, seed=seed, dense=True, with_index=False)
     if cfg == 4:
         g = torch.Generator().manual_seed(seed + 7919)
         offsets = torch.randint(0, 15873, (8,), generator=g).tolist()
-        return make_prefill("cfg4", offsets=offsets, chunk=512, P=1024, K=32, seed=seed)
+        return make_prefill("prefill_score_select", offsets=offsets, chunk=512, P=1024, K=32, seed=seed)
     if cfg == 5:
         return stress(seed=seed)
     raise ValueError("unknown config %r" % cfg)
@@ -279,7 +282,7 @@ def stress(seed: int = 1005, rows: int = 64, P: int = 8192, K: int = 64,
     padded = [0] * rows
     for r in pad_rows:
         padded[r] = int(torch.randint(1, n[r] + 1, (1,), generator=g))
-    return make_decode("cfg5" if rows == 64 else "stress%d" % rows, lengths=lengths,
+    return make_decode("stress_decode" if rows == 64 else "stress%d" % rows, lengths=lengths,
                        tokens_per_request=n, Hq=64, Hkv=8, D=128, Di=128, NB=128, P=P, K=K,
                        seed=seed, q_dist="student_t3", padded_tail=padded)
 

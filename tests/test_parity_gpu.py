@@ -174,7 +174,7 @@ def test_large_logits(spd, orc, kernel_policy):
     assert res["dense"][1] >= 0.9999
 
 
-def test_cfg1_tiny(spd, orc):
+def test_tiny_sparse_decode(spd, orc):
     full_check(spd, orc, W.config(1))
 
 
@@ -419,15 +419,15 @@ def test_fp8_index_cache_strided_queries(spd, orc):
     check_scores(out.cpu().numpy(), ref, "strided fp8 index scores")
 
 
-def test_fp8_index_cache_cfg2_and_cfg4(spd, orc):
+def test_fp8_index_cache_full_size(spd, orc):
     """The verification-decode and prefill index shapes with an FP8 index
-    cache: cfg2's whole sheet, sampled cfg4 rows."""
+    cache: the verification decode's whole sheet, sampled prefill rows."""
     w = W.with_fp8_index(W.config(2))
     g = w.to(DEV)
     s = gpu_scores(spd, g)
     ref = orc.block_score(w.q_idx, w.k_idx_cache, w.block_table, w.req_idx, w.seq_lens, f32(w.idx_scale))
-    check_scores(s.cpu().numpy(), ref, "cfg2 fp8 index scores")
-    check_topk(gpu_topk(spd, s, w.K).cpu().numpy(), ref, w.K, "cfg2 fp8 index topk")
+    check_scores(s.cpu().numpy(), ref, "verification decode fp8 index scores")
+    check_topk(gpu_topk(spd, s, w.K).cpu().numpy(), ref, w.K, "verification decode fp8 index topk")
     w = W.with_fp8_index(W.config(4))
     g = w.to(DEV)
     s = gpu_scores(spd, g)
@@ -435,26 +435,26 @@ def test_fp8_index_cache_cfg2_and_cfg4(spd, orc):
     ridx = torch.tensor(rows)
     ref = orc.block_score(w.q_idx[ridx], w.k_idx_cache, w.block_table, w.req_idx[ridx], w.seq_lens[ridx],
                           f32(w.idx_scale))
-    check_scores(s.cpu().numpy()[:, rows], ref, "cfg4 fp8 index scores")
+    check_scores(s.cpu().numpy()[:, rows], ref, "prefill fp8 index scores")
 
 
 # --------------------------------------------------------- full-size configs
 
-def test_cfg2_full(spd, orc):
+def test_verification_decode_full(spd, orc):
     full_check(spd, orc, W.config(2))
 
 
-def test_cfg3_full_dense_sampled(spd, orc):
+def test_dense_decode_full_sampled(spd, orc):
     w = W.config(3)
     g = w.to(DEV)
     out = gpu_attention(spd, g, None)
     rows = [0, 11]
     ref = oracle_rows(orc, w, rows, None)
-    check_attention(out.float().cpu().numpy()[rows], ref, "cfg3 dense")
+    check_attention(out.float().cpu().numpy()[rows], ref, "dense decode")
     assert torch.isfinite(out.float()).all()
 
 
-def test_cfg4_full_sampled(spd, orc):
+def test_prefill_score_select_full_sampled(spd, orc):
     w = W.config(4)
     g = w.to(DEV)
     s = gpu_scores(spd, g)
@@ -464,14 +464,14 @@ def test_cfg4_full_sampled(spd, orc):
     ridx = torch.tensor(rows)
     ref_s = orc.block_score(w.q_idx[ridx], w.k_idx_cache, w.block_table, w.req_idx[ridx], w.seq_lens[ridx],
                             f32(w.idx_scale))
-    check_scores(s.cpu().numpy()[:, rows], ref_s, "cfg4 scores")
-    check_topk(tk.cpu().numpy()[:, rows], ref_s, w.K, "cfg4 topk")
+    check_scores(s.cpu().numpy()[:, rows], ref_s, "prefill scores")
+    check_topk(tk.cpu().numpy()[:, rows], ref_s, w.K, "prefill topk")
     # causal visibility: no token selects a block past its own position
     pos_block = ((g.seq_lens - 1) // BS).view(1, -1, 1)
     assert torch.all((tk < 0) | (tk <= pos_block))
 
 
-def test_cfg5_full(spd, orc):
+def test_stress_decode_full(spd, orc):
     w = W.config(5)
     pad = [t for t in range(w.T) if int(w.seq_lens[t]) == 0]
     long_ = int(torch.argmax(w.seq_lens))

@@ -601,6 +601,29 @@ def pin_prefill_bruteforce(o):
     assert_close(gs, rs, rtol=1e-12, atol=1e-12, what="prefill scores, bad metadata")
 
 
+def pin_prefill_golden(o):
+    with open(os.path.join(GOLDEN, "prefill_policy.json")) as f:
+        fx = json.load(f)
+    P, pages = fx["pool_pages"], fx["pages"]
+    NB = len(pages)
+    k = torch.full((P * BS, 1, 1), 64.0)
+    L = fx["prefix"] + fx["chunk"]
+    for tau in range(L):
+        k[pages[tau // BS] * BS + tau % BS, 0, 0] = fx["block_values"][tau // BS]
+    for tau, val in fx["spikes"]:
+        k[pages[tau // BS] * BS + tau % BS, 0, 0] = val
+    q = torch.ones((fx["chunk"], 1, 1))
+    q[fx["negated_token"], 0, 0] = -1.0
+    bt = torch.tensor([[2] * NB, pages], dtype=torch.int32)
+    n_q = -(-fx["chunk"] // fx["block_size_q"])
+    i32 = lambda v: torch.tensor(v, dtype=torch.int32)  # noqa: E731
+    for K, key in ((4, "expected_top4"), (6, "expected_top6")):
+        ids, _ = o.prefill_topk(q, k, bt, i32([1]), i32([0, fx["chunk"]]), i32([L]), i32([fx["prefix"]]),
+                                i32([0, n_q]), fx["block_size_q"], fx["init_blocks"], fx["local_blocks"],
+                                fx["scale"], n_q, K)
+        assert ids[0].tolist() == fx[key], (K, ids[0].tolist())
+
+
 def pin_prefill_reduces_to_decode(o):
     """Query blocks of one token and no policy blocks: each row is the decode
     top-k of its token with seq_len = position + 1 (the pinned score sheet
@@ -664,6 +687,7 @@ PINS = [
     pin_sdpa_closed_forms,
     pin_sdpa_invariants,
     pin_prefill_bruteforce,
+    pin_prefill_golden,
     pin_prefill_reduces_to_decode,
     pin_prefill_invariants,
 ]

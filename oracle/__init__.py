@@ -99,7 +99,7 @@ class Oracle:
         L.oracle_block_score.restype = c_int
         L.oracle_select_topk.argtypes = [vp, i64, i64, i64, vp]
         L.oracle_select_topk.restype = c_int
-        L.oracle_paged_attention.argtypes = [vp, c_int, i64, i64, i64, vp, vp, i64, i64, vp, i64, i64,
+        L.oracle_paged_attention.argtypes = [vp, c_int, i64, i64, i64, vp, vp, c_int, i64, i64, vp, i64, i64,
                                              vp, vp, vp, i64, dbl, dbl, dbl, i64, vp]
         L.oracle_paged_attention.restype = c_int
         L.oracle_sdpa.argtypes = [vp, vp, vp, c_int, i64, i64, i64, i64, i64, dbl, c_int, vp]
@@ -157,10 +157,13 @@ class Oracle:
     def paged_attention(self, q, k_cache, v_cache, block_table, req_idx, seq_lens,
                         topk_idx, sm_scale: float, k_scale: float, v_scale: float,
                         block_size: int = 128) -> np.ndarray:
-        """Attention output [T, Hq, D] (fp64); ``topk_idx=None`` means dense."""
+        """Attention output [T, Hq, D] (fp64); ``topk_idx=None`` means dense.
+        The caches are FP8-E4M3 (float8 or uint8 codes) or BF16."""
         qa, qdt = _raw(q, "float")
-        k8, _ = _raw(k_cache, "e4m3")
-        v8, _ = _raw(v_cache, "e4m3")
+        k8, kdt = _raw(k_cache, "e4m3")
+        v8, vdt = _raw(v_cache, "e4m3")
+        if kdt != vdt or kdt not in (OR_E4M3, OR_BF16):
+            raise ValueError("oracle: K/V caches must both be E4M3 or both BF16")
         bt, _ = _raw(block_table, "int")
         ri, _ = _raw(req_idx, "int")
         sl, _ = _raw(seq_lens, "int")
@@ -185,7 +188,7 @@ class Oracle:
             K = tk.shape[2]
             tk_ptr = _ptr(tk)
         out = np.empty((T, Hq, D), dtype=np.float64)
-        rc = self.lib.oracle_paged_attention(_ptr(qa), qdt, T, Hq, D, _ptr(k8), _ptr(v8), n_slots, Hkv,
+        rc = self.lib.oracle_paged_attention(_ptr(qa), qdt, T, Hq, D, _ptr(k8), _ptr(v8), kdt, n_slots, Hkv,
                                              _ptr(bt), R, NB, _ptr(ri), _ptr(sl), tk_ptr, K,
                                              float(sm_scale), float(k_scale), float(v_scale),
                                              int(block_size), _ptr(out))

@@ -241,12 +241,16 @@ int oracle_select_topk(const double *scores, int64_t rows, int64_t NB, int64_t K
  * (two passes: the maximum first, then both sums).  No valid token -> 0.
  *
  * topk == NULL selects every block (dense paged decode, the degenerate case).
- * Layouts (contiguous): q [T][Hq][D], k8/v8 [n_slots][Hkv][D] (E4M3 bytes),
+ * kv_dtype is OR_E4M3 for the FP8 caches of the ATOM run or OR_BF16 for a
+ * dense BF16 cache ("Kernel ABI" -- attention.decode: the commissioned cache
+ * is dense BF16); the scales multiply the decoded values either way (1.0
+ * for a BF16 cache stored unscaled).
+ * Layouts (contiguous): q [T][Hq][D], k8/v8 [n_slots][Hkv][D] (E4M3 bytes or BF16),
  * block_table [R][NB], req_idx [T], seq_lens [T], topk [Hkv][T][K],
  * out [T][Hq][D].
  */
 int oracle_paged_attention(const void *q, int q_dtype, int64_t T, int64_t Hq, int64_t D,
-                           const uint8_t *k8, const uint8_t *v8, int64_t n_slots, int64_t Hkv,
+                           const void *k8, const void *v8, int kv_dtype, int64_t n_slots, int64_t Hkv,
                            const int32_t *block_table, int64_t R, int64_t NB,
                            const int32_t *req_idx, const int32_t *seq_lens,
                            const int32_t *topk, int64_t K,
@@ -305,7 +309,7 @@ int oracle_paged_attention(const void *q, int q_dtype, int64_t T, int64_t Hq, in
                 double dot = 0.0;
                 for (int64_t d = 0; d < D; ++d)
                     dot += load(q, q_dtype, (t * Hq + g) * D + d) *
-                           oracle_e4m3_value(k8[(slots[j] * Hkv + h) * D + d]);
+                           load(k8, kv_dtype, (slots[j] * Hkv + h) * D + d);
                 z[j] = sm_scale * k_scale * dot;
                 if (z[j] > zmax)
                     zmax = z[j];
@@ -319,7 +323,7 @@ int oracle_paged_attention(const void *q, int q_dtype, int64_t T, int64_t Hq, in
                 double w = exp(z[j] - zmax);
                 l += w;
                 for (int64_t d = 0; d < D; ++d)
-                    o[d] += w * v_scale * oracle_e4m3_value(v8[(slots[j] * Hkv + h) * D + d]);
+                    o[d] += w * v_scale * load(v8, kv_dtype, (slots[j] * Hkv + h) * D + d);
             }
             for (int64_t d = 0; d < D; ++d)
                 o[d] /= l;

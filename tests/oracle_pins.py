@@ -11,7 +11,9 @@ the oracle disagrees with what the pages and the mathematics fix:
     fixture and a closed-form ramp;
   * top-k against numpy's lexicographic sort, ties and padding included;
   * attention against torch's fp64 ``scaled_dot_product_attention`` with GQA
-    expansion on gathered, torch-dequantised keys and values, against a
+    expansion on gathered, torch-dequantised keys and values (FP8-E4M3
+    caches, and dense BF16 caches, which must also reproduce the E4M3 path
+    bit for bit when they hold its decoded values), against a
     hand-worked fixture and closed forms (uniform logits -> mean of V, one key
     -> that key's value), and the invariants "selecting every block equals
     dense decode", "a one-block context is that block's softmax", "permuting
@@ -78,6 +80,11 @@ def e4m3_to_f64(codes: torch.Tensor) -> torch.Tensor:
     return codes.view(torch.float8_e4m3fn).to(torch.float32).to(torch.float64)
 
 
+def cache_to_f64(cache: torch.Tensor) -> torch.Tensor:
+    """A K or V cache's values: torch's own decoding of E4M3 codes, or of bf16."""
+    return cache.to(torch.float64) if cache.dtype == torch.bfloat16 else e4m3_to_f64(cache)
+
+
 def np_valid_slots(bt, r, L, NB, P, blocks=None):
     """Logical tokens 0..L-1 of request r (optionally only in ``blocks``),
     ascending, as (tau, slot) pairs; tokens whose page is outside the pool are
@@ -121,8 +128,8 @@ def sdpa_reference(w, topk, bt=None, ri=None, sl=None):
     ri = w.req_idx if ri is None else ri
     sl = w.seq_lens if sl is None else sl
     G = w.Hq // w.Hkv
-    kf = e4m3_to_f64(w.k_cache) * w.k_scale
-    vf = e4m3_to_f64(w.v_cache) * w.v_scale
+    kf = cache_to_f64(w.k_cache) * w.k_scale
+    vf = cache_to_f64(w.v_cache) * w.v_scale
     q = w.q.to(torch.float64)
     out = torch.zeros((w.T, w.Hq, w.D), dtype=torch.float64)
     for t in range(w.T):
@@ -309,6 +316,44 @@ def pin_attention_vs_sdpa(o):
                                   w.sm_scale, w.k_scale, w.v_scale)
         ref_d = sdpa_reference(w, None, bt, ri, sl)
         assert_close(got_d, ref_d, rtol=1e-11, atol=1e-12, what="dense vs sdpa seed %d" % seed)
+
+
+def bf16_cache_copy(w, seed):
+    """The workload with dense BF16 K/V caches of fresh N(0, 1) values (not
+    quantised), unit scales and the same finite poison in unowned slots."""
+    g = torch.Generator().manual_seed(seed)
+    out = W.Workload(**{f: getattr(w, f) for f in w.__dataclass_fields__})
+    owned = torch.zeros(w.k_cache.shape[0], dtype=torch.bool)  # slots of the requests' tokens
+    for r, L in enumerate(w.request_lengths):
+        for tau in range(L):
+            owned[int(w.block_table[r, tau // BS]) * BS + tau % BS] = True
+    for name in ("k_cache", "v_cache"):
+        fresh = torch.randn(w.k_cache.shape, generator=g, dtype=torch.float64)
+        setattr(out, name, torch.where(owned[:, None, None], fresh, torch.full_like(fresh, 448.0)).to(torch.bfloat16))
+    out.k_scale = out.v_scale = 1.0
+    return out
+
+
+def pin_attention_bf16_cache(o):
+    w = tiny_decode(61, dtype=torch.bfloat16)
+    topk = o.select_topk(o.block_score(w.q_idx, w.k_idx_cache, w.block_table, w.req_idx, w.seq_lens,
+                                       w.idx_scale), w.K)
+    # BF16 caches holding the E4M3-decoded values give the E4M3 path's result bit for bit
+    same = W.Workload(**{f: getattr(w, f) for f in w.__dataclass_fields__})
+    same.k_cache = e4m3_to_f64(w.k_cache).to(torch.bfloat16)
+    same.v_cache = e4m3_to_f64(w.v_cache).to(torch.bfloat16)
+    for sel in (topk, None):
+        a = o.paged_attention(w.q, w.k_cache, w.v_cache, w.block_table, w.req_idx, w.seq_lens, sel,
+                              w.sm_scale, w.k_scale, w.v_scale)
+        b = o.paged_attention(same.q, same.k_cache, same.v_cache, w.block_table, w.req_idx, w.seq_lens, sel,
+                              w.sm_scale, w.k_scale, w.v_scale)
+        assert np.array_equal(a, b), "bf16 copy of the E4M3 cache differs"
+    # fresh BF16 values against torch's fp64 SDPA over the same selections
+    wb = bf16_cache_copy(w, 62)
+    for sel in (topk, None):
+        got = o.paged_attention(wb.q, wb.k_cache, wb.v_cache, wb.block_table, wb.req_idx, wb.seq_lens, sel,
+                                wb.sm_scale, 1.0, 1.0)
+        assert_close(got, sdpa_reference(wb, sel), rtol=1e-11, atol=1e-12, what="bf16 cache vs sdpa")
 
 
 def pin_attention_golden(o):
@@ -680,6 +725,7 @@ PINS = [
     pin_topk_sort,
     pin_topk_closed_form,
     pin_attention_vs_sdpa,
+    pin_attention_bf16_cache,
     pin_attention_golden,
     pin_attention_closed_forms,
     pin_attention_invariants,

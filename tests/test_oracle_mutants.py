@@ -33,6 +33,7 @@ MUTATIONS = [
     ("clip to one block short", "L = NB * bs;", "L = (NB - 1) * bs;"),
     ("dense skips last block", "for (int64_t b = 0; b < NB && L > 0; ++b) {", "for (int64_t b = 0; b + 1 < NB && L > 0; ++b) {"),
     ("no max subtraction guard on empty", "if (n == 0) {", "if (n < 0) {"),
+    ("attention reads every cache as e4m3", "load(k8, kv_dtype,", "load(k8, OR_E4M3,"),
     ("sdpa causal off by one", "n = t + (S - T) + 1;", "n = t + (S - T);"),
     ("sdpa causal aligned top-left", "n = t + (S - T) + 1;", "n = t + 1;"),
     ("sdpa gqa index", "int64_t kvh = g / G;", "int64_t kvh = g % Hkv;"),

@@ -247,3 +247,24 @@ def test_workspace_size_depends_on_capacities_only(spd):
     assert a > 0 and a % 256 == 0
     assert f(32, 64, 8, 128, 128, 128) >= a
     assert f(16, 64, 8, 128, 128, 64) == 0
+
+
+def test_binding_refuses_host_tensors_and_raises_library_errors(spd):
+    """The Python binding never computes on the host: non-empty CPU tensors
+    are refused before the library is called, and a call the library rejects
+    raises SpdError carrying the documented code (empty tensors carry no
+    device address, so validation runs without a GPU)."""
+    import torch
+
+    q = torch.zeros((2, 4, 8), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        spd.attention_sdpa(q, q.clone(), q.clone(), q.clone(), 0.3, True, stream=0)
+    e = lambda *shape, dt=torch.bfloat16: torch.empty(shape, dtype=dt)  # noqa: E731
+    with pytest.raises(spd.SpdError) as err:  # Hq = 6 is not a multiple of Hkv = 4
+        spd.attention_sdpa(e(0, 6, 8), e(0, 4, 8), e(0, 4, 8), e(0, 6, 8), 0.3, False, stream=0)
+    assert err.value.code == SPD_ERR_UNSUPPORTED
+    # a valid empty batch is accepted and launches nothing (stream 0: the
+    # legacy default stream, never touched)
+    with pytest.raises(ValueError, match="CUDA tensor"):  # k and v hold data: refused on the host
+        spd.attention_sdpa(e(0, 8, 8), e(3, 2, 8), e(3, 2, 8), e(0, 8, 8), 0.3, True, stream=0)
+    spd.attention_sdpa(e(0, 8, 8), e(0, 2, 8), e(0, 2, 8), e(0, 8, 8), 0.3, True, stream=0)

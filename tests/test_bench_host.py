@@ -58,3 +58,13 @@ def test_prefill_workload_shape():
     # the same sequences as the per-token prefill configuration
     w4 = W.config(4)
     assert [w4.request_lengths[i] for i in range(8)] == pb.seq_lens.tolist()
+
+
+def test_reference_arms_run_on_rank_zero_only():
+    """Under torchrun the oracle arm of every workload runs on rank 0 alone;
+    the other ranks return without work (and print nothing)."""
+    import types
+
+    args = types.SimpleNamespace(steps=1, warmup=3, config=2, index_cache="native", cpu_seconds=1.0)
+    for arm in (bench.run_reference, bench.run_dense_reference, bench.run_prefill_reference):
+        assert arm(args, 1, 2) is None

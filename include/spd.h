@@ -292,14 +292,20 @@ SPD_API void attention_sdpa(const spd_tensor *q, const spd_tensor *k, const spd_
  *
  * - Limit: shapes whose spd_decode_workspace_bytes(...) exceeds 16 MiB are
  *   rejected with SPD_ERR_UNSUPPORTED (use the workspace entry point).
- * - The array exists once per GPU on which this call is used and is held
- *   until the process exits.
+ * - The array is part of the library's device code: it is created on a GPU
+ *   when that code is loaded there and held until the process exits.  With
+ *   CUDA's default lazy module loading that is the first use of this call on
+ *   the GPU; under CUDA_MODULE_LOADING=EAGER every GPU on which the process
+ *   creates a context holds the 16 MiB, whether or not the call is used.
  * - The first call on a device looks up the array's device address, with
  *   that device current; make that first call before any stream capture.
  * - Every call shares the one array and it keeps the last call's contents
  *   (each call rewrites whatever it needs zeroed).  Calls that could run on
  *   the GPU at the same time -- on different streams, or from different host
  *   threads -- race on it: serialise them.
+ * - A device-side wait that timed out is recorded in the array's status
+ *   word, not in a caller buffer: spd_workspace_status(NULL, stream) reads it
+ *   for the current device.
  */
 SPD_API void paged_sparse_decode_attention_noalloc(const spd_tensor *q, const spd_tensor *k_cache,
                                                    const spd_tensor *v_cache, const spd_tensor *block_table,
@@ -344,20 +350,23 @@ SPD_API int spd_set_attention_kernel(int policy);
 /*
  * Diagnostics: kernel selection per stage on this thread's subsequent calls.
  * stage 1 = msa_block_score, 2 = msa_select_topk, 3 = the attention calls
- * (the same setting as spd_set_attention_kernel).  policy 0 (default) picks
- * the specialised kernel whenever the shapes and layouts allow it, 1 always
- * the general-layout kernel; for stage 2, policy 2 picks the shared-memory
- * rank kernel (the default sorts rows of up to 256 blocks in registers and
- * ranks longer ones).  All give identical selections.  Returns the previous
- * setting, or -1 for an unknown stage.
+ * (the same setting as spd_set_attention_kernel), 4 = attention_sdpa.  policy
+ * 0 (default) picks the specialised kernel whenever the shapes and layouts
+ * allow it, 1 always the general-layout kernel; for stage 2, policy 2 picks
+ * the shared-memory rank kernel (the default sorts rows of up to 256 blocks
+ * in registers and ranks longer ones).  All give identical selections, and
+ * attention results that agree within the stated tolerance.  Returns the
+ * previous setting, or -1 for an unknown stage.
  */
 SPD_API int spd_set_kernel_policy(int stage, int policy);
 
 /*
  * Diagnostics: status word an attention call left in its workspace (0 = ok;
  * bit 0 = a device-side wait timed out and the call's output is not valid).
+ * workspace = NULL reads the built-in scratch of
+ * paged_sparse_decode_attention_noalloc on the current device.
  * Synchronises with `stream` to read it -- never call it on a hot path.
- * Returns -1 when the status cannot be read.
+ * Returns -1 when the status cannot be read.  Leaves spd_last_error alone.
  */
 SPD_API int spd_workspace_status(const void *workspace, spd_stream_t stream);
 

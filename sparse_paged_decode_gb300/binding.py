@@ -245,13 +245,14 @@ def set_attention_kernel(policy: int) -> int:
     return int(lib.spd_set_attention_kernel(int(policy)))
 
 
-STAGE_SCORE, STAGE_SELECT, STAGE_ATTENTION = 1, 2, 3
+STAGE_SCORE, STAGE_SELECT, STAGE_ATTENTION, STAGE_SDPA = 1, 2, 3, 4
 
 
 def set_kernel_policy(stage: int, policy: int) -> int:
-    """Kernel choice of one stage (1 score, 2 select, 3 attention) on this
-    thread: 0 = specialised kernel where it applies (default), 1 =
-    general-layout kernel always.  Returns the previous policy."""
+    """Kernel choice of one stage (1 score, 2 select, 3 attention, 4 dense
+    attention) on this thread: 0 = specialised kernel where it applies
+    (default), 1 = general-layout kernel always.  Returns the previous
+    policy."""
     old = int(lib.spd_set_kernel_policy(int(stage), int(policy)))
     if old < 0:
         raise ValueError("unknown stage %r" % (stage,))
@@ -259,8 +260,12 @@ def set_kernel_policy(stage: int, policy: int) -> int:
 
 
 def workspace_status(workspace, stream=None) -> int:
-    """Status word an attention call left in ``workspace`` (synchronises)."""
-    return int(lib.spd_workspace_status(workspace.data_ptr(), _stream(stream)))
+    """Status word an attention call left in ``workspace`` (synchronises):
+    0 ok, bit 0 a device-side wait timed out.  ``workspace=None`` reads the
+    built-in scratch that paged_sparse_decode_attention_noalloc uses on the
+    current device."""
+    ptr = None if workspace is None else workspace.data_ptr()
+    return int(lib.spd_workspace_status(ptr, _stream(stream)))
 
 
 def launch_count() -> int:

@@ -25,9 +25,13 @@
 //        S^T[tok][n]  = K[tok][:] . Qs[n][:]      kind::f8f6f4, E4M3 K as read
 //        O^T[d][n]   += V^T[d][tok] . P[tok][n]    kind::f16, f16 V and P
 //    Queries enter as E4M3 terms (q = t0 + t1 (+ t2), each row scaled by a
-//    power of two into E4M3 range, the factor folded into the logit scale):
-//    two terms hold a bf16 query exactly (4 + 4 significant bits), other
-//    query types take three.  Two terms of a narrow group are stacked along
+//    power of two so its largest magnitude lies in [128, 256), the factor
+//    folded into the logit scale): for a bf16 query two terms (4 + 4
+//    significant bits) are exact for every element within 2^9 of its row's
+//    largest magnitude; a smaller element's second term falls in E4M3's
+//    subnormal range and is rounded there, an absolute error of at most
+//    2^-10 in the scaled units (2^-17 of the row's largest magnitude).  Other
+//    query types take three terms.  Two terms of a narrow group are stacked along
 //    N (one product per k-step, the softmax adds the halves); otherwise the
 //    terms accumulate into the same columns.  V is
 //    widened to f16 exactly (cvt.rn.f16x2.e4m3x2).  Probabilities are f16
@@ -1082,23 +1086,6 @@ bool make_tmap_q(CUtensorMap *m, const uint8_t *base, int64_t T, int64_t hq, int
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-struct DeviceInfo {
-    int sms = 0;
-    bool attr_set = false;
-};
-
-DeviceInfo &device_info() {
-    static DeviceInfo info[64];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    DeviceInfo &d = info[dev & 63];
-    if (d.sms == 0) {
-        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
-        if (d.sms <= 0) d.sms = 1;
-    }
-    return d;
-}
-
 // Query rows of one request that share a unit (a group).  A group reads each
 // block of the union of its rows' selections once, but the softmax cost of a
 // block grows with the group's width: 16 columns cost about half of 32 or 64
@@ -1133,12 +1120,10 @@ cudaError_t launch_attention_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cu
     if (!make_tmap(&tk, a.k, a.P * 128, a.Hkv, a.k_s0, a.k_s1)) return cudaSuccess;
     if (!make_tmap(&tv, a.v, a.P * 128, a.Hkv, a.v_s0, a.v_s1)) return cudaSuccess;
 
-    DeviceInfo &dev = device_info();
-    if (!dev.attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemBytes);
+    const int sms = device_sm_count();
+    {
+        cudaError_t e = opt_in_smem(reinterpret_cast<const void *>(attention_tc_kernel), kSmemBytes);
         if (e != cudaSuccess) return e;
-        dev.attr_set = true;
     }
 
     PlanArgs p{};
@@ -1149,7 +1134,7 @@ cudaError_t launch_attention_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cu
     p.T = a.T; p.R = a.R; p.NB = a.NB; p.K = a.K; p.Hkv = a.Hkv; p.G = G;
     p.gmax = group_rows(a, G);
     p.P = a.P;
-    p.num_ctas = dev.sms;
+    p.num_ctas = sms;
     p.ws = static_cast<char *>(ws);
     p.lay = lay;
     p.q = a.q; p.q_s0 = a.q_s0; p.q_s1 = a.q_s1; p.q_s2 = a.q_s2;
@@ -1168,7 +1153,7 @@ cudaError_t launch_attention_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cu
 
     const int64_t q_rows = static_cast<int64_t>(a.T) * a.Hq;
     // query conversion: 64 rows per CTA (four per warp), up to two CTAs per SM
-    const int conv_ctas = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(2 * dev.sms - 1, (q_rows + 63) / 64)));
+    const int conv_ctas = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(2 * sms - 1, (q_rows + 63) / 64)));
     cudaError_t e = launch_prepare(p, conv_ctas, stream);
     if (e != cudaSuccess) return e;
 
@@ -1183,7 +1168,7 @@ cudaError_t launch_attention_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cu
     t.ws = static_cast<char *>(ws);
     t.lay = lay;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(dev.sms);
+    cfg.gridDim = dim3(sms);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;

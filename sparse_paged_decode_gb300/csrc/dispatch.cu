@@ -2,8 +2,12 @@
 #include <stddef.h>
 
 #include <atomic>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "plan.cuh"
+#include "sdpa.cuh"
 #include "spd_dispatch.h"
 
 namespace spd {
@@ -15,17 +19,48 @@ std::atomic<uint64_t> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n), std::memory_order_relaxed); }
 uint64_t launch_count() { return g_launches.load(std::memory_order_relaxed); }
 
+namespace {
+std::mutex g_dev_mu;
+std::map<int, int> g_sms;                              // device -> SM count
+std::map<std::pair<int, const void *>, int> g_smem;    // (device, kernel) -> bytes opted in
+}  // namespace
+
+int device_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    auto it = g_sms.find(dev);
+    if (it != g_sms.end()) return it->second;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 1;
+    g_sms[dev] = sms;
+    return sms;
+}
+
+cudaError_t opt_in_smem(const void *func, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    int &have = g_smem[std::make_pair(dev, func)];
+    if (have >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) have = bytes;
+    return e;
+}
+
 cudaError_t launch_score_tc(const ScoreArgs &a, cudaStream_t stream, bool *used);
 cudaError_t launch_attention_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cudaStream_t stream, bool *used);
+cudaError_t launch_sdpa_tc(const SdpaArgs &a, cudaStream_t stream, bool *used);
 
 namespace {
 // per stage (index = spd stage code): 0 fastest kernel the shapes allow,
 // 1 the general-layout kernel, 2 (selection only) the rank kernel
-thread_local int g_policy[4] = {0, 0, 0, 0};
+thread_local int g_policy[5] = {0, 0, 0, 0, 0};
 }
 
 int set_kernel_policy(int stage, int policy) {
-    if (stage < 1 || stage > 3) return -1;
+    if (stage < 1 || stage > 4) return -1;
     const int old = g_policy[stage];
     g_policy[stage] = policy;
     return old;
@@ -59,6 +94,16 @@ cudaError_t dispatch_attention(const AttnArgs &a, void *workspace, size_t worksp
     }
     count_launches(1);
     return launch_attention_generic(a, stream);
+}
+
+cudaError_t dispatch_sdpa(const SdpaArgs &a, cudaStream_t stream) {
+    count_launches(1);
+    if (g_policy[4] == 0) {
+        bool used = false;
+        cudaError_t e = launch_sdpa_tc(a, stream, &used);
+        if (e != cudaSuccess || used) return e;
+    }
+    return launch_sdpa(a, stream);
 }
 
 int workspace_status(const void *workspace, cudaStream_t stream) {

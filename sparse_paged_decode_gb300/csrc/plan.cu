@@ -498,18 +498,10 @@ bool plan_configure(PlanArgs *a) {
 }
 
 cudaError_t launch_prepare(const PlanArgs &a, int conv_ctas, cudaStream_t stream) {
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (!attr_set[dev & 63]) {
-        cudaError_t e = cudaFuncSetAttribute(list_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPlanSmemMax);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(unit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPlanSmemMax);
-        if (e != cudaSuccess) return e;
-        attr_set[dev & 63] = true;
-    }
-    cudaError_t e =
-        launch_pdl(reinterpret_cast<const void *>(list_kernel), a.list_ctas, list_smem_bytes(a.T, a.NB), a, stream);
+    cudaError_t e = opt_in_smem(reinterpret_cast<const void *>(list_kernel), kPlanSmemMax);
+    if (e == cudaSuccess) e = opt_in_smem(reinterpret_cast<const void *>(unit_kernel), kPlanSmemMax);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(reinterpret_cast<const void *>(list_kernel), a.list_ctas, list_smem_bytes(a.T, a.NB), a, stream);
     if (e != cudaSuccess) return e;
     return launch_pdl(reinterpret_cast<const void *>(unit_kernel), 1 + conv_ctas,
                       unit_smem_bytes(a.T, a.heads_built), a, stream);

@@ -15,7 +15,7 @@
 // An FP8-E4M3 index cache with bf16 index queries (Di = 128) takes the
 // kind::f8f6f4 product instead: each lane's thread splits its query row,
 // scaled by a power of two into E4M3 range, into two E4M3 terms (q = t0 + t1
-// exactly for every element within 2^10 of the row's largest; below that t1
+// exactly for every element within 2^9 of the row's largest; below that t1
 // is rounded in E4M3's subnormal range) written straight into the swizzled
 // A tiles, the two terms accumulate into the same TMEM columns, and the
 // epilogue undoes the scale.
@@ -426,11 +426,6 @@ bool make_tmap_qidx(CUtensorMap *m, const ScoreArgs &a, int tq) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-struct ScoreDevice {
-    int sms = 0;
-    bool attr_set = false;
-};
-
 }  // namespace
 
 // Covers: q_idx and k_idx_cache both bf16 or both f16, Di in {64, 128, 192,
@@ -449,31 +444,23 @@ cudaError_t launch_score_tc(const ScoreArgs &a, cudaStream_t stream, bool *used)
     if (a.Hi > 1 && (a.q_s1 <= 0 || (a.q_s1 * 2) % 16)) return cudaSuccess;
     if (a.P * kBlock > (int64_t(1) << 31) - 1) return cudaSuccess;
 
-    static ScoreDevice devs[64];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    ScoreDevice &d = devs[dev & 63];
-    if (d.sms == 0) {
-        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
-        if (d.sms <= 0) d.sms = 1;
-    }
+    const int sms = device_sm_count();
     const int nkc = a.Di / 64;
     const int smem = fp8 ? static_cast<int>(1024 + kAtom * (2 + kMaxStages) + sizeof(ScoreShared))
                          : static_cast<int>(1024 + nkc * kAtom * (1 + key_stages(nkc)) + sizeof(ScoreShared));
-    if (!d.attr_set) {
+    {
         int smem_max = 0;
         for (int c = 1; c <= 4; ++c) {
             const int bytes = static_cast<int>(1024 + c * kAtom * (1 + key_stages(c)) + sizeof(ScoreShared));
             smem_max = bytes > smem_max ? bytes : smem_max;
         }
-        cudaError_t e = cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+        cudaError_t e = opt_in_smem(reinterpret_cast<const void *>(score_tc_kernel), smem_max);
         if (e != cudaSuccess) return e;
-        d.attr_set = true;
     }
 
     const int tq = kLanes / a.Hi;
     const int64_t n_tiles = (a.T + tq - 1) / tq;
-    int64_t chunk = (n_tiles * a.NB + 2 * d.sms - 1) / (2 * d.sms);
+    int64_t chunk = (n_tiles * a.NB + 2 * sms - 1) / (2 * sms);
     chunk = chunk < 1 ? 1 : chunk > kMaxChunk ? kMaxChunk : chunk;
     const int64_t n_chunks = (a.NB + chunk - 1) / chunk;
     if (n_tiles > INT32_MAX) return cudaSuccess;

@@ -408,8 +408,7 @@ bool sdpa(const spd_tensor *q, const spd_tensor *k, const spd_tensor *v, const s
     a.T = (int32_t)T; a.S = (int32_t)S; a.Hq = (int32_t)Hq; a.Hkv = (int32_t)Hkv; a.D = (int32_t)D;
     a.causal = causal != 0;
     a.sm_scale = sm_scale;
-    count_launches(1);
-    return check_cuda(launch_sdpa(a, stream), "attention_sdpa launch");
+    return check_cuda(dispatch_sdpa(a, stream), "attention_sdpa launch");
 }
 
 }  // namespace
@@ -570,6 +569,17 @@ int spd_set_attention_kernel(int policy) { return spd::set_kernel_policy(3, poli
 int spd_set_kernel_policy(int stage, int policy) { return spd::set_kernel_policy(stage, policy); }
 
 int spd_workspace_status(const void *workspace, spd_stream_t stream) {
+    if (workspace == nullptr) {
+        // the built-in scratch of paged_sparse_decode_attention_noalloc on the
+        // current device (a device array is zero when no call has used it)
+        const int saved = spd::g_status;
+        char saved_msg[sizeof spd::g_msg];
+        memcpy(saved_msg, spd::g_msg, sizeof saved_msg);
+        workspace = spd::noalloc_scratch();
+        spd::g_status = saved;  // a diagnostic leaves the last call's status alone
+        memcpy(spd::g_msg, saved_msg, sizeof saved_msg);
+        if (workspace == nullptr) return -1;
+    }
     return spd::workspace_status(workspace, reinterpret_cast<cudaStream_t>(stream));
 }
 

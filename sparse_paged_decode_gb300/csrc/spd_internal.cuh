@@ -81,6 +81,17 @@ cudaError_t launch_select_rank(const SelectArgs &a, cudaStream_t stream);
 cudaError_t launch_select_fast(const SelectArgs &a, cudaStream_t stream);  // sort for NB <= 256, else rank
 cudaError_t launch_attention_generic(const AttnArgs &a, cudaStream_t stream);
 
+// ------------------------------------------------------- per-device set-up
+// Both are safe to call from several host threads and cache their answer per
+// device ordinal (any ordinal the runtime reports).
+
+// SMs of the current device (at least 1).
+int device_sm_count();
+
+// Opts `func` in to `bytes` of dynamic shared memory on the current device,
+// once per (device, kernel); later calls with no more bytes do nothing.
+cudaError_t opt_in_smem(const void *func, int bytes);
+
 // ------------------------------------------------------------- device helpers
 
 __device__ __forceinline__ float e4m3_to_float(uint8_t code) {

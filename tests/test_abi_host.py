@@ -268,3 +268,17 @@ def test_binding_refuses_host_tensors_and_raises_library_errors(spd):
     with pytest.raises(ValueError, match="CUDA tensor"):  # k and v hold data: refused on the host
         spd.attention_sdpa(e(0, 8, 8), e(3, 2, 8), e(3, 2, 8), e(0, 8, 8), 0.3, True, stream=0)
     spd.attention_sdpa(e(0, 8, 8), e(0, 2, 8), e(0, 2, 8), e(0, 8, 8), 0.3, True, stream=0)
+
+
+def test_status_query_without_a_gpu_keeps_the_last_error(spd):
+    """spd_workspace_status is a diagnostic: with no device to read (here: no
+    GPU, for a caller workspace and for the built-in scratch alike) it returns
+    -1 and leaves the last call's recorded status untouched."""
+    q = Fake((4, 8, 64), BF16)
+    spd.lib.paged_decode_attention(q.ref(), None, None, None, None, None, None, ctypes.c_float(0.1), 128,
+                                   ctypes.c_float(1.0), ctypes.c_float(1.0), None, ctypes.c_size_t(0), None)
+    before = status(spd)
+    assert before[0] == SPD_ERR_INVALID_ARGUMENT
+    assert spd.lib.spd_workspace_status(None, None) == -1
+    assert spd.lib.spd_workspace_status(ctypes.c_void_p(1 << 40), None) == -1
+    assert status(spd) == before

@@ -90,6 +90,64 @@ def test_sdpa_small(spd, orc, case):
         assert not got[:T - S].float().any(), "rows that read no key must be zero"
 
 
+# The tensor-core kernel's domain (16-bit q, k, v of head dim 128, 16-bit
+# output, G a power of two): each case runs on it (policy 0) and on the
+# CUDA-core kernel (policy 1), both against the oracle.
+TC_CASES = [
+    # T, S, Hq, Hkv, causal, in dtype, out dtype, q distribution, sm_scale factor
+    (64, 1000, 64, 8, True, torch.bfloat16, torch.bfloat16, "normal", 1.0),     # tiles of 16 tokens, ragged keys
+    (77, 300, 16, 8, False, torch.float16, torch.float16, "student_t3", 1.0),   # G = 2, ragged token tail
+    (200, 200, 4, 4, True, torch.bfloat16, torch.float16, "normal", 1.0),       # MHA, square causal, 2 tiles
+    (50, 20, 16, 1, True, torch.bfloat16, torch.bfloat16, "normal", 1.0),      # G = 16, T > S: rows read nothing
+    (33, 700, 32, 2, True, torch.bfloat16, torch.bfloat16, "student_t3", -1.0),  # negative scale
+    (9, 129, 128, 1, False, torch.float16, torch.bfloat16, "normal", 3.0),     # G = 128: one token per tile
+]
+
+
+@pytest.mark.parametrize("policy", [0, 1], ids=["tensor_core", "cuda_core"])
+@pytest.mark.parametrize("case", TC_CASES, ids=["T%d_S%d_H%d_%d_%s_%s_%s_%s_x%g" % (
+    c[0], c[1], c[2], c[3], "causal" if c[4] else "full", str(c[5])[6:], str(c[6])[6:], c[7], c[8])
+    for c in TC_CASES])
+def test_sdpa_tensor_core_domain(spd, orc, case, policy):
+    T, S, Hq, Hkv, causal, dt, odt, qd, fac = case
+    w = W.make_dense("tc", T=T, S=S, Hq=Hq, Hkv=Hkv, D=128, causal=causal, seed=900 + T + S, dtype=dt, q_dist=qd)
+    sm = w.sm_scale * fac
+    ref = orc.sdpa(w.q, w.k, w.v, sm, causal)
+    g = w.to(DEV)
+    old = spd.set_kernel_policy(4, policy)
+    try:
+        got = run(spd, g.q, g.k, g.v, sm, causal, odt)
+    finally:
+        spd.set_kernel_policy(4, old)
+    check(got, ref, "sdpa %s policy %d" % (case, policy))
+    if causal and T > S:
+        assert not got[:T - S].float().any(), "rows that read no key must be zero"
+
+
+def test_sdpa_tensor_core_strided_views(spd, orc):
+    """q inside a packed [T, 3, Hq, 128] tensor and k, v as head-major caches
+    viewed [S, Hkv, 128] (16-byte aligned rows, so the tensor-core kernel
+    takes them through its TMA maps); the output a strided window whose
+    other elements stay untouched."""
+    T, S, Hq, Hkv, D = 40, 500, 16, 2, 128
+    gen = torch.Generator().manual_seed(78)
+    qkv = torch.randn((T, 3, Hq, D), generator=gen).to(torch.bfloat16)
+    kh = torch.randn((Hkv, S, D), generator=gen).to(torch.bfloat16)
+    vh = torch.randn((Hkv, S, D), generator=gen).to(torch.bfloat16)
+    sm = 0.09
+    ref = orc.sdpa(qkv[:, 1].contiguous(), kh.permute(1, 0, 2).contiguous(), vh.permute(1, 0, 2).contiguous(),
+                   sm, True)
+    qkv_d, kh_d, vh_d = qkv.to(DEV), kh.to(DEV), vh.to(DEV)
+    big = torch.full((T, Hq + 2, 2 * D), -5.0, dtype=torch.bfloat16, device=DEV)
+    out = big[:, 1:Hq + 1, ::2]
+    out.fill_(float("nan"))
+    run(spd, qkv_d[:, 1], kh_d.permute(1, 0, 2), vh_d.permute(1, 0, 2), sm, True, out=out)
+    check(out, ref, "tensor-core strided")
+    mask = torch.ones_like(big, dtype=torch.bool)
+    mask[:, 1:Hq + 1, ::2] = False
+    assert torch.all(big[mask] == -5.0), "wrote outside the output's cells"
+
+
 def test_sdpa_strided_inputs_and_output(spd, orc):
     """q inside a packed [T, 3, Hq, D] tensor, k and v as head-major caches
     viewed [S, Hkv, D], the output a strided window of a larger buffer whose
@@ -121,14 +179,24 @@ def test_sdpa_empty_batch(spd):
     torch.cuda.synchronize()
 
 
-def test_sdpa_full_size_sampled(spd, orc):
+def test_sdpa_full_size(spd, orc):
     """The benchmarked prefill chunk (512 query tokens after 7680 cached
     tokens, 64/8 heads, D=128, bf16), in the benchmark's launch
-    configuration, checked on sampled query tokens with all their heads."""
+    configuration, checked on every query token with all its heads: under
+    the causal flag token t is non-causal attention over its first
+    t + S - T + 1 keys, so the oracle runs token by token, from one host
+    thread per core."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+
     w = W.dense_prefill()
     g = w.to(DEV)
     got = run(spd, g.q, g.k, g.v, w.sm_scale, True).float().cpu().numpy()
-    for t in (0, 1, 63, 64, 200, 255, 256, 511):
+
+    def one(t):
         n = t + w.S - w.T + 1
-        ref = orc.sdpa(w.q[t:t + 1], w.k[:n], w.v[:n], w.sm_scale, False)
-        check_attention(got[t:t + 1], ref, "dense prefill token %d" % t)
+        return orc.sdpa(w.q[t:t + 1], w.k[:n], w.v[:n], w.sm_scale, False)
+
+    with ThreadPoolExecutor(max_workers=max(1, os.cpu_count() or 1)) as ex:
+        ref = np.concatenate(list(ex.map(one, range(w.T))), axis=0)
+    check_attention(got, ref, "dense prefill chunk")

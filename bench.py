@@ -1,15 +1,21 @@
 """Benchmark of the sparse paged decode hot path.
 
-One step = the three stages over one batch of the EAGLE-style verification
-decode workload (4 request rows x 4 query tokens, 64 q / 8 kv heads, head dim
-128, one index head of dim 128, seq_lens uniform in [2048, 16384] over a
-1024-page pool, top-16 blocks, FP8-E4M3 K/V): msa_block_score ->
-msa_select_topk -> paged_sparse_decode_attention, all through the C ABI.
+One step = the three stages over one batch of the stress sparse decode
+workload (64 request rows of 1, 4, 8 or 16 query tokens -- 496 rows, 13 of
+them padding --, 64 q / 8 kv heads, head dim 128, one index head of dim 128,
+seq_lens log-uniform in [256, 16384] over an 8192-page pool, top-64 blocks,
+FP8-E4M3 K/V, heavy-tailed queries): msa_block_score -> msa_select_topk ->
+paged_sparse_decode_attention, all through the C ABI.  --config 2 runs the
+EAGLE-style verification decode (4 rows x 4 tokens, top-16), --config 3 the
+dense paged decode (16 rows of 16384 tokens, every block) instead.
 
 Printed (rank 0, one JSON line): query rows per second (a query row is one
 non-padding query token with all its heads), the attention kernel's achieved
 HBM bandwidth against the measured peak, the end-to-end rate through the same
-calls with host buffers, and the CPU oracle's rate on a bounded sample.
+calls with host buffers, and the CPU oracle's rate on a bounded sample (the
+single-threaded oracle called from one host thread per core on disjoint query
+rows, and from one thread).  The run fails (exit 3) if an attention call
+recorded a device-side wait that timed out.
 
 Timing: CUDA events on the launching stream around each step; between timed
 steps a 256 MiB buffer is rewritten to flush the 129 MB L2, then a second
@@ -60,6 +66,10 @@ FLUSH_BYTES = 256 << 20
 
 
 # -------------------------------------------------------------------- helpers
+
+class TimedOutWait(RuntimeError):
+    """An attention call's workspace status says a device-side wait gave up."""
+
 
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -189,31 +199,75 @@ class ClockSampler:
 
 # ---------------------------------------------------------- the CPU baseline
 
-def oracle_rate(w, budget_s=12.0, max_rows=None):
+def host_cores():
+    """Cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def oracle_rate(w, budget_s=12.0, max_rows=None, threads=1):
     """The oracle's three stages, row by row, on a bounded sample of the
-    workload's query rows; returns (rows/s, rows timed, seconds)."""
+    workload's query rows; returns (rows/s, rows timed, seconds).
+
+    With threads > 1 the single-threaded oracle is called from that many host
+    threads at once, each taking the next untimed row (ctypes releases the
+    interpreter lock inside the call and the oracle keeps no state between
+    calls); every thread stops taking rows once the budget is spent, and the
+    rate is the rows finished over the wall time until the last one ends."""
     import oracle
 
     o = oracle.default()
     rows = [t for t in range(w.T) if int(w.seq_lens[t]) > 0]
-    done, t0 = 0, time.perf_counter()
-    for t in rows:
+    lock = threading.Lock()
+    state = {"next": 0, "done": 0}
+    t0 = time.perf_counter()
+
+    def one(t):
         idx = torch.tensor([t])
         s = o.block_score(w.q_idx[idx], w.k_idx_cache, w.block_table, w.req_idx[idx], w.seq_lens[idx],
                           float(np.float32(w.idx_scale)))
         tk = o.select_topk(s, w.K)
-        if w.q is None:  # prefill score-to-selection: no attention stage
-            done += 1
-            if time.perf_counter() - t0 >= budget_s or (max_rows and done >= max_rows):
-                break
-            continue
-        o.paged_attention(w.q[idx], w.k_cache, w.v_cache, w.block_table, w.req_idx[idx], w.seq_lens[idx], tk,
-                          float(np.float32(w.sm_scale)), float(np.float32(w.k_scale)), float(np.float32(w.v_scale)))
-        done += 1
-        if time.perf_counter() - t0 >= budget_s or (max_rows and done >= max_rows):
-            break
+        if w.q is not None:  # prefill score-to-selection has no attention stage
+            o.paged_attention(w.q[idx], w.k_cache, w.v_cache, w.block_table, w.req_idx[idx], w.seq_lens[idx], tk,
+                              float(np.float32(w.sm_scale)), float(np.float32(w.k_scale)),
+                              float(np.float32(w.v_scale)))
+
+    def worker():
+        while True:
+            with lock:
+                if (state["next"] >= len(rows) or time.perf_counter() - t0 >= budget_s
+                        or (max_rows and state["next"] >= max_rows)):
+                    return
+                t = rows[state["next"]]
+                state["next"] += 1
+            one(t)
+            with lock:
+                state["done"] += 1
+
+    if threads <= 1:
+        worker()
+    else:
+        pool = [threading.Thread(target=worker) for _ in range(threads)]
+        for th in pool:
+            th.start()
+        for th in pool:
+            th.join()
     dt = time.perf_counter() - t0
-    return done / dt, done, dt
+    return state["done"] / dt, state["done"], dt
+
+
+def cpu_baseline_record(rate_fn, what, budget_s):
+    """The oracle's rate on the host: all cores (one thread per core, the
+    reported value) and one core (context)."""
+    cores = host_cores()
+    rate, n, dt = rate_fn(budget_s, cores)
+    rate1, n1, dt1 = rate_fn(budget_s / 2, 1)
+    return {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "%d %s through the single-threaded oracle (plain C, fp64) called from %d host threads "
+                      "on disjoint rows, %.1f s" % (n, what, cores, dt),
+            "one_core": {"value": rate1, "cores": 1, "sample": "%d %s on one thread, %.1f s" % (n1, what, dt1)}}
 
 
 # ------------------------------------------------------------ replicas
@@ -253,12 +307,13 @@ def run_reference(args, rank, world):
     if rank != 0:
         return None
     w = make_workload(args, 1000 + args.config)
+    cores = host_cores()
     per_step_budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         oracle_rate(w, budget_s=per_step_budget / 4, max_rows=1)
     rates, rows, secs = [], 0, 0.0
     for _ in range(args.steps):
-        r, n, dt = oracle_rate(w, budget_s=per_step_budget)
+        r, n, dt = oracle_rate(w, budget_s=per_step_budget, threads=cores)
         rates.append(r)
         rows += n
         secs += dt
@@ -268,9 +323,10 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_desc(w),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": "%d query rows of the workload through the oracle's three stages "
-                                   "(single-threaded C, fp64), %.1f s per step" % (rows, per_step_budget)},
+                                   "(single-threaded C, fp64, called from %d host threads on disjoint rows), "
+                                   "%.1f s per step" % (rows, cores, per_step_budget)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -448,9 +504,15 @@ def run_gpu(args, rank, world, local_rank):
         if i >= args.warmup:
             e2e_ms.append(e0.elapsed_time(e1))
     clocks = sampler.stop() if sampler else None
+    # every attention call above left its status in the workspace: bit 0 =
+    # a device-side wait timed out, so the timed outputs are not valid
+    ws_status = spd.workspace_status(ws) if ws is not None else 0
 
     # max over ranks
-    total_ms, e2e_total = max_over_ranks([total_ms, sum(e2e_ms)], world, dev)
+    total_ms, e2e_total, bad = max_over_ranks([total_ms, sum(e2e_ms), float(ws_status != 0)], world, dev)
+    if bad:
+        raise TimedOutWait("an attention call recorded a device-side wait that timed out (workspace status %d)"
+                           % ws_status)
     if rank != 0:
         return None
 
@@ -463,8 +525,12 @@ def run_gpu(args, rank, world, local_rank):
     if os.path.exists(tpath):
         with open(tpath) as f:
             tj = json.load(f)
-        if tj.get("config") == args.config and tj.get("kernel_stamp") == _kernel_stamp():
-            traffic = tj.get("traffic_bytes_per_launch")
+        # a capture counts only while the attention call's sources are the
+        # ones it was taken on
+        for ent in tj.get("entries", []):
+            if (ent.get("config") == args.config and ent.get("index_cache", "native") == args.index_cache
+                    and ent.get("kernel_stamp") == _kernel_stamp()):
+                traffic = ent.get("traffic_bytes_per_launch")
     if prefill:
         # the score call is a contraction: tensor-bound against the peak of
         # its operand type (bf16; an FP8 index cache takes the f8 product,
@@ -492,11 +558,10 @@ def run_gpu(args, rank, world, local_rank):
                     "mean_launch_us": attn_mean_s * 1e6, "peak_source": peak_src}
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        rate, n, dt = oracle_rate(make_workload(args, 1000 + args.config), budget_s=args.cpu_seconds)
-        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": "%d query rows of this workload through the oracle's %s "
-                         "(single-threaded C, fp64), %.1f s" % (n, "score and select stages" if prefill
-                                                               else "three stages", dt)}
+        wc = make_workload(args, 1000 + args.config)
+        cpu = cpu_baseline_record(lambda b, n: oracle_rate(wc, budget_s=b, threads=n),
+                                  "query rows of this workload (the oracle's %s)"
+                                  % ("score and select stages" if prefill else "three stages"), args.cpu_seconds)
     return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -527,22 +592,40 @@ def dense_flops(w):
     return 4 * w.D * w.Hq * n_keys
 
 
-def dense_oracle_rate(w, budget_s=12.0, max_tokens=None):
+def dense_oracle_rate(w, budget_s=12.0, max_tokens=None, threads=1):
     """The oracle on query tokens of the dense workload, one at a time (token
     t under the causal flag is non-causal attention over its first
-    t + S - T + 1 keys); returns (query tokens/s, tokens timed, seconds)."""
+    t + S - T + 1 keys), the longest rows first (a conservative rate), from
+    `threads` host threads as in oracle_rate; returns (query tokens/s, tokens
+    timed, seconds)."""
     import oracle
 
     o = oracle.default()
-    done, t0 = 0, time.perf_counter()
-    for t in range(w.T - 1, -1, -1):  # the longest rows first: a conservative rate
-        n = t + w.S - w.T + 1 if w.causal else w.S
-        o.sdpa(w.q[t:t + 1], w.k[:max(0, n)], w.v[:max(0, n)], float(np.float32(w.sm_scale)), False)
-        done += 1
-        if time.perf_counter() - t0 >= budget_s or (max_tokens and done >= max_tokens):
-            break
+    order = list(range(w.T - 1, -1, -1))
+    lock = threading.Lock()
+    state = {"next": 0, "done": 0}
+    t0 = time.perf_counter()
+
+    def worker():
+        while True:
+            with lock:
+                if (state["next"] >= len(order) or time.perf_counter() - t0 >= budget_s
+                        or (max_tokens and state["next"] >= max_tokens)):
+                    return
+                t = order[state["next"]]
+                state["next"] += 1
+            n = t + w.S - w.T + 1 if w.causal else w.S
+            o.sdpa(w.q[t:t + 1], w.k[:max(0, n)], w.v[:max(0, n)], float(np.float32(w.sm_scale)), False)
+            with lock:
+                state["done"] += 1
+
+    pool = [threading.Thread(target=worker) for _ in range(max(1, threads))]
+    for th in pool:
+        th.start()
+    for th in pool:
+        th.join()
     dt = time.perf_counter() - t0
-    return done / dt, done, dt
+    return state["done"] / dt, state["done"], dt
 
 
 def dense_desc(w):
@@ -557,12 +640,13 @@ def run_dense_reference(args, rank, world):
     if rank != 0:
         return None
     w = W.dense_prefill()
+    cores = host_cores()
     per_step_budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         dense_oracle_rate(w, budget_s=per_step_budget / 4, max_tokens=1)
     rows, secs = 0, 0.0
     for _ in range(args.steps):
-        _, n, dt = dense_oracle_rate(w, budget_s=per_step_budget)
+        _, n, dt = dense_oracle_rate(w, budget_s=per_step_budget, threads=cores)
         rows += n
         secs += dt
     value = rows / secs
@@ -571,9 +655,10 @@ def run_dense_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": dense_desc(w),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": "%d query tokens (all heads) of the chunk through the oracle (single-threaded "
-                                   "C, fp64), %.1f s per step" % (rows, per_step_budget)},
+                                   "C, fp64, called from %d host threads), %.1f s per step"
+                                   % (rows, cores, per_step_budget)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -659,17 +744,15 @@ def run_dense_gpu(args, rank, world, local_rank):
     peak, peak_src = measured_bf16_peak()
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        rate, n, dt = dense_oracle_rate(w, budget_s=args.cpu_seconds)
-        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": "%d query tokens (all heads; the longest rows) of the chunk through the oracle "
-                         "(single-threaded C, fp64), %.1f s" % (n, dt)}
+        cpu = cpu_baseline_record(lambda b, n: dense_oracle_rate(w, budget_s=b, threads=n),
+                                  "query tokens (all heads; the longest rows) of the chunk", args.cpu_seconds)
     return {
         "metric": DENSE_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32 (CUDA-core FMA; bf16 inputs and output)",
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 mma (P bf16), f32 accumulate and softmax",
         "data": "synthetic", "config": dense_desc(w),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None, "kernel": "sdpa_kernel (direct launch)",
+                     "frac": achieved / peak, "traffic": None, "kernel": "sdpa_tc_kernel (direct launch)",
                      "algorithmic_flops_per_launch": flops, "mean_launch_us": mean_s * 1e6,
                      "peak_source": peak_src},
         "cpu_baseline": cpu,
@@ -703,17 +786,28 @@ def prefill_flops(pb):
     return float(2 * pb.Di * pb.Hi * sum(n * L for n, L in prefill_limits(pb)))
 
 
-def prefill_oracle_rate(pb, budget_s=12.0, max_rows=None):
+def prefill_oracle_rate(pb, budget_s=12.0, max_rows=None, threads=1):
     """The oracle on the batch's query blocks, one at a time (each as a batch
     of its own: its tokens, with the block's first position as the prefix),
-    until the budget is spent; returns (query tokens/s, tokens timed, s)."""
+    from `threads` host threads as in oracle_rate, until the budget is spent;
+    returns (query tokens/s, tokens timed, s)."""
     import oracle
 
     o = oracle.default()
     cu, cub, pre = pb.cu_seqlens.tolist(), pb.cu_seqblocks_q.tolist(), pb.prefix_lens.tolist()
-    done, blocks, t0 = 0, 0, time.perf_counter()
-    for b in range(pb.B):
-        for qb in range(cub[b + 1] - cub[b]):
+    work = [(b, qb) for b in range(pb.B) for qb in range(cub[b + 1] - cub[b])]
+    lock = threading.Lock()
+    state = {"next": 0, "done": 0}
+    t0 = time.perf_counter()
+
+    def worker():
+        while True:
+            with lock:
+                if (state["next"] >= len(work) or time.perf_counter() - t0 >= budget_s
+                        or (max_rows and state["next"] >= max_rows)):
+                    return
+                b, qb = work[state["next"]]
+                state["next"] += 1
             lo = cu[b] + qb * pb.block_size_q
             hi = min(lo + pb.block_size_q, cu[b + 1])
             o.prefill_topk(pb.q_idx[lo:hi], pb.k_idx_cache, pb.block_table, pb.slot_ids[b:b + 1],
@@ -721,13 +815,16 @@ def prefill_oracle_rate(pb, budget_s=12.0, max_rows=None):
                            torch.tensor([pre[b] + qb * pb.block_size_q], dtype=torch.int32),
                            torch.tensor([0, 1], dtype=torch.int32), pb.block_size_q, pb.init_blocks,
                            pb.local_blocks, float(np.float32(pb.scale)), 1, pb.topk)
-            done += hi - lo
-            blocks += 1
-            if time.perf_counter() - t0 >= budget_s or (max_rows and blocks >= max_rows):
-                dt = time.perf_counter() - t0
-                return done / dt, done, dt
+            with lock:
+                state["done"] += hi - lo
+
+    pool = [threading.Thread(target=worker) for _ in range(max(1, threads))]
+    for th in pool:
+        th.start()
+    for th in pool:
+        th.join()
     dt = time.perf_counter() - t0
-    return done / dt, done, dt
+    return state["done"] / dt, state["done"], dt
 
 
 def prefill_desc(pb):
@@ -744,12 +841,13 @@ def run_prefill_reference(args, rank, world):
     if rank != 0:
         return None
     pb = W.prefill_batch()
+    cores = host_cores()
     per_step_budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         prefill_oracle_rate(pb, budget_s=per_step_budget / 4, max_rows=1)
     rows, secs = 0, 0.0
     for _ in range(args.steps):
-        _, n, dt = prefill_oracle_rate(pb, budget_s=per_step_budget)
+        _, n, dt = prefill_oracle_rate(pb, budget_s=per_step_budget, threads=cores)
         rows += n
         secs += dt
     value = rows / secs
@@ -758,9 +856,10 @@ def run_prefill_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": prefill_desc(pb),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": "%d query tokens (whole query blocks) through the oracle (single-threaded "
-                                   "C, fp64), %.1f s per step" % (rows, per_step_budget)},
+                                   "C, fp64, called from %d host threads), %.1f s per step"
+                                   % (rows, cores, per_step_budget)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -847,10 +946,8 @@ def run_prefill_gpu(args, rank, world, local_rank):
     peak, peak_src = measured_bf16_peak()
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        rate, n, dt = prefill_oracle_rate(pb, budget_s=args.cpu_seconds)
-        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": "%d query tokens (whole query blocks) of the batch through the oracle "
-                         "(single-threaded C, fp64), %.1f s" % (n, dt)}
+        cpu = cpu_baseline_record(lambda b, n: prefill_oracle_rate(pb, budget_s=b, threads=n),
+                                  "query tokens (whole query blocks) of the batch", args.cpu_seconds)
     return {
         "metric": PREFILL_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -884,9 +981,10 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=lambda c: c if c in ("dense", "prefill") else int(c), default=2,
+    ap.add_argument("--config", type=lambda c: c if c in ("dense", "prefill") else int(c), default=5,
                     choices=[2, 3, 4, 5, "dense", "prefill"],
-                    help="workload (2 = EAGLE-style verification decode, the metric's workload; "
+                    help="workload (5 = stress sparse decode, the headline; 2 = EAGLE-style verification "
+                         "decode; 3 = dense paged decode; 4 = batched prefill score-to-selection; "
                          "dense = the dense-attention prefill chunk; prefill = the fused prefill "
                          "score-to-selection call)")
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
@@ -913,7 +1011,11 @@ def main():
     if world > 1:
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group(backend="nccl")
-    res = gpu_arm(args, rank, world, local_rank)
+    try:
+        res = gpu_arm(args, rank, world, local_rank)
+    except TimedOutWait as e:
+        print("bench: %s" % e, file=sys.stderr, flush=True)
+        sys.exit(3)
     if res is not None:
         print(json.dumps(res), flush=True)
     if world > 1:

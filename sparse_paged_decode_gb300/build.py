@@ -10,6 +10,7 @@ import concurrent.futures as cf
 import glob
 import hashlib
 import os
+import re
 import shutil
 import subprocess
 
@@ -42,16 +43,26 @@ def _sources():
 ATTENTION_SOURCES = ("attention_tc.cu", "plan.cu", "plan.cuh", "spd_internal.cuh", "tc_ptx.cuh", "tmap.cuh")
 
 
+def _code_only(text: bytes) -> bytes:
+    """C/C++ source without its comments and blank-line differences: what
+    the compiler sees, so a comment edit does not change a kernel stamp."""
+    t = text.decode("utf-8", errors="replace")
+    t = re.sub(r"/\*.*?\*/", " ", t, flags=re.S)
+    t = re.sub(r"//[^\n]*", "", t)
+    lines = [ln.rstrip() for ln in t.splitlines()]
+    return "\n".join(ln for ln in lines if ln).encode()
+
+
 def _stamp(names=None) -> str:
-    """Hash of the sources (all of them, or the named files of csrc) and the
-    compiler flags."""
+    """Hash of the sources (all of them, or -- comments stripped -- the named
+    files of csrc) and the compiler flags."""
     h = hashlib.sha256()
     paths = (sorted(glob.glob(os.path.join(CSRC, "*")) + [os.path.join(INCLUDE, "spd.h")]) if names is None
              else [os.path.join(CSRC, n) for n in sorted(names)])
     for path in paths:
         with open(path, "rb") as f:
             h.update(os.path.basename(path).encode())
-            h.update(f.read())
+            h.update(f.read() if names is None else _code_only(f.read()))
     # flags with the checkout's own paths made relative: the same sources
     # stamp the same on every machine
     flags = [os.path.relpath(f, ROOT) if f.startswith(ROOT) else f for f in ARCH + NVCC_FLAGS]

@@ -68,3 +68,16 @@ def test_reference_arms_run_on_rank_zero_only():
     args = types.SimpleNamespace(steps=1, warmup=3, config=2, index_cache="native", cpu_seconds=1.0)
     for arm in (bench.run_reference, bench.run_dense_reference, bench.run_prefill_reference):
         assert arm(args, 1, 2) is None
+
+
+def test_oracle_rate_threads_take_disjoint_rows():
+    """The CPU baseline's threaded oracle: each row is taken once, and with a
+    budget large enough every non-padding row of the workload is done."""
+    w = W.make_decode("rate", lengths=[300, 129, 0], tokens_per_request=[2, 1, 1], Hq=8, Hkv=2, D=64, Di=32, NB=4,
+                      P=16, K=2, seed=5, dtype=torch.float32)
+    n_valid = int((w.seq_lens > 0).sum())
+    rate, done, dt = bench.oracle_rate(w, budget_s=60.0, threads=3)
+    assert done == n_valid and rate > 0 and dt > 0
+    rate1, done1, _ = bench.oracle_rate(w, budget_s=60.0, max_rows=2, threads=1)
+    assert done1 == 2 and rate1 > 0
+    assert bench.host_cores() >= 1

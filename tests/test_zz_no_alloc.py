@@ -4,13 +4,12 @@ scratch instead of a caller workspace).
 
 It must give the same result as paged_sparse_decode_attention on the same
 inputs, call after call, while the built-in scratch keeps the previous call's
-contents.  This file is collected last on purpose.
+contents.  Both entry points run the same kernels on the same inputs, so the
+outputs must agree bit for bit.  This file is collected last on purpose.
 """
 import numpy as np
 import pytest
 import torch
-
-from parity import check_attention
 
 pytestmark = pytest.mark.gpu
 BS = 128
@@ -19,14 +18,18 @@ BS = 128
 def _run_both(spd, g, w, topk):
     dev = g.q.device
     ref = torch.full((w.T, w.Hq, w.D), float("nan"), dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(spd.decode_workspace_bytes(w.T, w.Hq, w.Hkv, w.D, w.NB), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(spd.decode_workspace_bytes(w.T, w.Hq, w.Hkv, w.D, w.NB), dtype=torch.uint8, device=dev)
     spd.paged_sparse_decode_attention(g.q, g.k_cache, g.v_cache, g.block_table, g.seq_lens, g.req_idx, topk, ref,
                                       g.sm_scale, BS, g.k_scale, g.v_scale, ws)
     got = torch.full_like(ref, float("nan"))
     spd.paged_sparse_decode_attention_noalloc(g.q, g.k_cache, g.v_cache, g.block_table, g.seq_lens, g.req_idx,
                                               topk, got, g.sm_scale, BS, g.k_scale, g.v_scale)
     torch.cuda.synchronize()
-    return got.float().cpu().numpy(), ref.float().cpu().numpy()
+    # neither call saw a device-side wait time out: the workspace's status
+    # word, and the built-in scratch's (workspace None)
+    assert spd.workspace_status(ws) == 0
+    assert spd.workspace_status(None) == 0
+    return got.cpu(), ref.cpu()
 
 
 def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
@@ -48,8 +51,9 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
         topk = torch.stack([torch.randperm(w.NB, generator=gen)[:w.K] for _ in range(w.T)]).to(torch.int32)
         topk = topk.view(1, w.T, w.K).to(dev).expand(w.Hkv, -1, -1)
         got, ref = _run_both(spd, g, w, topk)
-        assert np.all(np.isfinite(got)), "unwritten output cells"
-        check_attention(got, ref, "noalloc vs workspace entry point")
+        assert torch.isfinite(ref.float()).all(), "unwritten output cells"
+        assert np.array_equal(got.view(torch.int16).numpy(), ref.view(torch.int16).numpy()), \
+            "noalloc output differs from the workspace entry point's (bits)"
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():

@@ -104,7 +104,8 @@ def workload_desc(w):
         "tokens_per_request": w.tokens_per_request, "request_lengths": w.request_lengths,
         "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.D, "index_heads": w.Hi, "index_dim": w.Di,
         "block_size": w.block_size, "page_table_blocks": w.NB, "pool_pages": w.P, "top_k": w.K,
-        "kv_dtype": "e4m3 (static scalar scales)" if w.k_cache is not None else None,
+        "kv_dtype": (None if w.k_cache is None else "e4m3 (static scalar scales)"
+                     if w.k_cache.dtype == torch.float8_e4m3fn else "bfloat16 (dense)"),
         "q_dtype": str(w.q.dtype).replace("torch.", "") if w.q is not None else None,
         "index_dtype": str(w.q_idx.dtype).replace("torch.", "") if w.q_idx is not None else None,
         "index_cache_dtype": (str(w.k_idx_cache.dtype).replace("torch.", "")
@@ -137,7 +138,7 @@ def attention_bytes(w, topk_np):
                         blocks.add(b)
             for b in blocks:
                 valid = min(BS, min(L, w.NB * BS) - b * BS)
-                kv += 2 * valid * w.D
+                kv += 2 * valid * w.D * w.k_cache.element_size()
     q_bytes = w.q.numel() * w.q.element_size()
     out_bytes = w.T * w.Hq * w.D * 2
     tk_bytes = 0 if topk_np is None else w.T * w.K * 4
@@ -297,7 +298,7 @@ def job_rate(rows_per_rank, world, steps, total_ms):
 def make_workload(args, seed):
     """The configuration's batch; with --index-cache e4m3 its index cache is
     stored as FP8-E4M3 (scale folded into idx_scale)."""
-    w = W.config(args.config, seed=seed)
+    w = W.config(args.config, seed=seed, kv_dtype=args.kv_cache)
     return W.with_fp8_index(w) if args.index_cache == "e4m3" and w.k_idx_cache is not None else w
 
 
@@ -529,7 +530,7 @@ def run_gpu(args, rank, world, local_rank):
         # ones it was taken on
         for ent in tj.get("entries", []):
             if (ent.get("config") == args.config and ent.get("index_cache", "native") == args.index_cache
-                    and ent.get("kernel_stamp") == _kernel_stamp()):
+                    and ent.get("kv_cache", "e4m3") == args.kv_cache and ent.get("kernel_stamp") == _kernel_stamp()):
                 traffic = ent.get("traffic_bytes_per_launch")
     if prefill:
         # the score call is a contraction: tensor-bound against the peak of
@@ -552,7 +553,8 @@ def run_gpu(args, rank, world, local_rank):
         peak, peak_src = measured_peaks()
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                     "traffic": traffic,
-                    "kernel": "paged attention call (list, unit and attention kernels; %s)"
+                    "kernel": ("paged attention call (list, unit and attention kernels; %s)"
+                               if args.kv_cache == "e4m3" else "paged attention call (general-layout kernel; %s)")
                               % ("graph replay" if graph is not None else "direct launches"),
                     "algorithmic_bytes_per_launch": abytes,
                     "mean_launch_us": attn_mean_s * 1e6, "peak_source": peak_src}
@@ -567,7 +569,10 @@ def run_gpu(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": (("e4m3 mma (index queries as two e4m3 terms)" if args.index_cache == "e4m3" else "bf16 mma")
-                  + ", f32 accumulate") if prefill else "e4m3/f16 mma, f32 accumulate", "data": "synthetic",
+                  + ", f32 accumulate") if prefill else ("e4m3/f16 mma, f32 accumulate"
+                                                          if w.k_cache.dtype == torch.float8_e4m3fn
+                                                          else "f32 (CUDA-core FMA over bf16 K/V)"),
+        "data": "synthetic",
         "config": workload_desc(w),
         "roofline": roofline,
         "cpu_baseline": cpu,
@@ -993,6 +998,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="launch each call directly instead of replaying a graph")
     ap.add_argument("--index-cache", default="native", choices=["native", "e4m3"],
                     help="index cache as generated (bf16) or stored FP8-E4M3")
+    ap.add_argument("--kv-cache", default="e4m3", choices=["e4m3", "bf16"],
+                    help="K/V cache as FP8-E4M3 with static scalar scales (default) or dense BF16")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

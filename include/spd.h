@@ -141,9 +141,11 @@ SPD_API void msa_select_topk(const spd_tensor *scores, const spd_tensor *topk_id
  * Stage 3 -- paged sparse GQA decode attention.
  * "Kernel ABI" -- attention.decode: a query row reads the given block ids
  * that are >= 0 and nothing else; a -1 id selects nothing, and keys at
- * positions >= seq_lens are left out.  "Kernel ABI" -- attention.sdpa: Hq divisible by
- * Hkv; q head g reads kv head g / (Hq / Hkv).  "MiniMax-M3 decode through the
- * ATOM kernel library" -- static scalar K/V scales on FP8 caches.
+ * positions >= seq_lens are left out; the K/V tensors are described at this
+ * boundary, dense BF16 for the commissioned cache.  "Kernel ABI" --
+ * attention.sdpa: Hq divisible by Hkv; q head g reads kv head g / (Hq / Hkv).
+ * "MiniMax-M3 decode through the ATOM kernel library" -- static scalar K/V
+ * scales on FP8 caches.
  *
  *   z_tau = sm_scale * k_scale * (q[t][g] . k_cache[slot(tau)][h])
  *   out[t][g] = sum_tau softmax(z)_tau * v_scale * v_cache[slot(tau)][h]
@@ -154,8 +156,10 @@ SPD_API void msa_select_topk(const spd_tensor *scores, const spd_tensor *topk_id
  * rounded to bf16 (nearest even).
  *
  * q          [T, Hq, D] f32 | bf16 | f16
- * k_cache    [P*128, Hkv, D] e4m3 } innermost stride 1
- * v_cache    [P*128, Hkv, D] e4m3 } same shape as k_cache
+ * k_cache    [P*128, Hkv, D] e4m3 | bf16 } innermost stride 1
+ * v_cache    [P*128, Hkv, D] the dtype and shape of k_cache
+ *            (the scales multiply the decoded values either way; pass 1.0
+ *            for a BF16 cache stored unscaled)
  * block_table [R, NB] i32, seq_lens [T] i32, req_idx [T] i32 (see above)
  * topk_idx   [Hkv, T, K] i32; a stride of 0 on dim 0 shares one selection
  *            across kv heads (the usual case: one index head)

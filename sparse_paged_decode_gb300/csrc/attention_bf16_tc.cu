@@ -1,0 +1,689 @@
+// attention_bf16_tc.cu -- paged sparse / dense GQA decode attention over a
+// dense BF16 K/V cache ("Kernel ABI" -- attention.decode: the K/V tensors are
+// described at the boundary, dense BF16 for the commissioned cache) on the
+// sm_103a tensor cores, for bf16 queries of head dim 128.
+//
+// Work comes from the same device planner as the FP8 kernel (plan.cu): a
+// group of consecutive query rows of one request (up to 128 / G tokens) and
+// one kv head form a pair whose block list is the union of the rows'
+// selections; lists are cut into units, a persistent grid claims units from
+// the work counter, and a pair split over several units leaves fp32 partials
+// that the last unit to finish merges (an atomic ticket, no waiting).
+//
+// Per unit the query rows (token j, head g -> row j * G + g) lie on the M = 128
+// rows of the MMA, keys on N, as in a prefill flash kernel:
+//   S  = Q K^T       kind::f16 bf16, M = 128 rows, N = 128 keys of one page,
+//                    K = 128 dims, double-buffered in tensor memory
+//   P  = 2^(S c - m) one thread per row: the row's logits stay in its
+//                    registers (block max, sum, offset raise need no exchange)
+//   O += P V         kind::f16 bf16, P from shared memory, V as TMA loaded it
+// K and V pages are TMA-gathered straight from the paged cache through the
+// block list (two 64-dim boxes of 128 slots each, 128-byte swizzle).  A row's
+// keys in a block are those below its key limit, and none if the row did not
+// select the block.  c = sm_scale * k_scale * log2(e); the exponent offset of
+// a row is raised only when a block maximum exceeds it by more than 2^kRaise,
+// so p <= 2^kRaise fits bf16.
+//
+// Roles (6 warps): warp 0 claims units and issues the TMA loads, warp 1 owns
+// tensor memory and issues every MMA, warps 2-5 run the softmax and the unit
+// epilogue (warp w reads TMEM lanes 32 (w % 4) .. +31).  Q is double-buffered
+// by unit so the next unit's queries load under this unit's blocks.  Every
+// wait is bounded: a wait that gives up sets bit 0 of the workspace status
+// word and the CTA winds down.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "plan.cuh"
+#include "spd_internal.cuh"
+#include "tc_ptx.cuh"
+#include "tmap.cuh"
+
+namespace spd {
+
+cudaError_t launch_attention_bf16_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cudaStream_t stream, bool *used);
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kM = 128;         // query rows of a unit (padded)
+constexpr int kKeys = 128;      // keys per page
+constexpr int kThreads = 192;   // warp 0 TMA, 1 MMA, 2-5 softmax / epilogue
+constexpr int kSoftThreads = 128;
+constexpr int kBox = 128 * 128; // 128 rows x 64 bf16 dims
+constexpr int kTile = 2 * kBox; // 128 rows x 128 dims
+constexpr float kRaise = 8.0f;
+constexpr int kStride = kD + kPartialStride;  // floats per partial row
+
+constexpr int kOffQ = 0;                  // two unit buffers
+constexpr int kOffK = kOffQ + 2 * kTile;  // two stages
+constexpr int kOffV = kOffK + 2 * kTile;  // two stages
+constexpr int kOffP = kOffV + 2 * kTile;
+constexpr int kOffBar = kOffP + kTile;
+
+struct Shared {
+    uint64_t unit_full[4], unit_empty[4];
+    uint64_t q_full[2], q_empty[2];
+    uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+    uint64_t s_full[2], s_free[2];
+    uint64_t p_full, pv_done, o_free, drain;
+    PlanUnit ring[4];
+    uint32_t tmem_base;
+    int abort;
+    int last;     // the unit that took the last ticket of its pair merges
+    int Lj[16];   // key limit of each token of the current unit
+};
+
+constexpr int kSmemBytes = kOffBar + static_cast<int>(sizeof(Shared)) + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+// tensor memory: S buffers at columns 0 and 128, O at 256
+constexpr uint32_t kColS = 0, kColO = 256, kTmemCols = 512;
+// a unit record is released by the MMA issuer and the softmax threads
+constexpr uint32_t kUnitArrivals = 1 + kSoftThreads;
+
+struct Bf16Args {
+    const int32_t *ri;
+    int64_t ri_s0;
+    const int32_t *sl;
+    int64_t sl_s0;
+    __nv_bfloat16 *out;
+    int64_t o_s0, o_s1, o_s2;
+    int32_t T, Hq, Hkv, G, R, NB, gmax;
+    float c;  // sm_scale * k_scale * log2(e)
+    float v_scale;
+    char *ws;
+    PlanLayout lay;
+};
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+}
+
+__device__ __forceinline__ bool aborted(Shared &sh) { return *reinterpret_cast<volatile int *>(&sh.abort) != 0; }
+
+__device__ __forceinline__ void set_abort(Shared &sh, int32_t *status) {
+    *reinterpret_cast<volatile int *>(&sh.abort) = 1;
+    atomicOr(status, 1);
+}
+
+__device__ __forceinline__ bool wait_or_abort(Shared &sh, uint64_t *bar, uint32_t parity, int32_t *status) {
+    if (tc::mbar_wait(bar, parity)) return true;
+    set_abort(sh, status);
+    return false;
+}
+
+// Warp-uniform wait: the warp goes on only if every lane saw the phase.
+__device__ __forceinline__ bool warp_wait(Shared &sh, uint64_t *bar, uint32_t parity, int32_t *status) {
+    const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(bar, parity));
+    if (!ok) set_abort(sh, status);
+    return ok;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// softmax threads only (warps 2-5)
+__device__ __forceinline__ void soft_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__global__ void __launch_bounds__(kThreads, 1)
+attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                         const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ Bf16Args a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Shared &sh = *reinterpret_cast<Shared *>(smem + kOffBar);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    PlanHeader *hdr = reinterpret_cast<PlanHeader *>(a.ws + a.lay.header);
+    const PlanEntry *lists = reinterpret_cast<const PlanEntry *>(a.ws + a.lay.lists);
+    const PlanUnit *units = reinterpret_cast<const PlanUnit *>(a.ws + a.lay.units);
+    int32_t *status = &hdr->status;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 4; ++i) {
+            tc::mbar_init(&sh.unit_full[i], 1);
+            tc::mbar_init(&sh.unit_empty[i], kUnitArrivals);
+        }
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&sh.q_full[i], 1);
+            tc::mbar_init(&sh.q_empty[i], 1);
+            tc::mbar_init(&sh.k_full[i], 1);
+            tc::mbar_init(&sh.k_empty[i], 1);
+            tc::mbar_init(&sh.v_full[i], 1);
+            tc::mbar_init(&sh.v_empty[i], 1);
+            tc::mbar_init(&sh.s_full[i], 1);
+            tc::mbar_init(&sh.s_free[i], kSoftThreads);
+        }
+        tc::mbar_init(&sh.p_full, kSoftThreads);
+        tc::mbar_init(&sh.pv_done, 1);
+        tc::mbar_init(&sh.o_free, kSoftThreads);
+        tc::mbar_init(&sh.drain, 1);
+        sh.abort = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) tc::tmem_alloc(&sh.tmem_base, kTmemCols);
+    if (threadIdx.x == 32) {
+        tc::prefetch_tmap(&tmap_q);
+        tc::prefetch_tmap(&tmap_k);
+        tc::prefetch_tmap(&tmap_v);
+    }
+    // the prologue overlaps the planner; global memory only after this wait
+    tc::pdl_wait();
+    tc::pdl_trigger();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const int n_units = hdr->n_units;
+            const uint64_t policy = tc::policy_evict_first();
+            const uint32_t qbytes = static_cast<uint32_t>(2 * 64 * 2 * a.G * a.gmax);
+            uint32_t uc = 0, gb = 0;     // units and blocks claimed by this CTA
+            uint32_t nq = 0, nk = 0, nv = 0;  // Q, K and V loads issued
+            for (;;) {
+                PlanUnit un{};
+                un.pair = -1;
+                if (!aborted(sh)) {
+                    const int uu = atomicAdd(&hdr->next_unit, 1);
+                    if (uu < n_units) un = units[uu];
+                }
+                const int slot = uc & 3;
+                if (uc >= 4 && !wait_or_abort(sh, &sh.unit_empty[slot], ((uc >> 2) - 1) & 1, status)) un.pair = -1;
+                sh.ring[slot] = un;
+                tc::mbar_arrive(&sh.unit_full[slot]);
+                if (un.pair < 0) break;
+                const int qb = uc & 1;
+                if (uc >= 2 && !wait_or_abort(sh, &sh.q_empty[qb], ((uc >> 1) - 1) & 1, status)) break;
+                uint8_t *sQ = smem + kOffQ + qb * kTile;
+                tc::mbar_arrive_expect_tx(&sh.q_full[qb], qbytes);
+                tc::tma_load_3d(sQ, &tmap_q, &sh.q_full[qb], 0, un.h * a.G, un.t0);
+                tc::tma_load_3d(sQ + kBox, &tmap_q, &sh.q_full[qb], 64, un.h * a.G, un.t0);
+                ++nq;
+                ++uc;
+                bool ok = true;
+                for (int i = 0; i < un.count; ++i, ++gb) {
+                    const PlanEntry e = lists[un.entry + i];
+                    const int st = gb & 1;
+                    const uint32_t ph = ((gb >> 1) - 1) & 1;
+                    if (gb >= 2 && !(ok = wait_or_abort(sh, &sh.k_empty[st], ph, status))) break;
+                    uint8_t *sK = smem + kOffK + st * kTile;
+                    tc::mbar_arrive_expect_tx(&sh.k_full[st], kTile);
+                    tc::tma_load_3d(sK, &tmap_k, &sh.k_full[st], 0, un.h, e.page * kKeys, policy);
+                    tc::tma_load_3d(sK + kBox, &tmap_k, &sh.k_full[st], 64, un.h, e.page * kKeys, policy);
+                    ++nk;
+                    if (gb >= 2 && !(ok = wait_or_abort(sh, &sh.v_empty[st], ph, status))) break;
+                    uint8_t *sV = smem + kOffV + st * kTile;
+                    tc::mbar_arrive_expect_tx(&sh.v_full[st], kTile);
+                    tc::tma_load_3d(sV, &tmap_v, &sh.v_full[st], 0, un.h, e.page * kKeys, policy);
+                    tc::tma_load_3d(sV + kBox, &tmap_v, &sh.v_full[st], 64, un.h, e.page * kKeys, policy);
+                    ++nv;
+                }
+                if (!ok) break;
+            }
+            // every issued copy lands before the CTA may exit (the last
+            // phase of each barrier is the only one still pending)
+            for (uint32_t q = (nq > 2 ? nq - 2 : 0); q < nq; ++q) tc::mbar_wait(&sh.q_full[q & 1], (q >> 1) & 1);
+            for (uint32_t b = (nk > 2 ? nk - 2 : 0); b < nk; ++b) tc::mbar_wait(&sh.k_full[b & 1], (b >> 1) & 1);
+            for (uint32_t b = (nv > 2 ? nv - 2 : 0); b < nv; ++b) tc::mbar_wait(&sh.v_full[b & 1], (b >> 1) & 1);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_s = tc::idesc_f16_m128(kKeys, true);
+            const uint32_t idesc_o = tc::idesc_f16_m128(kD, true) | (1u << 16);  // B (V) MN-major
+            const uint32_t aP = tc::smem_u32(smem + kOffP);
+            uint32_t uc = 0, gb = 0;
+            bool ok = true;
+            while (ok) {
+                const int slot = uc & 3;
+                if (!wait_or_abort(sh, &sh.unit_full[slot], (uc >> 2) & 1, status)) break;
+                const PlanUnit un = sh.ring[slot];
+                tc::mbar_arrive(&sh.unit_empty[slot]);
+                if (un.pair < 0) break;
+                const int qb = uc & 1;
+                if (!wait_or_abort(sh, &sh.q_full[qb], (uc >> 1) & 1, status)) break;
+                tc::tc_fence_after();
+                const uint32_t aQ = tc::smem_u32(smem + kOffQ + qb * kTile);
+                for (int i = 0; ok && i <= un.count; ++i) {
+                    if (i < un.count) {
+                        const uint32_t b = gb + i;
+                        const int st = b & 1;
+                        ok = wait_or_abort(sh, &sh.k_full[st], (b >> 1) & 1, status);
+                        if (ok && b >= 2) ok = wait_or_abort(sh, &sh.s_free[st], ((b >> 1) - 1) & 1, status);
+                        if (!ok) break;
+                        tc::tc_fence_after();
+                        const uint32_t aK = tc::smem_u32(smem + kOffK + st * kTile);
+#pragma unroll
+                        for (int ks = 0; ks < kD / 16; ++ks) {
+                            const uint32_t off = (ks >> 2) * kBox + (ks & 3) * 32;
+                            tc::mma_f16(tmem + kColS + st * kKeys, tc::smem_desc(aQ + off, 16, 1024, tc::kSw128),
+                                        tc::smem_desc(aK + off, 16, 1024, tc::kSw128), idesc_s, ks > 0);
+                        }
+                        tc::mma_commit(&sh.s_full[st]);
+                        tc::mma_commit(&sh.k_empty[st]);
+                        if (i + 1 == un.count) tc::mma_commit(&sh.q_empty[qb]);
+                    }
+                    if (i >= 1) {
+                        const uint32_t b = gb + i - 1;
+                        const int st = b & 1;
+                        ok = wait_or_abort(sh, &sh.p_full, b & 1, status) &&
+                             wait_or_abort(sh, &sh.v_full[st], (b >> 1) & 1, status);
+                        // the first product of a unit overwrites O: the previous
+                        // unit's epilogue must have read it
+                        if (ok && i == 1 && uc >= 1) ok = wait_or_abort(sh, &sh.o_free, (uc - 1) & 1, status);
+                        if (!ok) break;
+                        tc::tc_fence_after();
+                        const uint32_t aV = tc::smem_u32(smem + kOffV + st * kTile);
+#pragma unroll
+                        for (int ks = 0; ks < kKeys / 16; ++ks) {
+                            const uint32_t offp = (ks >> 2) * kBox + (ks & 3) * 32;
+                            tc::mma_f16(tmem + kColO, tc::smem_desc(aP + offp, 16, 1024, tc::kSw128),
+                                        tc::smem_desc(aV + ks * 2048, kBox, 1024, tc::kSw128), idesc_o,
+                                        i > 1 || ks > 0);
+                        }
+                        tc::mma_commit(&sh.pv_done);
+                        tc::mma_commit(&sh.v_empty[st]);
+                    }
+                }
+                if (un.count == 0) tc::mma_commit(&sh.q_empty[qb]);
+                gb += un.count;
+                ++uc;
+            }
+            tc::mma_commit(&sh.drain);
+            tc::mbar_wait(&sh.drain, 0);
+        }
+    } else {
+        // --------------------------------------------- softmax and epilogue
+        const int st_id = threadIdx.x - 64;  // 0..127
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;  // row of the unit = TMEM lane
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        uint8_t *prow = smem + kOffP + r * 128;
+        const uint32_t sw = static_cast<uint32_t>(r & 7);
+        int32_t *counters = reinterpret_cast<int32_t *>(a.ws + a.lay.counters);
+        float *partials = reinterpret_cast<float *>(a.ws + a.lay.partials);
+        uint32_t uc = 0, gb = 0;
+        bool ok = true;
+        while (ok) {
+            const int slot = uc & 3;
+            ok = warp_wait(sh, &sh.unit_full[slot], (uc >> 2) & 1, status);
+            if (!ok) break;
+            const PlanUnit un = sh.ring[slot];
+            tc::mbar_arrive(&sh.unit_empty[slot]);
+            if (un.pair < 0) break;
+            const int rows = un.nt * a.G;
+            const bool active = r < rows;
+            const bool warp_active = __any_sync(0xffffffffu, active);
+            const int j = active ? r / a.G : 0, g = active ? r % a.G : 0;
+            int row_r;
+            const int L = active ? static_cast<int>(token_limit(a.ri, a.ri_s0, a.sl, a.sl_s0, un.t0 + j, a.R, a.NB,
+                                                                &row_r))
+                                 : 0;
+            // the unit's key limits, for the V rows no row of the unit may read
+            soft_sync();  // every thread is done with the previous unit's limits
+            if (st_id < un.nt) {
+                int rr;
+                sh.Lj[st_id] = static_cast<int>(
+                    token_limit(a.ri, a.ri_s0, a.sl, a.sl_s0, un.t0 + st_id, a.R, a.NB, &rr));
+            }
+            soft_sync();
+            int Lmin = 0x7fffffff;
+            for (int jj = 0; jj < un.nt; ++jj) Lmin = min(Lmin, sh.Lj[jj]);
+            float m_run = -INFINITY, l = 0.f;
+            PlanEntry e_next{};
+            if (un.count > 0) e_next = lists[un.entry];
+            for (int i = 0; i < un.count; ++i) {
+                const uint32_t b = gb + i;
+                const int sb = b & 1;
+                const PlanEntry e = e_next;
+                if (i + 1 < un.count) e_next = lists[un.entry + i + 1];
+                const bool sel = active && ((e.mask >> j) & 1);
+                const int lim = sel ? min(kKeys, max(0, L - static_cast<int>(e.block) * kKeys)) : 0;
+                ok = warp_wait(sh, &sh.s_full[sb], (b >> 1) & 1, status);
+                if (!ok) break;
+                tc::tc_fence_after();
+                float s[kKeys];
+                if (warp_active) {
+#pragma unroll
+                    for (int ch = 0; ch < kKeys / 32; ++ch) tmem_ld32(tmem + lane_base + kColS + sb * kKeys + ch * 32, s + ch * 32);
+                    tc::tmem_wait_ld();
+                }
+                tc::tc_fence_before();
+                tc::mbar_arrive(&sh.s_free[sb]);
+                uint32_t pk[kKeys / 2];
+                float alpha = 1.f;
+                if (warp_active) {
+                    if (lim < kKeys) {
+#pragma unroll
+                        for (int k = 0; k < kKeys; ++k)
+                            if (k >= lim) s[k] = -INFINITY;
+                    }
+                    float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+                    if (a.c >= 0.f) {
+#pragma unroll
+                        for (int k = 0; k < kKeys; k += 4) {
+                            mx0 = fmaxf(mx0, s[k]);
+                            mx1 = fmaxf(mx1, s[k + 1]);
+                            mx2 = fmaxf(mx2, s[k + 2]);
+                            mx3 = fmaxf(mx3, s[k + 3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < kKeys; k += 4) {
+                            mx0 = fmaxf(mx0, s[k] == -INFINITY ? -INFINITY : -s[k]);
+                            mx1 = fmaxf(mx1, s[k + 1] == -INFINITY ? -INFINITY : -s[k + 1]);
+                            mx2 = fmaxf(mx2, s[k + 2] == -INFINITY ? -INFINITY : -s[k + 2]);
+                            mx3 = fmaxf(mx3, s[k + 3] == -INFINITY ? -INFINITY : -s[k + 3]);
+                        }
+                    }
+                    const float mraw = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+                    const float bm = (mraw == -INFINITY) ? -INFINITY : mraw * fabsf(a.c);
+                    if (bm != -INFINITY && (m_run == -INFINITY || bm > m_run + kRaise)) {
+                        alpha = (m_run == -INFINITY) ? 0.f : tc::ex2(m_run - bm);
+                        m_run = bm;
+                        l *= alpha;
+                    }
+                    const float m_eff = (m_run == -INFINITY) ? 0.f : m_run;
+                    if (lim >= kKeys) {
+#pragma unroll
+                        for (int k = 0; k < kKeys; k += 2) {
+                            const float p0 = tc::ex2(fmaf(s[k], a.c, -m_eff));
+                            const float p1 = tc::ex2(fmaf(s[k + 1], a.c, -m_eff));
+                            l += p0 + p1;
+                            pk[k / 2] = pack_bf16(p0, p1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < kKeys; k += 2) {
+                            const float p0 = (k < lim) ? tc::ex2(fmaf(s[k], a.c, -m_eff)) : 0.f;
+                            const float p1 = (k + 1 < lim) ? tc::ex2(fmaf(s[k + 1], a.c, -m_eff)) : 0.f;
+                            l += p0 + p1;
+                            pk[k / 2] = pack_bf16(p0, p1);
+                        }
+                    }
+                }
+                // V rows past every row's limit (the tail of a request's last
+                // page: slots that may hold anything, NaN included) become
+                // zeros, so that 0-weight keys add exactly nothing
+                const int bstart = static_cast<int>(e.block) * kKeys;
+                if (bstart + kKeys > Lmin) {
+                    int vlim = 0;
+                    for (int jj = 0; jj < un.nt; ++jj)
+                        if ((e.mask >> jj) & 1) vlim = max(vlim, min(kKeys, sh.Lj[jj] - bstart));
+                    if (vlim < kKeys) {
+                        ok = warp_wait(sh, &sh.v_full[sb], (b >> 1) & 1, status);
+                        if (!ok) break;
+                        if (r >= vlim) {
+                            uint8_t *vrow = smem + kOffV + sb * kTile + r * 128;
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                reinterpret_cast<uint4 *>(vrow)[q] = make_uint4(0u, 0u, 0u, 0u);
+                                reinterpret_cast<uint4 *>(vrow + kBox)[q] = make_uint4(0u, 0u, 0u, 0u);
+                            }
+                            tc::fence_proxy_async();
+                        }
+                    }
+                }
+                // P is free once the previous block's product is done (it
+                // may belong to the previous unit)
+                if (b >= 1) {
+                    ok = warp_wait(sh, &sh.pv_done, (b - 1) & 1, status);
+                    if (!ok) break;
+                    tc::tc_fence_after();
+                }
+                if (warp_active) {
+                    // O holds this unit's earlier blocks: rescale rows whose
+                    // offset moved (the first block of a unit overwrites O)
+                    if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                        for (int ch = 0; ch < kD / 32; ++ch) {
+                            float o[32];
+                            const uint32_t ta = tmem + lane_base + kColO + ch * 32;
+                            tmem_ld32(ta, o);
+                            tc::tmem_wait_ld();
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) o[k] *= alpha;
+                            tmem_st32(ta, o);
+                        }
+                        tc::tmem_wait_st();
+                    }
+#pragma unroll
+                    for (int cidx = 0; cidx < 16; ++cidx) {
+                        const int half = cidx >> 3, chunk = cidx & 7;
+                        uint4 w;
+                        w.x = pk[cidx * 4 + 0];
+                        w.y = pk[cidx * 4 + 1];
+                        w.z = pk[cidx * 4 + 2];
+                        w.w = pk[cidx * 4 + 3];
+                        *reinterpret_cast<uint4 *>(prow + half * kBox + ((chunk ^ sw) << 4)) = w;
+                    }
+                    tc::fence_proxy_async();
+                }
+                tc::tc_fence_before();
+                tc::mbar_arrive(&sh.p_full);
+            }
+            if (!ok) break;
+            // ---- unit epilogue: this thread's row of O, 32 dims at a time
+            const bool have_o = un.count > 0 && warp_active;
+            if (un.count > 0) {
+                ok = warp_wait(sh, &sh.pv_done, (gb + un.count - 1) & 1, status);
+                if (!ok) break;
+                tc::tc_fence_after();
+            }
+            const bool split = un.part_row >= 0;
+            const float inv = (l > 0.f && have_o) ? a.v_scale / l : 0.f;
+            __nv_bfloat16 *dst = a.out + static_cast<int64_t>(un.t0 + j) * a.o_s0 +
+                                 static_cast<int64_t>(un.h * a.G + g) * a.o_s1;
+            const bool vec = a.o_s2 == 1 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0;
+            float *prt = partials + static_cast<int64_t>(split ? un.part_row + r : 0) * kStride;
+#pragma unroll 1
+            for (int ch = 0; ch < kD / 32; ++ch) {
+                float o[32];
+                __syncwarp();
+                if (have_o) {
+                    tmem_ld32(tmem + lane_base + kColO + ch * 32, o);
+                    tc::tmem_wait_ld();
+                }
+#pragma unroll
+                for (int k = 0; k < 32; ++k) o[k] = have_o ? o[k] : 0.f;
+                if (!active) {
+                } else if (split) {
+                    // partial of a split pair: unnormalised O
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        reinterpret_cast<float4 *>(prt + ch * 32)[q] =
+                            make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+                } else if (vec) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 w;
+                        w.x = pack_bf16(o[8 * q + 0] * inv, o[8 * q + 1] * inv);
+                        w.y = pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv);
+                        w.z = pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv);
+                        w.w = pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv);
+                        reinterpret_cast<uint4 *>(dst + ch * 32)[q] = w;
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k)
+                        dst[static_cast<int64_t>(ch * 32 + k) * a.o_s2] = __float2bfloat16_rn(o[k] * inv);
+                }
+            }
+            tc::tc_fence_before();
+            tc::mbar_arrive(&sh.o_free);
+            if (split) {
+                if (active) {
+                    prt[kD] = have_o ? m_run : -INFINITY;
+                    prt[kD + 1] = have_o ? l : 0.f;
+                }
+                __threadfence();
+                soft_sync();
+                if (st_id == 0) sh.last = (atomicAdd(&counters[un.pair], 1) == un.n_split - 1);
+                soft_sync();
+                if (sh.last) {
+                    // merge every unit of the pair: thread = head dim, rows in turn
+                    __threadfence();
+                    const int d = st_id;
+                    const float *pbase = partials + static_cast<int64_t>(un.part_base) * kStride;
+                    const int64_t kstep = static_cast<int64_t>(rows) * kStride;
+                    for (int rr = 0; rr < rows; ++rr) {
+                        float mstar = -INFINITY;
+                        for (int sp = 0; sp < un.n_split; ++sp)
+                            mstar = fmaxf(mstar, __ldcg(pbase + sp * kstep + rr * kStride + kD));
+                        float acc = 0.f, den = 0.f;
+                        if (mstar != -INFINITY) {
+                            for (int sp = 0; sp < un.n_split; ++sp) {
+                                const float *row = pbase + sp * kstep + rr * kStride;
+                                const float ms = __ldcg(row + kD);
+                                const float wgt = (ms == -INFINITY) ? 0.f : tc::ex2(ms - mstar);
+                                den = fmaf(wgt, __ldcg(row + kD + 1), den);
+                                acc = fmaf(wgt, __ldcg(row + d), acc);
+                            }
+                        }
+                        const float v = (den > 0.f) ? acc * a.v_scale / den : 0.f;
+                        a.out[static_cast<int64_t>(un.t0 + rr / a.G) * a.o_s0 +
+                              static_cast<int64_t>(un.h * a.G + rr % a.G) * a.o_s1 + static_cast<int64_t>(d) * a.o_s2] =
+                            __float2bfloat16_rn(v);
+                    }
+                }
+                soft_sync();  // sh.last is rewritten by the next split unit
+            }
+            gb += un.count;
+            ++uc;
+        }
+    }
+
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    if (warp == 1) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+// [rows, heads, 128] bf16 tensor as a 3-D map: box = 64 dims x heads_box
+// heads x rows_box rows, 128-byte swizzle.
+bool make_tmap_bf16(CUtensorMap *m, const void *base, int64_t rows, int64_t heads, int64_t s0, int64_t s1,
+                    int heads_box, int rows_box) {
+    auto fn = tensor_map_encoder();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(s1) * 2, static_cast<cuuint64_t>(s0) * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(heads_box), static_cast<cuuint32_t>(rows_box)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// Covers: BF16 K/V caches and bf16 queries of head dim 128, 16-byte aligned
+// cache rows and query rows, G = Hq / Hkv a power of two up to 16, page
+// tables of at most 256 blocks, at most 4096 rows, a workspace.  Anything
+// else: *used stays false.
+cudaError_t launch_attention_bf16_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cudaStream_t stream, bool *used) {
+    *used = false;
+    const int G = a.Hq / a.Hkv;
+    if (a.kv_dt != SPD_BF16 || a.q_dt != SPD_BF16 || a.D != kD) return cudaSuccess;
+    if (a.NB > kPlanMaxNB || a.T > kPlanMaxT || G < 1 || G > 16 || (G & (G - 1)) != 0) return cudaSuccess;
+    if ((a.k_s0 % 8) || (a.k_s1 % 8) || (a.v_s0 % 8) || (a.v_s1 % 8)) return cudaSuccess;
+    if ((reinterpret_cast<uintptr_t>(a.k) % 16) || (reinterpret_cast<uintptr_t>(a.v) % 16)) return cudaSuccess;
+    if (a.q_s2 != 1 || (reinterpret_cast<uintptr_t>(a.q) % 16)) return cudaSuccess;
+    if ((a.Hq > 1 && (a.q_s1 <= 0 || a.q_s1 % 8)) || (a.T > 1 && (a.q_s0 <= 0 || a.q_s0 % 8))) return cudaSuccess;
+    if (a.P * kKeys > (int64_t(1) << 31) - 1) return cudaSuccess;
+    PlanLayout lay(a.T, a.Hq, a.Hkv, a.D, a.NB);
+    if (ws == nullptr || ws_bytes < lay.total) return cudaSuccess;
+
+    // rows of a request share a unit: up to 128 / G tokens (16 at most, the
+    // planner's row mask), so one unit fills the M = 128 rows of the MMA
+    const int gmax = std::min(16, kM / G);
+    CUtensorMap tq, tk, tv;
+    const int64_t qs1 = a.Hq > 1 ? a.q_s1 : kD, qs0 = a.T > 1 ? a.q_s0 : static_cast<int64_t>(a.Hq) * qs1;
+    if (!make_tmap_bf16(&tq, a.q, a.T, a.Hq, qs0, qs1, G, gmax)) return cudaSuccess;
+    if (!make_tmap_bf16(&tk, a.k, a.P * kKeys, a.Hkv, a.k_s0, a.k_s1, 1, kKeys)) return cudaSuccess;
+    if (!make_tmap_bf16(&tv, a.v, a.P * kKeys, a.Hkv, a.v_s0, a.v_s1, 1, kKeys)) return cudaSuccess;
+
+    const int sms = device_sm_count();
+    cudaError_t e = opt_in_smem(reinterpret_cast<const void *>(attention_bf16_tc_kernel), kSmemBytes);
+    if (e != cudaSuccess) return e;
+
+    PlanArgs p{};
+    p.ri = a.ri; p.ri_s0 = a.ri_s0;
+    p.sl = a.sl; p.sl_s0 = a.sl_s0;
+    p.bt = a.bt; p.bt_s0 = a.bt_s0; p.bt_s1 = a.bt_s1;
+    p.tk = a.tk; p.tk_s0 = a.tk_s0; p.tk_s1 = a.tk_s1; p.tk_s2 = a.tk_s2;
+    p.T = a.T; p.R = a.R; p.NB = a.NB; p.K = a.K; p.Hkv = a.Hkv; p.G = G;
+    p.gmax = gmax;
+    p.P = a.P;
+    p.num_ctas = sms;
+    p.ws = static_cast<char *>(ws);
+    p.lay = lay;
+    p.q = a.q; p.q_s0 = a.q_s0; p.q_s1 = a.q_s1; p.q_s2 = a.q_s2;
+    p.q_dt = a.q_dt;
+    p.Hq = a.Hq;
+    p.zscale = 0.f;
+    if (!plan_configure(&p)) return cudaSuccess;
+    // the planner only: queries are read as they are (no E4M3 conversion)
+    e = launch_prepare(p, 0, stream);
+    if (e != cudaSuccess) return e;
+
+    Bf16Args t{};
+    t.ri = a.ri; t.ri_s0 = a.ri_s0;
+    t.sl = a.sl; t.sl_s0 = a.sl_s0;
+    t.out = a.out; t.o_s0 = a.o_s0; t.o_s1 = a.o_s1; t.o_s2 = a.o_s2;
+    t.T = a.T; t.Hq = a.Hq; t.Hkv = a.Hkv; t.G = G; t.R = a.R; t.NB = a.NB; t.gmax = gmax;
+    t.c = a.sm_scale * a.k_scale * 1.4426950408889634f;
+    t.v_scale = a.v_scale;
+    t.ws = static_cast<char *>(ws);
+    t.lay = lay;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sms);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, attention_bf16_tc_kernel, tq, tk, tv, t);
+    if (e == cudaSuccess) *used = true;
+    return e;
+}
+
+}  // namespace spd

@@ -1109,6 +1109,7 @@ int group_rows(const AttnArgs &a, int G) {
 cudaError_t launch_attention_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cudaStream_t stream, bool *used) {
     *used = false;
     const int G = a.Hq / a.Hkv;
+    if (a.kv_dt != SPD_E4M3) return cudaSuccess;
     if (a.D != kD || a.NB > kPlanMaxNB || a.T > kPlanMaxT || G > kNMax) return cudaSuccess;
     if ((a.k_s0 % 16) || (a.k_s1 % 16) || (a.v_s0 % 16) || (a.v_s1 % 16)) return cudaSuccess;
     if ((reinterpret_cast<uintptr_t>(a.k) % 16) || (reinterpret_cast<uintptr_t>(a.v) % 16)) return cudaSuccess;

@@ -51,6 +51,7 @@ cudaError_t opt_in_smem(const void *func, int bytes) {
 
 cudaError_t launch_score_tc(const ScoreArgs &a, cudaStream_t stream, bool *used);
 cudaError_t launch_attention_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cudaStream_t stream, bool *used);
+cudaError_t launch_attention_bf16_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cudaStream_t stream, bool *used);
 cudaError_t launch_sdpa_tc(const SdpaArgs &a, cudaStream_t stream, bool *used);
 
 namespace {
@@ -86,7 +87,10 @@ cudaError_t dispatch_select(const SelectArgs &a, cudaStream_t stream) {
 cudaError_t dispatch_attention(const AttnArgs &a, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
     bool used = false;
     cudaError_t e = cudaSuccess;
-    if (g_policy[3] == 0) e = launch_attention_tc(a, workspace, workspace_bytes, stream, &used);
+    if (g_policy[3] == 0) {
+        e = (a.kv_dt == SPD_BF16) ? launch_attention_bf16_tc(a, workspace, workspace_bytes, stream, &used)
+                                  : launch_attention_tc(a, workspace, workspace_bytes, stream, &used);
+    }
     if (e != cudaSuccess) return e;
     if (used) {
         count_launches(3);  // list and unit planner kernels + attention

@@ -289,12 +289,12 @@ attention_generic_kernel(AttnArgs a) {
         // logits of token tid for every q head
         const bool valid = static_cast<int64_t>(b) * kBlock + tid < L;
         if (valid) {
-            const uint8_t *krow = a.k + (base + tid) * a.k_s0 + h * a.k_s1;
+            const int64_t krow = (base + tid) * a.k_s0 + h * a.k_s1;
             float z[kMaxGroup];
 #pragma unroll
             for (int g = 0; g < kMaxGroup; ++g) z[g] = 0.f;
             for (int d = 0; d < a.D; ++d) {
-                const float kd = e4m3_to_float(krow[d]);
+                const float kd = kv_value(a.k, a.kv_dt, krow + d);
 #pragma unroll
                 for (int g = 0; g < kMaxGroup; ++g)
                     if (g < G) z[g] = fmaf(qs[g][d], kd, z[g]);
@@ -337,7 +337,7 @@ attention_generic_kernel(AttnArgs a) {
 #pragma unroll
             for (int g = 0; g < kMaxGroup; ++g) part[g] = 0.f;
             for (int i = 0; i < n_valid; ++i) {
-                const float vd = e4m3_to_float(a.v[(base + i) * a.v_s0 + h * a.v_s1 + d]);
+                const float vd = kv_value(a.v, a.kv_dt, (base + i) * a.v_s0 + h * a.v_s1 + d);
 #pragma unroll
                 for (int g = 0; g < kMaxGroup; ++g)
                     if (g < G) part[g] = fmaf(ps[g][i], vd, part[g]);

@@ -233,8 +233,9 @@ bool attention(const spd_tensor *q, const spd_tensor *k, const spd_tensor *v, co
                float sm_scale, int32_t block_size, float k_scale, float v_scale, void *ws, size_t ws_bytes,
                cudaStream_t stream, const char *entry) {
     if (!check_desc(q, "q", 3, {SPD_F32, SPD_BF16, SPD_F16})) return false;
-    if (!check_desc(k, "k_cache", 3, {SPD_E4M3})) return false;
-    if (!check_desc(v, "v_cache", 3, {SPD_E4M3})) return false;
+    if (!check_desc(k, "k_cache", 3, {SPD_E4M3, SPD_BF16})) return false;
+    if (!check_desc(v, "v_cache", 3, {SPD_E4M3, SPD_BF16})) return false;
+    if (k->dtype != v->dtype) return fail(SPD_ERR_INVALID_ARGUMENT, "k_cache and v_cache dtypes differ");
     if (!check_desc(out, "out", 3, {SPD_BF16})) return false;
     const int64_t T = q->shape[0], Hq = q->shape[1], D = q->shape[2];
     if (!check_paging(bt, sl, ri, T, block_size)) return false;
@@ -289,6 +290,7 @@ bool attention(const spd_tensor *q, const spd_tensor *k, const spd_tensor *v, co
     }
     a.out = static_cast<__nv_bfloat16 *>(out->data); a.o_s0 = out->stride[0]; a.o_s1 = out->stride[1]; a.o_s2 = out->stride[2];
     a.q_dt = q->dtype;
+    a.kv_dt = k->dtype;
     a.T = (int32_t)T; a.Hq = (int32_t)Hq; a.Hkv = (int32_t)Hkv; a.D = (int32_t)D;
     a.R = (int32_t)bt->shape[0]; a.NB = (int32_t)NB; a.K = (int32_t)K;
     a.P = k->shape[0] / kBlock;

@@ -53,7 +53,7 @@ struct SelectArgs {
 struct AttnArgs {
     const void *q;          // [T, Hq, D]
     int64_t q_s0, q_s1, q_s2;
-    const uint8_t *k;       // [S, Hkv, D] e4m3 bytes, innermost stride 1
+    const uint8_t *k;       // [S, Hkv, D] e4m3 or bf16 (kv_dt), innermost stride 1
     const uint8_t *v;
     int64_t k_s0, k_s1, v_s0, v_s1;
     const int32_t *bt;      // [R, NB]
@@ -66,7 +66,7 @@ struct AttnArgs {
     int64_t tk_s0, tk_s1, tk_s2;
     __nv_bfloat16 *out;     // [T, Hq, D]
     int64_t o_s0, o_s1, o_s2;
-    int32_t q_dt;
+    int32_t q_dt, kv_dt;    // kv_dt: SPD_E4M3 or SPD_BF16 (both caches)
     int32_t T, Hq, Hkv, D, R, NB, K;
     int64_t P;
     float sm_scale, k_scale, v_scale;
@@ -105,6 +105,12 @@ __device__ __forceinline__ float load_float(const void *base, int dt, int64_t of
     if (dt == SPD_BF16) return __bfloat162float(static_cast<const __nv_bfloat16 *>(base)[off]);
     if (dt == SPD_E4M3) return e4m3_to_float(static_cast<const uint8_t *>(base)[off]);
     return __half2float(static_cast<const __half *>(base)[off]);
+}
+
+// Element `off` of a K/V cache of dtype kv_dt (E4M3 or BF16) as fp32.
+__device__ __forceinline__ float kv_value(const uint8_t *base, int kv_dt, int64_t off) {
+    if (kv_dt == SPD_BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[off]);
+    return e4m3_to_float(base[off]);
 }
 
 // seq_len of query token t clipped to [0, NB*128]; 0 when its request row is

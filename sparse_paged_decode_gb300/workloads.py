@@ -23,7 +23,9 @@ Recipe shared by every workload
     (causal among the draft tokens of a verification row).
   * K and V are drawn in fp32 and stored as FP8-E4M3 with one static scalar
     scale each: ``scale = max|x| / 448`` over the stored (valid) values, codes
-    ``= e4m3(x / scale)`` (round to nearest even, via torch's cast).
+    ``= e4m3(x / scale)`` (round to nearest even, via torch's cast).  With
+    ``kv_dtype="bf16"`` they are stored as dense BF16 instead (rounded to
+    nearest even, scale 1.0; unowned slots hold the poison +/-448.0).
 """
 from __future__ import annotations
 
@@ -142,10 +144,13 @@ def make_decode(name: str, *, lengths: Sequence[int], tokens_per_request: Sequen
                 K: int, dtype: torch.dtype = torch.bfloat16, idx_dtype: Optional[torch.dtype] = None,
                 seed: int, dense: bool = False, q_dist: str = "normal",
                 padded_tail: Optional[Sequence[int]] = None, with_index: bool = True,
-                with_kv: bool = True) -> Workload:
+                with_kv: bool = True, kv_dtype: str = "e4m3") -> Workload:
     """A decode/verification batch: request r owns ``tokens_per_request[r]``
     consecutive query rows and has total length ``lengths[r]``.
-    ``padded_tail[r]`` trailing rows of request r get ``seq_len = 0``."""
+    ``padded_tail[r]`` trailing rows of request r get ``seq_len = 0``.
+    ``kv_dtype`` is "e4m3" (static scalar scales) or "bf16" (dense, scale 1)."""
+    if kv_dtype not in ("e4m3", "bf16"):
+        raise ValueError("kv_dtype must be 'e4m3' or 'bf16'")
     g = torch.Generator().manual_seed(seed)
     idx_dtype = idx_dtype or dtype
     R = len(lengths)
@@ -175,10 +180,15 @@ def make_decode(name: str, *, lengths: Sequence[int], tokens_per_request: Sequen
         w.q = q.to(dtype)
         for name_, attr in (("k", "k_cache"), ("v", "v_cache")):
             vals = torch.randn((all_slots.numel(), Hkv, D), generator=g)
-            codes, scale = _to_e4m3(vals)
+            if kv_dtype == "bf16":
+                cache = _poison_e4m3((n_slots, Hkv, D), g).to(torch.bfloat16)  # +/-448.0
+                cache.index_copy_(0, all_slots, vals.to(torch.bfloat16))
+                scale = 1.0
+            else:
+                codes, scale = _to_e4m3(vals)
+                cache = _poison_e4m3((n_slots, Hkv, D), g)
+                cache.view(torch.uint8).index_copy_(0, all_slots, codes.view(torch.uint8))
             del vals
-            cache = _poison_e4m3((n_slots, Hkv, D), g)
-            cache.view(torch.uint8).index_copy_(0, all_slots, codes.view(torch.uint8))
             setattr(w, attr, cache)
             setattr(w, name_ + "_scale", scale)
 
@@ -245,9 +255,12 @@ def with_fp8_index(w: Workload) -> Workload:
     return out
 
 
-def config(cfg: int, seed: Optional[int] = None) -> Workload:
-    """The five benchmark configurations, full size."""
+def config(cfg: int, seed: Optional[int] = None, kv_dtype: str = "e4m3") -> Workload:
+    """The five benchmark configurations, full size (``kv_dtype="bf16"``: the
+    same batch shapes over a dense BF16 K/V cache)."""
     seed = 1000 + cfg if seed is None else seed
+    if kv_dtype != "e4m3" and cfg in (1, 4):
+        raise ValueError("configuration %d has no BF16 K/V variant" % cfg)
     if cfg == 1:
         return make_decode("tiny_sparse_decode", lengths=[512], tokens_per_request=[1], Hq=8, Hkv=1, D=64,
                            Hi=1, Di=32, NB=4, P=16, K=2, dtype=torch.float32, seed=seed)
@@ -255,21 +268,21 @@ def config(cfg: int, seed: Optional[int] = None) -> Workload:
         g = torch.Generator().manual_seed(seed + 7919)
         lengths = torch.randint(2048, 16385, (4,), generator=g).tolist()
         return make_decode("verification_decode", lengths=lengths, tokens_per_request=[4] * 4, Hq=64, Hkv=8, D=128,
-                           Di=128, NB=128, P=1024, K=16, seed=seed)
+                           Di=128, NB=128, P=1024, K=16, seed=seed, kv_dtype=kv_dtype)
     if cfg == 3:
         return make_decode("dense_decode", lengths=[16384] * 16, tokens_per_request=[1] * 16, Hq=64, Hkv=8,
-                           D=128, NB=128, P=2048, K=0, seed=seed, dense=True, with_index=False)
+                           D=128, NB=128, P=2048, K=0, seed=seed, dense=True, with_index=False, kv_dtype=kv_dtype)
     if cfg == 4:
         g = torch.Generator().manual_seed(seed + 7919)
         offsets = torch.randint(0, 15873, (8,), generator=g).tolist()
         return make_prefill("prefill_score_select", offsets=offsets, chunk=512, P=1024, K=32, seed=seed)
     if cfg == 5:
-        return stress(seed=seed)
+        return stress(seed=seed, kv_dtype=kv_dtype)
     raise ValueError("unknown config %r" % cfg)
 
 
 def stress(seed: int = 1005, rows: int = 64, P: int = 8192, K: int = 64,
-           min_len: int = 256, max_len: int = 16384) -> Workload:
+           min_len: int = 256, max_len: int = 16384, kv_dtype: str = "e4m3") -> Workload:
     """Config 5 recipe, parameterised so tests can draw smaller copies."""
     g = torch.Generator().manual_seed(seed + 7919)
     buckets = torch.tensor([1, 4, 8, 16])
@@ -284,7 +297,7 @@ def stress(seed: int = 1005, rows: int = 64, P: int = 8192, K: int = 64,
         padded[r] = int(torch.randint(1, n[r] + 1, (1,), generator=g))
     return make_decode("stress_decode" if rows == 64 else "stress%d" % rows, lengths=lengths,
                        tokens_per_request=n, Hq=64, Hkv=8, D=128, Di=128, NB=128, P=P, K=K,
-                       seed=seed, q_dist="student_t3", padded_tail=padded)
+                       seed=seed, q_dist="student_t3", padded_tail=padded, kv_dtype=kv_dtype)
 
 
 # ------------------------------------------------------- dense attention

@@ -79,10 +79,10 @@ def status(spd):
 
 
 def attn_call(spd, T=4, Hq=8, Hkv=2, D=64, NB=4, P=8, K=2, q_dtype=BF16, out=None, ws_bytes=None,
-              block_size=128, tk=True, k_strides=None, sm_scale=0.125):
+              block_size=128, tk=True, k_strides=None, sm_scale=0.125, k_dtype=E4M3, v_dtype=E4M3):
     q = Fake((T, Hq, D), q_dtype)
-    k = Fake((P * 128, Hkv, D), E4M3, strides=k_strides)
-    v = Fake((P * 128, Hkv, D), E4M3)
+    k = Fake((P * 128, Hkv, D), k_dtype, strides=k_strides)
+    v = Fake((P * 128, Hkv, D), v_dtype)
     bt = Fake((2, NB), I32)
     sl = Fake((T,), I32)
     ri = Fake((T,), I32)
@@ -102,9 +102,10 @@ def attn_call(spd, T=4, Hq=8, Hkv=2, D=64, NB=4, P=8, K=2, q_dtype=BF16, out=Non
 
 def test_valid_attention_call_reaches_launch(spd):
     for tk in (True, False):
-        code, msg = attn_call(spd, tk=tk)
-        # validation passed; the launch itself needs a GPU
-        assert code in (SPD_OK, SPD_ERR_CUDA), msg
+        for kv in (E4M3, BF16):
+            code, msg = attn_call(spd, tk=tk, k_dtype=kv, v_dtype=kv)
+            # validation passed; the launch itself needs a GPU
+            assert code in (SPD_OK, SPD_ERR_CUDA), msg
 
 
 def test_attention_rejections(spd):
@@ -113,6 +114,9 @@ def test_attention_rejections(spd):
     assert attn_call(spd, Hq=64, Hkv=2)[0] == SPD_ERR_UNSUPPORTED  # group of 32
     assert attn_call(spd, D=512)[0] == SPD_ERR_UNSUPPORTED
     assert attn_call(spd, q_dtype=I32)[0] == SPD_ERR_UNSUPPORTED
+    # K and V caches must share their dtype; F16 / F32 caches are outside the domain
+    assert attn_call(spd, k_dtype=BF16, v_dtype=E4M3)[0] == SPD_ERR_INVALID_ARGUMENT
+    assert attn_call(spd, k_dtype=F16, v_dtype=F16)[0] == SPD_ERR_UNSUPPORTED
     assert attn_call(spd, ws_bytes=16)[0] == SPD_ERR_WORKSPACE
     assert attn_call(spd, k_strides=(2 * 64 * 2, 64 * 2, 2))[0] == SPD_ERR_UNSUPPORTED  # D not contiguous
     assert attn_call(spd, sm_scale=float("nan"))[0] == SPD_ERR_INVALID_ARGUMENT

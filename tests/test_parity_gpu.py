@@ -465,6 +465,77 @@ def test_fp8_index_cache_full_size(spd, orc):
     check_scores(s.cpu().numpy()[:, rows], ref, "prefill fp8 index scores")
 
 
+# ------------------------------------------------------ dense BF16 K/V cache
+
+BF16_KV = {
+    # tensor-core path (bf16 queries, D = 128): GQA 8, multi-token rows (a
+    # 16-token request fills the 128 MMA rows), ragged tails
+    "g8_d128": dict(lengths=[1500, 700, 129, 2048, 1], tokens_per_request=[4, 4, 1, 16, 1], Hq=64, Hkv=8, D=128,
+                    Di=128, NB=16, P=96, K=5),
+    # tensor-core path: group 16 (8 tokens per unit), long rows split over
+    # several units and merged, heavy-tailed queries
+    "g16_d128_split": dict(lengths=[7000, 5000, 300], tokens_per_request=[8, 3, 1], Hq=32, Hkv=2, D=128, Di=128,
+                           NB=64, P=128, K=40, q_dist="student_t3"),
+    # tensor-core path: MHA (G = 1, 16 tokens per unit)
+    "g1_d128": dict(lengths=[2000, 640], tokens_per_request=[5, 2], Hq=4, Hkv=4, D=128, Di=64, NB=16, P=32, K=6),
+    # head dim 64, fp32 queries, group 4
+    "g4_d64_f32q": dict(lengths=[300, 512, 77], tokens_per_request=[1, 2, 3], Hq=8, Hkv=2, D=64, Di=32, NB=4, P=16,
+                        K=2, dtype=torch.float32),
+    # group 16, f16 queries, heavy-tailed
+    "g16_d128_f16q": dict(lengths=[900, 2600], tokens_per_request=[3, 2], Hq=32, Hkv=2, D=128, Di=64, NB=24, P=48,
+                          K=7, dtype=torch.float16, q_dist="student_t3"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BF16_KV))
+def test_bf16_kv_cache_small(spd, orc, name, kernel_policy):
+    """Paged attention over a dense BF16 K/V cache (scale 1, unowned slots
+    poisoned with +/-448): sparse with the oracle's selection, end to end and
+    dense, every cell against the oracle's BF16 path."""
+    w = W.make_decode("bf16kv_" + name, seed=zlib.crc32(name.encode()) % 1000, kv_dtype="bf16", **BF16_KV[name])
+    assert w.k_cache.dtype == torch.bfloat16
+    full_check(spd, orc, w)
+
+
+def test_bf16_kv_cache_full_size(spd, orc):
+    """The verification-decode and dense-decode shapes over BF16 caches:
+    every row of each."""
+    full_check(spd, orc, W.config(2, kv_dtype="bf16"))
+    w = W.config(3, kv_dtype="bf16")
+    out = gpu_attention(spd, w.to(DEV), None)
+    ref = oracle_rows(orc, w, list(range(w.T)), None)
+    check_attention(out.float().cpu().numpy(), ref, "dense decode, BF16 cache")
+
+
+def test_bf16_kv_nan_slots_never_leak(spd, orc, kernel_policy):
+    """A BF16 cache whose unowned slots (unused pages and the tails of the
+    requests' last pages) hold NaN: no output cell may see them."""
+    w = W.make_decode("bf16nan", lengths=[700, 333, 129], tokens_per_request=[4, 2, 3], Hq=16, Hkv=2, D=128,
+                      Di=128, NB=8, P=24, K=3, seed=16, kv_dtype="bf16")
+    owned = set()
+    for r, L in enumerate(w.request_lengths):
+        for tau in range(L):
+            owned.add(int(w.block_table[r, tau // BS]) * BS + tau % BS)
+    mask = torch.ones(w.P * BS, dtype=torch.bool)
+    mask[torch.tensor(sorted(owned))] = False
+    for c in (w.k_cache, w.v_cache):
+        c[mask] = float("nan")
+    w.k_idx_cache[mask] = float("nan")
+    full_check(spd, orc, w)
+
+
+def test_kv_cache_dtypes_must_match(spd):
+    from sparse_paged_decode_gb300.binding import SpdError
+
+    w = W.make_decode("kvmix", lengths=[300], tokens_per_request=[1], Hq=8, Hkv=1, D=64, Di=32, NB=4, P=8, K=2,
+                      seed=3).to(DEV)
+    out = torch.empty((w.T, w.Hq, w.D), dtype=torch.bfloat16, device=DEV)
+    ws = torch.zeros(spd.decode_workspace_bytes(w.T, w.Hq, w.Hkv, w.D, w.NB), dtype=torch.uint8, device=DEV)
+    with pytest.raises(SpdError):
+        spd.paged_decode_attention(w.q, w.k_cache.to(torch.bfloat16), w.v_cache, w.block_table, w.seq_lens,
+                                   w.req_idx, out, w.sm_scale, BS, 1.0, 1.0, ws)
+
+
 # --------------------------------------------------------- full-size configs
 
 def test_verification_decode_full(spd, orc):

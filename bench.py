@@ -332,11 +332,15 @@ def run_reference(args, rank, world):
     }
 
 
+ATTENTION_POLICY = {"auto": 0, "general": 1}
+
+
 def run_gpu(args, rank, world, local_rank):
     import sparse_paged_decode_gb300 as spd
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
+    spd.set_kernel_policy(3, ATTENTION_POLICY[args.attention_kernel])
     w = make_workload(args, batch_seed(args.config, rank))
     g = w.to(dev)
     # the step's per-call inputs live in one device buffer (each tensor a
@@ -530,7 +534,9 @@ def run_gpu(args, rank, world, local_rank):
         # ones it was taken on
         for ent in tj.get("entries", []):
             if (ent.get("config") == args.config and ent.get("index_cache", "native") == args.index_cache
-                    and ent.get("kv_cache", "e4m3") == args.kv_cache and ent.get("kernel_stamp") == _kernel_stamp()):
+                    and ent.get("kv_cache", "e4m3") == args.kv_cache
+                    and ent.get("attention_kernel", "auto") == args.attention_kernel
+                    and ent.get("kernel_stamp") == _kernel_stamp()):
                 traffic = ent.get("traffic_bytes_per_launch")
     if prefill:
         # the score call is a contraction: tensor-bound against the peak of
@@ -553,9 +559,11 @@ def run_gpu(args, rank, world, local_rank):
         peak, peak_src = measured_peaks()
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                     "traffic": traffic,
-                    "kernel": ("paged attention call (list, unit and attention kernels; %s)"
-                               if args.kv_cache == "e4m3" else "paged attention call (general-layout kernel; %s)")
-                              % ("graph replay" if graph is not None else "direct launches"),
+                    "kernel": "paged attention call (%s; %s)"
+                              % ("general-layout kernel" if args.attention_kernel == "general" else
+                                 "list planner, unit planner, " + ("attention_tc_kernel" if args.kv_cache == "e4m3"
+                                                                  else "attention_bf16_tc_kernel"),
+                                 "graph replay" if graph is not None else "direct launches"),
                     "algorithmic_bytes_per_launch": abytes,
                     "mean_launch_us": attn_mean_s * 1e6, "peak_source": peak_src}
     cpu = None
@@ -571,7 +579,7 @@ def run_gpu(args, rank, world, local_rank):
         "dtype": (("e4m3 mma (index queries as two e4m3 terms)" if args.index_cache == "e4m3" else "bf16 mma")
                   + ", f32 accumulate") if prefill else ("e4m3/f16 mma, f32 accumulate"
                                                           if w.k_cache.dtype == torch.float8_e4m3fn
-                                                          else "f32 (CUDA-core FMA over bf16 K/V)"),
+                                                          else "bf16 mma, f32 accumulate"),
         "data": "synthetic",
         "config": workload_desc(w),
         "roofline": roofline,
@@ -1000,6 +1008,9 @@ def main():
                     help="index cache as generated (bf16) or stored FP8-E4M3")
     ap.add_argument("--kv-cache", default="e4m3", choices=["e4m3", "bf16"],
                     help="K/V cache as FP8-E4M3 with static scalar scales (default) or dense BF16")
+    ap.add_argument("--attention-kernel", default="auto", choices=["auto", "general"],
+                    help="paged attention kernel: the tensor-core kernel of the cache type (default) or the "
+                         "general-layout kernel")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

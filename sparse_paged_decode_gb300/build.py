@@ -40,7 +40,8 @@ def _sources():
 # sources of the sparse/dense attention call (planner kernels and the
 # tensor-core attention kernel): what a DRAM-traffic capture of that call
 # depends on
-ATTENTION_SOURCES = ("attention_tc.cu", "plan.cu", "plan.cuh", "spd_internal.cuh", "tc_ptx.cuh", "tmap.cuh")
+ATTENTION_SOURCES = ("attention_tc.cu", "attention_bf16_tc.cu", "dispatch.cu", "plan.cu", "plan.cuh",
+                     "spd_internal.cuh", "tc_ptx.cuh", "tmap.cuh")
 
 
 def _code_only(text: bytes) -> bytes:

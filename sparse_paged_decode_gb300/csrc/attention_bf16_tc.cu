@@ -156,8 +156,102 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// softmax threads only (warps 2-5)
+// Named barrier of the 128 softmax threads, and the same barrier reducing a
+// flag (true if any thread's is).  Every softmax thread reaches every one of
+// them: a failed wait never skips one, it only raises the flag of the next
+// vote, which all threads then act on together.
 __device__ __forceinline__ void soft_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ bool soft_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, 1, 128, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v))
+        : "memory");
+    return r != 0;
+}
+
+// The last unit of a split pair to finish merges every unit's partial: warp w
+// of the softmax takes rows w, w + 4, ... two at a time, each lane four head
+// dims; the (offset, sum) and output values of two partials of both rows are
+// loaded together, then folded with an online maximum.  Partials are
+// read with ld.global.cg: other CTAs wrote them during this launch.
+__device__ void merge_pair(const Bf16Args &a, const PlanUnit &un, const float *partials, int st_id) {
+    constexpr int kParts = 2;
+    const int rows = un.nt * a.G, ns = un.n_split;
+    const int w = st_id >> 5, d4 = (st_id & 31) * 4;
+    const float *pbase = partials + static_cast<int64_t>(un.part_base) * kStride;
+    const int64_t kstep = static_cast<int64_t>(rows) * kStride;
+    for (int r0 = w; r0 < rows; r0 += 8) {
+        float m[2] = {-INFINITY, -INFINITY}, den[2] = {0.f, 0.f};
+        float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+        for (int k0 = 0; k0 < ns; k0 += kParts) {
+            float2 ml[2][kParts];
+            float4 o[2][kParts];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int r = r0 + 4 * u;
+#pragma unroll
+                for (int q = 0; q < kParts; ++q) {
+                    if (r < rows && k0 + q < ns) {
+                        const float *row = pbase + (k0 + q) * kstep + static_cast<int64_t>(r) * kStride;
+                        ml[u][q] = __ldcg(reinterpret_cast<const float2 *>(row + kD));
+                        o[u][q] = __ldcg(reinterpret_cast<const float4 *>(row + d4));
+                    } else {
+                        ml[u][q] = make_float2(-INFINITY, 0.f);
+                        o[u][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                float mc = m[u];
+#pragma unroll
+                for (int q = 0; q < kParts; ++q) mc = fmaxf(mc, ml[u][q].x);
+                if (mc == -INFINITY) continue;
+                const float sc = (m[u] == -INFINITY) ? 0.f : tc::ex2(m[u] - mc);
+                den[u] *= sc;
+                acc[u].x *= sc;
+                acc[u].y *= sc;
+                acc[u].z *= sc;
+                acc[u].w *= sc;
+#pragma unroll
+                for (int q = 0; q < kParts; ++q) {
+                    const float wt = (ml[u][q].x == -INFINITY) ? 0.f : tc::ex2(ml[u][q].x - mc);
+                    den[u] = fmaf(wt, ml[u][q].y, den[u]);
+                    acc[u].x = fmaf(wt, o[u][q].x, acc[u].x);
+                    acc[u].y = fmaf(wt, o[u][q].y, acc[u].y);
+                    acc[u].z = fmaf(wt, o[u][q].z, acc[u].z);
+                    acc[u].w = fmaf(wt, o[u][q].w, acc[u].w);
+                }
+                m[u] = mc;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int r = r0 + 4 * u;
+            if (r >= rows) continue;
+            const float inv = (den[u] > 0.f) ? a.v_scale / den[u] : 0.f;
+            __nv_bfloat16 *dst = a.out + static_cast<int64_t>(un.t0 + r / a.G) * a.o_s0 +
+                                 static_cast<int64_t>(un.h * a.G + r % a.G) * a.o_s1;
+            if (a.o_s2 == 1 && (reinterpret_cast<uintptr_t>(dst + d4) & 7) == 0) {
+                uint2 wv;
+                wv.x = pack_bf16(acc[u].x * inv, acc[u].y * inv);
+                wv.y = pack_bf16(acc[u].z * inv, acc[u].w * inv);
+                *reinterpret_cast<uint2 *>(dst + d4) = wv;
+            } else {
+                dst[static_cast<int64_t>(d4 + 0) * a.o_s2] = __float2bfloat16_rn(acc[u].x * inv);
+                dst[static_cast<int64_t>(d4 + 1) * a.o_s2] = __float2bfloat16_rn(acc[u].y * inv);
+                dst[static_cast<int64_t>(d4 + 2) * a.o_s2] = __float2bfloat16_rn(acc[u].z * inv);
+                dst[static_cast<int64_t>(d4 + 3) * a.o_s2] = __float2bfloat16_rn(acc[u].w * inv);
+            }
+        }
+    }
+}
+
 
 __global__ void __launch_bounds__(kThreads, 1)
 attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -340,13 +434,40 @@ attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gri
         float *partials = reinterpret_cast<float *>(a.ws + a.lay.partials);
         uint32_t uc = 0, gb = 0;
         bool ok = true;
-        while (ok) {
+        // a split unit's ticket, resolved one unit later
+        PlanUnit pend{};
+        pend.pair = -1;
+        int ticket = 0;
+        auto resolve = [&]() {
+            if (pend.pair < 0) return;
+            if (st_id == 0) sh.last = (ticket == pend.n_split - 1);
+            soft_sync();
+            if (sh.last) {
+                __threadfence();  // the other units' partials before the merge reads them
+                merge_pair(a, pend, partials, st_id);
+            }
+            soft_sync();  // sh.last is rewritten by the next resolution
+            pend.pair = -1;
+        };
+        bool finished = false;  // the sentinel unit was reached with no failure
+        for (;;) {
             const int slot = uc & 3;
-            ok = warp_wait(sh, &sh.unit_full[slot], (uc >> 2) & 1, status);
-            if (!ok) break;
-            const PlanUnit un = sh.ring[slot];
-            tc::mbar_arrive(&sh.unit_empty[slot]);
-            if (un.pair < 0) break;
+            PlanUnit un{};
+            un.pair = -1;
+            if (ok && warp_wait(sh, &sh.unit_full[slot], (uc >> 2) & 1, status)) {
+                un = sh.ring[slot];
+                tc::mbar_arrive(&sh.unit_empty[slot]);
+            } else {
+                ok = false;
+            }
+            // leave together: on any failure, or at the sentinel (the same
+            // record for every thread); this barrier also separates the
+            // previous unit's use of the limits from this one's
+            if (soft_any(!ok || aborted(sh))) break;
+            if (un.pair < 0) {
+                finished = true;
+                break;
+            }
             const int rows = un.nt * a.G;
             const bool active = r < rows;
             const bool warp_active = __any_sync(0xffffffffu, active);
@@ -356,7 +477,6 @@ attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gri
                                                                 &row_r))
                                  : 0;
             // the unit's key limits, for the V rows no row of the unit may read
-            soft_sync();  // every thread is done with the previous unit's limits
             if (st_id < un.nt) {
                 int rr;
                 sh.Lj[st_id] = static_cast<int>(
@@ -498,14 +618,15 @@ attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gri
                 tc::tc_fence_before();
                 tc::mbar_arrive(&sh.p_full);
             }
-            if (!ok) break;
+            if (soft_any(!ok || aborted(sh))) break;
+            // the previous split unit's ticket has had this unit's pages to return
+            resolve();
             // ---- unit epilogue: this thread's row of O, 32 dims at a time
-            const bool have_o = un.count > 0 && warp_active;
             if (un.count > 0) {
                 ok = warp_wait(sh, &sh.pv_done, (gb + un.count - 1) & 1, status);
-                if (!ok) break;
                 tc::tc_fence_after();
             }
+            const bool have_o = ok && un.count > 0 && warp_active;
             const bool split = un.part_row >= 0;
             const float inv = (l > 0.f && have_o) ? a.v_scale / l : 0.f;
             __nv_bfloat16 *dst = a.out + static_cast<int64_t>(un.t0 + j) * a.o_s0 +
@@ -552,41 +673,17 @@ attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gri
                     prt[kD] = have_o ? m_run : -INFINITY;
                     prt[kD + 1] = have_o ? l : 0.f;
                 }
+                // every thread's partial row before the ticket; its result is
+                // looked at after the next unit's pages
                 __threadfence();
                 soft_sync();
-                if (st_id == 0) sh.last = (atomicAdd(&counters[un.pair], 1) == un.n_split - 1);
-                soft_sync();
-                if (sh.last) {
-                    // merge every unit of the pair: thread = head dim, rows in turn
-                    __threadfence();
-                    const int d = st_id;
-                    const float *pbase = partials + static_cast<int64_t>(un.part_base) * kStride;
-                    const int64_t kstep = static_cast<int64_t>(rows) * kStride;
-                    for (int rr = 0; rr < rows; ++rr) {
-                        float mstar = -INFINITY;
-                        for (int sp = 0; sp < un.n_split; ++sp)
-                            mstar = fmaxf(mstar, __ldcg(pbase + sp * kstep + rr * kStride + kD));
-                        float acc = 0.f, den = 0.f;
-                        if (mstar != -INFINITY) {
-                            for (int sp = 0; sp < un.n_split; ++sp) {
-                                const float *row = pbase + sp * kstep + rr * kStride;
-                                const float ms = __ldcg(row + kD);
-                                const float wgt = (ms == -INFINITY) ? 0.f : tc::ex2(ms - mstar);
-                                den = fmaf(wgt, __ldcg(row + kD + 1), den);
-                                acc = fmaf(wgt, __ldcg(row + d), acc);
-                            }
-                        }
-                        const float v = (den > 0.f) ? acc * a.v_scale / den : 0.f;
-                        a.out[static_cast<int64_t>(un.t0 + rr / a.G) * a.o_s0 +
-                              static_cast<int64_t>(un.h * a.G + rr % a.G) * a.o_s1 + static_cast<int64_t>(d) * a.o_s2] =
-                            __float2bfloat16_rn(v);
-                    }
-                }
-                soft_sync();  // sh.last is rewritten by the next split unit
+                if (st_id == 0) ticket = atomicAdd(&counters[un.pair], 1);
+                pend = un;
             }
             gb += un.count;
             ++uc;
         }
+        if (finished) resolve();
     }
 
     tc::tc_fence_before();

@@ -87,6 +87,7 @@ cudaError_t dispatch_select(const SelectArgs &a, cudaStream_t stream) {
 cudaError_t dispatch_attention(const AttnArgs &a, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
     bool used = false;
     cudaError_t e = cudaSuccess;
+    // policy 0: the tensor-core kernel of the cache type; 1: the general kernel
     if (g_policy[3] == 0) {
         e = (a.kv_dt == SPD_BF16) ? launch_attention_bf16_tc(a, workspace, workspace_bytes, stream, &used)
                                   : launch_attention_tc(a, workspace, workspace_bytes, stream, &used);

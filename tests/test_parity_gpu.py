@@ -114,8 +114,25 @@ def oracle_rows(orc, w, rows, topk_np):
     return ref
 
 
-def full_check(spd, orc, w, attn_rows=None, score_rows=None, per_head_topk=False):
-    """Score + select + sparse attention + dense attention against the oracle."""
+class _policy:
+    """Stage-3 kernel policy for the duration of a block (None: as set)."""
+
+    def __init__(self, spd, pol):
+        self.spd, self.pol, self.old = spd, pol, None
+
+    def __enter__(self):
+        if self.pol is not None:
+            self.old = self.spd.set_kernel_policy(3, self.pol)
+
+    def __exit__(self, *exc):
+        if self.pol is not None:
+            self.spd.set_kernel_policy(3, self.old)
+
+
+def full_check(spd, orc, w, attn_rows=None, score_rows=None, per_head_topk=False, policies=(None,)):
+    """Score + select + sparse attention + dense attention against the oracle;
+    the attention calls run once per stage-3 kernel policy in ``policies``
+    (None: the policy as set), all against the same oracle outputs."""
     g = w.to(DEV)
     res = {}
     full_s = None
@@ -145,16 +162,23 @@ def full_check(spd, orc, w, attn_rows=None, score_rows=None, per_head_topk=False
             tk_dev = torch.from_numpy(ref_tk).to(DEV)
         else:
             tk_dev = torch.from_numpy(ref_tk).to(DEV).expand(w.Hkv, -1, -1)
-        out = gpu_attention(spd, g, tk_dev)
         ref = oracle_rows(orc, w, rows, ref_tk)
-        res["sparse"] = check_attention(out.float().cpu().numpy()[rows], ref, "sparse attention", pad)
         # end to end: the GPU's own selection feeds the GPU attention
-        out_e2e = gpu_attention(spd, g, tk.expand(w.Hkv, -1, -1))
         ref_e2e = oracle_rows(orc, w, rows, tk.cpu().numpy())
-        res["e2e"] = check_attention(out_e2e.float().cpu().numpy()[rows], ref_e2e, "end-to-end attention", pad)
-    out_d = gpu_attention(spd, g, None)
+        for pol in policies:
+            with _policy(spd, pol):
+                out = gpu_attention(spd, g, tk_dev)
+                res["sparse"] = check_attention(out.float().cpu().numpy()[rows], ref,
+                                                "sparse attention (policy %s)" % pol, pad)
+                out_e2e = gpu_attention(spd, g, tk.expand(w.Hkv, -1, -1))
+                res["e2e"] = check_attention(out_e2e.float().cpu().numpy()[rows], ref_e2e,
+                                             "end-to-end attention (policy %s)" % pol, pad)
     ref_d = oracle_rows(orc, w, rows, None)
-    res["dense"] = check_attention(out_d.float().cpu().numpy()[rows], ref_d, "dense attention", pad)
+    for pol in policies:
+        with _policy(spd, pol):
+            out_d = gpu_attention(spd, g, None)
+            res["dense"] = check_attention(out_d.float().cpu().numpy()[rows], ref_d,
+                                           "dense attention (policy %s)" % pol, pad)
     return res
 
 
@@ -346,11 +370,12 @@ def test_strided_inputs_and_outputs(spd, orc):
     assert torch.all(o_big[:, :, :4] == 7.0) and torch.all(o_big[:, :, -4:] == 7.0)
 
 
-def test_graph_capture_and_replay_with_new_inputs(spd, orc):
+@pytest.mark.parametrize("kv", ["e4m3", "bf16"])
+def test_graph_capture_and_replay_with_new_inputs(spd, orc, kv):
     """"Slot contract" -- CUDA graph contract: capture, mutate every dynamic
-    input in place, replay, re-verify."""
+    input in place, replay, re-verify (FP8 and BF16 caches)."""
     w = W.make_decode("graph", lengths=[1500, 900], tokens_per_request=[4, 2], Hq=16, Hkv=2, D=128, Di=128,
-                      NB=16, P=40, K=4, seed=13)
+                      NB=16, P=40, K=4, seed=13, kv_dtype=kv)
     g = w.to(DEV)
     s = torch.empty((1, w.T, w.NB), device=DEV)
     tk = torch.empty((1, w.T, w.K), dtype=torch.int32, device=DEV)
@@ -546,9 +571,9 @@ def test_dense_decode_full(spd, orc):
     """Dense decode at full size (16 rows of 16384 tokens): every row."""
     w = W.config(3)
     g = w.to(DEV)
-    out = gpu_attention(spd, g, None)
     rows = list(range(w.T))
     ref = oracle_rows(orc, w, rows, None)
+    out = gpu_attention(spd, g, None)
     check_attention(out.float().cpu().numpy(), ref, "dense decode")
 
 

@@ -10,9 +10,9 @@
 //   S  = Q K^T       tcgen05.mma kind::f16, M = 128 rows, N = 128 keys, K = 128
 //                    dims, into one of two tensor-memory buffers, so the next
 //                    block's product runs while the softmax reads this one
-//   P  = 2^(S c - m) two threads per row (its TMEM lane), 64 keys each: the
-//                    logits sit in registers; the two halves exchange one
-//                    block maximum per block and the row sum at the end
+//   P  = 2^(S c - m) one thread per row (its TMEM lane): the row's 128 logits
+//                    sit in that thread's registers, so the block maximum and
+//                    the row sum need no exchange between threads
 //   O += P V         kind::f16, M = 128 rows, N = 128 dims, K = 128 keys, with
 //                    P written by the softmax into shared memory (K-major)
 //                    and V used as loaded (MN-major)
@@ -27,12 +27,11 @@
 // past a tile's last readable key are not loaded, and the tiles with the most
 // keys are scheduled first.
 //
-// Roles (10 warps): warp 0 issues the TMA loads, warp 1 owns tensor memory and
-// issues every MMA, warps 2-9 run the softmax and the epilogue, two threads
-// per row (warp w reads TMEM lanes 32 (w % 4) .. +31; warps 2-5 take keys and
-// head dims 0-63, warps 6-9 64-127).  Every mbarrier wait is bounded; a wait
-// that gives up makes the CTA wind down and write NaN into its output rows
-// instead of results.
+// Roles (6 warps): warp 0 issues the TMA loads, warp 1 owns tensor memory and
+// issues every MMA, warps 2-5 run the softmax and the epilogue (warp w reads
+// TMEM lanes 32 (w % 4) .. +31, i.e. rows of that quadrant).  Every mbarrier
+// wait is bounded; a wait that gives up makes the CTA wind down and write NaN
+// into its output rows instead of results.
 #include <math.h>
 
 #include <cuda_bf16.h>
@@ -53,9 +52,7 @@ namespace {
 constexpr int kD = 128;              // head dim of this path
 constexpr int kRowsTile = 128;       // query rows per CTA (M)
 constexpr int kKeysBlock = 128;      // keys per block (N of S, K of P V)
-constexpr int kThreads = 320;        // warps 0 TMA, 1 MMA, 2-9 softmax (two threads per row)
-constexpr int kWarpSoft = 2;
-constexpr int kSoftThreads = 256;
+constexpr int kThreads = 192;        // warps 0 TMA, 1 MMA, 2-5 softmax
 constexpr int kStages = 2;           // K and V stages each
 constexpr int kBox = 128 * 128;      // one 64-dim box of 128 rows, bytes (16-bit elements)
 constexpr int kTile = 2 * kBox;      // 128 rows x 128 dims of 16-bit values
@@ -77,7 +74,6 @@ struct SdpaShared {
     uint64_t p_full, pv_done, drain;
     uint32_t tmem_base;
     int abort;
-    float red[2][2][128];  // [block parity][half][row]: the halves' block maxima, then row sums
 };
 
 constexpr int kSmemBytes = kOffBar + static_cast<int>(sizeof(SdpaShared)) + 1024;  // + alignment slack
@@ -171,9 +167,6 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// the 256 softmax threads (warps 2-9)
-__device__ __forceinline__ void soft_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-
 __global__ void __launch_bounds__(kThreads, 1)
 sdpa_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ SdpaTcArgs a) {
@@ -200,9 +193,9 @@ sdpa_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         }
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&sh.s_full[i], 1);
-            tc::mbar_init(&sh.s_free[i], kSoftThreads);
+            tc::mbar_init(&sh.s_free[i], 128);
         }
-        tc::mbar_init(&sh.p_full, kSoftThreads);
+        tc::mbar_init(&sh.p_full, 128);
         tc::mbar_init(&sh.pv_done, 1);
         tc::mbar_init(&sh.drain, 1);
         sh.abort = 0;
@@ -304,14 +297,6 @@ sdpa_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         }
     } else {
         // --------------------------------------------- softmax and epilogue
-        // Two threads per row: warps 2-5 take keys 0-63 of each block and
-        // dims 0-63 of O, warps 6-9 keys 64-127 and dims 64-127 (TMEM lane
-        // quadrant warp % 4).  They agree on the row's block maximum through
-        // shared memory, so both raise the offset at the same blocks.  Every
-        // softmax thread reaches every named barrier: a failed wait only
-        // marks the CTA aborted, and the remaining blocks are skipped, not
-        // the barriers.
-        const int half = (warp - kWarpSoft) >> 2;  // 0: keys/dims 0-63, 1: 64-127
         const int quad = warp & 3;
         const int r = quad * 32 + lane;  // row of the tile = TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
@@ -320,43 +305,55 @@ sdpa_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         const int n_row = readable(a, t);
         const bool bf16 = a.in_bf16 != 0;
         const float c = a.c;
-        const float sg = (c >= 0.f) ? 1.f : -1.f;
         float m_run = -INFINITY;  // offset of the row's exponents (log2 units)
-        float l = 0.f;            // this half's row sum of 2^(s c - m_run)
+        float l = 0.f;            // row sum of 2^(s c - m_run)
         bool ok = true;
-        uint8_t *prow = smem + kOffP + half * kBox + r * 128;
+        uint8_t *prow = smem + kOffP + r * 128;
         const uint32_t sw = static_cast<uint32_t>(r & 7);
-        const uint32_t tS0 = tmem + lane_base + kColS + half * 64;
-        const uint32_t tO = tmem + lane_base + kColO + half * 64;
         for (int j = 0; j < nb; ++j) {
             const int sb = j & 1;
-            const bool go = __all_sync(0xffffffffu, ok && !aborted(sh));  // warp-uniform
-            ok = go && warp_wait(sh, &sh.s_full[sb], (j >> 1) & 1);
-            float s[64];
-            // keys at or past the row's limit (and past S) take no weight
-            const int lim = n_row - j * kKeysBlock - half * 64;
-            float mx = -INFINITY;
-            if (ok) {
-                tc::tc_fence_after();
-                tmem_ld32(tS0 + sb * kKeysBlock, s);
-                tmem_ld32(tS0 + sb * kKeysBlock + 32, s + 32);
-                tc::tmem_wait_ld();
-                if (lim >= 64) {
+            ok = warp_wait(sh, &sh.s_full[sb], (j >> 1) & 1);
+            if (!ok) break;
+            tc::tc_fence_after();
+            float s[kKeysBlock];
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) mx = fmaxf(mx, sg * s[i]);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 64; ++i)
-                        if (i < lim) mx = fmaxf(mx, sg * s[i]);
-                }
-            }
+            for (int ch = 0; ch < kKeysBlock / 32; ++ch)
+                tmem_ld32(tmem + lane_base + kColS + sb * kKeysBlock + ch * 32, s + ch * 32);
+            tc::tmem_wait_ld();
             tc::tc_fence_before();
             tc::mbar_arrive(&sh.s_free[sb]);
-            // the row's block maximum: this half's and the other's
-            sh.red[sb][half][r] = mx;
-            soft_sync();
-            mx = fmaxf(mx, sh.red[sb][half ^ 1][r]);
-            const float bm = (mx == -INFINITY) ? -INFINITY : mx * fabsf(c);
+            // keys at or past the row's limit (and past S) take no weight
+            const int lim = n_row - j * kKeysBlock;
+            if (lim < kKeysBlock) {
+#pragma unroll
+                for (int i = 0; i < kKeysBlock; ++i)
+                    if (i >= lim) s[i] = -INFINITY;
+            }
+            // block maximum of s c (c may be negative: then the minimum of s)
+            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+            if (c >= 0.f) {
+#pragma unroll
+                for (int i = 0; i < kKeysBlock; i += 4) {
+                    mx0 = fmaxf(mx0, s[i]);
+                    mx1 = fmaxf(mx1, s[i + 1]);
+                    mx2 = fmaxf(mx2, s[i + 2]);
+                    mx3 = fmaxf(mx3, s[i + 3]);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < kKeysBlock; i += 4) {
+                    const float n0 = s[i] == -INFINITY ? -INFINITY : -s[i];
+                    const float n1 = s[i + 1] == -INFINITY ? -INFINITY : -s[i + 1];
+                    const float n2 = s[i + 2] == -INFINITY ? -INFINITY : -s[i + 2];
+                    const float n3 = s[i + 3] == -INFINITY ? -INFINITY : -s[i + 3];
+                    mx0 = fmaxf(mx0, n0);
+                    mx1 = fmaxf(mx1, n1);
+                    mx2 = fmaxf(mx2, n2);
+                    mx3 = fmaxf(mx3, n3);
+                }
+            }
+            const float mraw = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+            const float bm = (mraw == -INFINITY) ? -INFINITY : mraw * fabsf(c);
             // raise the offset if the block's maximum runs more than 2^kRaise
             // above it (or the row had none yet)
             float alpha = 1.f;
@@ -368,67 +365,60 @@ sdpa_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             const float m_eff = (m_run == -INFINITY) ? 0.f : m_run;
             // p = 2^(s c - m) in [0, 2^kRaise], packed in the inputs' type;
             // masked keys take p = 0 whatever the sign of c
-            uint32_t pk[32];
-            if (ok) {
-                if (lim >= 64) {
+            uint32_t pk[kKeysBlock / 2];
+            if (lim >= kKeysBlock) {
 #pragma unroll
-                    for (int i = 0; i < 64; i += 2) {
-                        const float p0 = tc::ex2(fmaf(s[i], c, -m_eff));
-                        const float p1 = tc::ex2(fmaf(s[i + 1], c, -m_eff));
-                        l += p0 + p1;
-                        pk[i / 2] = pack2(p0, p1, bf16);
-                    }
-                } else {
+                for (int i = 0; i < kKeysBlock; i += 2) {
+                    const float p0 = tc::ex2(fmaf(s[i], c, -m_eff));
+                    const float p1 = tc::ex2(fmaf(s[i + 1], c, -m_eff));
+                    l += p0 + p1;
+                    pk[i / 2] = pack2(p0, p1, bf16);
+                }
+            } else {
 #pragma unroll
-                    for (int i = 0; i < 64; i += 2) {
-                        const float p0 = (i < lim) ? tc::ex2(fmaf(s[i], c, -m_eff)) : 0.f;
-                        const float p1 = (i + 1 < lim) ? tc::ex2(fmaf(s[i + 1], c, -m_eff)) : 0.f;
-                        l += p0 + p1;
-                        pk[i / 2] = pack2(p0, p1, bf16);
-                    }
+                for (int i = 0; i < kKeysBlock; i += 2) {
+                    const float p0 = (i < lim) ? tc::ex2(fmaf(s[i], c, -m_eff)) : 0.f;
+                    const float p1 = (i + 1 < lim) ? tc::ex2(fmaf(s[i + 1], c, -m_eff)) : 0.f;
+                    l += p0 + p1;
+                    pk[i / 2] = pack2(p0, p1, bf16);
                 }
             }
             // P of the previous block has been consumed and O holds every
-            // earlier block: rescale this half of the row's O if its offset moved
-            if (ok && j > 0) {
+            // earlier block: rescale this row's O if its offset moved
+            if (j > 0) {
                 ok = warp_wait(sh, &sh.pv_done, (j - 1) & 1);
-                if (ok) {
-                    tc::tc_fence_after();
-                    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                if (!ok) break;
+                tc::tc_fence_after();
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-                        for (int ch = 0; ch < 2; ++ch) {
-                            float o[32];
-                            tmem_ld32(tO + ch * 32, o);
-                            tc::tmem_wait_ld();
+                    for (int ch = 0; ch < kD / 32; ++ch) {
+                        float o[32];
+                        const uint32_t ta = tmem + lane_base + kColO + ch * 32;
+                        tmem_ld32(ta, o);
+                        tc::tmem_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                            tmem_st32(tO + ch * 32, o);
-                        }
-                        tc::tmem_wait_st();
+                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                        tmem_st32(ta, o);
                     }
+                    tc::tmem_wait_st();
                 }
             }
-            // this half's 64 keys of the row's P: one 64-key box, 16-byte
-            // chunks swizzled by the row
-            if (ok) {
+            // the row's P: keys 0-63 in the first 64-key box, 64-127 in the
+            // second, 16-byte chunks swizzled by the row
 #pragma unroll
-                for (int chunk = 0; chunk < 8; ++chunk) {
-                    uint4 w;
-                    w.x = pk[chunk * 4 + 0];
-                    w.y = pk[chunk * 4 + 1];
-                    w.z = pk[chunk * 4 + 2];
-                    w.w = pk[chunk * 4 + 3];
-                    *reinterpret_cast<uint4 *>(prow + ((chunk ^ sw) << 4)) = w;
-                }
-                tc::fence_proxy_async();
+            for (int cidx = 0; cidx < 16; ++cidx) {
+                const int half = cidx >> 3, chunk = cidx & 7;
+                uint4 w;
+                w.x = pk[cidx * 4 + 0];
+                w.y = pk[cidx * 4 + 1];
+                w.z = pk[cidx * 4 + 2];
+                w.w = pk[cidx * 4 + 3];
+                *reinterpret_cast<uint4 *>(prow + half * kBox + ((chunk ^ sw) << 4)) = w;
             }
+            tc::fence_proxy_async();
             tc::tc_fence_before();
             tc::mbar_arrive(&sh.p_full);
         }
-        // the row's sum: this half's and the other's
-        sh.red[0][half][r] = l;
-        soft_sync();
-        l += sh.red[0][half ^ 1][r];
         // epilogue: O / l for rows that read keys, zeros for rows that read
         // none, NaN if the CTA gave up.  The tensor-memory loads are
         // warp-collective, so every lane of a warp takes them (rows past T
@@ -438,14 +428,14 @@ sdpa_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             have_o = warp_wait(sh, &sh.pv_done, (nb - 1) & 1);
             tc::tc_fence_after();
         }
-        const bool bad = !have_o && nb > 0;
+        const bool bad = !ok || aborted(sh);
         const float inv = (l > 0.f) ? 1.f / l : 0.f;
-        const int64_t obase = t * a.o_s0 + static_cast<int64_t>(h * a.G + g) * a.o_s1 + half * 64 * a.o_s2;
+        const int64_t obase = t * a.o_s0 + static_cast<int64_t>(h * a.G + g) * a.o_s1;
         const bool vec = a.o_s2 == 1 && ((reinterpret_cast<uintptr_t>(a.out) + obase * 2) & 15) == 0;
-        for (int ch = 0; ch < 2; ++ch) {
+        for (int ch = 0; ch < kD / 32; ++ch) {
             float o[32];
             if (have_o) {
-                tmem_ld32(tO + ch * 32, o);
+                tmem_ld32(tmem + lane_base + kColO + ch * 32, o);
                 tc::tmem_wait_ld();
             }
 #pragma unroll

@@ -536,7 +536,7 @@ def run_gpu(args, rank, world, local_rank):
             if (ent.get("config") == args.config and ent.get("index_cache", "native") == args.index_cache
                     and ent.get("kv_cache", "e4m3") == args.kv_cache
                     and ent.get("attention_kernel", "auto") == args.attention_kernel
-                    and ent.get("kernel_stamp") == _kernel_stamp()):
+                    and ent.get("kernel_stamp") == _kernel_stamp(args.kv_cache)):
                 traffic = ent.get("traffic_bytes_per_launch")
     if prefill:
         # the score call is a contraction: tensor-bound against the peak of
@@ -980,11 +980,11 @@ def run_prefill_gpu(args, rank, world, local_rank):
     }
 
 
-def _kernel_stamp():
+def _kernel_stamp(kv_cache="e4m3"):
     try:
         from sparse_paged_decode_gb300 import build as b
 
-        return b._stamp(b.ATTENTION_SOURCES)[:16]
+        return b._stamp(b.ATTENTION_SOURCES[kv_cache])[:16]
     except Exception:  # pragma: no cover
         return None
 

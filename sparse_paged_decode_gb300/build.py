@@ -37,11 +37,12 @@ def _sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-# sources of the sparse/dense attention call (planner kernels and the
-# tensor-core attention kernel): what a DRAM-traffic capture of that call
-# depends on
-ATTENTION_SOURCES = ("attention_tc.cu", "attention_bf16_tc.cu", "dispatch.cu", "plan.cu", "plan.cuh",
-                     "spd_internal.cuh", "tc_ptx.cuh", "tmap.cuh")
+# sources of the sparse/dense attention call per K/V cache type (planner
+# kernels and that cache type's tensor-core attention kernel): what a
+# DRAM-traffic capture of that call depends on
+_PLAN_SOURCES = ("dispatch.cu", "plan.cu", "plan.cuh", "spd_internal.cuh", "tc_ptx.cuh", "tmap.cuh")
+ATTENTION_SOURCES = {"e4m3": ("attention_tc.cu",) + _PLAN_SOURCES,
+                     "bf16": ("attention_bf16_tc.cu",) + _PLAN_SOURCES}
 
 
 def _code_only(text: bytes) -> bytes:

@@ -41,7 +41,7 @@
 //    of its O.  A thread reads its lane's logits of a block from tensor
 //    memory in one batch; its row sums stay in registers and are reduced
 //    over the lanes once per unit.  The exponent offset per query row is a
-//    running maximum raised only when a logit exceeds it by more than 2^6
+//    running maximum raised only when a logit exceeds it by more than 2^14
 //    (then O is rescaled in tensor memory): most blocks need no cross-lane
 //    reduction.
 //
@@ -73,7 +73,11 @@ constexpr int kStages = 3;
 constexpr int kTile = 128 * 128;      // bytes of one K or V tile
 constexpr int kNMax = 64;             // query rows per group (padded)
 constexpr int kMaxEntries = kPlanMaxNB;
-constexpr float kRaise = 6.0f;        // log2 headroom before the offset is raised (p <= 64)
+// log2 headroom before a column's offset is raised: p <= 2^14 stays inside
+// f16's range with a factor of 4 to spare, and a raise (a group-wide maximum
+// and an O rescale, about 2 us) is needed only when a block's logits run more
+// than 2^14 above the offset
+constexpr float kRaise = 14.0f;
 constexpr int kD = 128;
 constexpr int kTerms = kQueryTerms;   // E4M3 terms per query element (12 significant bits)
 constexpr int kStride = kD + kPartialStride;
@@ -418,8 +422,9 @@ __device__ __forceinline__ bool unit_blocks(const Soft &c, const TcArgs &a, cons
 
         // this group's P tile was read by the product of its previous block
         if (b >= 2) wait_or_abort(sh, &sh.pv_done[wg], (k - 1) & 1, c.status);
-        // probabilities p = 2^u <= 64 in f16 (11-bit significand, normal down
-        // to 2^-14), the B operand of P V; masked columns have u = -inf, p = 0
+        // probabilities p = 2^u <= 2^14 in f16 (11-bit significand, normal
+        // from 2^-14 to 65504), the B operand of P V; masked columns have
+        // u = -inf, p = 0
 #pragma unroll
         for (int c8 = 0; c8 < kNMax; c8 += 8) {
             if (c8 < n) {

@@ -28,6 +28,8 @@
 // NaN in the cells it could not compute.
 #include <math.h>
 
+#include <algorithm>
+
 #include "spd_internal.cuh"
 #include "tc_ptx.cuh"
 #include "tmap.cuh"
@@ -458,9 +460,17 @@ cudaError_t launch_score_tc(const ScoreArgs &a, cudaStream_t stream, bool *used)
         if (e != cudaSuccess) return e;
     }
 
-    const int tq = kLanes / a.Hi;
+    // A CTA runs its (request, block) steps one after another, so its time
+    // grows with the steps it owns.  Decode batches (a few query rows per
+    // page-table row) put many short requests in one lane tile, and the low
+    // block ids, which every request has, carry the most steps: there a CTA
+    // takes half a tile of lanes and one block id.  Prefill batches (long
+    // runs of one request) keep full tiles and several block ids a CTA, so
+    // each K tile serves many lanes.
+    const bool decode_like = a.R > 0 && a.T <= 32LL * a.R;
+    const int tq = decode_like ? std::max(1, kLanes / a.Hi / 2) : kLanes / a.Hi;
     const int64_t n_tiles = (a.T + tq - 1) / tq;
-    int64_t chunk = (n_tiles * a.NB + 2 * sms - 1) / (2 * sms);
+    int64_t chunk = decode_like ? 1 : (n_tiles * a.NB + 2 * sms - 1) / (2 * sms);
     chunk = chunk < 1 ? 1 : chunk > kMaxChunk ? kMaxChunk : chunk;
     const int64_t n_chunks = (a.NB + chunk - 1) / chunk;
     if (n_tiles > INT32_MAX) return cudaSuccess;

@@ -561,6 +561,21 @@ def test_kv_cache_dtypes_must_match(spd):
                                    w.req_idx, out, w.sm_scale, BS, 1.0, 1.0, ws)
 
 
+# ------------------------------------------------- capability-domain edges
+
+def test_domain_edges_head_dim_256_index_dim_512_and_1024_blocks(spd, orc):
+    """The largest shapes the calls declare: head dim 256, index dim 512, a
+    page table of 1024 blocks with one request using all of them (131072
+    tokens), a top-k wider than one selection kernel's register row (the
+    rank kernel takes rows of more than 256 blocks).  Every cell of the score
+    sheet, the top-k and the sparse, end-to-end and dense attention
+    outputs."""
+    w = W.make_decode("edges", lengths=[1024 * BS, 2000], tokens_per_request=[1, 3], Hq=4, Hkv=1, D=256, Di=512,
+                      NB=1024, P=1056, K=40, seed=1024)
+    assert w.NB == 1024 and w.D == 256 and w.Di == 512 and int(w.seq_lens.max()) == 1024 * BS
+    full_check(spd, orc, w)
+
+
 # --------------------------------------------------------- full-size configs
 
 def test_verification_decode_full(spd, orc):

@@ -105,8 +105,17 @@ struct TcArgs {
     PlanLayout lay;
 };
 
+// What the softmax needs of a block-list entry: the block and which rows
+// selected it.
+struct BlockRows {
+    uint16_t block;
+    uint16_t mask;
+};
+
 struct __align__(16) Shared {
     float m_run[2][kNMax];   // running exponent offset per group and query row (log2 units)
+    float m_eff[2][kNMax];   // the offset, 0 while a column has none
+    float thr[2][kNMax];     // logit above which a column needs a raise: 2^kRaise, -inf while it has no offset
     float cfac[2][kNMax];    // logit factor per query row (double-buffered by unit)
     float alpha[2][kNMax];   // rescale factor of a group's last offset raise
     float delta[2][kNMax];   // change of each offset in that raise
@@ -130,7 +139,7 @@ struct __align__(16) Shared {
     int vote[2][2][4];
     int unit_vote[8];
     int Lj[2][16];                  // key limit of each group row (double-buffered by unit)
-    PlanEntry ent[2][kMaxEntries];  // the unit's block list (double-buffered by unit)
+    BlockRows ent[2][kMaxEntries];  // the unit's block list (double-buffered by unit)
     uint8_t nvalid[4][kMaxEntries];  // per V-widening warp: tokens of each block valid for some row
 };
 
@@ -265,9 +274,12 @@ __device__ __forceinline__ void chunk16(const float (&x)[kNMax], int ch, float (
 // read from S in one batch and masked (-inf where the column is not valid on
 // the lane): u = s * cfac - m (log2 units), m the column's offset or 0 while
 // it has none.  Returns whether some column needs a raise: a logit more than
-// 2^kRaise above its offset, or a valid logit in a column without one.
-__device__ __forceinline__ bool load_u(const Shared &sh, int mb, int nch, bool stacked, uint32_t tS,
-                                       const float *m_run, uint64_t colmask, float (&u)[kNMax]) {
+// 2^kRaise above its offset, or a valid logit in a column without one.  The
+// raise keeps both forms of each offset in shared memory (m or 0, and the
+// threshold: 2^kRaise, or -inf without an offset), so a column costs one
+// FMA, the mask and one compare.
+__device__ __forceinline__ bool load_u(const Shared &sh, int wg, int mb, int nch, bool stacked, uint32_t tS,
+                                       uint64_t colmask, float (&u)[kNMax]) {
     // stacked: the second term's logits follow in chunks nch..2nch-1
     const int nld = stacked ? 2 * nch : nch;
 #pragma unroll
@@ -288,15 +300,16 @@ __device__ __forceinline__ bool load_u(const Shared &sh, int mb, int nch, bool s
     for (int c4 = 0; c4 < kNMax; c4 += 4) {
         if (c4 < 16 * nch) {
             const float4 cf = *reinterpret_cast<const float4 *>(&sh.cfac[mb][c4]);
-            const float4 mr = *reinterpret_cast<const float4 *>(&m_run[c4]);
-            const float cfs[4] = {cf.x, cf.y, cf.z, cf.w}, mrs[4] = {mr.x, mr.y, mr.z, mr.w};
+            const float4 me = *reinterpret_cast<const float4 *>(&sh.m_eff[wg][c4]);
+            const float4 th = *reinterpret_cast<const float4 *>(&sh.thr[wg][c4]);
+            const float cfs[4] = {cf.x, cf.y, cf.z, cf.w}, mes[4] = {me.x, me.y, me.z, me.w};
+            const float ths[4] = {th.x, th.y, th.z, th.w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int col = c4 + q;
-                const bool unset = mrs[q] == -INFINITY;
-                const float v = fmaf(u[col], cfs[q], unset ? 0.f : -mrs[q]);
+                const float v = fmaf(u[col], cfs[q], -mes[q]);
                 u[col] = ((colmask >> col) & 1) ? v : -INFINITY;
-                need[q] |= u[col] > (unset ? -INFINITY : kRaise);
+                need[q] |= u[col] > ths[q];
             }
         }
     }
@@ -324,7 +337,7 @@ __device__ __forceinline__ bool unit_blocks(const Soft &c, const TcArgs &a, cons
     for (int i = ((gb & 1u) == static_cast<uint32_t>(wg)) ? 0 : 1; i < un.count; i += 2) {
         const uint32_t b = gb + i;  // b % 2 == wg
         const uint32_t k = b >> 1;  // this group's block ordinal
-        const PlanEntry e = sh.ent[mb][i];
+        const BlockRows e = sh.ent[mb][i];
         // columns valid on this token lane: selected by the column's row and
         // below that row's key limit
         uint64_t colmask = 0;
@@ -341,7 +354,7 @@ __device__ __forceinline__ bool unit_blocks(const Soft &c, const TcArgs &a, cons
         const bool have = warp_wait(sh, &sh.s_full[wg][sb], (k >> 1) & 1, c.status);
         if (have) {
             tc::tc_fence_after();
-            need = load_u(sh, mb, nch, stacked, tS, m_run, colmask, u);
+            need = load_u(sh, wg, mb, nch, stacked, tS, colmask, u);
         }
         // votes alternate between two slots by block parity: a warp can be at
         // most one block ahead of the slowest reader of its group
@@ -387,6 +400,9 @@ __device__ __forceinline__ bool unit_blocks(const Soft &c, const TcArgs &a, cons
                     }
                     sh.alpha[wg][col] = al;
                     sh.delta[wg][col] = delta;
+                    const bool set = m_run[col] != -INFINITY;
+                    sh.m_eff[wg][col] = set ? m_run[col] : 0.f;
+                    sh.thr[wg][col] = set ? kRaise : -INFINITY;
                 }
                 any = __any_sync(0xffffffffu, any);
                 if (c.lane == 0) sh.rescale[wg] = any;
@@ -929,7 +945,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
                 }
                 if (i < un.count) {
                     nvalid[i] = static_cast<uint8_t>(min(128, max(0, m - e.block * 128)));
-                    if (cw == 0) sh.ent[mb][i] = e;
+                    if (cw == 0) sh.ent[mb][i] = BlockRows{e.block, e.mask};
                 }
             }
             if (cw == 0) {
@@ -1030,7 +1046,12 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_con
         while (state == 0) {
             c.mb = uc & 1;
             wait_or_abort(sh, &sh.meta_full[c.mb], (uc >> 1) & 1, c.status);  // a timeout shows in the votes
-            if (c.st_id < 2 * kNMax) sh.m_run[c.st_id / kNMax][c.st_id % kNMax] = -INFINITY;
+            if (c.st_id < 2 * kNMax) {
+                const int g = c.st_id / kNMax, col = c.st_id % kNMax;
+                sh.m_run[g][col] = -INFINITY;
+                sh.m_eff[g][col] = 0.f;
+                sh.thr[g][col] = -INFINITY;
+            }
             soft_sync();
             const bool ok = unit_blocks(c, a, un, gb);
             unit_finish(c, a, un, gb, ok);

@@ -4,21 +4,23 @@
 //
 // A CTA owns one tile of 128 query rows of one kv head: 128 / G consecutive
 // query tokens, each with its G q heads (row = token * G + head), so every
-// row of the tile reads the same keys.  It streams that kv head's keys 128 at
+// row of the tile reads the same keys.  It streams that kv head's keys 64 at
 // a time (one "key block"):
 //
-//   S  = Q K^T       tcgen05.mma kind::f16, M = 128 rows, N = 128 keys, K = 128
+//   S  = Q K^T       tcgen05.mma kind::f16, M = 128 rows, N = 64 keys, K = 128
 //                    dims, into one of two tensor-memory buffers, so the next
 //                    block's product runs while the softmax reads this one
-//   P  = 2^(S c - m) one thread per row (its TMEM lane): the row's 128 logits
+//   P  = 2^(S c - m) one thread per row (its TMEM lane): the row's 64 logits
 //                    sit in that thread's registers, so the block maximum and
 //                    the row sum need no exchange between threads
-//   O += P V         kind::f16, M = 128 rows, N = 128 dims, K = 128 keys, with
+//   O += P V         kind::f16, M = 128 rows, N = 128 dims, K = 64 keys, with
 //                    P written by the softmax into shared memory (K-major)
 //                    and V used as loaded (MN-major)
 //
-// Q, K and V arrive by TMA straight from the caller's tensors (two 64-dim
-// boxes of 128 rows each, 128-byte swizzle); keys past the end read as zeros
+// Two CTAs share an SM (113 KB of shared memory and 256 tensor-memory
+// columns each), so one CTA's softmax runs while the other's products keep
+// the tensor pipe busy.  Q, K and V arrive by TMA straight from the caller's
+// tensors (64-dim boxes, 128-byte swizzle); keys past the end read as zeros
 // and are masked.  c = sm_scale * log2(e).  The exponent offset m of a row is
 // raised only when a block's maximum exceeds it by more than 2^kRaise (then
 // the row's O is rescaled in tensor memory and its sum in a register), so
@@ -33,6 +35,9 @@
 // wait is bounded; a wait that gives up makes the CTA wind down and write NaN
 // into its output rows instead of results.
 #include <math.h>
+
+#include <mutex>
+#include <set>
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -51,20 +56,23 @@ namespace {
 
 constexpr int kD = 128;              // head dim of this path
 constexpr int kRowsTile = 128;       // query rows per CTA (M)
-constexpr int kKeysBlock = 128;      // keys per block (N of S, K of P V)
+constexpr int kKeysBlock = 64;       // keys per block (N of S, K of P V)
 constexpr int kThreads = 192;        // warps 0 TMA, 1 MMA, 2-5 softmax
 constexpr int kStages = 2;           // K and V stages each
-constexpr int kBox = 128 * 128;      // one 64-dim box of 128 rows, bytes (16-bit elements)
-constexpr int kTile = 2 * kBox;      // 128 rows x 128 dims of 16-bit values
+constexpr int kBoxQ = 128 * 128;     // one 64-dim box of 128 query rows, bytes (16-bit elements)
+constexpr int kTileQ = 2 * kBoxQ;    // 128 rows x 128 dims
+constexpr int kBoxKV = kKeysBlock * 128;  // one 64-dim box of a key block
+constexpr int kTileKV = 2 * kBoxKV;       // 64 keys x 128 dims
+constexpr int kTileP = 128 * kKeysBlock * 2;  // 128 rows x 64 keys: one 128-byte row each
 constexpr float kRaise = 8.0f;       // log2 headroom before a row's offset is raised
 constexpr float kLog2e = 1.4426950408889634f;
 
-// dynamic shared memory: Q, K stages, V stages, P (each kTile), barriers
+// dynamic shared memory (1024-byte aligned tiles): Q, K stages, V stages, P
 constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTile;
-constexpr int kOffV = kOffK + kStages * kTile;
-constexpr int kOffP = kOffV + kStages * kTile;
-constexpr int kOffBar = kOffP + kTile;
+constexpr int kOffK = kOffQ + kTileQ;
+constexpr int kOffV = kOffK + kStages * kTileKV;
+constexpr int kOffP = kOffV + kStages * kTileKV;
+constexpr int kTilesEnd = kOffP + kTileP;
 
 struct SdpaShared {
     uint64_t q_full;
@@ -76,11 +84,15 @@ struct SdpaShared {
     int abort;
 };
 
-constexpr int kSmemBytes = kOffBar + static_cast<int>(sizeof(SdpaShared)) + 1024;  // + alignment slack
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+// The barriers sit in the padding below the aligned tiles when it is large
+// enough, else after them; either way the CTA needs the tiles plus 1023
+// bytes, which lets two CTAs share an SM.
+static_assert(sizeof(SdpaShared) <= 511, "barriers fit the alignment padding or after the tiles");
+constexpr int kSmemBytes = kTilesEnd + 1023;
+static_assert(2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
 
-// tensor memory: S buffers at columns 0 and 128, O at 256
-constexpr uint32_t kColS = 0, kColO = 256, kTmemCols = 512;
+// tensor memory: S buffers at columns 0 and 64, O at 128
+constexpr uint32_t kColS = 0, kColO = 2 * kKeysBlock, kTmemCols = 256;
 
 struct SdpaTcArgs {
     void *out;
@@ -167,12 +179,13 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 sdpa_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ SdpaTcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    SdpaShared &sh = *reinterpret_cast<SdpaShared *>(smem + kOffBar);
+    const bool bar_below = static_cast<size_t>(smem - smem_raw) >= sizeof(SdpaShared);
+    SdpaShared &sh = *reinterpret_cast<SdpaShared *>(bar_below ? smem_raw : smem + kTilesEnd);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // heaviest tiles first: under the causal flag later tokens read more keys
@@ -216,25 +229,25 @@ sdpa_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         // ------------------------------------------------------ TMA producer
         if (lane == 0 && nb > 0) {
             uint8_t *sQ = smem + kOffQ;
-            tc::mbar_arrive_expect_tx(&sh.q_full, kTile);
+            tc::mbar_arrive_expect_tx(&sh.q_full, kTileQ);
             tc::tma_load_3d(sQ, &tmap_q, &sh.q_full, 0, h * a.G, static_cast<int>(t0));
-            tc::tma_load_3d(sQ + kBox, &tmap_q, &sh.q_full, 64, h * a.G, static_cast<int>(t0));
+            tc::tma_load_3d(sQ + kBoxQ, &tmap_q, &sh.q_full, 64, h * a.G, static_cast<int>(t0));
             int nk = 0, nv = 0;  // K and V blocks issued
             for (int j = 0; j < nb && !aborted(sh); ++j) {
                 const int st = j % kStages;
                 const uint32_t ph = ((j / kStages) - 1) & 1;
                 const int key0 = j * kKeysBlock;
                 if (j >= kStages && !wait_or_abort(sh, &sh.k_empty[st], ph)) break;
-                uint8_t *sK = smem + kOffK + st * kTile;
-                tc::mbar_arrive_expect_tx(&sh.k_full[st], kTile);
+                uint8_t *sK = smem + kOffK + st * kTileKV;
+                tc::mbar_arrive_expect_tx(&sh.k_full[st], kTileKV);
                 tc::tma_load_3d(sK, &tmap_k, &sh.k_full[st], 0, h, key0);
-                tc::tma_load_3d(sK + kBox, &tmap_k, &sh.k_full[st], 64, h, key0);
+                tc::tma_load_3d(sK + kBoxKV, &tmap_k, &sh.k_full[st], 64, h, key0);
                 ++nk;
                 if (j >= kStages && !wait_or_abort(sh, &sh.v_empty[st], ph)) break;
-                uint8_t *sV = smem + kOffV + st * kTile;
-                tc::mbar_arrive_expect_tx(&sh.v_full[st], kTile);
+                uint8_t *sV = smem + kOffV + st * kTileKV;
+                tc::mbar_arrive_expect_tx(&sh.v_full[st], kTileKV);
                 tc::tma_load_3d(sV, &tmap_v, &sh.v_full[st], 0, h, key0);
-                tc::tma_load_3d(sV + kBox, &tmap_v, &sh.v_full[st], 64, h, key0);
+                tc::tma_load_3d(sV + kBoxKV, &tmap_v, &sh.v_full[st], 64, h, key0);
                 ++nv;
             }
             // every issued copy lands before the CTA may exit (the last use
@@ -263,12 +276,15 @@ sdpa_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                     if (ok && j >= 2) ok = wait_or_abort(sh, &sh.s_free[sb], ((j >> 1) - 1) & 1);
                     if (!ok) break;
                     tc::tc_fence_after();
-                    const uint32_t aK = tc::smem_u32(smem + kOffK + st * kTile);
+                    const uint32_t aK = tc::smem_u32(smem + kOffK + st * kTileKV);
 #pragma unroll
                     for (int ks = 0; ks < kD / 16; ++ks) {
-                        const uint32_t off = (ks >> 2) * kBox + (ks & 3) * 32;
-                        tc::mma_f16(tmem + kColS + sb * kKeysBlock, tc::smem_desc(aQ + off, 16, 1024, tc::kSw128),
-                                    tc::smem_desc(aK + off, 16, 1024, tc::kSw128), idesc_s, ks > 0);
+                        // 16 dims a step: 32 bytes into a 128-byte row, the
+                        // second 64 dims one box on
+                        const uint32_t offq = (ks >> 2) * kBoxQ + (ks & 3) * 32;
+                        const uint32_t offk = (ks >> 2) * kBoxKV + (ks & 3) * 32;
+                        tc::mma_f16(tmem + kColS + sb * kKeysBlock, tc::smem_desc(aQ + offq, 16, 1024, tc::kSw128),
+                                    tc::smem_desc(aK + offk, 16, 1024, tc::kSw128), idesc_s, ks > 0);
                     }
                     tc::mma_commit(&sh.s_full[sb]);
                     tc::mma_commit(&sh.k_empty[st]);
@@ -278,14 +294,14 @@ sdpa_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                     ok = wait_or_abort(sh, &sh.p_full, i & 1) && wait_or_abort(sh, &sh.v_full[st], (i / kStages) & 1);
                     if (!ok) break;
                     tc::tc_fence_after();
-                    const uint32_t aV = tc::smem_u32(smem + kOffV + st * kTile);
+                    const uint32_t aV = tc::smem_u32(smem + kOffV + st * kTileKV);
 #pragma unroll
                     for (int ks = 0; ks < kKeysBlock / 16; ++ks) {
-                        // P: K-major like Q; V: 16 keys = two 8-row groups of
-                        // 128 bytes per step, the second 64 dims 16 KiB on
-                        const uint32_t offp = (ks >> 2) * kBox + (ks & 3) * 32;
-                        tc::mma_f16(tmem + kColO, tc::smem_desc(aP + offp, 16, 1024, tc::kSw128),
-                                    tc::smem_desc(aV + ks * 2048, kBox, 1024, tc::kSw128), idesc_o, i > 0 || ks > 0);
+                        // P: K-major, one 128-byte row (64 keys) per query row;
+                        // V: 16 keys = two 8-row groups of 128 bytes per step,
+                        // the second 64 dims one box (8 KiB) on
+                        tc::mma_f16(tmem + kColO, tc::smem_desc(aP + ks * 32, 16, 1024, tc::kSw128),
+                                    tc::smem_desc(aV + ks * 2048, kBoxKV, 1024, tc::kSw128), idesc_o, i > 0 || ks > 0);
                     }
                     tc::mma_commit(&sh.pv_done);
                     tc::mma_commit(&sh.v_empty[st]);
@@ -403,17 +419,15 @@ sdpa_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                     tc::tmem_wait_st();
                 }
             }
-            // the row's P: keys 0-63 in the first 64-key box, 64-127 in the
-            // second, 16-byte chunks swizzled by the row
+            // the row's P: one 128-byte row, 16-byte chunks swizzled by the row
 #pragma unroll
-            for (int cidx = 0; cidx < 16; ++cidx) {
-                const int half = cidx >> 3, chunk = cidx & 7;
+            for (int chunk = 0; chunk < 8; ++chunk) {
                 uint4 w;
-                w.x = pk[cidx * 4 + 0];
-                w.y = pk[cidx * 4 + 1];
-                w.z = pk[cidx * 4 + 2];
-                w.w = pk[cidx * 4 + 3];
-                *reinterpret_cast<uint4 *>(prow + half * kBox + ((chunk ^ sw) << 4)) = w;
+                w.x = pk[chunk * 4 + 0];
+                w.y = pk[chunk * 4 + 1];
+                w.z = pk[chunk * 4 + 2];
+                w.w = pk[chunk * 4 + 3];
+                *reinterpret_cast<uint4 *>(prow + ((chunk ^ sw) << 4)) = w;
             }
             tc::fence_proxy_async();
             tc::tc_fence_before();
@@ -494,6 +508,22 @@ bool tma_strides_ok(const void *base, int64_t s0, int64_t s1, int64_t s2, int64_
     return true;
 }
 
+// The largest shared-memory carveout for the kernel on the current device
+// (two CTAs of 113 KB per SM), once per device.
+cudaError_t prefer_shared_carveout(const void *func) {
+    static std::mutex mu;
+    static std::set<int> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count(dev)) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             static_cast<int>(cudaSharedmemCarveoutMaxShared));
+    if (e == cudaSuccess) done.insert(dev);
+    return e;
+}
+
 }  // namespace
 
 // Covers: q, k, v all bf16 or all f16 with head dim 128 and 16-byte aligned
@@ -523,6 +553,7 @@ cudaError_t launch_sdpa_tc(const SdpaArgs &a, cudaStream_t stream, bool *used) {
     if (!make_tmap_16(&tv, a.v, a.S, a.Hkv, vs0, vs1, 1, kKeysBlock)) return cudaSuccess;
 
     cudaError_t e = opt_in_smem(reinterpret_cast<const void *>(sdpa_tc_kernel), kSmemBytes);
+    if (e == cudaSuccess) e = prefer_shared_carveout(reinterpret_cast<const void *>(sdpa_tc_kernel));
     if (e != cudaSuccess) return e;
 
     SdpaTcArgs t{};

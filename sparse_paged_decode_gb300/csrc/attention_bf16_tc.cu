@@ -11,14 +11,18 @@
 // that the last unit to finish merges (an atomic ticket, no waiting).
 //
 // Per unit the query rows (token j, head g -> row j * G + g) lie on the M = 128
-// rows of the MMA, keys on N, as in a prefill flash kernel:
-//   S  = Q K^T       kind::f16 bf16, M = 128 rows, N = 128 keys of one page,
-//                    K = 128 dims, double-buffered in tensor memory
+// rows of the MMA, keys on N, as in a prefill flash kernel, half a page (64
+// keys) at a time:
+//   S  = Q K^T       kind::f16 bf16, M = 128 rows, N = 64 keys, K = 128 dims,
+//                    double-buffered in tensor memory
 //   P  = 2^(S c - m) one thread per row: the row's logits stay in its
 //                    registers (block max, sum, offset raise need no exchange)
 //   O += P V         kind::f16 bf16, P from shared memory, V as TMA loaded it
-// K and V pages are TMA-gathered straight from the paged cache through the
-// block list (two 64-dim boxes of 128 slots each, 128-byte swizzle).  A row's
+// K and V half pages are TMA-gathered straight from the paged cache through
+// the block list (two 64-dim boxes of 64 slots each, 128-byte swizzle).  A
+// CTA takes 112 KB of shared memory and 256 tensor-memory columns, so two
+// share an SM and one's per-block chain runs while the other waits on its
+// own.  A row's
 // keys in a block are those below its key limit, and none if the row did not
 // select the block.  c = sm_scale * k_scale * log2(e); the exponent offset of
 // a row is raised only when a block maximum exceeds it by more than 2^kRaise,
@@ -26,8 +30,8 @@
 //
 // Roles (6 warps): warp 0 claims units and issues the TMA loads, warp 1 owns
 // tensor memory and issues every MMA, warps 2-5 run the softmax and the unit
-// epilogue (warp w reads TMEM lanes 32 (w % 4) .. +31).  Q is double-buffered
-// by unit so the next unit's queries load under this unit's blocks.  Every
+// epilogue (warp w reads TMEM lanes 32 (w % 4) .. +31).  The next unit's
+// queries load once this unit's last Q K^T is done.  Every
 // wait is bounded: a wait that gives up sets bit 0 of the workspace status
 // word and the CTA winds down.
 #include <cuda.h>
@@ -35,6 +39,8 @@
 
 #include <algorithm>
 #include <cmath>
+#include <mutex>
+#include <set>
 
 #include "plan.cuh"
 #include "spd_internal.cuh"
@@ -49,23 +55,29 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kM = 128;         // query rows of a unit (padded)
-constexpr int kKeys = 128;      // keys per page
+constexpr int kKeys = 128;      // slots per page
+constexpr int kHalf = 64;       // keys per block of the products: half a page
 constexpr int kThreads = 192;   // warp 0 TMA, 1 MMA, 2-5 softmax / epilogue
 constexpr int kSoftThreads = 128;
-constexpr int kBox = 128 * 128; // 128 rows x 64 bf16 dims
-constexpr int kTile = 2 * kBox; // 128 rows x 128 dims
+constexpr int kBoxQ = 128 * 128;    // 128 query rows x 64 bf16 dims
+constexpr int kTileQ = 2 * kBoxQ;   // 128 rows x 128 dims
+constexpr int kBoxH = kHalf * 128;  // 64 slots x 64 dims
+constexpr int kTileH = 2 * kBoxH;   // 64 slots x 128 dims
+constexpr int kTileP = 128 * kHalf * 2;  // 128 rows x 64 keys: one 128-byte row each
 constexpr float kRaise = 8.0f;
 constexpr int kStride = kD + kPartialStride;  // floats per partial row
 
-constexpr int kOffQ = 0;                  // two unit buffers
-constexpr int kOffK = kOffQ + 2 * kTile;  // two stages
-constexpr int kOffV = kOffK + 2 * kTile;  // two stages
-constexpr int kOffP = kOffV + 2 * kTile;
-constexpr int kOffBar = kOffP + kTile;
+// dynamic shared memory (1024-byte aligned tiles): Q, two K stages, two V
+// stages, P
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kTileQ;
+constexpr int kOffV = kOffK + 2 * kTileH;
+constexpr int kOffP = kOffV + 2 * kTileH;
+constexpr int kTilesEnd = kOffP + kTileP;
 
 struct Shared {
     uint64_t unit_full[4], unit_empty[4];
-    uint64_t q_full[2], q_empty[2];
+    uint64_t q_full, q_empty;
     uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
     uint64_t s_full[2], s_free[2];
     uint64_t p_full, pv_done, o_free, drain;
@@ -76,11 +88,15 @@ struct Shared {
     int Lj[16];   // key limit of each token of the current unit
 };
 
-constexpr int kSmemBytes = kOffBar + static_cast<int>(sizeof(Shared)) + 1024;  // + alignment slack
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+// The barriers sit in the padding below the aligned tiles when it is large
+// enough, else after them; either way a CTA needs the tiles plus 1023 bytes,
+// which lets two CTAs share an SM.
+static_assert(sizeof(Shared) <= 511, "barriers fit the alignment padding or after the tiles");
+constexpr int kSmemBytes = kTilesEnd + 1023;
+static_assert(2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
 
-// tensor memory: S buffers at columns 0 and 128, O at 256
-constexpr uint32_t kColS = 0, kColO = 256, kTmemCols = 512;
+// tensor memory: S buffers at columns 0 and 64, O at 128
+constexpr uint32_t kColS = 0, kColO = 2 * kHalf, kTmemCols = 256;
 // a unit record is released by the MMA issuer and the softmax threads
 constexpr uint32_t kUnitArrivals = 1 + kSoftThreads;
 
@@ -253,12 +269,13 @@ __device__ void merge_pair(const Bf16Args &a, const PlanUnit &un, const float *p
 }
 
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                          const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ Bf16Args a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Shared &sh = *reinterpret_cast<Shared *>(smem + kOffBar);
+    const bool bar_below = static_cast<size_t>(smem - smem_raw) >= sizeof(Shared);
+    Shared &sh = *reinterpret_cast<Shared *>(bar_below ? smem_raw : smem + kTilesEnd);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     PlanHeader *hdr = reinterpret_cast<PlanHeader *>(a.ws + a.lay.header);
@@ -271,9 +288,9 @@ attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gri
             tc::mbar_init(&sh.unit_full[i], 1);
             tc::mbar_init(&sh.unit_empty[i], kUnitArrivals);
         }
+        tc::mbar_init(&sh.q_full, 1);
+        tc::mbar_init(&sh.q_empty, 1);
         for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(&sh.q_full[i], 1);
-            tc::mbar_init(&sh.q_empty[i], 1);
             tc::mbar_init(&sh.k_full[i], 1);
             tc::mbar_init(&sh.k_empty[i], 1);
             tc::mbar_init(&sh.v_full[i], 1);
@@ -322,44 +339,46 @@ attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gri
                 sh.ring[slot] = un;
                 tc::mbar_arrive(&sh.unit_full[slot]);
                 if (un.pair < 0) break;
-                const int qb = uc & 1;
-                if (uc >= 2 && !wait_or_abort(sh, &sh.q_empty[qb], ((uc >> 1) - 1) & 1, status)) break;
-                uint8_t *sQ = smem + kOffQ + qb * kTile;
-                tc::mbar_arrive_expect_tx(&sh.q_full[qb], qbytes);
-                tc::tma_load_3d(sQ, &tmap_q, &sh.q_full[qb], 0, un.h * a.G, un.t0);
-                tc::tma_load_3d(sQ + kBox, &tmap_q, &sh.q_full[qb], 64, un.h * a.G, un.t0);
+                // the previous unit's last Q K^T has read the query tile
+                if (uc >= 1 && !wait_or_abort(sh, &sh.q_empty, (uc - 1) & 1, status)) break;
+                uint8_t *sQ = smem + kOffQ;
+                tc::mbar_arrive_expect_tx(&sh.q_full, qbytes);
+                tc::tma_load_3d(sQ, &tmap_q, &sh.q_full, 0, un.h * a.G, un.t0);
+                tc::tma_load_3d(sQ + kBoxQ, &tmap_q, &sh.q_full, 64, un.h * a.G, un.t0);
                 ++nq;
                 ++uc;
                 bool ok = true;
-                for (int i = 0; i < un.count; ++i, ++gb) {
-                    const PlanEntry e = lists[un.entry + i];
+                PlanEntry e{};
+                for (int i = 0; i < 2 * un.count; ++i, ++gb) {
+                    if ((i & 1) == 0) e = lists[un.entry + (i >> 1)];
+                    const int key0 = e.page * kKeys + (i & 1) * kHalf;  // half i & 1 of the page
                     const int st = gb & 1;
                     const uint32_t ph = ((gb >> 1) - 1) & 1;
                     if (gb >= 2 && !(ok = wait_or_abort(sh, &sh.k_empty[st], ph, status))) break;
-                    uint8_t *sK = smem + kOffK + st * kTile;
-                    tc::mbar_arrive_expect_tx(&sh.k_full[st], kTile);
-                    tc::tma_load_3d(sK, &tmap_k, &sh.k_full[st], 0, un.h, e.page * kKeys, policy);
-                    tc::tma_load_3d(sK + kBox, &tmap_k, &sh.k_full[st], 64, un.h, e.page * kKeys, policy);
+                    uint8_t *sK = smem + kOffK + st * kTileH;
+                    tc::mbar_arrive_expect_tx(&sh.k_full[st], kTileH);
+                    tc::tma_load_3d(sK, &tmap_k, &sh.k_full[st], 0, un.h, key0, policy);
+                    tc::tma_load_3d(sK + kBoxH, &tmap_k, &sh.k_full[st], 64, un.h, key0, policy);
                     ++nk;
                     if (gb >= 2 && !(ok = wait_or_abort(sh, &sh.v_empty[st], ph, status))) break;
-                    uint8_t *sV = smem + kOffV + st * kTile;
-                    tc::mbar_arrive_expect_tx(&sh.v_full[st], kTile);
-                    tc::tma_load_3d(sV, &tmap_v, &sh.v_full[st], 0, un.h, e.page * kKeys, policy);
-                    tc::tma_load_3d(sV + kBox, &tmap_v, &sh.v_full[st], 64, un.h, e.page * kKeys, policy);
+                    uint8_t *sV = smem + kOffV + st * kTileH;
+                    tc::mbar_arrive_expect_tx(&sh.v_full[st], kTileH);
+                    tc::tma_load_3d(sV, &tmap_v, &sh.v_full[st], 0, un.h, key0, policy);
+                    tc::tma_load_3d(sV + kBoxH, &tmap_v, &sh.v_full[st], 64, un.h, key0, policy);
                     ++nv;
                 }
                 if (!ok) break;
             }
             // every issued copy lands before the CTA may exit (the last
             // phase of each barrier is the only one still pending)
-            for (uint32_t q = (nq > 2 ? nq - 2 : 0); q < nq; ++q) tc::mbar_wait(&sh.q_full[q & 1], (q >> 1) & 1);
+            if (nq > 0) tc::mbar_wait(&sh.q_full, (nq - 1) & 1);
             for (uint32_t b = (nk > 2 ? nk - 2 : 0); b < nk; ++b) tc::mbar_wait(&sh.k_full[b & 1], (b >> 1) & 1);
             for (uint32_t b = (nv > 2 ? nv - 2 : 0); b < nv; ++b) tc::mbar_wait(&sh.v_full[b & 1], (b >> 1) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            const uint32_t idesc_s = tc::idesc_f16_m128(kKeys, true);
+            const uint32_t idesc_s = tc::idesc_f16_m128(kHalf, true);
             const uint32_t idesc_o = tc::idesc_f16_m128(kD, true) | (1u << 16);  // B (V) MN-major
             const uint32_t aP = tc::smem_u32(smem + kOffP);
             uint32_t uc = 0, gb = 0;
@@ -370,28 +389,31 @@ attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gri
                 const PlanUnit un = sh.ring[slot];
                 tc::mbar_arrive(&sh.unit_empty[slot]);
                 if (un.pair < 0) break;
-                const int qb = uc & 1;
-                if (!wait_or_abort(sh, &sh.q_full[qb], (uc >> 1) & 1, status)) break;
+                if (!wait_or_abort(sh, &sh.q_full, uc & 1, status)) break;
                 tc::tc_fence_after();
-                const uint32_t aQ = tc::smem_u32(smem + kOffQ + qb * kTile);
-                for (int i = 0; ok && i <= un.count; ++i) {
-                    if (i < un.count) {
+                const uint32_t aQ = tc::smem_u32(smem + kOffQ);
+                const int nblk = 2 * un.count;  // half pages
+                for (int i = 0; ok && i <= nblk; ++i) {
+                    if (i < nblk) {
                         const uint32_t b = gb + i;
                         const int st = b & 1;
                         ok = wait_or_abort(sh, &sh.k_full[st], (b >> 1) & 1, status);
                         if (ok && b >= 2) ok = wait_or_abort(sh, &sh.s_free[st], ((b >> 1) - 1) & 1, status);
                         if (!ok) break;
                         tc::tc_fence_after();
-                        const uint32_t aK = tc::smem_u32(smem + kOffK + st * kTile);
+                        const uint32_t aK = tc::smem_u32(smem + kOffK + st * kTileH);
 #pragma unroll
                         for (int ks = 0; ks < kD / 16; ++ks) {
-                            const uint32_t off = (ks >> 2) * kBox + (ks & 3) * 32;
-                            tc::mma_f16(tmem + kColS + st * kKeys, tc::smem_desc(aQ + off, 16, 1024, tc::kSw128),
-                                        tc::smem_desc(aK + off, 16, 1024, tc::kSw128), idesc_s, ks > 0);
+                            // 16 dims a step: 32 bytes into a 128-byte row, the
+                            // second 64 dims one box on
+                            const uint32_t offq = (ks >> 2) * kBoxQ + (ks & 3) * 32;
+                            const uint32_t offk = (ks >> 2) * kBoxH + (ks & 3) * 32;
+                            tc::mma_f16(tmem + kColS + st * kHalf, tc::smem_desc(aQ + offq, 16, 1024, tc::kSw128),
+                                        tc::smem_desc(aK + offk, 16, 1024, tc::kSw128), idesc_s, ks > 0);
                         }
                         tc::mma_commit(&sh.s_full[st]);
                         tc::mma_commit(&sh.k_empty[st]);
-                        if (i + 1 == un.count) tc::mma_commit(&sh.q_empty[qb]);
+                        if (i + 1 == nblk) tc::mma_commit(&sh.q_empty);
                     }
                     if (i >= 1) {
                         const uint32_t b = gb + i - 1;
@@ -403,20 +425,22 @@ attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gri
                         if (ok && i == 1 && uc >= 1) ok = wait_or_abort(sh, &sh.o_free, (uc - 1) & 1, status);
                         if (!ok) break;
                         tc::tc_fence_after();
-                        const uint32_t aV = tc::smem_u32(smem + kOffV + st * kTile);
+                        const uint32_t aV = tc::smem_u32(smem + kOffV + st * kTileH);
 #pragma unroll
-                        for (int ks = 0; ks < kKeys / 16; ++ks) {
-                            const uint32_t offp = (ks >> 2) * kBox + (ks & 3) * 32;
-                            tc::mma_f16(tmem + kColO, tc::smem_desc(aP + offp, 16, 1024, tc::kSw128),
-                                        tc::smem_desc(aV + ks * 2048, kBox, 1024, tc::kSw128), idesc_o,
+                        for (int ks = 0; ks < kHalf / 16; ++ks) {
+                            // P: one 128-byte row (64 keys) per query row; V:
+                            // 16 slots of 128 bytes per step, the second 64
+                            // dims one box on
+                            tc::mma_f16(tmem + kColO, tc::smem_desc(aP + ks * 32, 16, 1024, tc::kSw128),
+                                        tc::smem_desc(aV + ks * 2048, kBoxH, 1024, tc::kSw128), idesc_o,
                                         i > 1 || ks > 0);
                         }
                         tc::mma_commit(&sh.pv_done);
                         tc::mma_commit(&sh.v_empty[st]);
                     }
                 }
-                if (un.count == 0) tc::mma_commit(&sh.q_empty[qb]);
-                gb += un.count;
+                if (un.count == 0) tc::mma_commit(&sh.q_empty);
+                gb += nblk;
                 ++uc;
             }
             tc::mma_commit(&sh.drain);
@@ -486,38 +510,42 @@ attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gri
             int Lmin = 0x7fffffff;
             for (int jj = 0; jj < un.nt; ++jj) Lmin = min(Lmin, sh.Lj[jj]);
             float m_run = -INFINITY, l = 0.f;
-            PlanEntry e_next{};
+            PlanEntry e_next{}, e{};
             if (un.count > 0) e_next = lists[un.entry];
-            for (int i = 0; i < un.count; ++i) {
+            const int nblk = 2 * un.count;  // half pages
+            for (int i = 0; i < nblk; ++i) {
                 const uint32_t b = gb + i;
                 const int sb = b & 1;
-                const PlanEntry e = e_next;
-                if (i + 1 < un.count) e_next = lists[un.entry + i + 1];
+                if ((i & 1) == 0) {
+                    e = e_next;
+                    if ((i >> 1) + 1 < un.count) e_next = lists[un.entry + (i >> 1) + 1];
+                }
+                const int bstart = static_cast<int>(e.block) * kKeys + (i & 1) * kHalf;  // first key of the half
                 const bool sel = active && ((e.mask >> j) & 1);
-                const int lim = sel ? min(kKeys, max(0, L - static_cast<int>(e.block) * kKeys)) : 0;
+                const int lim = sel ? min(kHalf, max(0, L - bstart)) : 0;
                 ok = warp_wait(sh, &sh.s_full[sb], (b >> 1) & 1, status);
                 if (!ok) break;
                 tc::tc_fence_after();
-                float s[kKeys];
+                float s[kHalf];
                 if (warp_active) {
 #pragma unroll
-                    for (int ch = 0; ch < kKeys / 32; ++ch) tmem_ld32(tmem + lane_base + kColS + sb * kKeys + ch * 32, s + ch * 32);
+                    for (int ch = 0; ch < kHalf / 32; ++ch) tmem_ld32(tmem + lane_base + kColS + sb * kHalf + ch * 32, s + ch * 32);
                     tc::tmem_wait_ld();
                 }
                 tc::tc_fence_before();
                 tc::mbar_arrive(&sh.s_free[sb]);
-                uint32_t pk[kKeys / 2];
+                uint32_t pk[kHalf / 2];
                 float alpha = 1.f;
                 if (warp_active) {
-                    if (lim < kKeys) {
+                    if (lim < kHalf) {
 #pragma unroll
-                        for (int k = 0; k < kKeys; ++k)
+                        for (int k = 0; k < kHalf; ++k)
                             if (k >= lim) s[k] = -INFINITY;
                     }
                     float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
                     if (a.c >= 0.f) {
 #pragma unroll
-                        for (int k = 0; k < kKeys; k += 4) {
+                        for (int k = 0; k < kHalf; k += 4) {
                             mx0 = fmaxf(mx0, s[k]);
                             mx1 = fmaxf(mx1, s[k + 1]);
                             mx2 = fmaxf(mx2, s[k + 2]);
@@ -525,7 +553,7 @@ attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gri
                         }
                     } else {
 #pragma unroll
-                        for (int k = 0; k < kKeys; k += 4) {
+                        for (int k = 0; k < kHalf; k += 4) {
                             mx0 = fmaxf(mx0, s[k] == -INFINITY ? -INFINITY : -s[k]);
                             mx1 = fmaxf(mx1, s[k + 1] == -INFINITY ? -INFINITY : -s[k + 1]);
                             mx2 = fmaxf(mx2, s[k + 2] == -INFINITY ? -INFINITY : -s[k + 2]);
@@ -540,9 +568,9 @@ attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gri
                         l *= alpha;
                     }
                     const float m_eff = (m_run == -INFINITY) ? 0.f : m_run;
-                    if (lim >= kKeys) {
+                    if (lim >= kHalf) {
 #pragma unroll
-                        for (int k = 0; k < kKeys; k += 2) {
+                        for (int k = 0; k < kHalf; k += 2) {
                             const float p0 = tc::ex2(fmaf(s[k], a.c, -m_eff));
                             const float p1 = tc::ex2(fmaf(s[k + 1], a.c, -m_eff));
                             l += p0 + p1;
@@ -550,7 +578,7 @@ attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gri
                         }
                     } else {
 #pragma unroll
-                        for (int k = 0; k < kKeys; k += 2) {
+                        for (int k = 0; k < kHalf; k += 2) {
                             const float p0 = (k < lim) ? tc::ex2(fmaf(s[k], a.c, -m_eff)) : 0.f;
                             const float p1 = (k + 1 < lim) ? tc::ex2(fmaf(s[k + 1], a.c, -m_eff)) : 0.f;
                             l += p0 + p1;
@@ -561,20 +589,19 @@ attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gri
                 // V rows past every row's limit (the tail of a request's last
                 // page: slots that may hold anything, NaN included) become
                 // zeros, so that 0-weight keys add exactly nothing
-                const int bstart = static_cast<int>(e.block) * kKeys;
-                if (bstart + kKeys > Lmin) {
+                if (bstart + kHalf > Lmin) {
                     int vlim = 0;
                     for (int jj = 0; jj < un.nt; ++jj)
-                        if ((e.mask >> jj) & 1) vlim = max(vlim, min(kKeys, sh.Lj[jj] - bstart));
-                    if (vlim < kKeys) {
+                        if ((e.mask >> jj) & 1) vlim = max(vlim, min(kHalf, sh.Lj[jj] - bstart));
+                    if (vlim < kHalf) {
                         ok = warp_wait(sh, &sh.v_full[sb], (b >> 1) & 1, status);
                         if (!ok) break;
-                        if (r >= vlim) {
-                            uint8_t *vrow = smem + kOffV + sb * kTile + r * 128;
+                        if (r >= vlim && r < kHalf) {
+                            uint8_t *vrow = smem + kOffV + sb * kTileH + r * 128;
 #pragma unroll
                             for (int q = 0; q < 8; ++q) {
                                 reinterpret_cast<uint4 *>(vrow)[q] = make_uint4(0u, 0u, 0u, 0u);
-                                reinterpret_cast<uint4 *>(vrow + kBox)[q] = make_uint4(0u, 0u, 0u, 0u);
+                                reinterpret_cast<uint4 *>(vrow + kBoxH)[q] = make_uint4(0u, 0u, 0u, 0u);
                             }
                             tc::fence_proxy_async();
                         }
@@ -604,14 +631,13 @@ attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gri
                         tc::tmem_wait_st();
                     }
 #pragma unroll
-                    for (int cidx = 0; cidx < 16; ++cidx) {
-                        const int half = cidx >> 3, chunk = cidx & 7;
+                    for (int chunk = 0; chunk < 8; ++chunk) {
                         uint4 w;
-                        w.x = pk[cidx * 4 + 0];
-                        w.y = pk[cidx * 4 + 1];
-                        w.z = pk[cidx * 4 + 2];
-                        w.w = pk[cidx * 4 + 3];
-                        *reinterpret_cast<uint4 *>(prow + half * kBox + ((chunk ^ sw) << 4)) = w;
+                        w.x = pk[chunk * 4 + 0];
+                        w.y = pk[chunk * 4 + 1];
+                        w.z = pk[chunk * 4 + 2];
+                        w.w = pk[chunk * 4 + 3];
+                        *reinterpret_cast<uint4 *>(prow + ((chunk ^ sw) << 4)) = w;
                     }
                     tc::fence_proxy_async();
                 }
@@ -623,7 +649,7 @@ attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gri
             resolve();
             // ---- unit epilogue: this thread's row of O, 32 dims at a time
             if (un.count > 0) {
-                ok = warp_wait(sh, &sh.pv_done, (gb + un.count - 1) & 1, status);
+                ok = warp_wait(sh, &sh.pv_done, (gb + nblk - 1) & 1, status);
                 tc::tc_fence_after();
             }
             const bool have_o = ok && un.count > 0 && warp_active;
@@ -680,7 +706,7 @@ attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gri
                 if (st_id == 0) ticket = atomicAdd(&counters[un.pair], 1);
                 pend = un;
             }
-            gb += un.count;
+            gb += nblk;
             ++uc;
         }
         if (finished) resolve();
@@ -705,6 +731,22 @@ bool make_tmap_bf16(CUtensorMap *m, const void *base, int64_t rows, int64_t head
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The largest shared-memory carveout for the kernel on the current device
+// (two CTAs of 113 KB per SM), once per device.
+cudaError_t prefer_shared_carveout(const void *func) {
+    static std::mutex mu;
+    static std::set<int> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count(dev)) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             static_cast<int>(cudaSharedmemCarveoutMaxShared));
+    if (e == cudaSuccess) done.insert(dev);
+    return e;
 }
 
 }  // namespace
@@ -732,11 +774,13 @@ cudaError_t launch_attention_bf16_tc(const AttnArgs &a, void *ws, size_t ws_byte
     CUtensorMap tq, tk, tv;
     const int64_t qs1 = a.Hq > 1 ? a.q_s1 : kD, qs0 = a.T > 1 ? a.q_s0 : static_cast<int64_t>(a.Hq) * qs1;
     if (!make_tmap_bf16(&tq, a.q, a.T, a.Hq, qs0, qs1, G, gmax)) return cudaSuccess;
-    if (!make_tmap_bf16(&tk, a.k, a.P * kKeys, a.Hkv, a.k_s0, a.k_s1, 1, kKeys)) return cudaSuccess;
-    if (!make_tmap_bf16(&tv, a.v, a.P * kKeys, a.Hkv, a.v_s0, a.v_s1, 1, kKeys)) return cudaSuccess;
+    if (!make_tmap_bf16(&tk, a.k, a.P * kKeys, a.Hkv, a.k_s0, a.k_s1, 1, kHalf)) return cudaSuccess;
+    if (!make_tmap_bf16(&tv, a.v, a.P * kKeys, a.Hkv, a.v_s0, a.v_s1, 1, kHalf)) return cudaSuccess;
 
-    const int sms = device_sm_count();
+    // two persistent CTAs per SM
+    const int ctas = 2 * device_sm_count();
     cudaError_t e = opt_in_smem(reinterpret_cast<const void *>(attention_bf16_tc_kernel), kSmemBytes);
+    if (e == cudaSuccess) e = prefer_shared_carveout(reinterpret_cast<const void *>(attention_bf16_tc_kernel));
     if (e != cudaSuccess) return e;
 
     PlanArgs p{};
@@ -747,7 +791,7 @@ cudaError_t launch_attention_bf16_tc(const AttnArgs &a, void *ws, size_t ws_byte
     p.T = a.T; p.R = a.R; p.NB = a.NB; p.K = a.K; p.Hkv = a.Hkv; p.G = G;
     p.gmax = gmax;
     p.P = a.P;
-    p.num_ctas = sms;
+    p.num_ctas = ctas;
     p.ws = static_cast<char *>(ws);
     p.lay = lay;
     p.q = a.q; p.q_s0 = a.q_s0; p.q_s1 = a.q_s1; p.q_s2 = a.q_s2;
@@ -769,7 +813,7 @@ cudaError_t launch_attention_bf16_tc(const AttnArgs &a, void *ws, size_t ws_byte
     t.ws = static_cast<char *>(ws);
     t.lay = lay;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(sms);
+    cfg.gridDim = dim3(ctas);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;

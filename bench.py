@@ -115,6 +115,15 @@ def workload_desc(w):
     }
 
 
+def fp8_attention_kernel(w):
+    """Name of the tensor-core kernel the library's default picks for an FP8
+    cache and bf16 queries: the query-rows kernel when the batch averages at
+    least 48 query rows (tokens x q heads of one kv head) per request."""
+    G = w.Hq // w.Hkv
+    R = w.block_table.shape[0]
+    return "attention_e4m3_rows_kernel" if w.T * G >= 48 * R else "attention_tc_kernel"
+
+
 def attention_bytes(w, topk_np):
     """Algorithmic bytes of one attention launch: every selected (request, kv
     head, block) page of K and V read once for its valid tokens (query rows of
@@ -332,7 +341,7 @@ def run_reference(args, rank, world):
     }
 
 
-ATTENTION_POLICY = {"auto": 0, "general": 1}
+ATTENTION_POLICY = {"auto": 0, "general": 1, "lanes": 2, "rows": 3}
 
 
 def run_gpu(args, rank, world, local_rank):
@@ -561,8 +570,11 @@ def run_gpu(args, rank, world, local_rank):
                     "traffic": traffic,
                     "kernel": "paged attention call (%s; %s)"
                               % ("general-layout kernel" if args.attention_kernel == "general" else
-                                 "list planner, unit planner, " + ("attention_tc_kernel" if args.kv_cache == "e4m3"
-                                                                  else "attention_bf16_tc_kernel"),
+                                 "list planner, unit planner, " + (
+                                     "attention_bf16_tc_kernel" if args.kv_cache == "bf16" else
+                                     "attention_tc_kernel" if args.attention_kernel == "lanes" else
+                                     "attention_e4m3_rows_kernel" if args.attention_kernel == "rows" else
+                                     fp8_attention_kernel(w)),
                                  "graph replay" if graph is not None else "direct launches"),
                     "algorithmic_bytes_per_launch": abytes,
                     "mean_launch_us": attn_mean_s * 1e6, "peak_source": peak_src}
@@ -1008,9 +1020,10 @@ def main():
                     help="index cache as generated (bf16) or stored FP8-E4M3")
     ap.add_argument("--kv-cache", default="e4m3", choices=["e4m3", "bf16"],
                     help="K/V cache as FP8-E4M3 with static scalar scales (default) or dense BF16")
-    ap.add_argument("--attention-kernel", default="auto", choices=["auto", "general"],
-                    help="paged attention kernel: the tensor-core kernel of the cache type (default) or the "
-                         "general-layout kernel")
+    ap.add_argument("--attention-kernel", default="auto", choices=["auto", "general", "lanes", "rows"],
+                    help="paged attention kernel: the tensor-core kernel of the cache type (default), the "
+                         "general-layout kernel, or for an FP8 cache the keys-on-lanes or the query-rows "
+                         "tensor-core kernel")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -358,7 +358,12 @@ SPD_API int spd_set_attention_kernel(int policy);
  * 0 (default) picks the specialised kernel whenever the shapes and layouts
  * allow it, 1 always the general-layout kernel; for stage 2, policy 2 picks
  * the shared-memory rank kernel (the default sorts rows of up to 256 blocks
- * in registers and ranks longer ones).  All give identical selections, and
+ * in registers and ranks longer ones); for stage 3 and an FP8-E4M3 cache,
+ * policy 2 picks the keys-on-lanes tensor-core kernel and 3 the query-rows
+ * one (the default takes the query-rows kernel for bf16 queries of head dim
+ * 128, G <= 16 and on average at least 48 query rows per request and kv
+ * head, the keys-on-lanes one otherwise; a shape the picked kernel does not
+ * cover runs on the general-layout kernel).  All give identical selections, and
  * attention results that agree within the stated tolerance.  Returns the
  * previous setting, or -1 for an unknown stage.
  */

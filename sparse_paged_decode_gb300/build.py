@@ -41,7 +41,7 @@ def _sources():
 # kernels and that cache type's tensor-core attention kernel): what a
 # DRAM-traffic capture of that call depends on
 _PLAN_SOURCES = ("dispatch.cu", "plan.cu", "plan.cuh", "spd_internal.cuh", "tc_ptx.cuh", "tmap.cuh")
-ATTENTION_SOURCES = {"e4m3": ("attention_tc.cu",) + _PLAN_SOURCES,
+ATTENTION_SOURCES = {"e4m3": ("attention_e4m3_rows_tc.cu", "attention_tc.cu") + _PLAN_SOURCES,
                      "bf16": ("attention_bf16_tc.cu",) + _PLAN_SOURCES}
 
 

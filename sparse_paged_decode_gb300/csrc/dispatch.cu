@@ -52,6 +52,8 @@ cudaError_t opt_in_smem(const void *func, int bytes) {
 cudaError_t launch_score_tc(const ScoreArgs &a, cudaStream_t stream, bool *used);
 cudaError_t launch_attention_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cudaStream_t stream, bool *used);
 cudaError_t launch_attention_bf16_tc(const AttnArgs &a, void *ws, size_t ws_bytes, cudaStream_t stream, bool *used);
+cudaError_t launch_attention_e4m3_rows(const AttnArgs &a, void *ws, size_t ws_bytes, cudaStream_t stream,
+                                       bool *used);
 cudaError_t launch_sdpa_tc(const SdpaArgs &a, cudaStream_t stream, bool *used);
 
 namespace {
@@ -87,10 +89,22 @@ cudaError_t dispatch_select(const SelectArgs &a, cudaStream_t stream) {
 cudaError_t dispatch_attention(const AttnArgs &a, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
     bool used = false;
     cudaError_t e = cudaSuccess;
-    // policy 0: the tensor-core kernel of the cache type; 1: the general kernel
-    if (g_policy[3] == 0) {
-        e = (a.kv_dt == SPD_BF16) ? launch_attention_bf16_tc(a, workspace, workspace_bytes, stream, &used)
-                                  : launch_attention_tc(a, workspace, workspace_bytes, stream, &used);
+    // policy 0: the tensor-core kernel of the cache type; 1: the general
+    // kernel; for an E4M3 cache, 2: the keys-on-lanes kernel only, 3: the
+    // query-rows kernel only.  By default an E4M3 cache takes the query-rows
+    // kernel when a request's rows fill wide groups -- on average at least
+    // 48 query rows (tokens x q heads of one kv head) per request -- and the
+    // keys-on-lanes kernel otherwise: the first one's time per page does not
+    // grow with the group's width up to 128 rows, the second one's does, and
+    // it is the faster of the two for narrow groups.
+    const int pol = g_policy[3];
+    if (pol == 0 && a.kv_dt == SPD_BF16) {
+        e = launch_attention_bf16_tc(a, workspace, workspace_bytes, stream, &used);
+    } else if (a.kv_dt == SPD_E4M3 && (pol == 0 || pol == 2 || pol == 3)) {
+        const int64_t G = a.Hkv > 0 ? a.Hq / a.Hkv : 0;
+        const bool wide = static_cast<int64_t>(a.T) * G >= 48LL * a.R;
+        if (pol == 3 || (pol == 0 && wide)) e = launch_attention_e4m3_rows(a, workspace, workspace_bytes, stream, &used);
+        if (e == cudaSuccess && !used && pol != 3) e = launch_attention_tc(a, workspace, workspace_bytes, stream, &used);
     }
     if (e != cudaSuccess) return e;
     if (used) {

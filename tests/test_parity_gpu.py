@@ -214,6 +214,18 @@ def test_small_cases(spd, orc, name, kernel_policy):
     full_check(spd, orc, w)
 
 
+# stage-3 policies that force one of the two FP8-cache tensor-core kernels
+FP8_KERNELS = (2, 3)  # keys on the TMEM lanes, query rows on the MMA rows
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_small_cases_both_fp8_kernels(spd, orc, name):
+    """Each small case through each of the two FP8-cache kernels (a shape a
+    kernel does not cover runs on the general-layout kernel)."""
+    w = W.make_decode(name, seed=zlib.crc32(name.encode()) % 1000, **SMALL[name])
+    full_check(spd, orc, w, policies=FP8_KERNELS)
+
+
 def test_large_logits(spd, orc, kernel_policy):
     """Heavy-tailed queries scaled up: logits of tens of units and outputs
     dominated by a few keys, where rounding of the queries or of the
@@ -579,17 +591,20 @@ def test_domain_edges_head_dim_256_index_dim_512_and_1024_blocks(spd, orc):
 # --------------------------------------------------------- full-size configs
 
 def test_verification_decode_full(spd, orc):
-    full_check(spd, orc, W.config(2))
+    full_check(spd, orc, W.config(2), policies=(None,) + FP8_KERNELS)
 
 
 def test_dense_decode_full(spd, orc):
-    """Dense decode at full size (16 rows of 16384 tokens): every row."""
+    """Dense decode at full size (16 rows of 16384 tokens): every row, through
+    the default kernel choice and each of the two FP8-cache kernels."""
     w = W.config(3)
     g = w.to(DEV)
     rows = list(range(w.T))
     ref = oracle_rows(orc, w, rows, None)
-    out = gpu_attention(spd, g, None)
-    check_attention(out.float().cpu().numpy(), ref, "dense decode")
+    for pol in (None,) + FP8_KERNELS:
+        with _policy(spd, pol):
+            out = gpu_attention(spd, g, None)
+        check_attention(out.float().cpu().numpy(), ref, "dense decode (policy %s)" % pol)
 
 
 def test_prefill_score_select_full_sampled(spd, orc):
@@ -614,8 +629,9 @@ def test_stress_decode_full(spd, orc):
     the top-k and the sparse (oracle selection), end-to-end (GPU selection)
     and dense attention outputs of every query row -- all four bucket sizes,
     every group the planner forms, every pair it splits and merges, the
-    padded rows (exact zeros) and the longest row."""
+    padded rows (exact zeros) and the longest row; through the default
+    kernel choice and each of the two FP8-cache tensor-core kernels."""
     w = W.config(5)
     assert set(w.tokens_per_request) == {1, 4, 8, 16}
     assert any(int(x) == 0 for x in w.seq_lens), "the configuration has padded rows"
-    full_check(spd, orc, w)
+    full_check(spd, orc, w, policies=(None,) + FP8_KERNELS)

@@ -23,15 +23,15 @@
 //                    registers (block max, sum, offset raise need no
 //                    exchange); p <= 2^kRaise, stored as f16
 //   O += P V         kind::f16, P from shared memory, V widened from E4M3 to
-//                    f16 (exact) by two warps, MN-major
+//                    f16 (exact) by the softmax threads, MN-major
 // K and V half pages are TMA-gathered straight from the paged cache through
 // the block list (64 slots of 128 bytes, 128-byte swizzle).  A CTA takes 112
 // KB of shared memory and 256 tensor-memory columns, so two share an SM and
 // one's per-block chain runs while the other waits on its own.
 //
-// Roles (8 warps): warps 0-3 run the softmax and the unit epilogue (warp w
-// reads TMEM lanes 32 w .. +31), warp 4 claims units and issues the TMA
-// loads, warp 5 owns tensor memory and issues every MMA, warps 6-7 widen V.
+// Roles (8 warps): warps 0-3 run the softmax, widen V and run the unit
+// epilogue (warp w reads TMEM lanes 32 w .. +31), warp 4 claims units and
+// issues the TMA loads, warp 5 owns tensor memory and issues every MMA.
 // Every wait is bounded: a wait that gives up sets bit 0 of the workspace
 // status word and the CTA winds down.
 #include <cuda.h>
@@ -58,10 +58,10 @@ constexpr int kD = 128;
 constexpr int kM = 128;            // query rows of a unit (padded)
 constexpr int kKeys = 128;         // slots per page
 constexpr int kHalf = 64;          // keys per block of the products: half a page
-constexpr int kThreads = 256;      // warps 0-3 softmax / epilogue, 4 TMA, 5 MMA, 6-7 V widening
+constexpr int kThreads = 256;      // warps 0-3 softmax / V widening / epilogue, 4 TMA, 5 MMA, 6-7 idle
 constexpr int kSoftThreads = 128;
-constexpr int kConvThreads = 64;
-constexpr int kWarpTma = 4, kWarpMma = 5, kWarpConv = 6;
+constexpr int kWarpTma = 4, kWarpMma = 5;
+constexpr int kStages = 3;         // K and V half-page stages of E4M3
 constexpr int kTerms = 2;               // E4M3 terms of a bf16 query
 constexpr int kQTile = kM * 128;        // one query term: 128 rows x 128 bytes
 constexpr int kKVHalf = kHalf * 128;    // E4M3 half page of one kv head: 64 slots x 128 bytes
@@ -71,26 +71,26 @@ constexpr int kPTile = kM * kHalf * 2;  // 128 rows x 64 keys of f16: one 128-by
 constexpr float kRaise = 8.0f;
 constexpr int kStride = kD + kPartialStride;  // floats per partial row
 
-// dynamic shared memory (1024-byte aligned tiles): two query terms, two K
-// and two V stages of E4M3, two widened V tiles, P
+// dynamic shared memory (1024-byte aligned tiles): two query terms, three K
+// and three V stages of E4M3, the widened V tile, P
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kTerms * kQTile;
-constexpr int kOffV = kOffK + 2 * kKVHalf;
-constexpr int kOffV16 = kOffV + 2 * kKVHalf;
-constexpr int kOffP = kOffV16 + 2 * kV16Tile;
+constexpr int kOffV = kOffK + kStages * kKVHalf;
+constexpr int kOffV16 = kOffV + kStages * kKVHalf;
+constexpr int kOffP = kOffV16 + kV16Tile;
 constexpr int kTilesEnd = kOffP + kPTile;
 
 struct Shared {
     uint64_t unit_full[4], unit_empty[4];
     uint64_t q_full, q_empty;
-    uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
-    uint64_t v16_full[2], v16_free[2];
+    uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
     uint64_t s_full[2], s_free[2];
     uint64_t p_full, pv_done, o_free, drain;
     PlanUnit ring[4];
     uint32_t tmem_base;
     int abort;
-    int last;  // the unit that took the last ticket of its pair merges
+    int last;     // the unit that took the last ticket of its pair merges
+    int Lj[16];   // key limit of each token of the current unit
 };
 
 // The barriers sit in the padding below the aligned tiles when it is large
@@ -102,11 +102,11 @@ static_assert(2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
 
 // tensor memory: S buffers at columns 0 and 64, O at 128
 constexpr uint32_t kColS = 0, kColO = 2 * kHalf, kTmemCols = 256;
-// a unit record is released by the MMA issuer, the softmax and the V-widening threads
-constexpr uint32_t kUnitArrivals = 1 + kSoftThreads + kConvThreads;
+// a unit record is released by the MMA issuer and the softmax threads
+constexpr uint32_t kUnitArrivals = 1 + kSoftThreads;
 // Registers: the launch gives 128 per thread (two CTAs of 256 threads per
-// SM); the softmax warpgroup rises to 192 and the other one (TMA, MMA,
-// V widening) drops to 64: 128 x 192 + 128 x 64 = 256 x 128.
+// SM); the softmax warpgroup rises to 192 and the other one (TMA, MMA) drops
+// to 64: 128 x 192 + 128 x 64 = 256 x 128.
 constexpr uint32_t kRegsSoft = 192, kRegsOther = 64;
 static_assert(128 * kRegsSoft + 128 * kRegsOther <= kThreads * 128, "register split");
 
@@ -295,13 +295,13 @@ attention_e4m3_rows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __g
         }
         tc::mbar_init(&sh.q_full, 1);
         tc::mbar_init(&sh.q_empty, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kStages; ++i) {
             tc::mbar_init(&sh.k_full[i], 1);
             tc::mbar_init(&sh.k_empty[i], 1);
             tc::mbar_init(&sh.v_full[i], 1);
-            tc::mbar_init(&sh.v_empty[i], kConvThreads);
-            tc::mbar_init(&sh.v16_full[i], kConvThreads);
-            tc::mbar_init(&sh.v16_free[i], 1);
+            tc::mbar_init(&sh.v_empty[i], kSoftThreads);
+        }
+        for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&sh.s_full[i], 1);
             tc::mbar_init(&sh.s_free[i], kSoftThreads);
         }
@@ -362,13 +362,13 @@ attention_e4m3_rows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __g
                     for (int i = 0; i < 2 * un.count; ++i, ++gb) {
                         if ((i & 1) == 0) e = lists[un.entry + (i >> 1)];
                         const int key0 = e.page * kKeys + (i & 1) * kHalf;  // half i & 1 of the page
-                        const int st = gb & 1;
-                        const uint32_t ph = ((gb >> 1) - 1) & 1;
-                        if (gb >= 2 && !(ok = wait_or_abort(sh, &sh.k_empty[st], ph, status))) break;
+                        const int st = gb % kStages;
+                        const uint32_t ph = ((gb / kStages) - 1) & 1;
+                        if (gb >= kStages && !(ok = wait_or_abort(sh, &sh.k_empty[st], ph, status))) break;
                         tc::mbar_arrive_expect_tx(&sh.k_full[st], kKVHalf);
                         tc::tma_load_3d(smem + kOffK + st * kKVHalf, &tmap_k, &sh.k_full[st], 0, un.h, key0, policy);
                         ++nk;
-                        if (gb >= 2 && !(ok = wait_or_abort(sh, &sh.v_empty[st], ph, status))) break;
+                        if (gb >= kStages && !(ok = wait_or_abort(sh, &sh.v_empty[st], ph, status))) break;
                         tc::mbar_arrive_expect_tx(&sh.v_full[st], kKVHalf);
                         tc::tma_load_3d(smem + kOffV + st * kKVHalf, &tmap_v, &sh.v_full[st], 0, un.h, key0, policy);
                         ++nv;
@@ -378,8 +378,10 @@ attention_e4m3_rows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __g
                 // every issued copy lands before the CTA may exit (the last
                 // phase of each barrier is the only one still pending)
                 if (nq > 0) tc::mbar_wait(&sh.q_full, (nq - 1) & 1);
-                for (uint32_t b = (nk > 2 ? nk - 2 : 0); b < nk; ++b) tc::mbar_wait(&sh.k_full[b & 1], (b >> 1) & 1);
-                for (uint32_t b = (nv > 2 ? nv - 2 : 0); b < nv; ++b) tc::mbar_wait(&sh.v_full[b & 1], (b >> 1) & 1);
+                for (uint32_t b = (nk > kStages ? nk - kStages : 0); b < nk; ++b)
+                    tc::mbar_wait(&sh.k_full[b % kStages], (b / kStages) & 1);
+                for (uint32_t b = (nv > kStages ? nv - kStages : 0); b < nv; ++b)
+                    tc::mbar_wait(&sh.v_full[b % kStages], (b / kStages) & 1);
             }
         } else if (warp == kWarpMma) {
             // --------------------------------------------------- MMA issuer
@@ -402,9 +404,9 @@ attention_e4m3_rows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __g
                     for (int i = 0; ok && i <= nblk; ++i) {
                         if (i < nblk) {
                             const uint32_t b = gb + i;
-                            const int st = b & 1;
-                            ok = wait_or_abort(sh, &sh.k_full[st], (b >> 1) & 1, status);
-                            if (ok && b >= 2) ok = wait_or_abort(sh, &sh.s_free[st], ((b >> 1) - 1) & 1, status);
+                            const int st = b % kStages, sb = b & 1;
+                            ok = wait_or_abort(sh, &sh.k_full[st], (b / kStages) & 1, status);
+                            if (ok && b >= 2) ok = wait_or_abort(sh, &sh.s_free[sb], ((b >> 1) - 1) & 1, status);
                             if (!ok) break;
                             tc::tc_fence_after();
                             const uint32_t aK = aK0 + st * kKVHalf;
@@ -414,25 +416,25 @@ attention_e4m3_rows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __g
                             for (int term = 0; term < kTerms; ++term)
 #pragma unroll
                                 for (int ks = 0; ks < kD / 32; ++ks)
-                                    tc::mma_f8(tmem + kColS + st * kHalf,
+                                    tc::mma_f8(tmem + kColS + sb * kHalf,
                                                tc::smem_desc(aQ + term * kQTile + ks * 32, 16, 1024, tc::kSw128),
                                                tc::smem_desc(aK + ks * 32, 16, 1024, tc::kSw128), idesc_s,
                                                term > 0 || ks > 0);
-                            tc::mma_commit(&sh.s_full[st]);
+                            tc::mma_commit(&sh.s_full[sb]);
                             tc::mma_commit(&sh.k_empty[st]);
                             if (i + 1 == nblk) tc::mma_commit(&sh.q_empty);
                         }
                         if (i >= 1) {
                             const uint32_t b = gb + i - 1;
-                            const int x = b & 1;
-                            ok = wait_or_abort(sh, &sh.p_full, b & 1, status) &&
-                                 wait_or_abort(sh, &sh.v16_full[x], (b >> 1) & 1, status);
+                            // P and the widened V of half page b are both written
+                            // by the softmax threads before p_full
+                            ok = wait_or_abort(sh, &sh.p_full, b & 1, status);
                             // the first product of a unit overwrites O: the previous
                             // unit's epilogue must have read it
                             if (ok && i == 1 && uc >= 1) ok = wait_or_abort(sh, &sh.o_free, (uc - 1) & 1, status);
                             if (!ok) break;
                             tc::tc_fence_after();
-                            const uint32_t aV = aV0 + x * kV16Tile;
+                            const uint32_t aV = aV0;
 #pragma unroll
                             for (int ks = 0; ks < kHalf / 16; ++ks) {
                                 // P: one 128-byte row (64 keys) per query row; V: 16
@@ -443,7 +445,6 @@ attention_e4m3_rows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __g
                                             i > 1 || ks > 0);
                             }
                             tc::mma_commit(&sh.pv_done);
-                            tc::mma_commit(&sh.v16_free[x]);
                         }
                     }
                     if (un.count == 0) tc::mma_commit(&sh.q_empty);
@@ -453,80 +454,8 @@ attention_e4m3_rows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __g
                 tc::mma_commit(&sh.drain);
                 tc::mbar_wait(&sh.drain, 0);
             }
-        } else {
-            // -------------------------------------------------- V widening
-            // Thread ct widens slot ct of each V half page: E4M3 (128-byte
-            // swizzled TMA row) -> f16 in two 64-dim halves with 128-byte
-            // swizzle, the B operand of P V.  Slots past every selecting
-            // row's key limit (the tail of a request's last page: they may
-            // hold anything, NaN included) become zeros, so that 0-weight
-            // keys add exactly nothing.
-            const int ct = threadIdx.x - kWarpConv * 32;
-            const int sw8 = ct & 7;
-            uint32_t uc = 0, gb = 0;
-            for (;;) {
-                const int slot = uc & 3;
-                if (!wait_or_abort(sh, &sh.unit_full[slot], (uc >> 2) & 1, status)) break;
-                const PlanUnit un = sh.ring[slot];
-                tc::mbar_arrive(&sh.unit_empty[slot]);
-                if (un.pair < 0) break;
-                // key limit of the unit's token `lane` (all lanes of a warp hold them)
-                int my_lim = 0;
-                if (lane < un.nt) {
-                    int r;
-                    my_lim = static_cast<int>(token_limit(a.ri, a.ri_s0, a.sl, a.sl_s0, un.t0 + lane, a.R, a.NB, &r));
-                }
-                bool ok = true;
-                PlanEntry e{};
-                for (int i = 0; i < 2 * un.count; ++i) {
-                    const uint32_t b = gb + i;
-                    const int st = b & 1;
-                    if ((i & 1) == 0) e = lists[un.entry + (i >> 1)];
-                    const int bstart = static_cast<int>(e.block) * kKeys + (i & 1) * kHalf;
-                    int vlim = 0;
-                    for (int j = 0; j < un.nt; ++j) {
-                        const int lj = __shfl_sync(0xffffffffu, my_lim, j);
-                        if ((e.mask >> j) & 1) vlim = max(vlim, min(kHalf, lj - bstart));
-                    }
-                    ok = wait_or_abort(sh, &sh.v_full[st], (b >> 1) & 1, status);
-                    // the widened tile was read by the product of half page b - 2
-                    if (ok && b >= 2) ok = wait_or_abort(sh, &sh.v16_free[st], ((b >> 1) - 1) & 1, status);
-                    if (!ok) break;
-                    const uint8_t *src = smem + kOffV + st * kKVHalf + ct * 128;
-                    uint8_t *dst = smem + kOffV16 + st * kV16Tile + ct * 128;
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        uint4 x[4];
-                        if (ct < vlim) {
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                x[q] = *reinterpret_cast<const uint4 *>(src + (((4 * hh + q) ^ sw8) << 4));
-                        } else {
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) x[q] = make_uint4(0u, 0u, 0u, 0u);
-                        }
-                        uint8_t *half = dst + hh * kV16Box;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint32_t f[8];
-                            tc::e4m3x4_to_f16x4(x[q].x, f[0], f[1]);
-                            tc::e4m3x4_to_f16x4(x[q].y, f[2], f[3]);
-                            tc::e4m3x4_to_f16x4(x[q].z, f[4], f[5]);
-                            tc::e4m3x4_to_f16x4(x[q].w, f[6], f[7]);
-                            *reinterpret_cast<uint4 *>(half + (((2 * q) ^ sw8) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
-                            *reinterpret_cast<uint4 *>(half + (((2 * q + 1) ^ sw8) << 4)) =
-                                make_uint4(f[4], f[5], f[6], f[7]);
-                        }
-                    }
-                    tc::fence_proxy_async();
-                    tc::mbar_arrive(&sh.v_empty[st]);
-                    tc::mbar_arrive(&sh.v16_full[st]);
-                }
-                if (!ok) break;
-                gb += 2 * un.count;
-                ++uc;
-            }
         }
+        // warps 6-7 have no role
     } else {
         tc::regs_inc<kRegsSoft>();
         // --------------------------------------------- softmax and epilogue
@@ -583,6 +512,13 @@ attention_e4m3_rows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __g
                                  : 0;
             // the row's logit factor: s c is the logit in log2 units
             const float c = active ? cfac[static_cast<int64_t>(un.t0 + j) * a.Hq + un.h * a.G + g] : 0.f;
+            // the unit's key limits, for the V slots no row of the unit may read
+            if (st_id < un.nt) {
+                int rr;
+                sh.Lj[st_id] = static_cast<int>(
+                    token_limit(a.ri, a.ri_s0, a.sl, a.sl_s0, un.t0 + st_id, a.R, a.NB, &rr));
+            }
+            soft_sync();
             float m_run = -INFINITY, l = 0.f;
             PlanEntry e_next{}, e{};
             if (un.count > 0) e_next = lists[un.entry];
@@ -673,6 +609,43 @@ attention_e4m3_rows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __g
                     if (!ok) break;
                     tc::tc_fence_after();
                 }
+                // V of this half page, widened by all 128 threads into the f16
+                // tile (free: the products before this one are done): thread
+                // (slot, d-half) = (st_id & 63, st_id >> 6); slots past every
+                // selecting row's key limit (the tail of a request's last page:
+                // they may hold anything, NaN included) become zeros, so that
+                // 0-weight keys add exactly nothing
+                {
+                    const int st = b % kStages;
+                    int vlim = 0;
+                    for (int jj = 0; jj < un.nt; ++jj)
+                        if ((e.mask >> jj) & 1) vlim = max(vlim, min(kHalf, sh.Lj[jj] - bstart));
+                    ok = warp_wait(sh, &sh.v_full[st], (b / kStages) & 1, status);
+                    if (!ok) break;
+                    const int slot = st_id & 63, hh = st_id >> 6, sw8 = slot & 7;
+                    const uint8_t *src = smem + kOffV + st * kKVHalf + slot * 128;
+                    uint8_t *half = smem + kOffV16 + hh * kV16Box + slot * 128;
+                    uint4 x[4];
+                    if (slot < vlim) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            x[q] = *reinterpret_cast<const uint4 *>(src + (((4 * hh + q) ^ sw8) << 4));
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) x[q] = make_uint4(0u, 0u, 0u, 0u);
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t f[8];
+                        tc::e4m3x4_to_f16x4(x[q].x, f[0], f[1]);
+                        tc::e4m3x4_to_f16x4(x[q].y, f[2], f[3]);
+                        tc::e4m3x4_to_f16x4(x[q].z, f[4], f[5]);
+                        tc::e4m3x4_to_f16x4(x[q].w, f[6], f[7]);
+                        *reinterpret_cast<uint4 *>(half + (((2 * q) ^ sw8) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
+                        *reinterpret_cast<uint4 *>(half + (((2 * q + 1) ^ sw8) << 4)) = make_uint4(f[4], f[5], f[6], f[7]);
+                    }
+                    tc::mbar_arrive(&sh.v_empty[st]);
+                }
                 if (warp_active) {
                     // O holds this unit's earlier blocks: rescale rows whose
                     // offset moved (the first block of a unit overwrites O)
@@ -698,8 +671,8 @@ attention_e4m3_rows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __g
                         w.w = pk[chunk * 4 + 3];
                         *reinterpret_cast<uint4 *>(prow + ((chunk ^ sw) << 4)) = w;
                     }
-                    tc::fence_proxy_async();
                 }
+                tc::fence_proxy_async();  // P and the widened V, for the product
                 tc::tc_fence_before();
                 tc::mbar_arrive(&sh.p_full);
             }

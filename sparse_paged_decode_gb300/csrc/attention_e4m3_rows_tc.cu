@@ -22,12 +22,15 @@
 //   P  = 2^(S c - m) one thread per row: the row's 64 logits stay in its
 //                    registers (block max, sum, offset raise need no
 //                    exchange); p <= 2^kRaise, stored as f16
-//   O += P V         kind::f16, P from shared memory, V widened from E4M3 to
-//                    f16 (exact) by the softmax threads, MN-major
+//   O += P V         kind::f16, P from tensor memory (written over its own S
+//                    buffer), V widened from E4M3 to f16 (exact) by the
+//                    softmax threads into one of two tiles, MN-major
 // K and V half pages are TMA-gathered straight from the paged cache through
 // the block list (64 slots of 128 bytes, 128-byte swizzle).  A CTA takes 112
 // KB of shared memory and 256 tensor-memory columns, so two share an SM and
-// one's per-block chain runs while the other waits on its own.
+// one's per-block chain runs while the other waits on its own.  With P in
+// tensor memory the softmax of a half page no longer waits for the previous
+// half page's product (only to rescale O after an offset raise).
 //
 // Roles (8 warps): warps 0-3 run the softmax, widen V and run the unit
 // epilogue (warp w reads TMEM lanes 32 w .. +31), warp 4 claims units and
@@ -67,25 +70,27 @@ constexpr int kQTile = kM * 128;        // one query term: 128 rows x 128 bytes
 constexpr int kKVHalf = kHalf * 128;    // E4M3 half page of one kv head: 64 slots x 128 bytes
 constexpr int kV16Box = kHalf * 128;    // 64 dims of a widened half page: 64 keys x 128 bytes
 constexpr int kV16Tile = 2 * kV16Box;   // 64 keys x 128 dims of f16
-constexpr int kPTile = kM * kHalf * 2;  // 128 rows x 64 keys of f16: one 128-byte row each
 constexpr float kRaise = 8.0f;
 constexpr int kStride = kD + kPartialStride;  // floats per partial row
 
 // dynamic shared memory (1024-byte aligned tiles): two query terms, three K
-// and three V stages of E4M3, the widened V tile, P
+// and three V stages of E4M3, two widened V tiles (P lives in tensor memory)
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kTerms * kQTile;
 constexpr int kOffV = kOffK + kStages * kKVHalf;
 constexpr int kOffV16 = kOffV + kStages * kKVHalf;
-constexpr int kOffP = kOffV16 + kV16Tile;
-constexpr int kTilesEnd = kOffP + kPTile;
+constexpr int kTilesEnd = kOffV16 + 2 * kV16Tile;
 
 struct Shared {
     uint64_t unit_full[4], unit_empty[4];
     uint64_t q_full, q_empty;
     uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
-    uint64_t s_full[2], s_free[2];
-    uint64_t p_full, pv_done, o_free, drain;
+    uint64_t s_full[2], s_free[2];  // S buffer free: the product that read its P is done
+    uint64_t v16_free[2];           // widened V tile free: the product that read it is done
+    uint64_t p_full[2];  // P of S buffer b % 2 written (one barrier per buffer: the
+                         // softmax may hand off the next buffer's P before the
+                         // product of this one is issued)
+    uint64_t pv_done, o_free, drain;
     PlanUnit ring[4];
     uint32_t tmem_base;
     int abort;
@@ -105,9 +110,9 @@ constexpr uint32_t kColS = 0, kColO = 2 * kHalf, kTmemCols = 256;
 // a unit record is released by the MMA issuer and the softmax threads
 constexpr uint32_t kUnitArrivals = 1 + kSoftThreads;
 // Registers: the launch gives 128 per thread (two CTAs of 256 threads per
-// SM); the softmax warpgroup rises to 192 and the other one (TMA, MMA) drops
-// to 64: 128 x 192 + 128 x 64 = 256 x 128.
-constexpr uint32_t kRegsSoft = 192, kRegsOther = 64;
+// SM); the softmax warpgroup rises to 184 and the other one (TMA, MMA) drops
+// to 72: 128 x 184 + 128 x 72 = 256 x 128.
+constexpr uint32_t kRegsSoft = 184, kRegsOther = 72;
 static_assert(128 * kRegsSoft + 128 * kRegsOther <= kThreads * 128, "register split");
 
 struct RowsArgs {
@@ -303,9 +308,11 @@ attention_e4m3_rows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __g
         }
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&sh.s_full[i], 1);
-            tc::mbar_init(&sh.s_free[i], kSoftThreads);
+            tc::mbar_init(&sh.s_free[i], 1);
+            tc::mbar_init(&sh.v16_free[i], 1);
         }
-        tc::mbar_init(&sh.p_full, kSoftThreads);
+        tc::mbar_init(&sh.p_full[0], kSoftThreads);
+        tc::mbar_init(&sh.p_full[1], kSoftThreads);
         tc::mbar_init(&sh.pv_done, 1);
         tc::mbar_init(&sh.o_free, kSoftThreads);
         tc::mbar_init(&sh.drain, 1);
@@ -389,7 +396,7 @@ attention_e4m3_rows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __g
                 const uint32_t idesc_s = tc::idesc_m128(kHalf, false, false);    // E4M3 x E4M3, K-major
                 const uint32_t idesc_o = tc::idesc_f16_m128(kD, false) | (1u << 16);  // f16, V MN-major
                 const uint32_t aQ = tc::smem_u32(smem + kOffQ), aK0 = tc::smem_u32(smem + kOffK);
-                const uint32_t aP = tc::smem_u32(smem + kOffP), aV0 = tc::smem_u32(smem + kOffV16);
+                const uint32_t aV0 = tc::smem_u32(smem + kOffV16);
                 uint32_t uc = 0, gb = 0;
                 bool ok = true;
                 while (ok) {
@@ -426,25 +433,28 @@ attention_e4m3_rows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __g
                         }
                         if (i >= 1) {
                             const uint32_t b = gb + i - 1;
-                            // P and the widened V of half page b are both written
-                            // by the softmax threads before p_full
-                            ok = wait_or_abort(sh, &sh.p_full, b & 1, status);
+                            const int pb = b & 1;
+                            // P (in S buffer pb) and the widened V of half page b
+                            // are both written by the softmax threads before p_full
+                            ok = wait_or_abort(sh, &sh.p_full[pb], (b >> 1) & 1, status);
                             // the first product of a unit overwrites O: the previous
                             // unit's epilogue must have read it
                             if (ok && i == 1 && uc >= 1) ok = wait_or_abort(sh, &sh.o_free, (uc - 1) & 1, status);
                             if (!ok) break;
                             tc::tc_fence_after();
-                            const uint32_t aV = aV0;
+                            const uint32_t aV = aV0 + pb * kV16Tile;
 #pragma unroll
                             for (int ks = 0; ks < kHalf / 16; ++ks) {
-                                // P: one 128-byte row (64 keys) per query row; V: 16
-                                // keys of 128 bytes per step, the second 64 dims one
-                                // box on
-                                tc::mma_f16(tmem + kColO, tc::smem_desc(aP + ks * 32, 16, 1024, tc::kSw128),
-                                            tc::smem_desc(aV + ks * 2048, kV16Box, 1024, tc::kSw128), idesc_o,
-                                            i > 1 || ks > 0);
+                                // P from tensor memory: lane = query row, 16 keys =
+                                // 8 columns of f16 pairs per step; V: 16 keys of 128
+                                // bytes per step, the second 64 dims one box on
+                                tc::mma_f16_tmem_a(tmem + kColO, tmem + kColS + pb * kHalf + ks * 8,
+                                                   tc::smem_desc(aV + ks * 2048, kV16Box, 1024, tc::kSw128), idesc_o,
+                                                   i > 1 || ks > 0);
                             }
                             tc::mma_commit(&sh.pv_done);
+                            tc::mma_commit(&sh.s_free[pb]);
+                            tc::mma_commit(&sh.v16_free[pb]);
                         }
                     }
                     if (un.count == 0) tc::mma_commit(&sh.q_empty);
@@ -462,8 +472,6 @@ attention_e4m3_rows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __g
         const int st_id = threadIdx.x;  // 0..127
         const int r = st_id;            // row of the unit = TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-        uint8_t *prow = smem + kOffP + r * 128;
-        const uint32_t sw = static_cast<uint32_t>(r & 7);
         int32_t *counters = reinterpret_cast<int32_t *>(a.ws + a.lay.counters);
         float *partials = reinterpret_cast<float *>(a.ws + a.lay.partials);
         const float *cfac = reinterpret_cast<const float *>(a.ws + a.lay.cfac);
@@ -543,8 +551,6 @@ attention_e4m3_rows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __g
                         tmem_ld32(tmem + lane_base + kColS + sb * kHalf + ch * 32, s + ch * 32);
                     tc::tmem_wait_ld();
                 }
-                tc::tc_fence_before();
-                tc::mbar_arrive(&sh.s_free[sb]);
                 uint32_t pk[kHalf / 2];
                 float alpha = 1.f;
                 if (warp_active) {
@@ -602,29 +608,50 @@ attention_e4m3_rows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __g
                         }
                     }
                 }
-                // P is free once the previous block's product is done (it
-                // may belong to the previous unit)
-                if (b >= 1) {
-                    ok = warp_wait(sh, &sh.pv_done, (b - 1) & 1, status);
-                    if (!ok) break;
-                    tc::tc_fence_after();
+                if (warp_active) {
+                    // O holds this unit's earlier blocks: rescale rows whose
+                    // offset moved (the first block of a unit overwrites O),
+                    // once the previous product is done
+                    if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                        if (!warp_wait(sh, &sh.pv_done, (b - 1) & 1, status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc::tc_fence_after();
+#pragma unroll 1
+                        for (int ch = 0; ch < kD / 32; ++ch) {
+                            float o[32];
+                            const uint32_t ta = tmem + lane_base + kColO + ch * 32;
+                            tmem_ld32(ta, o);
+                            tc::tmem_wait_ld();
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) o[k] *= alpha;
+                            tmem_st32(ta, o);
+                        }
+                        tc::tmem_wait_st();
+                    }
+                    // P over this half page's S (its logits are in registers):
+                    // 64 f16 in 32 columns of the row's lane
+                    tc::tmem_st32u(tmem + lane_base + kColS + sb * kHalf, pk);
+                    tc::tmem_wait_st();
                 }
-                // V of this half page, widened by all 128 threads into the f16
-                // tile (free: the products before this one are done): thread
-                // (slot, d-half) = (st_id & 63, st_id >> 6); slots past every
-                // selecting row's key limit (the tail of a request's last page:
-                // they may hold anything, NaN included) become zeros, so that
-                // 0-weight keys add exactly nothing
+                // V of this half page, widened by all 128 threads into f16 tile
+                // b & 1 (free once the product of half page b - 2 is done):
+                // thread (slot, d-half) = (st_id & 63, st_id >> 6); slots past
+                // every selecting row's key limit (the tail of a request's last
+                // page: they may hold anything, NaN included) become zeros, so
+                // that 0-weight keys add exactly nothing
                 {
                     const int st = b % kStages;
                     int vlim = 0;
                     for (int jj = 0; jj < un.nt; ++jj)
                         if ((e.mask >> jj) & 1) vlim = max(vlim, min(kHalf, sh.Lj[jj] - bstart));
                     ok = warp_wait(sh, &sh.v_full[st], (b / kStages) & 1, status);
+                    if (ok && b >= 2) ok = warp_wait(sh, &sh.v16_free[sb], ((b >> 1) - 1) & 1, status);
                     if (!ok) break;
                     const int slot = st_id & 63, hh = st_id >> 6, sw8 = slot & 7;
                     const uint8_t *src = smem + kOffV + st * kKVHalf + slot * 128;
-                    uint8_t *half = smem + kOffV16 + hh * kV16Box + slot * 128;
+                    uint8_t *half = smem + kOffV16 + sb * kV16Tile + hh * kV16Box + slot * 128;
                     uint4 x[4];
                     if (slot < vlim) {
 #pragma unroll
@@ -646,35 +673,9 @@ attention_e4m3_rows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __g
                     }
                     tc::mbar_arrive(&sh.v_empty[st]);
                 }
-                if (warp_active) {
-                    // O holds this unit's earlier blocks: rescale rows whose
-                    // offset moved (the first block of a unit overwrites O)
-                    if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-                        for (int ch = 0; ch < kD / 32; ++ch) {
-                            float o[32];
-                            const uint32_t ta = tmem + lane_base + kColO + ch * 32;
-                            tmem_ld32(ta, o);
-                            tc::tmem_wait_ld();
-#pragma unroll
-                            for (int k = 0; k < 32; ++k) o[k] *= alpha;
-                            tmem_st32(ta, o);
-                        }
-                        tc::tmem_wait_st();
-                    }
-#pragma unroll
-                    for (int chunk = 0; chunk < 8; ++chunk) {
-                        uint4 w;
-                        w.x = pk[chunk * 4 + 0];
-                        w.y = pk[chunk * 4 + 1];
-                        w.z = pk[chunk * 4 + 2];
-                        w.w = pk[chunk * 4 + 3];
-                        *reinterpret_cast<uint4 *>(prow + ((chunk ^ sw) << 4)) = w;
-                    }
-                }
-                tc::fence_proxy_async();  // P and the widened V, for the product
+                tc::fence_proxy_async();  // the widened V, for the product
                 tc::tc_fence_before();
-                tc::mbar_arrive(&sh.p_full);
+                tc::mbar_arrive(&sh.p_full[sb]);
             }
             if (soft_any(!ok || aborted(sh))) break;
             // the previous split unit's ticket has had this unit's pages to return

@@ -17,12 +17,15 @@
 //                    double-buffered in tensor memory
 //   P  = 2^(S c - m) one thread per row: the row's logits stay in its
 //                    registers (block max, sum, offset raise need no exchange)
-//   O += P V         kind::f16 bf16, P from shared memory, V as TMA loaded it
+//   O += P V         kind::f16 bf16, P from tensor memory (written over its
+//                    own S buffer), V as TMA loaded it
 // K and V half pages are TMA-gathered straight from the paged cache through
 // the block list (two 64-dim boxes of 64 slots each, 128-byte swizzle).  A
-// CTA takes 112 KB of shared memory and 256 tensor-memory columns, so two
+// CTA takes 96 KB of shared memory and 256 tensor-memory columns, so two
 // share an SM and one's per-block chain runs while the other waits on its
-// own.  A row's
+// own.  With P in tensor memory the softmax of a half page does not wait
+// for the previous half page's product (only to rescale O after an offset
+// raise).  A row's
 // keys in a block are those below its key limit, and none if the row did not
 // select the block.  c = sm_scale * k_scale * log2(e); the exponent offset of
 // a row is raised only when a block maximum exceeds it by more than 2^kRaise,
@@ -63,7 +66,6 @@ constexpr int kBoxQ = 128 * 128;    // 128 query rows x 64 bf16 dims
 constexpr int kTileQ = 2 * kBoxQ;   // 128 rows x 128 dims
 constexpr int kBoxH = kHalf * 128;  // 64 slots x 64 dims
 constexpr int kTileH = 2 * kBoxH;   // 64 slots x 128 dims
-constexpr int kTileP = 128 * kHalf * 2;  // 128 rows x 64 keys: one 128-byte row each
 constexpr float kRaise = 8.0f;
 constexpr int kStride = kD + kPartialStride;  // floats per partial row
 
@@ -72,15 +74,17 @@ constexpr int kStride = kD + kPartialStride;  // floats per partial row
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kTileQ;
 constexpr int kOffV = kOffK + 2 * kTileH;
-constexpr int kOffP = kOffV + 2 * kTileH;
-constexpr int kTilesEnd = kOffP + kTileP;
+constexpr int kTilesEnd = kOffV + 2 * kTileH;
 
 struct Shared {
     uint64_t unit_full[4], unit_empty[4];
     uint64_t q_full, q_empty;
     uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
-    uint64_t s_full[2], s_free[2];
-    uint64_t p_full, pv_done, o_free, drain;
+    uint64_t s_full[2], s_free[2];  // S buffer free: the product that read its P is done
+    uint64_t p_full[2];  // P of S buffer b % 2 written (one barrier per buffer: the
+                         // softmax may hand off the next buffer's P before the
+                         // product of this one is issued)
+    uint64_t pv_done, o_free, drain;
     PlanUnit ring[4];
     uint32_t tmem_base;
     int abort;
@@ -296,9 +300,10 @@ attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gri
             tc::mbar_init(&sh.v_full[i], 1);
             tc::mbar_init(&sh.v_empty[i], 1);
             tc::mbar_init(&sh.s_full[i], 1);
-            tc::mbar_init(&sh.s_free[i], kSoftThreads);
+            tc::mbar_init(&sh.s_free[i], 1);
         }
-        tc::mbar_init(&sh.p_full, kSoftThreads);
+        tc::mbar_init(&sh.p_full[0], kSoftThreads);
+        tc::mbar_init(&sh.p_full[1], kSoftThreads);
         tc::mbar_init(&sh.pv_done, 1);
         tc::mbar_init(&sh.o_free, kSoftThreads);
         tc::mbar_init(&sh.drain, 1);
@@ -380,7 +385,6 @@ attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gri
         if (lane == 0) {
             const uint32_t idesc_s = tc::idesc_f16_m128(kHalf, true);
             const uint32_t idesc_o = tc::idesc_f16_m128(kD, true) | (1u << 16);  // B (V) MN-major
-            const uint32_t aP = tc::smem_u32(smem + kOffP);
             uint32_t uc = 0, gb = 0;
             bool ok = true;
             while (ok) {
@@ -418,7 +422,7 @@ attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gri
                     if (i >= 1) {
                         const uint32_t b = gb + i - 1;
                         const int st = b & 1;
-                        ok = wait_or_abort(sh, &sh.p_full, b & 1, status) &&
+                        ok = wait_or_abort(sh, &sh.p_full[st], (b >> 1) & 1, status) &&
                              wait_or_abort(sh, &sh.v_full[st], (b >> 1) & 1, status);
                         // the first product of a unit overwrites O: the previous
                         // unit's epilogue must have read it
@@ -428,15 +432,17 @@ attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gri
                         const uint32_t aV = tc::smem_u32(smem + kOffV + st * kTileH);
 #pragma unroll
                         for (int ks = 0; ks < kHalf / 16; ++ks) {
-                            // P: one 128-byte row (64 keys) per query row; V:
-                            // 16 slots of 128 bytes per step, the second 64
-                            // dims one box on
-                            tc::mma_f16(tmem + kColO, tc::smem_desc(aP + ks * 32, 16, 1024, tc::kSw128),
-                                        tc::smem_desc(aV + ks * 2048, kBoxH, 1024, tc::kSw128), idesc_o,
-                                        i > 1 || ks > 0);
+                            // P from tensor memory (its S buffer): lane = query
+                            // row, 16 keys = 8 columns of bf16 pairs per step; V:
+                            // 16 slots of 128 bytes per step, the second 64 dims
+                            // one box on
+                            tc::mma_f16_tmem_a(tmem + kColO, tmem + kColS + st * kHalf + ks * 8,
+                                               tc::smem_desc(aV + ks * 2048, kBoxH, 1024, tc::kSw128), idesc_o,
+                                               i > 1 || ks > 0);
                         }
                         tc::mma_commit(&sh.pv_done);
                         tc::mma_commit(&sh.v_empty[st]);
+                        tc::mma_commit(&sh.s_free[st]);
                     }
                 }
                 if (un.count == 0) tc::mma_commit(&sh.q_empty);
@@ -452,8 +458,6 @@ attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gri
         const int quad = warp & 3;
         const int r = quad * 32 + lane;  // row of the unit = TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        uint8_t *prow = smem + kOffP + r * 128;
-        const uint32_t sw = static_cast<uint32_t>(r & 7);
         int32_t *counters = reinterpret_cast<int32_t *>(a.ws + a.lay.counters);
         float *partials = reinterpret_cast<float *>(a.ws + a.lay.partials);
         uint32_t uc = 0, gb = 0;
@@ -532,8 +536,6 @@ attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gri
                     for (int ch = 0; ch < kHalf / 32; ++ch) tmem_ld32(tmem + lane_base + kColS + sb * kHalf + ch * 32, s + ch * 32);
                     tc::tmem_wait_ld();
                 }
-                tc::tc_fence_before();
-                tc::mbar_arrive(&sh.s_free[sb]);
                 uint32_t pk[kHalf / 2];
                 float alpha = 1.f;
                 if (warp_active) {
@@ -607,17 +609,26 @@ attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gri
                         }
                     }
                 }
-                // P is free once the previous block's product is done (it
-                // may belong to the previous unit)
-                if (b >= 1) {
+                // On the unit's last half page L the previous product must be
+                // done before P(L) is handed off: the epilogue then waits for
+                // product L by parity, which is exact only once L - 1 is done
+                // (seeing S(b) guarantees product b - 2 only, since P no longer
+                // waits for the product before it)
+                if (i == nblk - 1 && b >= 1) {
                     ok = warp_wait(sh, &sh.pv_done, (b - 1) & 1, status);
                     if (!ok) break;
                     tc::tc_fence_after();
                 }
                 if (warp_active) {
                     // O holds this unit's earlier blocks: rescale rows whose
-                    // offset moved (the first block of a unit overwrites O)
+                    // offset moved (the first block of a unit overwrites O),
+                    // once the previous product is done
                     if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                        if (!warp_wait(sh, &sh.pv_done, (b - 1) & 1, status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc::tc_fence_after();
 #pragma unroll 1
                         for (int ch = 0; ch < kD / 32; ++ch) {
                             float o[32];
@@ -630,25 +641,21 @@ attention_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __gri
                         }
                         tc::tmem_wait_st();
                     }
-#pragma unroll
-                    for (int chunk = 0; chunk < 8; ++chunk) {
-                        uint4 w;
-                        w.x = pk[chunk * 4 + 0];
-                        w.y = pk[chunk * 4 + 1];
-                        w.z = pk[chunk * 4 + 2];
-                        w.w = pk[chunk * 4 + 3];
-                        *reinterpret_cast<uint4 *>(prow + ((chunk ^ sw) << 4)) = w;
-                    }
-                    tc::fence_proxy_async();
+                    // P over this half page's S (its logits are in registers):
+                    // 64 bf16 in 32 columns of the row's lane
+                    tc::tmem_st32u(tmem + lane_base + kColS + sb * kHalf, pk);
+                    tc::tmem_wait_st();
                 }
                 tc::tc_fence_before();
-                tc::mbar_arrive(&sh.p_full);
+                tc::mbar_arrive(&sh.p_full[sb]);
             }
             if (soft_any(!ok || aborted(sh))) break;
             // the previous split unit's ticket has had this unit's pages to return
             resolve();
             // ---- unit epilogue: this thread's row of O, 32 dims at a time
             if (un.count > 0) {
+                // the unit's last product (the one before it is done: see the
+                // last half page's hand-off)
                 ok = warp_wait(sh, &sh.pv_done, (gb + nblk - 1) & 1, status);
                 tc::tc_fence_after();
             }

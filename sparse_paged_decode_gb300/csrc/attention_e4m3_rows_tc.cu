@@ -608,6 +608,16 @@ attention_e4m3_rows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __g
                         }
                     }
                 }
+                // On the unit's last half page L the previous product must be
+                // done before P(L) is handed off: the epilogue then waits for
+                // product L by parity, which is exact only once L - 1 is done
+                // (seeing S(b) guarantees product b - 2 only, since P no longer
+                // waits for the product before it)
+                if (i == nblk - 1 && b >= 1) {
+                    ok = warp_wait(sh, &sh.pv_done, (b - 1) & 1, status);
+                    if (!ok) break;
+                    tc::tc_fence_after();
+                }
                 if (warp_active) {
                     // O holds this unit's earlier blocks: rescale rows whose
                     // offset moved (the first block of a unit overwrites O),
@@ -682,6 +692,8 @@ attention_e4m3_rows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __g
             resolve();
             // ---- unit epilogue: this thread's row of O, 32 dims at a time
             if (un.count > 0) {
+                // the unit's last product (the one before it is done: see the
+                // last half page's hand-off)
                 ok = warp_wait(sh, &sh.pv_done, (gb + nblk - 1) & 1, status);
                 tc::tc_fence_after();
             }

@@ -23,8 +23,8 @@
 //                    registers (block max, sum, offset raise need no
 //                    exchange); p <= 2^kRaise, stored as f16
 //   O += P V         kind::f16, P from tensor memory (written over its own S
-//                    buffer), V widened from E4M3 to f16 (exact) by the
-//                    softmax threads into one of two tiles, MN-major
+//                    buffer), V widened from E4M3 to f16 (exact) by two
+//                    warps into one of two tiles, MN-major
 // K and V half pages are TMA-gathered straight from the paged cache through
 // the block list (64 slots of 128 bytes, 128-byte swizzle).  A CTA takes 112
 // KB of shared memory and 256 tensor-memory columns, so two share an SM and
@@ -32,9 +32,9 @@
 // tensor memory the softmax of a half page no longer waits for the previous
 // half page's product (only to rescale O after an offset raise).
 //
-// Roles (8 warps): warps 0-3 run the softmax, widen V and run the unit
-// epilogue (warp w reads TMEM lanes 32 w .. +31), warp 4 claims units and
-// issues the TMA loads, warp 5 owns tensor memory and issues every MMA.
+// Roles (8 warps): warps 0-3 run the softmax and the unit epilogue (warp w
+// reads TMEM lanes 32 w .. +31), warp 4 claims units and issues the TMA
+// loads, warp 5 owns tensor memory and issues every MMA, warps 6-7 widen V.
 // Every wait is bounded: a wait that gives up sets bit 0 of the workspace
 // status word and the CTA winds down.
 #include <cuda.h>
@@ -61,9 +61,10 @@ constexpr int kD = 128;
 constexpr int kM = 128;            // query rows of a unit (padded)
 constexpr int kKeys = 128;         // slots per page
 constexpr int kHalf = 64;          // keys per block of the products: half a page
-constexpr int kThreads = 256;      // warps 0-3 softmax / V widening / epilogue, 4 TMA, 5 MMA, 6-7 idle
+constexpr int kThreads = 256;      // warps 0-3 softmax / epilogue, 4 TMA, 5 MMA, 6-7 V widening
 constexpr int kSoftThreads = 128;
-constexpr int kWarpTma = 4, kWarpMma = 5;
+constexpr int kConvThreads = 64;
+constexpr int kWarpTma = 4, kWarpMma = 5, kWarpConv = 6;
 constexpr int kStages = 3;         // K and V half-page stages of E4M3
 constexpr int kTerms = 2;               // E4M3 terms of a bf16 query
 constexpr int kQTile = kM * 128;        // one query term: 128 rows x 128 bytes
@@ -87,6 +88,7 @@ struct Shared {
     uint64_t k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
     uint64_t s_full[2], s_free[2];  // S buffer free: the product that read its P is done
     uint64_t v16_free[2];           // widened V tile free: the product that read it is done
+    uint64_t v16_full[2];           // widened V tile written
     uint64_t p_full[2];  // P of S buffer b % 2 written (one barrier per buffer: the
                          // softmax may hand off the next buffer's P before the
                          // product of this one is issued)
@@ -95,7 +97,6 @@ struct Shared {
     uint32_t tmem_base;
     int abort;
     int last;     // the unit that took the last ticket of its pair merges
-    int Lj[16];   // key limit of each token of the current unit
 };
 
 // The barriers sit in the padding below the aligned tiles when it is large
@@ -107,11 +108,11 @@ static_assert(2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
 
 // tensor memory: S buffers at columns 0 and 64, O at 128
 constexpr uint32_t kColS = 0, kColO = 2 * kHalf, kTmemCols = 256;
-// a unit record is released by the MMA issuer and the softmax threads
-constexpr uint32_t kUnitArrivals = 1 + kSoftThreads;
+// a unit record is released by the MMA issuer, the softmax and the V-widening threads
+constexpr uint32_t kUnitArrivals = 1 + kSoftThreads + kConvThreads;
 // Registers: the launch gives 128 per thread (two CTAs of 256 threads per
-// SM); the softmax warpgroup rises to 184 and the other one (TMA, MMA) drops
-// to 72: 128 x 184 + 128 x 72 = 256 x 128.
+// SM); the softmax warpgroup rises to 184 and the other one (TMA, MMA,
+// V widening) drops to 72: 128 x 184 + 128 x 72 = 256 x 128.
 constexpr uint32_t kRegsSoft = 184, kRegsOther = 72;
 static_assert(128 * kRegsSoft + 128 * kRegsOther <= kThreads * 128, "register split");
 
@@ -304,12 +305,13 @@ attention_e4m3_rows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __g
             tc::mbar_init(&sh.k_full[i], 1);
             tc::mbar_init(&sh.k_empty[i], 1);
             tc::mbar_init(&sh.v_full[i], 1);
-            tc::mbar_init(&sh.v_empty[i], kSoftThreads);
+            tc::mbar_init(&sh.v_empty[i], kConvThreads);
         }
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&sh.s_full[i], 1);
             tc::mbar_init(&sh.s_free[i], 1);
             tc::mbar_init(&sh.v16_free[i], 1);
+            tc::mbar_init(&sh.v16_full[i], kConvThreads);
         }
         tc::mbar_init(&sh.p_full[0], kSoftThreads);
         tc::mbar_init(&sh.p_full[1], kSoftThreads);
@@ -434,9 +436,10 @@ attention_e4m3_rows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __g
                         if (i >= 1) {
                             const uint32_t b = gb + i - 1;
                             const int pb = b & 1;
-                            // P (in S buffer pb) and the widened V of half page b
-                            // are both written by the softmax threads before p_full
-                            ok = wait_or_abort(sh, &sh.p_full[pb], (b >> 1) & 1, status);
+                            // P (in S buffer pb) by the softmax threads, the
+                            // widened V of half page b by the V-widening warps
+                            ok = wait_or_abort(sh, &sh.p_full[pb], (b >> 1) & 1, status) &&
+                                 wait_or_abort(sh, &sh.v16_full[pb], (b >> 1) & 1, status);
                             // the first product of a unit overwrites O: the previous
                             // unit's epilogue must have read it
                             if (ok && i == 1 && uc >= 1) ok = wait_or_abort(sh, &sh.o_free, (uc - 1) & 1, status);
@@ -464,8 +467,79 @@ attention_e4m3_rows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __g
                 tc::mma_commit(&sh.drain);
                 tc::mbar_wait(&sh.drain, 0);
             }
+        } else {
+            // ------------------------------------------------ V widening (6-7)
+            // Thread ct widens slot ct of each V half page: E4M3 (128-byte
+            // swizzled TMA row) -> f16 in two 64-dim halves with 128-byte
+            // swizzle, into tile b % 2 once the product of half page b - 2 is
+            // done.  Slots past every selecting row's key limit (the tail of a
+            // request's last page: they may hold anything, NaN included)
+            // become zeros, so that 0-weight keys add exactly nothing.
+            const int ct = threadIdx.x - kWarpConv * 32;
+            const int sw8 = ct & 7;
+            uint32_t uc = 0, gb = 0;
+            for (;;) {
+                const int slot = uc & 3;
+                if (!wait_or_abort(sh, &sh.unit_full[slot], (uc >> 2) & 1, status)) break;
+                const PlanUnit un = sh.ring[slot];
+                tc::mbar_arrive(&sh.unit_empty[slot]);
+                if (un.pair < 0) break;
+                // key limit of the unit's token `lane` (every lane of the warp holds them)
+                int my_lim = 0;
+                if (lane < un.nt) {
+                    int r;
+                    my_lim = static_cast<int>(token_limit(a.ri, a.ri_s0, a.sl, a.sl_s0, un.t0 + lane, a.R, a.NB, &r));
+                }
+                bool ok = true;
+                PlanEntry e{};
+                for (int i = 0; i < 2 * un.count; ++i) {
+                    const uint32_t b = gb + i;
+                    const int st = b % kStages, x = b & 1;
+                    if ((i & 1) == 0) e = lists[un.entry + (i >> 1)];
+                    const int bstart = static_cast<int>(e.block) * kKeys + (i & 1) * kHalf;
+                    int vlim = 0;
+                    for (int j = 0; j < un.nt; ++j) {
+                        const int lj = __shfl_sync(0xffffffffu, my_lim, j);
+                        if ((e.mask >> j) & 1) vlim = max(vlim, min(kHalf, lj - bstart));
+                    }
+                    ok = wait_or_abort(sh, &sh.v_full[st], (b / kStages) & 1, status);
+                    if (ok && b >= 2) ok = wait_or_abort(sh, &sh.v16_free[x], ((b >> 1) - 1) & 1, status);
+                    if (!ok) break;
+                    const uint8_t *src = smem + kOffV + st * kKVHalf + ct * 128;
+                    uint8_t *dst = smem + kOffV16 + x * kV16Tile + ct * 128;
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint4 xv[4];
+                        if (ct < vlim) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                xv[q] = *reinterpret_cast<const uint4 *>(src + (((4 * hh + q) ^ sw8) << 4));
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) xv[q] = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        uint8_t *half = dst + hh * kV16Box;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t f[8];
+                            tc::e4m3x4_to_f16x4(xv[q].x, f[0], f[1]);
+                            tc::e4m3x4_to_f16x4(xv[q].y, f[2], f[3]);
+                            tc::e4m3x4_to_f16x4(xv[q].z, f[4], f[5]);
+                            tc::e4m3x4_to_f16x4(xv[q].w, f[6], f[7]);
+                            *reinterpret_cast<uint4 *>(half + (((2 * q) ^ sw8) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
+                            *reinterpret_cast<uint4 *>(half + (((2 * q + 1) ^ sw8) << 4)) =
+                                make_uint4(f[4], f[5], f[6], f[7]);
+                        }
+                    }
+                    tc::fence_proxy_async();
+                    tc::mbar_arrive(&sh.v_empty[st]);
+                    tc::mbar_arrive(&sh.v16_full[x]);
+                }
+                if (!ok) break;
+                gb += 2 * un.count;
+                ++uc;
+            }
         }
-        // warps 6-7 have no role
     } else {
         tc::regs_inc<kRegsSoft>();
         // --------------------------------------------- softmax and epilogue
@@ -520,13 +594,6 @@ attention_e4m3_rows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __g
                                  : 0;
             // the row's logit factor: s c is the logit in log2 units
             const float c = active ? cfac[static_cast<int64_t>(un.t0 + j) * a.Hq + un.h * a.G + g] : 0.f;
-            // the unit's key limits, for the V slots no row of the unit may read
-            if (st_id < un.nt) {
-                int rr;
-                sh.Lj[st_id] = static_cast<int>(
-                    token_limit(a.ri, a.ri_s0, a.sl, a.sl_s0, un.t0 + st_id, a.R, a.NB, &rr));
-            }
-            soft_sync();
             float m_run = -INFINITY, l = 0.f;
             PlanEntry e_next{}, e{};
             if (un.count > 0) e_next = lists[un.entry];
@@ -645,45 +712,6 @@ attention_e4m3_rows_kernel(const __grid_constant__ CUtensorMap tmap_q, const __g
                     tc::tmem_st32u(tmem + lane_base + kColS + sb * kHalf, pk);
                     tc::tmem_wait_st();
                 }
-                // V of this half page, widened by all 128 threads into f16 tile
-                // b & 1 (free once the product of half page b - 2 is done):
-                // thread (slot, d-half) = (st_id & 63, st_id >> 6); slots past
-                // every selecting row's key limit (the tail of a request's last
-                // page: they may hold anything, NaN included) become zeros, so
-                // that 0-weight keys add exactly nothing
-                {
-                    const int st = b % kStages;
-                    int vlim = 0;
-                    for (int jj = 0; jj < un.nt; ++jj)
-                        if ((e.mask >> jj) & 1) vlim = max(vlim, min(kHalf, sh.Lj[jj] - bstart));
-                    ok = warp_wait(sh, &sh.v_full[st], (b / kStages) & 1, status);
-                    if (ok && b >= 2) ok = warp_wait(sh, &sh.v16_free[sb], ((b >> 1) - 1) & 1, status);
-                    if (!ok) break;
-                    const int slot = st_id & 63, hh = st_id >> 6, sw8 = slot & 7;
-                    const uint8_t *src = smem + kOffV + st * kKVHalf + slot * 128;
-                    uint8_t *half = smem + kOffV16 + sb * kV16Tile + hh * kV16Box + slot * 128;
-                    uint4 x[4];
-                    if (slot < vlim) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            x[q] = *reinterpret_cast<const uint4 *>(src + (((4 * hh + q) ^ sw8) << 4));
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) x[q] = make_uint4(0u, 0u, 0u, 0u);
-                    }
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t f[8];
-                        tc::e4m3x4_to_f16x4(x[q].x, f[0], f[1]);
-                        tc::e4m3x4_to_f16x4(x[q].y, f[2], f[3]);
-                        tc::e4m3x4_to_f16x4(x[q].z, f[4], f[5]);
-                        tc::e4m3x4_to_f16x4(x[q].w, f[6], f[7]);
-                        *reinterpret_cast<uint4 *>(half + (((2 * q) ^ sw8) << 4)) = make_uint4(f[0], f[1], f[2], f[3]);
-                        *reinterpret_cast<uint4 *>(half + (((2 * q + 1) ^ sw8) << 4)) = make_uint4(f[4], f[5], f[6], f[7]);
-                    }
-                    tc::mbar_arrive(&sh.v_empty[st]);
-                }
-                tc::fence_proxy_async();  // the widened V, for the product
                 tc::tc_fence_before();
                 tc::mbar_arrive(&sh.p_full[sb]);
             }

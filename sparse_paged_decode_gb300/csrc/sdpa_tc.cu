@@ -14,12 +14,15 @@
 //                    sit in that thread's registers, so the block maximum and
 //                    the row sum need no exchange between threads
 //   O += P V         kind::f16, M = 128 rows, N = 128 dims, K = 64 keys, with
-//                    P written by the softmax into shared memory (K-major)
-//                    and V used as loaded (MN-major)
+//                    P written by the softmax into tensor memory over its own
+//                    S buffer (the A operand read from there) and V used as
+//                    loaded (MN-major)
 //
-// Two CTAs share an SM (113 KB of shared memory and 256 tensor-memory
+// Two CTAs share an SM (97 KB of shared memory and 256 tensor-memory
 // columns each), so one CTA's softmax runs while the other's products keep
-// the tensor pipe busy.  Q, K and V arrive by TMA straight from the caller's
+// the tensor pipe busy.  With P in tensor memory a block's softmax does not
+// wait for the previous block's product (only to rescale O, and on the last
+// block).  Q, K and V arrive by TMA straight from the caller's
 // tensors (64-dim boxes, 128-byte swizzle); keys past the end read as zeros
 // and are masked.  c = sm_scale * log2(e).  The exponent offset m of a row is
 // raised only when a block's maximum exceeds it by more than 2^kRaise (then
@@ -63,23 +66,25 @@ constexpr int kBoxQ = 128 * 128;     // one 64-dim box of 128 query rows, bytes 
 constexpr int kTileQ = 2 * kBoxQ;    // 128 rows x 128 dims
 constexpr int kBoxKV = kKeysBlock * 128;  // one 64-dim box of a key block
 constexpr int kTileKV = 2 * kBoxKV;       // 64 keys x 128 dims
-constexpr int kTileP = 128 * kKeysBlock * 2;  // 128 rows x 64 keys: one 128-byte row each
 constexpr float kRaise = 8.0f;       // log2 headroom before a row's offset is raised
 constexpr float kLog2e = 1.4426950408889634f;
 
-// dynamic shared memory (1024-byte aligned tiles): Q, K stages, V stages, P
+// dynamic shared memory (1024-byte aligned tiles): Q, K stages, V stages (P
+// lives in tensor memory)
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kTileQ;
 constexpr int kOffV = kOffK + kStages * kTileKV;
-constexpr int kOffP = kOffV + kStages * kTileKV;
-constexpr int kTilesEnd = kOffP + kTileP;
+constexpr int kTilesEnd = kOffV + kStages * kTileKV;
 
 struct SdpaShared {
     uint64_t q_full;
     uint64_t k_full[kStages], k_empty[kStages];
     uint64_t v_full[kStages], v_empty[kStages];
-    uint64_t s_full[2], s_free[2];
-    uint64_t p_full, pv_done, drain;
+    uint64_t s_full[2], s_free[2];  // S buffer free: the product that read its P is done
+    uint64_t p_full[2];  // P of S buffer j % 2 written (one barrier per buffer: the
+                         // softmax may hand off the next buffer's P before the
+                         // product of this one is issued)
+    uint64_t pv_done, drain;
     uint32_t tmem_base;
     int abort;
 };
@@ -206,9 +211,10 @@ sdpa_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         }
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&sh.s_full[i], 1);
-            tc::mbar_init(&sh.s_free[i], 128);
+            tc::mbar_init(&sh.s_free[i], 1);
         }
-        tc::mbar_init(&sh.p_full, 128);
+        tc::mbar_init(&sh.p_full[0], 128);
+        tc::mbar_init(&sh.p_full[1], 128);
         tc::mbar_init(&sh.pv_done, 1);
         tc::mbar_init(&sh.drain, 1);
         sh.abort = 0;
@@ -266,7 +272,7 @@ sdpa_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             const bool bf16 = a.in_bf16 != 0;
             const uint32_t idesc_s = tc::idesc_f16_m128(kKeysBlock, bf16);
             const uint32_t idesc_o = idesc_f16_m128_bmn(kD, bf16);
-            const uint32_t aQ = tc::smem_u32(smem + kOffQ), aP = tc::smem_u32(smem + kOffP);
+            const uint32_t aQ = tc::smem_u32(smem + kOffQ);
             bool ok = wait_or_abort(sh, &sh.q_full, 0);
             tc::tc_fence_after();
             for (int j = 0; ok && j <= nb; ++j) {
@@ -290,21 +296,25 @@ sdpa_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                     tc::mma_commit(&sh.k_empty[st]);
                 }
                 if (j >= 1) {
-                    const int i = j - 1, st = i % kStages;
-                    ok = wait_or_abort(sh, &sh.p_full, i & 1) && wait_or_abort(sh, &sh.v_full[st], (i / kStages) & 1);
+                    const int i = j - 1, st = i % kStages, pb = i & 1;
+                    ok = wait_or_abort(sh, &sh.p_full[pb], (i >> 1) & 1) &&
+                         wait_or_abort(sh, &sh.v_full[st], (i / kStages) & 1);
                     if (!ok) break;
                     tc::tc_fence_after();
                     const uint32_t aV = tc::smem_u32(smem + kOffV + st * kTileKV);
 #pragma unroll
                     for (int ks = 0; ks < kKeysBlock / 16; ++ks) {
-                        // P: K-major, one 128-byte row (64 keys) per query row;
+                        // P from tensor memory (its S buffer): lane = query
+                        // row, 16 keys = 8 columns of 16-bit pairs per step;
                         // V: 16 keys = two 8-row groups of 128 bytes per step,
                         // the second 64 dims one box (8 KiB) on
-                        tc::mma_f16(tmem + kColO, tc::smem_desc(aP + ks * 32, 16, 1024, tc::kSw128),
-                                    tc::smem_desc(aV + ks * 2048, kBoxKV, 1024, tc::kSw128), idesc_o, i > 0 || ks > 0);
+                        tc::mma_f16_tmem_a(tmem + kColO, tmem + kColS + pb * kKeysBlock + ks * 8,
+                                           tc::smem_desc(aV + ks * 2048, kBoxKV, 1024, tc::kSw128), idesc_o,
+                                           i > 0 || ks > 0);
                     }
                     tc::mma_commit(&sh.pv_done);
                     tc::mma_commit(&sh.v_empty[st]);
+                    tc::mma_commit(&sh.s_free[pb]);
                 }
             }
             // every issued product completes before tensor memory is released
@@ -324,8 +334,6 @@ sdpa_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
         float m_run = -INFINITY;  // offset of the row's exponents (log2 units)
         float l = 0.f;            // row sum of 2^(s c - m_run)
         bool ok = true;
-        uint8_t *prow = smem + kOffP + r * 128;
-        const uint32_t sw = static_cast<uint32_t>(r & 7);
         for (int j = 0; j < nb; ++j) {
             const int sb = j & 1;
             ok = warp_wait(sh, &sh.s_full[sb], (j >> 1) & 1);
@@ -336,8 +344,6 @@ sdpa_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
             for (int ch = 0; ch < kKeysBlock / 32; ++ch)
                 tmem_ld32(tmem + lane_base + kColS + sb * kKeysBlock + ch * 32, s + ch * 32);
             tc::tmem_wait_ld();
-            tc::tc_fence_before();
-            tc::mbar_arrive(&sh.s_free[sb]);
             // keys at or past the row's limit (and past S) take no weight
             const int lim = n_row - j * kKeysBlock;
             if (lim < kKeysBlock) {
@@ -399,9 +405,11 @@ sdpa_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                     pk[i / 2] = pack2(p0, p1, bf16);
                 }
             }
-            // P of the previous block has been consumed and O holds every
-            // earlier block: rescale this row's O if its offset moved
-            if (j > 0) {
+            // Seeing S(j) means the product of block j - 2 is done (S(j) waited
+            // for it), so a parity wait for product j - 1 is exact here.  It is
+            // made to rescale O after an offset raise, and on the last block
+            // (so that the epilogue's wait for the last product is exact too)
+            if (j > 0 && (j == nb - 1 || __any_sync(0xffffffffu, alpha != 1.f))) {
                 ok = warp_wait(sh, &sh.pv_done, (j - 1) & 1);
                 if (!ok) break;
                 tc::tc_fence_after();
@@ -419,19 +427,12 @@ sdpa_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant
                     tc::tmem_wait_st();
                 }
             }
-            // the row's P: one 128-byte row, 16-byte chunks swizzled by the row
-#pragma unroll
-            for (int chunk = 0; chunk < 8; ++chunk) {
-                uint4 w;
-                w.x = pk[chunk * 4 + 0];
-                w.y = pk[chunk * 4 + 1];
-                w.z = pk[chunk * 4 + 2];
-                w.w = pk[chunk * 4 + 3];
-                *reinterpret_cast<uint4 *>(prow + ((chunk ^ sw) << 4)) = w;
-            }
-            tc::fence_proxy_async();
+            // the row's P over this block's S (its logits are in registers):
+            // 64 16-bit values in 32 columns of the row's lane
+            tc::tmem_st32u(tmem + lane_base + kColS + sb * kKeysBlock, pk);
+            tc::tmem_wait_st();
             tc::tc_fence_before();
-            tc::mbar_arrive(&sh.p_full);
+            tc::mbar_arrive(&sh.p_full[sb]);
         }
         // epilogue: O / l for rows that read keys, zeros for rows that read
         // none, NaN if the CTA gave up.  The tensor-memory loads are

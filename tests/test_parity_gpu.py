@@ -382,10 +382,12 @@ def test_strided_inputs_and_outputs(spd, orc):
     assert torch.all(o_big[:, :, :4] == 7.0) and torch.all(o_big[:, :, -4:] == 7.0)
 
 
-@pytest.mark.parametrize("kv", ["e4m3", "bf16"])
-def test_graph_capture_and_replay_with_new_inputs(spd, orc, kv):
+@pytest.mark.parametrize("kv,policy", [("e4m3", None), ("e4m3", 3), ("bf16", None)],
+                         ids=["e4m3", "e4m3_query_rows_kernel", "bf16"])
+def test_graph_capture_and_replay_with_new_inputs(spd, orc, kv, policy):
     """"Slot contract" -- CUDA graph contract: capture, mutate every dynamic
-    input in place, replay, re-verify (FP8 and BF16 caches)."""
+    input in place, replay, re-verify (FP8 and BF16 caches; for FP8 the
+    default kernel choice and the query-rows kernel forced at capture)."""
     w = W.make_decode("graph", lengths=[1500, 900], tokens_per_request=[4, 2], Hq=16, Hkv=2, D=128, Di=128,
                       NB=16, P=40, K=4, seed=13, kv_dtype=kv)
     g = w.to(DEV)
@@ -402,13 +404,14 @@ def test_graph_capture_and_replay_with_new_inputs(spd, orc, kv):
 
     stream = torch.cuda.Stream()
     stream.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(stream):
-        step()  # warm up outside capture
-    torch.cuda.current_stream().wait_stream(stream)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        step()
+    with _policy(spd, policy):
+        with torch.cuda.stream(stream):
+            step()  # warm up outside capture
+        torch.cuda.current_stream().wait_stream(stream)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
     for it in range(3):
         gen = torch.Generator().manual_seed(100 + it)
         w.q.copy_(torch.randn(w.q.shape, generator=gen).to(w.q.dtype))

@@ -44,6 +44,10 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
                       D=128, Di=128, NB=64, P=128, K=12, seed=501),
         W.make_decode("noalloc_b", lengths=[700, 3000], tokens_per_request=[2, 4], Hq=32, Hkv=4, D=128, Di=128,
                       NB=32, P=64, K=6, seed=502),
+        # wide groups (24 rows of 8 q heads over 2 requests): the query-rows
+        # FP8 kernel by default, where the first two take the keys-on-lanes one
+        W.make_decode("noalloc_c", lengths=[3000, 1200], tokens_per_request=[16, 8], Hq=64, Hkv=8, D=128,
+                      Di=128, NB=32, P=64, K=10, seed=503),
     ]
     for w in batches:
         g = w.to(dev)
